@@ -1,0 +1,364 @@
+"""Plain fp64 CPU oracle of the DFlash draft step (test infrastructure only).
+
+This module is the checker the CUDA library is compared against. Only the tests,
+`__graft_entry__.smoke()` and the CPU-baseline leg of `bench.py` may import it. It
+shares no code, table or helper with the CUDA path: numpy in float64, matrix
+products through numpy's BLAS, everything else written out row by row.
+
+Sources (cited by page title and section):
+  [P1] "LLM的推理加速-DFlash" — 架构设计; 关键创新 Step 1-3 (multi-layer features,
+       concat + projection, K/V injection prepended to every layer's attention);
+       核心推理伪代码 (the draft/verify loop); 验证 (left-to-right acceptance).
+  [P2] "DFlash 2 块扩散投机解码技术详解" — §2.1 (anchor + mask block, mask_token_id),
+       §2.2 (shared embedding x input_embedding_scale; fc + RMSNorm fusion; shared LM
+       head), §2.3 (rejection sampling; greedy prefix formula), §4.2 (fallback to p).
+  [P3] "DFlash：块扩散 + KV 注入，让投机解码的草稿不再串行" — §四 (immediate
+       materialisation: K/V projection then norm + RoPE post-processing).
+  [P4] "DFlash：把串行 Draft 变成并行“填空”" — §2 (at most K+1 tokens per round),
+       §4-4.4 (context / anchor / mask roles; K+1 queries, K outputs), §5.1
+       (normalise, K/V-project, RoPE, write the draft KV cache), §5.3 (non-causal
+       in-block attention), §5.6 (the draft KV cache holds the injected context).
+
+Readings where the pages leave a step open (each is also listed in the design notes):
+  * g = RMSNorm(fc(concat_f h_f)) once; the per-layer input norm is not applied to g.
+  * Per-head RMSNorm on q and k (learned weight over head_dim) before RoPE, switchable
+    with `qk_norm`.
+  * Rotate-half RoPE with inv_freq_i = theta^(-2i/head_dim); context position p is its
+    index in the sequence, block row j (0 = anchor) sits at position ctx_len + j.
+  * In-block attention is bidirectional (no mask); every block query sees the whole
+    injected context.
+  * Block K/V are never written to the cache; after a verify the caller injects the
+    anchor plus the accepted drafts (a + 1 positions).
+  * RMSNorm: y = x / sqrt(mean(x^2) + eps) * w.
+  * Storage rounding ("contract points"): every stored activation is rounded to the
+    storage type (bf16, round-to-nearest-even, or fp32): the fc output, g, every GEMM
+    output (q, k, v, o-proj, gate, up, down, context K/V), normed activations, the
+    residual stream after each add, the SwiGLU product, the attention output and the
+    roped q/k. Logits are not rounded (they stay fp64 here, fp32 on the GPU); argmax
+    and top-k are decided on the logits rounded to fp32, ties to the lowest index.
+  * top-k: k values sorted descending, indices tie-broken by lowest index.
+
+Parity status: every function here is pinned by the CPU tests (brute force, closed
+forms, library routines or exact rational arithmetic) — see tests/test_oracle_pins.py.
+"""
+from fractions import Fraction
+
+import numpy as np
+
+__all__ = [
+    "round_to", "bf16_round", "f32_round", "rmsnorm", "rope", "silu", "softmax",
+    "OracleDraft", "topk_desc", "argmax_lowest", "verify_greedy",
+    "accept_prob", "residual_dist", "sample_index", "verify_sample", "as_fraction_dist",
+]
+
+
+# ----------------------------------------------------------------------------- rounding
+def bf16_round(x):
+    """Round float64 values to the nearest bfloat16 value (ties to even), as float64.
+
+    bfloat16 keeps 8 significant bits (1 implicit + 7 stored) and the float32 exponent
+    range; below 2^-126 the spacing stays 2^-133 (gradual underflow). Written from that
+    definition: scale the significand to 8 bits, round half to even, scale back.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, copy=True)
+    finite = np.isfinite(x) & (x != 0)
+    xf = x[finite]
+    _, e = np.frexp(xf)                 # xf = m * 2^e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)             # bf16 min normal is 2^-126 = 0.5 * 2^-125
+    scale = np.ldexp(1.0, 8 - e)        # 8 significant bits
+    r = np.rint(xf * scale) / scale     # np.rint rounds half to even
+    bf16_max = 3.3895313892515355e38    # (2 - 2^-7) * 2^127
+    out[finite] = np.where(np.abs(r) > bf16_max, np.copysign(np.inf, r), r)
+    return out
+
+
+def f32_round(x):
+    """Round float64 values to the nearest float32 value (IEEE, ties to even)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def round_to(dtype):
+    """The storage rounding used at every contract point for the given storage dtype."""
+    if dtype == "bf16":
+        return bf16_round
+    if dtype == "f32":
+        return f32_round
+    if dtype == "f64":          # no rounding at all (used by the oracle's own pins)
+        return lambda x: np.asarray(x, dtype=np.float64)
+    raise ValueError(dtype)
+
+
+# ----------------------------------------------------------------------------- elementwise
+def rmsnorm(x, w, eps):
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * w."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
+
+
+def rope(x, pos, theta):
+    """Rotate-half rotary embedding of x [..., n, head_dim] at integer positions pos [n].
+
+    For i < head_dim/2 the pair (x_i, x_{i+head_dim/2}) is rotated by the angle
+    pos * theta^(-2i/head_dim).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    hd = x.shape[-1]
+    half = hd // 2
+    inv_freq = theta ** (-(2.0 * np.arange(half)) / hd)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]   # [n, half]
+    c, s = np.cos(ang), np.sin(ang)
+    # broadcast [n, half] against x [n, heads, half] when x has a head axis
+    while c.ndim < x.ndim:
+        c, s = c[:, None, :], s[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def silu(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def softmax(s, axis=-1):
+    s = np.asarray(s, dtype=np.float64)
+    m = np.max(s, axis=axis, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=axis, keepdims=True)
+
+
+# ----------------------------------------------------------------------------- the draft
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+class OracleDraft:
+    """The DFlash draft model and its per-request context cache, in float64.
+
+    `cfg` needs the attributes hidden, n_layers, n_q_heads, n_kv_heads, head_dim,
+    intermediate, vocab, n_feat, target_hidden, block_k, topk, mask_id, qk_norm,
+    rms_eps, rope_theta, input_embedding_scale, dtype. `weights` holds float arrays
+    (float32 or float64) in [out, in] layout: embed, lm_head, fc, fc_norm, final_norm
+    and layers = [dict(in_norm, wq, wk, wv, q_norm, k_norm, wo, post_norm, w_gate, w_up,
+    w_down)]. The cache maps a request id to per-layer lists of context K and V rows.
+    """
+
+    def __init__(self, cfg, weights):
+        self.cfg = cfg
+        self.w = weights
+        self.r = round_to(cfg.dtype)
+        self.cache = {}   # req -> {"K": [L arrays [n, nkv, hd]], "V": [...]}
+
+    # -- context fusion and injection ([P1] Step 2-3, [P2] §2.2, [P3] §四, [P4] §5.1)
+    def fuse(self, feats):
+        """g = RMSNorm(concat_f(h_f) @ W_fc^T) for rows of n_feat hidden-state arrays."""
+        c, r = self.cfg, self.r
+        cat = np.concatenate([_f64(f) for f in feats], axis=1)           # [n, n_feat*H_t]
+        fc_out = r(cat @ _f64(self.w["fc"]).T)                          # [n, H]
+        return r(rmsnorm(fc_out, self.w["fc_norm"], c.rms_eps))
+
+    def project_kv(self, g, pos, layer):
+        """Context K/V of one draft layer for fused rows g at positions pos."""
+        c, r, lw = self.cfg, self.r, self.w["layers"][layer]
+        n = g.shape[0]
+        k = r(g @ _f64(lw["wk"]).T).reshape(n, c.n_kv_heads, c.head_dim)
+        v = r(g @ _f64(lw["wv"]).T).reshape(n, c.n_kv_heads, c.head_dim)
+        if c.qk_norm:
+            k = rmsnorm(k, lw["k_norm"], c.rms_eps)
+        k = r(rope(k, pos, c.rope_theta))
+        return k, v
+
+    def inject(self, req, feats, reset=False):
+        """Append the K/V of newly accepted positions (rows of feats) to req's cache."""
+        c = self.cfg
+        if reset or req not in self.cache:
+            self.cache[req] = {"K": [np.zeros((0, c.n_kv_heads, c.head_dim))] * c.n_layers,
+                               "V": [np.zeros((0, c.n_kv_heads, c.head_dim))] * c.n_layers}
+        ent = self.cache[req]
+        n = feats[0].shape[0]
+        if n == 0:
+            return
+        start = ent["K"][0].shape[0]
+        pos = np.arange(start, start + n)
+        g = self.fuse(feats)
+        for l in range(c.n_layers):
+            k, v = self.project_kv(g, pos, l)
+            ent["K"][l] = np.concatenate([ent["K"][l], k], axis=0)
+            ent["V"][l] = np.concatenate([ent["V"][l], v], axis=0)
+
+    def context_len(self, req):
+        return self.cache[req]["K"][0].shape[0]
+
+    def truncate(self, req, n):
+        ent = self.cache[req]
+        ent["K"] = [k[:n] for k in ent["K"]]
+        ent["V"] = [v[:n] for v in ent["V"]]
+
+    # -- the query block forward ([P2] §2.1-2.2, [P4] §4-4.4 and §5.3, [P1] Step 3)
+    def block_tokens(self, anchor):
+        """[anchor, mask x K] — the anchor is the last verified token."""
+        return [int(anchor)] + [self.cfg.mask_id] * self.cfg.block_k
+
+    def layer(self, x, l, ctx_k, ctx_v, pos):
+        """One pre-norm decoder layer over the block rows x [K+1, H]."""
+        c, r, lw = self.cfg, self.r, self.w["layers"][l]
+        nq, nkv, hd = c.n_q_heads, c.n_kv_heads, c.head_dim
+        q_rows = x.shape[0]
+        xn = r(rmsnorm(x, lw["in_norm"], c.rms_eps))
+        q = r(xn @ _f64(lw["wq"]).T).reshape(q_rows, nq, hd)
+        k = r(xn @ _f64(lw["wk"]).T).reshape(q_rows, nkv, hd)
+        v = r(xn @ _f64(lw["wv"]).T).reshape(q_rows, nkv, hd)
+        if c.qk_norm:
+            q = rmsnorm(q, lw["q_norm"], c.rms_eps)
+            k = rmsnorm(k, lw["k_norm"], c.rms_eps)
+        q = r(rope(q, pos, c.rope_theta))
+        k = r(rope(k, pos, c.rope_theta))
+        # context K/V first, then the block's own K/V; no mask inside the block
+        keys = np.concatenate([ctx_k, k], axis=0)         # [n_ctx + K + 1, nkv, hd]
+        vals = np.concatenate([ctx_v, v], axis=0)
+        group = nq // nkv
+        o = np.empty((q_rows, nq, hd))
+        for h in range(nq):
+            kvh = h // group
+            s = (q[:, h, :] @ keys[:, kvh, :].T) / np.sqrt(hd)   # [K+1, n_keys]
+            o[:, h, :] = softmax(s, axis=-1) @ vals[:, kvh, :]
+        o = r(o.reshape(q_rows, nq * hd))
+        x = r(x + r(o @ _f64(lw["wo"]).T))
+        xn2 = r(rmsnorm(x, lw["post_norm"], c.rms_eps))
+        gate = r(xn2 @ _f64(lw["w_gate"]).T)
+        up = r(xn2 @ _f64(lw["w_up"]).T)
+        hmid = r(silu(gate) * up)
+        x = r(x + r(hmid @ _f64(lw["w_down"]).T))
+        return x
+
+    def hidden(self, req, anchor):
+        """Final-normed hidden rows of the K mask positions, [K, H]."""
+        c, r = self.cfg, self.r
+        ent = self.cache[req]
+        n_ctx = ent["K"][0].shape[0]
+        toks = self.block_tokens(anchor)
+        x = r(_f64(self.w["embed"][toks]) * c.input_embedding_scale)
+        pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
+        for l in range(c.n_layers):
+            x = self.layer(x, l, ent["K"][l], ent["V"][l], pos)
+        # the anchor row yields no candidate ([P4] §4.3): only the K mask rows go on
+        return r(rmsnorm(x[1:], self.w["final_norm"], c.rms_eps))
+
+    def logits(self, req, anchor, chunk=16384):
+        """fp64 logits [K, V] of the K mask positions (LM head in vocabulary chunks)."""
+        h = self.hidden(req, anchor)
+        lm = self.w["lm_head"]
+        V = lm.shape[0]
+        out = np.empty((h.shape[0], V))
+        for v0 in range(0, V, chunk):
+            out[:, v0:v0 + chunk] = h @ _f64(lm[v0:v0 + chunk]).T
+        return out
+
+    def draft(self, req, anchor):
+        """(argmax [K], topk_idx [K, k], topk_val [K, k], logits [K, V]) for one request."""
+        lg = self.logits(req, anchor)
+        lg32 = f32_round(lg)
+        idx, val = topk_desc(lg32, self.cfg.topk)
+        return argmax_lowest(lg32), idx, val, lg
+
+
+# ----------------------------------------------------------------------------- selection
+def argmax_lowest(x):
+    """Row-wise argmax; among equal maxima the lowest index wins."""
+    x = np.asarray(x)
+    return np.argmax(x, axis=-1)   # numpy returns the first occurrence
+
+
+def topk_desc(x, k):
+    """Row-wise top-k: values descending, equal values ordered by lowest index."""
+    x = np.asarray(x, dtype=np.float64)
+    # stable sort on (-value) keeps lower indices first among equal values
+    order = np.argsort(-x, axis=-1, kind="stable")[..., :k]
+    return order, np.take_along_axis(x, order, axis=-1)
+
+
+# ----------------------------------------------------------------------------- verification
+def verify_greedy(draft, target):
+    """Greedy verification of one block per request ([P2] §2.3, [P1] 核心推理伪代码).
+
+    draft [B, K]: the draft's tokens for the K mask positions. target [B, K+1]: the
+    target's greedy token after the anchor and after each draft token. The accepted
+    count a is the number of leading positions with draft == target; the round emits
+    draft[:a] followed by target[a] (a correction, or the bonus when a == K), so at most
+    K+1 tokens ([P4] §2). Returns (accept_len [B], out_tokens [B, K+1] padded with -1,
+    next_anchor [B]).
+    """
+    draft = np.asarray(draft)
+    target = np.asarray(target)
+    B, K = draft.shape
+    acc = np.zeros(B, dtype=np.int32)
+    out = np.full((B, K + 1), -1, dtype=np.int32)
+    nxt = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        a = 0
+        while a < K and draft[b, a] == target[b, a]:
+            a += 1
+        acc[b] = a
+        out[b, :a] = draft[b, :a]
+        out[b, a] = target[b, a]
+        nxt[b] = target[b, a]
+    return acc, out, nxt
+
+
+def accept_prob(p, q, d):
+    """Probability of accepting draft token d: min(1, p[d] / q[d]) ([P2] §2.3)."""
+    return min(1, p[d] / q[d])
+
+
+def residual_dist(p, q):
+    """norm(max(p - q, 0)); falls back to p when nothing is left ([P2] §2.3, §4.2).
+
+    Works on any number type (floats or fractions.Fraction) given as sequences.
+    """
+    res = [max(pi - qi, 0) for pi, qi in zip(p, q)]
+    total = sum(res)
+    if total <= 0:
+        return list(p)
+    return [x / total for x in res]
+
+
+def sample_index(dist, u):
+    """Inverse-CDF draw: smallest i with cumsum(dist)[:i+1] > u * sum(dist)."""
+    total = sum(dist)
+    acc = 0
+    for i, pi in enumerate(dist):
+        acc += pi
+        if acc > u * total:
+            return i
+    return len(dist) - 1
+
+
+def verify_sample(p_rows, q_rows, draft, u_accept, u_resample):
+    """Rejection-sampling verification of one block ([P2] §2.3, §4.2).
+
+    p_rows [K+1][V]: the target's distribution at each block position given the anchor
+    and the drafts before it; q_rows [K][V]: the draft's distribution per mask position;
+    draft [K]: the drafted tokens; u_accept [K], u_resample: uniforms in [0, 1).
+    Position j accepts draft[j] when u_accept[j] < min(1, p/q). On the first rejection
+    the token is drawn from the residual norm(max(p_j - q_j, 0)) (p_j when that vanishes)
+    and the round ends; when all K are accepted a bonus is drawn from p_K.
+    Returns (accepted count a, emitted tokens, a + 1 of them).
+    """
+    K = len(draft)
+    out = []
+    for j in range(K):
+        d = int(draft[j])
+        if u_accept[j] < accept_prob(p_rows[j], q_rows[j], d):
+            out.append(d)
+            continue
+        out.append(sample_index(residual_dist(p_rows[j], q_rows[j]), u_resample))
+        return j, out
+    out.append(sample_index(list(p_rows[K]), u_resample))
+    return K, out
+
+
+def as_fraction_dist(values):
+    """Helper for exact tests: normalise a sequence of positive ints to Fractions."""
+    total = sum(values)
+    return [Fraction(v, total) for v in values]

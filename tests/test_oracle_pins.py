@@ -1,0 +1,462 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test fixes one part of the oracle by brute force, a closed form, an independent
+library routine, an invariant the pages state, or exact rational arithmetic, chosen
+so that a plausible slip (dropped term, wrong sign, wrong index, transposed operand)
+fails at least one of them.
+"""
+import itertools
+import json
+import os
+import types
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _cfg(**kw):
+    base = dict(hidden=64, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=16,
+                intermediate=96, vocab=300, n_feat=3, target_hidden=32, block_k=5,
+                topk=8, mask_id=299, qk_norm=1, rms_eps=1e-6, rope_theta=1e4,
+                input_embedding_scale=1.0, dtype="f64")
+    base.update(kw)
+    return types.SimpleNamespace(**base)
+
+
+def _weights(c, seed=0, norm_std=0.1):
+    rng = np.random.default_rng(seed)
+    n = lambda *s: rng.normal(0, 0.02, s)
+    nw = lambda *s: 1.0 + rng.normal(0, norm_std, s)
+    w = dict(embed=n(c.vocab, c.hidden) * 20, lm_head=n(c.vocab, c.hidden),
+             fc=n(c.hidden, c.n_feat * c.target_hidden) * 5, fc_norm=nw(c.hidden),
+             final_norm=nw(c.hidden), layers=[])
+    q, kv = c.n_q_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    for _ in range(c.n_layers):
+        w["layers"].append(dict(
+            in_norm=nw(c.hidden), wq=n(q, c.hidden) * 10, wk=n(kv, c.hidden) * 10,
+            wv=n(kv, c.hidden) * 10, q_norm=nw(c.head_dim), k_norm=nw(c.head_dim),
+            wo=n(c.hidden, q) * 5, post_norm=nw(c.hidden), w_gate=n(c.intermediate, c.hidden) * 5,
+            w_up=n(c.intermediate, c.hidden) * 5, w_down=n(c.hidden, c.intermediate) * 5))
+    return w
+
+
+def _feats(c, n, seed):
+    rng = np.random.default_rng(seed)
+    return [rng.normal(0, 1, (n, c.target_hidden)) for _ in range(c.n_feat)]
+
+
+# ----------------------------------------------------------------------------- rounding
+def test_bf16_round_matches_torch_conversion():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.normal(0, 1, 20000), rng.normal(0, 1e-3, 2000), rng.normal(0, 1e30, 2000),
+        rng.uniform(-1, 1, 2000) * 2.0 ** -130,          # bf16 subnormal range
+    ]).astype(np.float32)
+    # exact ties: 1 + 2^-8 style values with odd and even neighbours
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(2 + 2 ** -7), 3 * 2 ** -9 + 2 ** -1], np.float32)
+    x = np.concatenate([x, ties])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_round(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_round_ties_to_even_by_hand():
+    assert O.bf16_round(np.array([1 + 2 ** -8]))[0] == 1.0                # even neighbour is 1.0
+    assert O.bf16_round(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6    # even neighbour above
+    assert O.bf16_round(np.array([1 + 2 ** -8 + 2 ** -30]))[0] == 1 + 2 ** -7  # past the tie
+    assert np.isinf(O.bf16_round(np.array([3.5e38]))[0])
+
+
+def test_f32_round_is_ieee_single():
+    x = np.array([1 + 2 ** -24, 1 + 3 * 2 ** -24, 0.1])
+    np.testing.assert_array_equal(O.f32_round(x), x.astype(np.float32).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------- elementwise
+def test_rmsnorm_matches_torch():
+    rng = np.random.default_rng(2)
+    x, w = rng.normal(0, 3, (7, 48)), rng.normal(1, 0.2, 48)
+    want = F.rms_norm(torch.from_numpy(x), (48,), torch.from_numpy(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rmsnorm(x, w, 1e-6), want, rtol=1e-13, atol=1e-13)
+
+
+def test_silu_softmax_match_torch():
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 4, (5, 33))
+    np.testing.assert_allclose(O.silu(x), F.silu(torch.from_numpy(x)).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(O.softmax(x), torch.softmax(torch.from_numpy(x), -1).numpy(),
+                               rtol=1e-13, atol=1e-15)
+
+
+def test_rope_closed_forms():
+    hd, theta = 16, 1e6
+    half = hd // 2
+    # position 0 is the identity
+    x = np.random.default_rng(4).normal(size=(3, 2, hd))
+    np.testing.assert_allclose(O.rope(x, np.zeros(3), theta), x, atol=0)
+    # pairs are (i, i + hd/2): e_0 at position p -> cos p at 0, sin p at hd/2 (frequency 1)
+    e0 = np.zeros((1, hd)); e0[0, 0] = 1.0
+    r = O.rope(e0, np.array([3]), theta)
+    want = np.zeros(hd); want[0] = np.cos(3); want[half] = np.sin(3)
+    np.testing.assert_allclose(r[0], want, atol=1e-15)
+    # second pair rotates with frequency theta^(-2/hd); x2 maps with the opposite sign
+    e1 = np.zeros((1, hd)); e1[0, half + 1] = 1.0
+    ang = 5 * theta ** (-2.0 / hd)
+    r = O.rope(e1, np.array([5]), theta)
+    want = np.zeros(hd); want[1] = -np.sin(ang); want[half + 1] = np.cos(ang)
+    np.testing.assert_allclose(r[0], want, atol=1e-15)
+
+
+def test_rope_composition_and_relative_position():
+    rng = np.random.default_rng(5)
+    hd, theta = 32, 1e6
+    q, k = rng.normal(size=(1, hd)), rng.normal(size=(1, hd))
+    a, b = 1234, 40000
+    np.testing.assert_allclose(O.rope(O.rope(q, [a], theta), [b], theta),
+                               O.rope(q, [a + b], theta), atol=1e-9)
+    d1 = np.dot(O.rope(q, [700], theta)[0], O.rope(k, [650], theta)[0])
+    d2 = np.dot(O.rope(q, [30050], theta)[0], O.rope(k, [30000], theta)[0])
+    assert abs(d1 - d2) < 1e-9
+    # rotation keeps the norm
+    assert abs(np.linalg.norm(O.rope(q, [99], theta)) - np.linalg.norm(q)) < 1e-12
+
+
+# ----------------------------------------------------------------------------- context fusion
+def test_fc_concat_order_block_decomposition():
+    c = _cfg()
+    w = _weights(c)
+    od = O.OracleDraft(c, w)
+    fe = _feats(c, 6, 7)
+    acc = sum(fe[f] @ w["fc"][:, f * c.target_hidden:(f + 1) * c.target_hidden].T
+              for f in range(c.n_feat))
+    want = O.rmsnorm(acc, w["fc_norm"], c.rms_eps)
+    np.testing.assert_allclose(od.fuse(fe), want, rtol=1e-12, atol=1e-12)
+    # the norm really is applied: with unit weights every fused row has RMS 1
+    w2 = dict(w, fc_norm=np.ones(c.hidden))
+    g = O.OracleDraft(c, w2).fuse(fe)
+    np.testing.assert_allclose(np.sqrt(np.mean(g * g, -1)), 1.0, rtol=1e-6)
+
+
+def test_fc_shape_chain_golden():
+    gold = json.load(open(os.path.join(GOLDEN, "fc_shape_chain.json")))
+    c = _cfg(hidden=gold["fused_width"], n_feat=gold["n_feat"], target_hidden=gold["target_hidden"])
+    rng = np.random.default_rng(0)
+    w = dict(fc=rng.normal(0, 0.02, (c.hidden, c.n_feat * c.target_hidden)).astype(np.float32),
+             fc_norm=np.ones(c.hidden))
+    fe = [rng.normal(size=(gold["tokens"], c.target_hidden)) for _ in range(c.n_feat)]
+    assert np.concatenate(fe, 1).shape == (gold["tokens"], gold["concat_width"])
+    g = O.OracleDraft(c, w).fuse(fe)
+    assert g.shape == (gold["tokens"], gold["fused_width"])
+
+
+# ----------------------------------------------------------------------------- layer vs library
+def _torch_layer(c, lw, x, ctx_k, ctx_v, pos):
+    """Independent composition of the decoder layer from torch fp64 library routines."""
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    n = x.shape[0]
+    X = t(x)
+    xn = F.rms_norm(X, (c.hidden,), t(lw["in_norm"]), eps=c.rms_eps)
+    q = F.linear(xn, t(lw["wq"])).view(n, c.n_q_heads, c.head_dim)
+    k = F.linear(xn, t(lw["wk"])).view(n, c.n_kv_heads, c.head_dim)
+    v = F.linear(xn, t(lw["wv"])).view(n, c.n_kv_heads, c.head_dim)
+    q = F.rms_norm(q, (c.head_dim,), t(lw["q_norm"]), eps=c.rms_eps)
+    k = F.rms_norm(k, (c.head_dim,), t(lw["k_norm"]), eps=c.rms_eps)
+    q = t(O.rope(q.numpy(), pos, c.rope_theta))          # rope is pinned on its own
+    k = t(O.rope(k.numpy(), pos, c.rope_theta))
+    keys = torch.cat([t(ctx_k), k], 0).transpose(0, 1)    # [nkv, S, hd]
+    vals = torch.cat([t(ctx_v), v], 0).transpose(0, 1)
+    o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], keys[None], vals[None],
+                                       enable_gqa=True)[0]           # no mask: bidirectional
+    o = o.transpose(0, 1).reshape(n, -1)
+    X = X + F.linear(o, t(lw["wo"]))
+    xn2 = F.rms_norm(X, (c.hidden,), t(lw["post_norm"]), eps=c.rms_eps)
+    h = F.silu(F.linear(xn2, t(lw["w_gate"]))) * F.linear(xn2, t(lw["w_up"]))
+    return (X + F.linear(h, t(lw["w_down"]))).numpy()
+
+
+@pytest.mark.parametrize("nq,nkv", [(4, 2), (4, 4), (6, 2), (4, 1)])
+def test_layer_matches_torch_library_composition(nq, nkv):
+    c = _cfg(n_q_heads=nq, n_kv_heads=nkv)
+    w = _weights(c, seed=nq * 10 + nkv)
+    od = O.OracleDraft(c, w)
+    rng = np.random.default_rng(8)
+    n_ctx = 37
+    x = rng.normal(0, 1, (c.block_k + 1, c.hidden))
+    ck = rng.normal(0, 1, (n_ctx, nkv, c.head_dim))
+    cv = rng.normal(0, 1, (n_ctx, nkv, c.head_dim))
+    pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
+    np.testing.assert_allclose(od.layer(x, 0, ck, cv, pos),
+                               _torch_layer(c, w["layers"][0], x, ck, cv, pos),
+                               rtol=1e-10, atol=1e-11)
+
+
+def test_gqa_head_mapping_equals_duplicated_kv_heads():
+    """nq=4, nkv=2 must equal nq=4, nkv=4 whose kv heads are [h0, h0, h1, h1]."""
+    c2 = _cfg(n_q_heads=4, n_kv_heads=2, n_layers=1)
+    w2 = _weights(c2, seed=11)
+    c4 = _cfg(n_q_heads=4, n_kv_heads=4, n_layers=1)
+    hd = c2.head_dim
+    lw = dict(w2["layers"][0])
+    dup = lambda m: np.concatenate([m[0:hd], m[0:hd], m[hd:2 * hd], m[hd:2 * hd]], 0)
+    lw4 = dict(lw, wk=dup(lw["wk"]), wv=dup(lw["wv"]))
+    w4 = dict(w2, layers=[lw4])
+    rng = np.random.default_rng(12)
+    x = rng.normal(0, 1, (c2.block_k + 1, c2.hidden))
+    ck = rng.normal(0, 1, (9, 2, hd)); cv = rng.normal(0, 1, (9, 2, hd))
+    ck4 = ck[:, [0, 0, 1, 1]]; cv4 = cv[:, [0, 0, 1, 1]]
+    pos = np.arange(9, 9 + c2.block_k + 1)
+    a = O.OracleDraft(c2, w2).layer(x, 0, ck, cv, pos)
+    b = O.OracleDraft(c4, w4).layer(x, 0, ck4, cv4, pos)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+def test_in_block_attention_is_bidirectional_and_context_is_a_set():
+    c = _cfg(n_layers=1)
+    w = _weights(c, seed=13)
+    od = O.OracleDraft(c, w)
+    rng = np.random.default_rng(14)
+    x = rng.normal(0, 1, (c.block_k + 1, c.hidden))
+    ck = rng.normal(0, 1, (20, c.n_kv_heads, c.head_dim))
+    cv = rng.normal(0, 1, (20, c.n_kv_heads, c.head_dim))
+    pos = np.arange(20, 20 + c.block_k + 1)
+    base = od.layer(x, 0, ck, cv, pos)
+    x2 = x.copy(); x2[-1] += 1.0                    # change the last mask row only
+    assert np.max(np.abs(od.layer(x2, 0, ck, cv, pos)[0] - base[0])) > 1e-6   # anchor sees it
+    perm = rng.permutation(20)                      # context K/V order does not matter
+    np.testing.assert_allclose(od.layer(x, 0, ck[perm], cv[perm], pos), base, rtol=1e-12, atol=1e-13)
+
+
+def test_injected_kv_equal_inline_prepended_rows():
+    """Context K/V injected from g equal the K/V the layer computes for g rows placed in
+    front of the block ([P1] Step 3: g goes through the same K/V projection and is prepended).
+
+    With unit input-norm weights, eps = 0 and fc_norm = 1, rmsnorm(g) == g, so feeding the g
+    rows through the layer's own input path reproduces exactly the injected projection.
+    """
+    for qk in (0, 1):
+        c = _cfg(n_layers=1, rms_eps=0.0, qk_norm=qk)
+        w = _weights(c, seed=15)
+        w["fc_norm"] = np.ones(c.hidden)
+        w["layers"][0]["in_norm"] = np.ones(c.hidden)
+        od = O.OracleDraft(c, w)
+        n = 11
+        g = od.fuse(_feats(c, n, 16))
+        kc, vc = od.project_kv(g, np.arange(n), 0)
+        rng = np.random.default_rng(17)
+        xb = rng.normal(0, 1, (c.block_k + 1, c.hidden))
+        pos_b = np.arange(n, n + c.block_k + 1)
+        injected = od.layer(xb, 0, kc, vc, pos_b)
+        empty = np.zeros((0, c.n_kv_heads, c.head_dim))
+        inline = od.layer(np.concatenate([g, xb]), 0, empty, empty, np.arange(n + c.block_k + 1))[n:]
+        np.testing.assert_allclose(injected, inline, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- request-level invariants
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_incremental_injection_equals_one_shot(dtype):
+    c = _cfg(dtype=dtype)
+    w = _weights(c, seed=18)
+    rng = np.random.default_rng(19)
+    n = 70
+    fe = _feats(c, n, 20)
+    one = O.OracleDraft(c, w); one.inject(0, fe)
+    inc = O.OracleDraft(c, w)
+    s = 0
+    while s < n:
+        m = min(int(rng.integers(1, 17)), n - s)
+        inc.inject(0, [f[s:s + m] for f in fe])
+        s += m
+    for l in range(c.n_layers):
+        np.testing.assert_array_equal(one.cache[0]["K"][l], inc.cache[0]["K"][l])
+        np.testing.assert_array_equal(one.cache[0]["V"][l], inc.cache[0]["V"][l])
+    np.testing.assert_array_equal(one.logits(0, 5), inc.logits(0, 5))
+
+
+def test_anchor_gives_no_candidate_and_k_candidates_per_request():
+    gold = json.load(open(os.path.join(GOLDEN, "block_layout.json")))
+    for case in gold["cases"]:
+        c = _cfg(block_k=case["K"], n_layers=1)
+        w = _weights(c, seed=21)
+        od = O.OracleDraft(c, w)
+        od.inject(0, _feats(c, 8, 22))
+        assert len(od.block_tokens(3)) == case["queries"]
+        am, idx, val, lg = od.draft(0, 3)
+        assert lg.shape == (case["candidates"], c.vocab)
+        assert am.shape == (case["candidates"],)
+        assert idx.shape == (case["candidates"], c.topk)
+
+
+def test_mask_rows_depend_on_the_anchor_and_context():
+    c = _cfg()
+    w = _weights(c, seed=23)
+    od = O.OracleDraft(c, w)
+    od.inject(0, _feats(c, 12, 24))
+    a = od.logits(0, 3)
+    assert np.max(np.abs(a - od.logits(0, 4))) > 1e-6       # anchor token matters
+    od.inject(0, _feats(c, 1, 25))
+    assert np.max(np.abs(a - od.logits(0, 3))) > 1e-6       # one more context position matters
+
+
+def test_requests_are_independent():
+    c = _cfg(dtype="bf16")
+    w = _weights(c, seed=26)
+    solo = O.OracleDraft(c, w); solo.inject(7, _feats(c, 30, 27))
+    mixed = O.OracleDraft(c, w)
+    mixed.inject(3, _feats(c, 50, 28)); mixed.inject(7, _feats(c, 30, 27)); mixed.inject(9, _feats(c, 5, 29))
+    np.testing.assert_array_equal(solo.logits(7, 11), mixed.logits(7, 11))
+
+
+# ----------------------------------------------------------------------------- selection
+def test_topk_and_argmax_brute_force_with_ties():
+    rng = np.random.default_rng(30)
+    for trial in range(200):
+        n = int(rng.integers(1, 40))
+        k = int(rng.integers(1, n + 1))
+        x = rng.integers(-3, 4, n).astype(np.float64)      # many exact ties
+        want = sorted(range(n), key=lambda i: (-x[i], i))[:k]
+        idx, val = O.topk_desc(x[None], k)
+        assert list(idx[0]) == want
+        assert list(val[0]) == [x[i] for i in want]
+        assert O.argmax_lowest(x[None])[0] == want[0]
+
+
+# ----------------------------------------------------------------------------- greedy verify
+def test_greedy_verify_brute_force_against_prefix_formula():
+    """All (draft, target) pairs with V=3, K<=3 against the cumprod formula of [P2] §2.3."""
+    V = 3
+    for K in range(1, 4):
+        drafts = np.array(list(itertools.product(range(V), repeat=K)))
+        targets = np.array(list(itertools.product(range(V), repeat=K + 1)))
+        D = np.repeat(drafts, len(targets), 0)
+        T = np.tile(targets, (len(drafts), 1))
+        acc, out, nxt = O.verify_greedy(D, T)
+        a_formula = np.cumprod(D == T[:, :-1], axis=1).sum(axis=1)
+        np.testing.assert_array_equal(acc, a_formula)
+        assert np.all(acc <= K)
+        for i in range(len(D)):
+            a = acc[i]
+            emitted = out[i][out[i] >= 0]
+            assert len(emitted) == a + 1 <= K + 1
+            np.testing.assert_array_equal(emitted[:a], D[i, :a])
+            assert emitted[a] == T[i, a] == nxt[i]
+
+
+def test_greedy_verify_worked_example_golden():
+    gold = json.load(open(os.path.join(GOLDEN, "verify_worked_example.json")))
+    vocab = gold["vocab"]
+    d = np.array([[vocab[t] for t in gold["draft"]]])
+    t = np.array([[vocab[t] for t in gold["target"]]])
+    acc, out, nxt = O.verify_greedy(d, t)
+    assert acc[0] == gold["expected_accept_len"]
+    assert list(out[0][out[0] >= 0]) == [vocab[t] for t in gold["expected_emitted"]]
+    assert nxt[0] == vocab[gold["expected_next_anchor"]]
+
+
+# ----------------------------------------------------------------------------- rejection sampling
+def _rand_dist(rng, V, zeros=False):
+    v = [int(x) for x in rng.integers(1, 9, V)]
+    if zeros:
+        v[int(rng.integers(0, V))] = 0
+    return O.as_fraction_dist(v)
+
+
+def _exact_output_distribution(p_of, q_rows, V, K):
+    """Exact law of the emitted tokens, completed by the target to K+1 tokens."""
+    out = {}
+
+    def complete(seq, prob):
+        if len(seq) == K + 1:
+            out[tuple(seq)] = out.get(tuple(seq), 0) + prob
+            return
+        p = p_of(tuple(seq))
+        for t in range(V):
+            if p[t]:
+                complete(seq + [t], prob * p[t])
+
+    for d in itertools.product(range(V), repeat=K):
+        pd = Fraction(1)
+        for j in range(K):
+            pd *= q_rows[j][d[j]]
+        if pd == 0:
+            continue
+        prefix, prob = [], pd
+        for j in range(K):
+            p = p_of(tuple(prefix))
+            a = O.accept_prob(p, q_rows[j], d[j])
+            if a < 1:                                   # rejection branch
+                res = O.residual_dist(p, q_rows[j])
+                for t in range(V):
+                    if res[t]:
+                        complete(prefix + [t], prob * (1 - a) * res[t])
+            prob *= a
+            if prob == 0:
+                break
+            prefix = prefix + [d[j]]
+        else:
+            p = p_of(tuple(prefix))                     # all accepted: bonus from p_K
+            for t in range(V):
+                if p[t]:
+                    complete(prefix + [t], prob * p[t])
+    return out
+
+
+@pytest.mark.parametrize("V,K,seed", [(3, 1, 0), (3, 2, 1), (4, 2, 2), (4, 2, 3), (2, 3, 4)])
+def test_rejection_sampling_reproduces_target_exactly(V, K, seed):
+    rng = np.random.default_rng(100 + seed)
+    table = {}
+
+    def p_of(prefix):
+        if prefix not in table:
+            table[prefix] = _rand_dist(rng, V, zeros=(len(prefix) % 2 == 1))
+        return table[prefix]
+
+    q_rows = [_rand_dist(rng, V, zeros=(j == 0)) for j in range(K)]
+    got = _exact_output_distribution(p_of, q_rows, V, K)
+    for seq in itertools.product(range(V), repeat=K + 1):
+        want = Fraction(1)
+        for i in range(K + 1):
+            want *= p_of(tuple(seq[:i]))[seq[i]]
+        assert got.get(seq, 0) == want, (seq, got.get(seq, 0), want)
+
+
+def test_residual_falls_back_to_target_when_nothing_is_left():
+    p = O.as_fraction_dist([1, 2, 3])
+    assert O.residual_dist(p, p) == p
+    q = O.as_fraction_dist([3, 2, 1])
+    r = O.residual_dist(p, q)
+    assert r == [0, 0, 1]
+
+
+def test_verify_sample_monte_carlo_matches_exact_law():
+    V, K = 3, 2
+    rng = np.random.default_rng(7)
+    table = {}
+
+    def p_of(prefix):
+        if prefix not in table:
+            table[prefix] = _rand_dist(rng, V)
+        return table[prefix]
+
+    q_rows = [_rand_dist(rng, V) for _ in range(K)]
+    first_exact = p_of(())
+    n = 20000
+    counts = np.zeros(V)
+    mc = np.random.default_rng(8)
+    for _ in range(n):
+        d = [int(mc.choice(V, p=[float(x) for x in q_rows[j]])) for j in range(K)]
+        p_rows = [p_of(tuple(d[:j])) for j in range(K + 1)]
+        p_rows = [[float(x) for x in r] for r in p_rows]
+        a, toks = O.verify_sample(p_rows, [[float(x) for x in r] for r in q_rows], d,
+                                  mc.random(K), mc.random())
+        assert 1 <= len(toks) == a + 1 <= K + 1
+        counts[toks[0]] += 1
+    # the first emitted token follows p(. | prefix) exactly; 5 sigma tolerance
+    f = np.array([float(x) for x in first_exact])
+    assert np.all(np.abs(counts / n - f) < 5 * np.sqrt(f * (1 - f) / n) + 1e-3)
