@@ -1,0 +1,229 @@
+"""DFlash batched draft step on one GB300: Python binding of libdflash (include/dflash.h).
+
+The binding only marshals arguments: torch provides device memory and streams, every
+step of the path runs in the library's CUDA kernels. If libdflash.so is missing the
+import of the library raises; there is no fallback implementation.
+
+Functions with the C names take torch tensors (device buffers) and Python ints:
+
+    ctx = dflash_create(cfg, weights, limits)                 # -> Context
+    dflash_inject_context(ctx, req_ids, n_new, feats, reset=False)
+    dflash_draft_step(ctx, req_ids, anchors, argmax, topk_idx=None, topk_val=None, logits=None)
+    dflash_verify_greedy(ctx, draft, target, accept_len, out_tokens, next_anchor)
+    dflash_release / dflash_truncate / dflash_context_len / dflash_export_kv / dflash_destroy
+
+`Context` wraps the same calls as methods and allocates outputs when asked to.
+"""
+import ctypes
+
+import torch
+
+from . import _ffi
+
+__all__ = ["DFlashError", "Context", "Limits", "dflash_create", "dflash_destroy",
+           "dflash_inject_context", "dflash_draft_step", "dflash_verify_greedy",
+           "dflash_release", "dflash_truncate", "dflash_context_len", "dflash_export_kv",
+           "dflash_validate_config", "make_config", "library"]
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status, message=""):
+        self.status = status
+        super().__init__(f"{_ffi.STATUS.get(status, status)}: {message}")
+
+
+def library():
+    return _ffi.load()
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _i32_array(vals):
+    vals = [int(v) for v in vals]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+class Limits:
+    """Context capacity: batch, live requests, pages, positions, injection chunk rows."""
+
+    def __init__(self, max_batch=1, max_requests=None, max_pages=1024, max_positions=4096,
+                 max_inject_rows=4096):
+        self.max_batch = max_batch
+        self.max_requests = max_requests if max_requests is not None else max_batch
+        self.max_pages = max_pages
+        self.max_positions = max_positions
+        self.max_inject_rows = max_inject_rows
+
+
+def make_config(cfg, limits: Limits):
+    """A dflash_config from a draft shape (any object with the DraftConfig attributes)."""
+    return _ffi.Config(
+        hidden=cfg.hidden, n_layers=cfg.n_layers, n_q_heads=cfg.n_q_heads,
+        n_kv_heads=cfg.n_kv_heads, head_dim=cfg.head_dim, intermediate=cfg.intermediate,
+        vocab=cfg.vocab, n_feat=cfg.n_feat, target_hidden=cfg.target_hidden,
+        block_k=cfg.block_k, topk=cfg.topk, mask_token_id=cfg.mask_id, qk_norm=cfg.qk_norm,
+        max_batch=limits.max_batch, max_requests=limits.max_requests,
+        max_pages=limits.max_pages, page_size=64, max_positions=limits.max_positions,
+        max_inject_rows=limits.max_inject_rows, rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta,
+        input_embedding_scale=cfg.input_embedding_scale,
+        dtype=_ffi.BF16 if cfg.dtype == "bf16" else _ffi.F32)
+
+
+def dflash_validate_config(cfg, limits: Limits):
+    lib = library()
+    c = make_config(cfg, limits)
+    buf = ctypes.create_string_buffer(256)
+    st = lib.dflash_validate_config(ctypes.byref(c), buf, 256)
+    return st, buf.value.decode()
+
+
+class Context:
+    """Owns one dflash_ctx. Weights are torch CUDA tensors kept alive by this object."""
+
+    def __init__(self, cfg, weights, limits: Limits, device=0):
+        self.lib = library()
+        self.cfg = cfg
+        self.limits = limits
+        self._weights = weights
+        self._c = make_config(cfg, limits)
+        layers = (_ffi.LayerWeights * cfg.n_layers)()
+        for i, lw in enumerate(weights["layers"]):
+            for k in _ffi.LayerWeights._fields_:
+                name = k[0]
+                setattr(layers[i], name, lw[name].data_ptr() if lw.get(name) is not None else None)
+        self._layers = layers
+        self._w = _ffi.Weights(embed=weights["embed"].data_ptr(), lm_head=weights["lm_head"].data_ptr(),
+                               fc=weights["fc"].data_ptr(), fc_norm=weights["fc_norm"].data_ptr(),
+                               final_norm=weights["final_norm"].data_ptr(),
+                               layers=ctypes.cast(layers, ctypes.POINTER(_ffi.LayerWeights)))
+        h = ctypes.c_void_p()
+        st = self.lib.dflash_create(ctypes.byref(self._c), ctypes.byref(self._w), device, ctypes.byref(h))
+        if st != _ffi.OK:
+            raise DFlashError(st, "dflash_create failed")
+        self.h = h
+        self.device = device
+
+    # -- helpers
+    def _check(self, st):
+        if st != _ffi.OK:
+            raise DFlashError(st, self.lib.dflash_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- calls
+    def inject(self, req_ids, n_new, feats, reset=False, stream=None):
+        n = len(req_ids)
+        arr = (ctypes.c_void_p * len(feats))(*[f.data_ptr() for f in feats]) if feats else None
+        st = self.lib.dflash_inject_context(self.h, _stream_ptr(stream), n, _i32_array(req_ids),
+                                            _i32_array(n_new), 1 if reset else 0, arr)
+        self._check(st)
+
+    def draft(self, req_ids, anchors, argmax=None, topk_idx=None, topk_val=None, logits=None,
+              want_topk=True, want_logits=False, stream=None):
+        B, K, k, V = len(req_ids), self.cfg.block_k, self.cfg.topk, self.cfg.vocab
+        dev = anchors.device
+        if argmax is None:
+            argmax = torch.empty((B, K), dtype=torch.int32, device=dev)
+        if want_topk and topk_idx is None:
+            topk_idx = torch.empty((B, K, k), dtype=torch.int32, device=dev)
+            topk_val = torch.empty((B, K, k), dtype=torch.float32, device=dev)
+        if want_logits and logits is None:
+            logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+        st = self.lib.dflash_draft_step(self.h, _stream_ptr(stream), B, _i32_array(req_ids),
+                                        _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
+                                        _ptr(topk_val), _ptr(logits))
+        self._check(st)
+        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits)
+
+    def verify(self, draft, target, accept_len=None, out_tokens=None, next_anchor=None, stream=None):
+        B, K = draft.shape
+        dev = draft.device
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+            out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+            next_anchor = torch.empty((B,), dtype=torch.int32, device=dev)
+        st = self.lib.dflash_verify_greedy(self.h, _stream_ptr(stream), B, _ptr(draft), _ptr(target),
+                                           _ptr(accept_len), _ptr(out_tokens), _ptr(next_anchor))
+        self._check(st)
+        return accept_len, out_tokens, next_anchor
+
+    def release(self, req_id):
+        self._check(self.lib.dflash_release(self.h, int(req_id)))
+
+    def truncate(self, req_id, new_len):
+        self._check(self.lib.dflash_truncate(self.h, int(req_id), int(new_len)))
+
+    def context_len(self, req_id):
+        v = ctypes.c_int32()
+        self._check(self.lib.dflash_context_len(self.h, int(req_id), ctypes.byref(v)))
+        return v.value
+
+    def export_kv(self, req_id, layer, pos0, n, stream=None):
+        dt = torch.bfloat16 if self.cfg.dtype == "bf16" else torch.float32
+        shape = (n, self.cfg.n_kv_heads, self.cfg.head_dim)
+        k = torch.empty(shape, dtype=dt, device=f"cuda:{self.device}")
+        v = torch.empty(shape, dtype=dt, device=f"cuda:{self.device}")
+        self._check(self.lib.dflash_export_kv(self.h, _stream_ptr(stream), int(req_id), int(layer),
+                                              int(pos0), int(n), _ptr(k), _ptr(v)))
+        return k, v
+
+    def free_pages(self):
+        return self.lib.dflash_free_pages(self.h)
+
+    def launch_count(self):
+        return self.lib.dflash_launch_count(self.h)
+
+
+# ----------------------------------------------------------------- C-named functions
+def dflash_create(cfg, weights, limits: Limits, device=0):
+    return Context(cfg, weights, limits, device)
+
+
+def dflash_destroy(ctx: Context):
+    ctx.close()
+
+
+def dflash_inject_context(ctx: Context, req_ids, n_new, feats, reset=False, stream=None):
+    ctx.inject(req_ids, n_new, feats, reset=reset, stream=stream)
+
+
+def dflash_draft_step(ctx: Context, req_ids, anchors, argmax, topk_idx=None, topk_val=None,
+                      logits=None, stream=None):
+    return ctx.draft(req_ids, anchors, argmax=argmax, topk_idx=topk_idx, topk_val=topk_val,
+                     logits=logits, want_topk=topk_idx is not None, stream=stream)
+
+
+def dflash_verify_greedy(ctx: Context, draft, target, accept_len, out_tokens, next_anchor, stream=None):
+    return ctx.verify(draft, target, accept_len, out_tokens, next_anchor, stream=stream)
+
+
+def dflash_release(ctx: Context, req_id):
+    ctx.release(req_id)
+
+
+def dflash_truncate(ctx: Context, req_id, new_len):
+    ctx.truncate(req_id, new_len)
+
+
+def dflash_context_len(ctx: Context, req_id):
+    return ctx.context_len(req_id)
+
+
+def dflash_export_kv(ctx: Context, req_id, layer, pos0, n, stream=None):
+    return ctx.export_kv(req_id, layer, pos0, n, stream=stream)

@@ -1,0 +1,649 @@
+// Host side of libdflash: the C ABI, the paged KV pool and its free list, per-request
+// page tables, the per-call device descriptors (staged through pinned memory), and the
+// launch sequence of injection, draft step and verification.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "kernels.h"
+#include "gemm_tc.h"
+
+using namespace dflash;
+
+namespace {
+constexpr int kPage = 64;
+constexpr int kMaxSplit = 16;
+constexpr int kRing = 8;
+
+struct Stage {
+  void *h = nullptr;
+  void *d = nullptr;
+  cudaEvent_t ev = nullptr;
+  bool used = false;
+};
+
+struct Req {
+  int32_t len = 0;
+  std::vector<int32_t> pages;
+};
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+}  // namespace
+
+struct dflash_ctx {
+  dflash_config cfg{};
+  ModelDims m{};
+  int dtype = 0;
+  size_t esz = 4;
+  int device = 0;
+  int num_sms = 0;
+  dflash_weights w{};
+  std::vector<dflash_layer_weights> layers;
+
+  void *pool = nullptr;
+  size_t page_elems = 0;
+  std::vector<int32_t> free_pages;
+  std::unordered_map<int32_t, Req> reqs;
+  int max_pages_per_req = 0;
+  float2 *rope = nullptr;
+
+  // draft scratch
+  void *x = nullptr, *xn = nullptr, *qkv = nullptr, *ao = nullptr, *gu = nullptr,
+       *hmid = nullptr, *xf = nullptr;
+  float *logits = nullptr, *part_o = nullptr, *part_ml = nullptr;
+  // injection scratch
+  void *fc_out = nullptr, *g = nullptr, *kvproj = nullptr;
+
+  std::vector<Stage> ring;
+  size_t stage_cap = 0;
+  int ring_next = 0;
+  int *err_h = nullptr, *err_d = nullptr;
+
+  TcGemm *tc = nullptr;   // tensor-core GEMM plans (bf16 only)
+  std::string last_error;
+  int64_t launches = 0;
+};
+
+// ------------------------------------------------------------------------------ helpers
+static dflash_status set_err(dflash_ctx *c, dflash_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c) c->last_error = buf;
+  return s;
+}
+
+#define CK(ctx, expr)                                                                      \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess)                                                                 \
+      return set_err(ctx, DFLASH_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+namespace {
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) err = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+}  // namespace
+
+static dflash_status check_device_flag(dflash_ctx *c) {
+  if (!c->err_h) return DFLASH_OK;
+  int v = __atomic_exchange_n(c->err_h, 0, __ATOMIC_SEQ_CST);
+  if (v)
+    return set_err(c, DFLASH_ERR_DEVICE, "device-side check failed earlier (code 0x%x:%s%s%s)", v,
+                   (v & DEV_ERR_TOKEN) ? " token id out of range" : "",
+                   (v & DEV_ERR_BOUNDS) ? " index out of bounds" : "",
+                   (v & DEV_ERR_TIMEOUT) ? " bounded wait expired" : "");
+  return DFLASH_OK;
+}
+
+static dflash_status stage_upload(dflash_ctx *c, cudaStream_t s, const void *src, size_t bytes,
+                                  const int32_t **dev_out) {
+  if (bytes > c->stage_cap)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "descriptor of %zu bytes exceeds staging %zu", bytes,
+                   c->stage_cap);
+  Stage &st = c->ring[c->ring_next];
+  c->ring_next = (c->ring_next + 1) % (int)c->ring.size();
+  if (st.used) CK(c, cudaEventSynchronize(st.ev));
+  memcpy(st.h, src, bytes);
+  CK(c, cudaMemcpyAsync(st.d, st.h, bytes, cudaMemcpyHostToDevice, s));
+  CK(c, cudaEventRecord(st.ev, s));
+  st.used = true;
+  *dev_out = (const int32_t *)st.d;
+  return DFLASH_OK;
+}
+
+static dflash_status run_gemm(dflash_ctx *c, const GemmDesc &d, cudaStream_t s) {
+  if (c->tc && c->dtype == DFLASH_BF16) {
+    int n = 0;
+    cudaError_t e = tc_gemm_run(c->tc, d, s, &n);
+    if (e != cudaSuccess)
+      return set_err(c, DFLASH_ERR_CUDA, "tensor-core GEMM launch failed: %s", cudaGetErrorString(e));
+    c->launches += n;
+    return DFLASH_OK;
+  }
+  CK(c, gemm_simt(c->dtype, d, s));
+  c->launches += 1;
+  return DFLASH_OK;
+}
+
+static GemmDesc gemm_desc(int M, int N, int K, const void *x, int ldx, int epi, void *y, int ldy) {
+  GemmDesc d{};
+  d.M = M;
+  d.N = N;
+  d.K = K;
+  d.n_xseg = 1;
+  d.x[0] = x;
+  d.x_k0[0] = 0;
+  d.x_k0[1] = K;
+  d.ldx[0] = ldx;
+  d.epi = epi;
+  d.y = y;
+  d.ldy = ldy;
+  return d;
+}
+
+static void add_wseg(GemmDesc &d, const void *w, int rows) {
+  int i = d.n_wseg++;
+  d.w[i] = w;
+  if (i == 0) d.w_n0[0] = 0;
+  d.w_n0[i + 1] = d.w_n0[i] + rows;
+}
+
+// ------------------------------------------------------------------------------ config
+extern "C" dflash_status dflash_validate_config(const dflash_config *c, char *msg, int32_t msg_len) {
+  auto bad = [&](dflash_status s, const char *why) {
+    if (msg && msg_len > 0) snprintf(msg, (size_t)msg_len, "%s", why);
+    return s;
+  };
+  if (!c) return bad(DFLASH_ERR_INVALID_ARG, "config is NULL");
+  if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return bad(DFLASH_ERR_INVALID_ARG, "dtype");
+  if (c->hidden <= 0 || c->hidden % 128) return bad(DFLASH_ERR_UNSUPPORTED, "hidden must be a positive multiple of 128");
+  if (c->intermediate <= 0 || c->intermediate % 128) return bad(DFLASH_ERR_UNSUPPORTED, "intermediate must be a positive multiple of 128");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad(DFLASH_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
+    return bad(DFLASH_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (c->n_q_heads / c->n_kv_heads > 8) return bad(DFLASH_ERR_UNSUPPORTED, "GQA group above 8");
+  if ((c->n_q_heads * c->head_dim) % 128 || (c->n_kv_heads * c->head_dim) % 128)
+    return bad(DFLASH_ERR_UNSUPPORTED, "q and kv widths must be multiples of 128");
+  if (c->n_layers < 1 || c->n_layers > 8) return bad(DFLASH_ERR_UNSUPPORTED, "n_layers must be 1..8");
+  if (c->n_feat < 1 || c->n_feat > 8) return bad(DFLASH_ERR_UNSUPPORTED, "n_feat must be 1..8");
+  if (c->target_hidden <= 0 || c->target_hidden % 64) return bad(DFLASH_ERR_UNSUPPORTED, "target_hidden must be a positive multiple of 64");
+  if (c->block_k < 1 || c->block_k > 31) return bad(DFLASH_ERR_UNSUPPORTED, "block_k must be 1..31");
+  if ((c->n_q_heads / c->n_kv_heads) * (c->block_k + 1) > 128)
+    return bad(DFLASH_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*(block_k+1) above 128");
+  if (c->vocab < 1) return bad(DFLASH_ERR_INVALID_ARG, "vocab");
+  if (c->topk < 1 || c->topk > 32 || c->topk > c->vocab) return bad(DFLASH_ERR_UNSUPPORTED, "topk must be 1..min(32, vocab)");
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return bad(DFLASH_ERR_INVALID_ARG, "mask_token_id out of range");
+  if (c->page_size != kPage) return bad(DFLASH_ERR_UNSUPPORTED, "page_size must be 64");
+  if (c->max_batch < 1 || c->max_requests < 1 || c->max_pages < 1 || c->max_inject_rows < 1)
+    return bad(DFLASH_ERR_INVALID_ARG, "max_batch, max_requests, max_pages, max_inject_rows must be >= 1");
+  if (c->max_positions < c->block_k + 2 || c->max_positions > (1 << 22))
+    return bad(DFLASH_ERR_INVALID_ARG, "max_positions must be in [block_k + 2, 2^22]");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad(DFLASH_ERR_INVALID_ARG, "rms_eps / rope_theta");
+  if (msg && msg_len > 0) msg[0] = 0;
+  return DFLASH_OK;
+}
+
+extern "C" const char *dflash_status_string(dflash_status s) {
+  switch (s) {
+    case DFLASH_OK: return "DFLASH_OK";
+    case DFLASH_ERR_INVALID_ARG: return "DFLASH_ERR_INVALID_ARG";
+    case DFLASH_ERR_OUT_OF_PAGES: return "DFLASH_ERR_OUT_OF_PAGES";
+    case DFLASH_ERR_UNKNOWN_REQUEST: return "DFLASH_ERR_UNKNOWN_REQUEST";
+    case DFLASH_ERR_CUDA: return "DFLASH_ERR_CUDA";
+    case DFLASH_ERR_DEVICE: return "DFLASH_ERR_DEVICE";
+    case DFLASH_ERR_UNSUPPORTED: return "DFLASH_ERR_UNSUPPORTED";
+  }
+  return "unknown status";
+}
+
+// ------------------------------------------------------------------------------ create / destroy
+static void free_all(dflash_ctx *c) {
+  void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits,
+                 c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj};
+  for (void *p : dev)
+    if (p) cudaFree(p);
+  for (auto &st : c->ring) {
+    if (st.h) cudaFreeHost(st.h);
+    if (st.d) cudaFree(st.d);
+    if (st.ev) cudaEventDestroy(st.ev);
+  }
+  if (c->err_h) cudaFreeHost(c->err_h);
+  if (c->tc) tc_gemm_destroy(c->tc);
+}
+
+extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_weights *w,
+                                       int32_t device, dflash_ctx **out) {
+  if (!out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  char msg[256];
+  dflash_status st = dflash_validate_config(cfg, msg, sizeof msg);
+  if (st != DFLASH_OK) return st;
+  if (!w || !w->embed || !w->lm_head || !w->fc || !w->fc_norm || !w->final_norm || !w->layers)
+    return DFLASH_ERR_INVALID_ARG;
+  const void *top[] = {w->embed, w->lm_head, w->fc, w->fc_norm, w->final_norm};
+  for (const void *p : top)
+    if (!aligned16(p)) return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const dflash_layer_weights &lw = w->layers[l];
+    const void *ps[] = {lw.in_norm, lw.wq, lw.wk, lw.wv, lw.wo, lw.post_norm, lw.w_gate, lw.w_up, lw.w_down};
+    for (const void *p : ps)
+      if (!p || !aligned16(p)) return DFLASH_ERR_INVALID_ARG;
+    if (cfg->qk_norm && (!lw.q_norm || !lw.k_norm)) return DFLASH_ERR_INVALID_ARG;
+  }
+
+  dflash_ctx *c = new dflash_ctx();
+  c->cfg = *cfg;
+  c->dtype = cfg->dtype;
+  c->esz = cfg->dtype == DFLASH_BF16 ? 2 : 4;
+  c->device = device;
+  c->w = *w;
+  c->layers.assign(w->layers, w->layers + cfg->n_layers);
+  c->w.layers = c->layers.data();
+  ModelDims &m = c->m;
+  m.H = cfg->hidden; m.L = cfg->n_layers; m.nq = cfg->n_q_heads; m.nkv = cfg->n_kv_heads;
+  m.hd = cfg->head_dim; m.I = cfg->intermediate; m.V = cfg->vocab; m.K = cfg->block_k;
+  m.n_feat = cfg->n_feat; m.Ht = cfg->target_hidden; m.topk = cfg->topk; m.qk_norm = cfg->qk_norm;
+  m.eps = cfg->rms_eps; m.emb_scale = cfg->input_embedding_scale;
+
+  auto fail = [&](dflash_status s) {
+    free_all(c);
+    delete c;
+    return s;
+  };
+  DeviceGuard guard(device);
+  if (guard.err != cudaSuccess) return fail(DFLASH_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return fail(DFLASH_ERR_CUDA);
+
+  const size_t es = c->esz;
+  const int R = cfg->max_batch * m.Q();
+  const int RK = cfg->max_batch * m.K;
+  const int C = cfg->max_inject_rows;
+  c->page_elems = (size_t)m.L * 2 * m.nkv * kPage * m.hd;
+  c->max_pages_per_req = (cfg->max_positions + kPage - 1) / kPage;
+  struct Alloc { void **p; size_t bytes; } allocs[] = {
+      {&c->pool, (size_t)cfg->max_pages * c->page_elems * es},
+      {(void **)&c->rope, (size_t)cfg->max_positions * (m.hd / 2) * sizeof(float2)},
+      {&c->x, (size_t)R * m.H * es},
+      {&c->xn, (size_t)R * m.H * es},
+      {&c->qkv, (size_t)R * m.qkv_dim() * es},
+      {&c->ao, (size_t)R * m.q_dim() * es},
+      {&c->gu, (size_t)R * 2 * m.I * es},
+      {&c->hmid, (size_t)R * m.I * es},
+      {&c->xf, (size_t)RK * m.H * es},
+      {(void **)&c->logits, (size_t)RK * m.V * sizeof(float)},
+      {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * sizeof(float)},
+      {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * sizeof(float)},
+      {&c->fc_out, (size_t)C * m.H * es},
+      {&c->g, (size_t)C * m.H * es},
+      {&c->kvproj, (size_t)C * m.L * 2 * m.kv_dim() * es},
+  };
+  for (auto &a : allocs)
+    if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
+
+  // RoPE table: cos/sin(pos * theta^(-2i/hd)) evaluated in double, stored as fp32
+  {
+    const int half = m.hd / 2;
+    std::vector<float2> tab((size_t)cfg->max_positions * half);
+    for (int i = 0; i < half; ++i) {
+      double inv = std::pow((double)cfg->rope_theta, -2.0 * i / m.hd);
+      for (int p = 0; p < cfg->max_positions; ++p) {
+        double a = (double)p * inv;
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    }
+    if (cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(DFLASH_ERR_CUDA);
+  }
+
+  c->free_pages.reserve(cfg->max_pages);
+  for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
+
+  size_t inj = (size_t)2 * C * sizeof(int32_t);
+  size_t drf = (size_t)(4 * cfg->max_batch + 1) * sizeof(int32_t) +
+               (size_t)cfg->max_batch * c->max_pages_per_req * sizeof(int32_t);
+  c->stage_cap = (std::max(inj, drf) + 255) / 256 * 256;
+  c->ring.resize(kRing);
+  for (auto &s : c->ring) {
+    if (cudaHostAlloc(&s.h, c->stage_cap, cudaHostAllocDefault) != cudaSuccess ||
+        cudaMalloc(&s.d, c->stage_cap) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess)
+      return fail(DFLASH_ERR_CUDA);
+  }
+  if (cudaHostAlloc((void **)&c->err_h, sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
+      cudaHostGetDevicePointer((void **)&c->err_d, c->err_h, 0) != cudaSuccess)
+    return fail(DFLASH_ERR_CUDA);
+  *c->err_h = 0;
+
+  if (c->dtype == DFLASH_BF16) {
+    cudaError_t e = tc_gemm_create(&c->tc, device, c->num_sms);
+    if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA);
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(DFLASH_ERR_CUDA);
+  *out = c;
+  return DFLASH_OK;
+}
+
+extern "C" void dflash_destroy(dflash_ctx *c) {
+  if (!c) return;
+  DeviceGuard guard(c->device);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+}
+
+extern "C" const char *dflash_last_error(const dflash_ctx *c) { return c ? c->last_error.c_str() : ""; }
+extern "C" int64_t dflash_launch_count(const dflash_ctx *c) { return c ? c->launches : 0; }
+extern "C" int32_t dflash_free_pages(const dflash_ctx *c) { return c ? (int32_t)c->free_pages.size() : 0; }
+
+extern "C" dflash_status dflash_context_len(const dflash_ctx *c, int32_t req_id, int32_t *len) {
+  if (!c || !len) return DFLASH_ERR_INVALID_ARG;
+  auto it = c->reqs.find(req_id);
+  if (it == c->reqs.end()) return DFLASH_ERR_UNKNOWN_REQUEST;
+  *len = it->second.len;
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_release(dflash_ctx *c, int32_t req_id) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  auto it = c->reqs.find(req_id);
+  if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_id);
+  for (int32_t p : it->second.pages) c->free_pages.push_back(p);
+  c->reqs.erase(it);
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_truncate(dflash_ctx *c, int32_t req_id, int32_t new_len) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  auto it = c->reqs.find(req_id);
+  if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_id);
+  Req &r = it->second;
+  if (new_len < 0 || new_len > r.len)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "truncate to %d outside [0, %d]", new_len, r.len);
+  size_t keep = (size_t)(new_len + kPage - 1) / kPage;
+  while (r.pages.size() > keep) {
+    c->free_pages.push_back(r.pages.back());
+    r.pages.pop_back();
+  }
+  r.len = new_len;
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------------------ injection
+extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int32_t n_req,
+                                               const int32_t *req_ids, const int32_t *n_new,
+                                               int32_t reset, const void *const *feats) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if (n_req < 0) return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req < 0");
+  if (n_req == 0) return DFLASH_OK;
+  if (!req_ids || !n_new) return set_err(c, DFLASH_ERR_INVALID_ARG, "req_ids / n_new is NULL");
+  const ModelDims &m = c->m;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  // ---- plan on the host; nothing changes until every check passed
+  std::unordered_set<int32_t> seen;
+  long total = 0;
+  int new_reqs = 0;
+  long pages_needed = 0, pages_freed = 0;
+  std::vector<int32_t> start(n_req);
+  for (int b = 0; b < n_req; ++b) {
+    if (!seen.insert(req_ids[b]).second)
+      return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d appears twice", req_ids[b]);
+    if (n_new[b] < 0) return set_err(c, DFLASH_ERR_INVALID_ARG, "n_new[%d] < 0", b);
+    auto it = c->reqs.find(req_ids[b]);
+    bool exists = it != c->reqs.end();
+    if (!exists) ++new_reqs;
+    int cur = (exists && !reset) ? it->second.len : 0;
+    long have = (exists && !reset) ? (long)it->second.pages.size() : 0;
+    if (exists && reset) pages_freed += (long)it->second.pages.size();
+    long new_len = (long)cur + n_new[b];
+    if (new_len + m.Q() > c->cfg.max_positions)
+      return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d would reach %ld positions (max %d incl. block)",
+                     req_ids[b], new_len, c->cfg.max_positions);
+    pages_needed += std::max(0L, (new_len + kPage - 1) / kPage - have);
+    start[b] = cur;
+    total += n_new[b];
+  }
+  if ((long)c->reqs.size() + new_reqs > c->cfg.max_requests)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "more than max_requests=%d live requests", c->cfg.max_requests);
+  if (pages_needed > (long)c->free_pages.size() + pages_freed)
+    return set_err(c, DFLASH_ERR_OUT_OF_PAGES, "need %ld pages, %zu free", pages_needed,
+                   c->free_pages.size() + (size_t)pages_freed);
+  if (total > 0) {
+    if (!feats) return set_err(c, DFLASH_ERR_INVALID_ARG, "feats is NULL");
+    for (int f = 0; f < m.n_feat; ++f)
+      if (!feats[f] || !aligned16(feats[f]))
+        return set_err(c, DFLASH_ERR_INVALID_ARG, "feats[%d] is NULL or not 16-byte aligned", f);
+  }
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+
+  // ---- commit: pages and lengths
+  std::vector<int32_t> slot(total), pos(total);
+  long r = 0;
+  for (int b = 0; b < n_req; ++b) {
+    Req &q = c->reqs[req_ids[b]];
+    if (reset) {
+      for (int32_t p : q.pages) c->free_pages.push_back(p);
+      q.pages.clear();
+      q.len = 0;
+    }
+    int new_len = start[b] + n_new[b];
+    while ((int)q.pages.size() * kPage < new_len) {
+      q.pages.push_back(c->free_pages.back());
+      c->free_pages.pop_back();
+    }
+    for (int i = 0; i < n_new[b]; ++i, ++r) {
+      int p = start[b] + i;
+      slot[r] = q.pages[p / kPage] * kPage + p % kPage;
+      pos[r] = p;
+    }
+    q.len = new_len;
+  }
+
+  // ---- launches, in chunks of max_inject_rows rows
+  const int C = c->cfg.max_inject_rows;
+  const int F = m.n_feat * m.Ht;
+  const int kvw = m.L * 2 * m.kv_dim();
+  std::vector<int32_t> buf;
+  std::vector<const void *> knorm(m.L);
+  for (int l = 0; l < m.L; ++l) knorm[l] = c->layers[l].k_norm;
+  for (long r0 = 0; r0 < total; r0 += C) {
+    int n = (int)std::min<long>(C, total - r0);
+    buf.assign(slot.begin() + r0, slot.begin() + r0 + n);
+    buf.insert(buf.end(), pos.begin() + r0, pos.begin() + r0 + n);
+    const int32_t *dslot = nullptr;
+    if ((st = stage_upload(c, s, buf.data(), buf.size() * 4, &dslot)) != DFLASH_OK) return st;
+    // fc over the n_feat feature tensors read in place (K segments)
+    GemmDesc d{};
+    d.M = n; d.N = m.H; d.K = F; d.epi = EPI_STORE; d.y = c->fc_out; d.ldy = m.H;
+    d.n_xseg = m.n_feat;
+    for (int f = 0; f < m.n_feat; ++f) {
+      d.x[f] = (const char *)feats[f] + (size_t)r0 * m.Ht * c->esz;
+      d.x_k0[f] = f * m.Ht;
+      d.ldx[f] = m.Ht;
+    }
+    d.x_k0[m.n_feat] = F;
+    add_wseg(d, c->w.fc, m.H);
+    if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
+    CK(c, launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, c->g, m.H, c->w.fc_norm, m.eps, 0, s));
+    c->launches++;
+    // every layer's [Wk; Wv] in one GEMM
+    GemmDesc e = gemm_desc(n, kvw, m.H, c->g, m.H, EPI_STORE, c->kvproj, kvw);
+    for (int l = 0; l < m.L; ++l) {
+      add_wseg(e, c->layers[l].wk, m.kv_dim());
+      add_wseg(e, c->layers[l].wv, m.kv_dim());
+    }
+    if ((st = run_gemm(c, e, s)) != DFLASH_OK) return st;
+    CK(c, launch_inject_kv(c->dtype, m, n, c->kvproj, dslot, dslot + n, c->rope, knorm.data(),
+                           c->pool, s));
+    c->launches++;
+  }
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------------------ draft step
+static void plan_splits(int S, int *n_split, int *split_len) {
+  int ns = std::min(kMaxSplit, std::max(1, (S + 511) / 512));
+  int len = round_up((S + ns - 1) / ns, 32);
+  *n_split = ns;
+  *split_len = len;
+}
+
+extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t n_req,
+                                           const int32_t *req_ids, const int32_t *anchors,
+                                           int32_t *argmax, int32_t *topk_idx, float *topk_val,
+                                           float *logits) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if (n_req < 1 || n_req > c->cfg.max_batch)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req=%d outside [1, max_batch=%d]", n_req, c->cfg.max_batch);
+  if (!req_ids || !anchors || !argmax) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
+  if ((topk_idx == nullptr) != (topk_val == nullptr))
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "topk_idx and topk_val must both be given or both NULL");
+  const ModelDims &m = c->m;
+  const int B = n_req, Q = m.Q();
+  std::vector<int32_t> desc(4 * B + 1);
+  std::vector<const Req *> rq(B);
+  std::unordered_set<int32_t> seen;
+  int max_split = 1;
+  for (int b = 0; b < B; ++b) {
+    if (!seen.insert(req_ids[b]).second)
+      return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d appears twice", req_ids[b]);
+    auto it = c->reqs.find(req_ids[b]);
+    if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_ids[b]);
+    rq[b] = &it->second;
+    int ns, sl;
+    plan_splits(rq[b]->len + Q, &ns, &sl);
+    desc[b] = rq[b]->len;
+    desc[B + b] = ns;
+    desc[2 * B + b] = sl;
+    max_split = std::max(max_split, ns);
+  }
+  int off = 0;
+  for (int b = 0; b < B; ++b) {
+    desc[3 * B + b] = off;
+    off += (int)rq[b]->pages.size();
+  }
+  desc[4 * B] = off;
+  for (int b = 0; b < B; ++b) desc.insert(desc.end(), rq[b]->pages.begin(), rq[b]->pages.end());
+
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t *dd = nullptr;
+  if ((st = stage_upload(c, s, desc.data(), desc.size() * 4, &dd)) != DFLASH_OK) return st;
+  DraftBatch bt{dd, dd + B, dd + 2 * B, dd + 3 * B, dd + 4 * B + 1, B, max_split};
+
+  const int R = B * Q;
+  CK(c, launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x, c->err_d, s));
+  c->launches++;
+  for (int l = 0; l < m.L; ++l) {
+    const dflash_layer_weights &lw = c->layers[l];
+    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, c->xn, m.H, lw.in_norm, m.eps, 0, s));
+    c->launches++;
+    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, c->xn, m.H, EPI_STORE, c->qkv, m.qkv_dim());
+    add_wseg(d, lw.wq, m.q_dim());
+    add_wseg(d, lw.wk, m.kv_dim());
+    add_wseg(d, lw.wv, m.kv_dim());
+    if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
+    CK(c, launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm, lw.k_norm, s));
+    c->launches++;
+    CK(c, launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, c->ao, s));
+    c->launches += 2;
+    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), c->ao, m.q_dim(), EPI_RESID, c->x, m.H);
+    o.resid = c->x;
+    add_wseg(o, lw.wo, m.H);
+    if ((st = run_gemm(c, o, s)) != DFLASH_OK) return st;
+    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, c->xn, m.H, lw.post_norm, m.eps, 0, s));
+    c->launches++;
+    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, c->xn, m.H, EPI_STORE, c->gu, 2 * m.I);
+    add_wseg(gu, lw.w_gate, m.I);
+    add_wseg(gu, lw.w_up, m.I);
+    if ((st = run_gemm(c, gu, s)) != DFLASH_OK) return st;
+    CK(c, launch_swiglu(c->dtype, R, m.I, c->gu, c->hmid, s));
+    c->launches++;
+    GemmDesc dn = gemm_desc(R, m.H, m.I, c->hmid, m.I, EPI_RESID, c->x, m.H);
+    dn.resid = c->x;
+    add_wseg(dn, lw.w_down, m.H);
+    if ((st = run_gemm(c, dn, s)) != DFLASH_OK) return st;
+  }
+  // final norm on the K mask rows only (the anchor row yields no candidate)
+  const int RK = B * m.K;
+  CK(c, launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, c->xf, m.H, c->w.final_norm, m.eps, m.K, s));
+  c->launches++;
+  float *lg = logits ? logits : c->logits;
+  GemmDesc lm = gemm_desc(RK, m.V, m.H, c->xf, m.H, EPI_F32, lg, m.V);
+  add_wseg(lm, c->w.lm_head, m.V);
+  if ((st = run_gemm(c, lm, s)) != DFLASH_OK) return st;
+  CK(c, launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s));
+  c->launches++;
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------------------ verify / export
+extern "C" dflash_status dflash_verify_greedy(dflash_ctx *c, void *stream, int32_t n_req,
+                                              const int32_t *draft, const int32_t *target,
+                                              int32_t *accept_len, int32_t *out_tokens,
+                                              int32_t *next_anchor) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if (n_req < 0) return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req < 0");
+  if (n_req == 0) return DFLASH_OK;
+  if (!draft || !target || !accept_len || !out_tokens || !next_anchor)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  CK(c, launch_verify(n_req, c->m.K, draft, target, accept_len, out_tokens, next_anchor,
+                      (cudaStream_t)stream));
+  c->launches++;
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_export_kv(dflash_ctx *c, void *stream, int32_t req_id, int32_t layer,
+                                          int32_t pos0, int32_t n, void *k_out, void *v_out) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  auto it = c->reqs.find(req_id);
+  if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_id);
+  const Req &q = it->second;
+  if (layer < 0 || layer >= c->m.L || pos0 < 0 || n < 0 || pos0 + n > q.len)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "export range outside the context");
+  if (n == 0) return DFLASH_OK;
+  if (!k_out || !v_out) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL output");
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t *dp = nullptr;
+  if ((st = stage_upload(c, s, q.pages.data(), q.pages.size() * 4, &dp)) != DFLASH_OK) return st;
+  CK(c, launch_export_kv(c->dtype, c->m, layer, pos0, n, dp, c->pool, k_out, v_out, s));
+  c->launches++;
+  return DFLASH_OK;
+}

@@ -1,0 +1,16 @@
+// Tensor-core (tcgen05 / TMEM / TMA) GEMM for bf16 operands — internal interface.
+#pragma once
+#include "common.cuh"
+
+namespace dflash {
+
+struct TcGemm;
+
+// Creates the per-context GEMM state (driver entry points, SM count). *out may be set to
+// nullptr, in which case callers use the FFMA GEMM.
+cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms);
+void tc_gemm_destroy(TcGemm *t);
+// Runs Y = epilogue(X . W^T) for bf16 X, W; *launches receives the kernel count.
+cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s, int *launches);
+
+}  // namespace dflash

@@ -1,0 +1,184 @@
+// Split-KV GQA attention of the query block over a paged, ragged context.
+//
+// Per request b the keys are [context positions 0..ctx_len-1 (paged cache) ; the block's
+// own K+1 keys], with no mask anywhere ("LLM的推理加速-DFlash" 关键创新 Step 3: target
+// features first, block keys after; "DFlash：把串行 Draft 变成并行“填空”" §5.3: non-causal).
+// One CTA handles (split s, kv head, request b): its rows are the G = nq/nkv query heads
+// sharing that kv head times the K+1 block rows; the key range of split s is
+// [s*split_len, min((s+1)*split_len, ctx_len + K + 1)). Partial results (unnormalised
+// accumulator, running max, running sum) are combined across splits in a fixed order.
+#include "kernels.h"
+
+namespace dflash {
+
+constexpr int AT_KT = 32;       // keys per tile (one per lane for the scores)
+constexpr int AT_MAXR = 128;    // rows per CTA (G * (K+1))
+constexpr int AT_PAGE = 64;
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) k_attn_split(
+    int L, int nq, int nkv, int Q, int layer, const T *qkv, const T *pool,
+    const int32_t *ctx_len, const int32_t *n_split, const int32_t *split_len,
+    const int32_t *page_off, const int32_t *pages, int max_split, float scale, float *part_o,
+    float *part_ml) {
+  extern __shared__ float sm[];
+  float *qs = sm;                              // [R][HD]
+  float *ks = qs + AT_MAXR * HD;               // [KT][HD+1]
+  float *vs = ks + AT_KT * (HD + 1);           // [KT][HD]
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  if (s >= n_split[b]) return;
+  const int G = nq / nkv, R = G * Q;
+  const int qkv_dim = (nq + 2 * nkv) * HD;
+  const int n_ctx = ctx_len[b];
+  const int S = n_ctx + Q;
+  const int k_begin = s * split_len[b];
+  const int k_end = min(k_begin + split_len[b], S);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row0 = (size_t)b * Q;
+  const int32_t *pg = pages + page_off[b];
+
+  for (int i = tid; i < R * HD; i += 256) {
+    int r = i / HD, d = i % HD;
+    int g = r / Q, j = r % Q;
+    qs[i] = to_f(qkv[(row0 + j) * qkv_dim + (size_t)(kvh * G + g) * HD + d]);
+  }
+
+  constexpr int DPL = HD / 32;                 // dims per lane in the PV accumulator
+  constexpr int RPW = AT_MAXR / 8;             // most rows per warp
+  float m_run[RPW], l_run[RPW], acc[RPW][DPL];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[i][d] = 0.f;
+  }
+
+  const int kv_dim = nkv * HD;
+  for (int t0 = k_begin; t0 < k_end; t0 += AT_KT) {
+    __syncthreads();
+    for (int i = tid; i < AT_KT * HD; i += 256) {
+      int kk = i / HD, d = i % HD;
+      int key = t0 + kk;
+      float kval = 0.f, vval = 0.f;
+      if (key < k_end) {
+        if (key < n_ctx) {
+          int page = pg[key / AT_PAGE], off = key % AT_PAGE;
+          size_t base = ((((size_t)page * L + layer) * 2) * nkv + kvh) * (size_t)(AT_PAGE * HD) +
+                        (size_t)off * HD + d;
+          kval = to_f(pool[base]);
+          vval = to_f(pool[base + (size_t)nkv * AT_PAGE * HD]);
+        } else {
+          size_t r = row0 + (key - n_ctx);
+          kval = to_f(qkv[r * qkv_dim + (size_t)nq * HD + (size_t)kvh * HD + d]);
+          vval = to_f(qkv[r * qkv_dim + (size_t)nq * HD + kv_dim + (size_t)kvh * HD + d]);
+        }
+      }
+      ks[kk * (HD + 1) + d] = kval;
+      vs[kk * HD + d] = vval;
+    }
+    __syncthreads();
+    const bool valid = t0 + lane < k_end;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      int r = warp + 8 * i;
+      if (r >= R) continue;
+      const float *qr = qs + r * HD;
+      const float *kr = ks + lane * (HD + 1);
+      float sc = 0.f;
+#pragma unroll 8
+      for (int d = 0; d < HD; ++d) sc = fmaf(qr[d], kr[d], sc);
+      sc = valid ? sc * scale : -INFINITY;
+      float mt = warp_max(sc);
+      float m_new = fmaxf(m_run[i], mt);
+      float p = valid ? expf(sc - m_new) : 0.f;
+      float corr = expf(m_run[i] - m_new);      // exp(-inf) = 0 on the first tile
+      l_run[i] = l_run[i] * corr + warp_sum(p);
+      m_run[i] = m_new;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[i][d] *= corr;
+      for (int kk = 0; kk < AT_KT; ++kk) {
+        float pk = __shfl_sync(0xffffffffu, p, kk);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[i][d] = fmaf(pk, vs[kk * HD + lane + 32 * d], acc[i][d]);
+      }
+    }
+  }
+
+  // partial outputs: part_o[((b*Q + j)*nq + h)*max_split + s][HD], part_ml[...][2]
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    int r = warp + 8 * i;
+    if (r >= R) continue;
+    int g = r / Q, j = r % Q;
+    size_t idx = (((size_t)b * Q + j) * nq + (kvh * G + g)) * max_split + s;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) part_o[idx * HD + lane + 32 * d] = acc[i][d];
+    if (lane == 0) {
+      part_ml[idx * 2] = m_run[i];
+      part_ml[idx * 2 + 1] = l_run[i];
+    }
+  }
+}
+
+// o[b*Q + j, h*HD + d] = sum_s acc_s * exp(m_s - M) / sum_s l_s * exp(m_s - M), in split order.
+template <typename T, int HD>
+__global__ void k_attn_combine(int nq, int Q, const int32_t *n_split, int max_split,
+                               const float *part_o, const float *part_ml, T *o) {
+  int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  int b = blockIdx.y;
+  if (w >= Q * nq) return;
+  int j = w / nq, h = w % nq;
+  size_t base = (((size_t)b * Q + j) * nq + h) * max_split;
+  int ns = n_split[b];
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
+  float Lsum = 0.f;
+  float acc[HD / 32] = {};
+  for (int s = 0; s < ns; ++s) {
+    float c = expf(part_ml[(base + s) * 2] - M);
+    Lsum += part_ml[(base + s) * 2 + 1] * c;
+#pragma unroll
+    for (int d = 0; d < HD / 32; ++d) acc[d] += part_o[(base + s) * HD + lane + 32 * d] * c;
+  }
+  float inv = 1.f / Lsum;
+  T *dst = o + ((size_t)b * Q + j) * (nq * HD) + (size_t)h * HD;
+#pragma unroll
+  for (int d = 0; d < HD / 32; ++d) dst[lane + 32 * d] = from_f<T>(acc[d] * inv);
+}
+
+template <typename T, int HD>
+static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer, const void *qkv,
+                             const void *pool, float *part_o, float *part_ml, void *o,
+                             cudaStream_t s) {
+  size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_attn_split<T, HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 g(bt.max_split, m.nkv, bt.B);
+  k_attn_split<T, HD><<<g, 256, smem, s>>>(
+      m.L, m.nq, m.nkv, m.Q(), layer, (const T *)qkv, (const T *)pool, bt.ctx_len, bt.n_split,
+      bt.split_len, bt.page_off, bt.pages, bt.max_split, 1.f / sqrtf((float)HD), part_o, part_ml);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2((m.Q() * m.nq + 7) / 8, bt.B);
+  k_attn_combine<T, HD><<<g2, 256, 0, s>>>(m.nq, m.Q(), bt.n_split, bt.max_split, part_o, part_ml,
+                                            (T *)o);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &bt, int layer,
+                             const void *qkv, const void *pool, float *part_o, float *part_ml,
+                             void *o, cudaStream_t s) {
+  if (bt.B <= 0) return cudaSuccess;
+  if (m.hd == 128)
+    return dtype ? attn_impl<bf16, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, s)
+                 : attn_impl<float, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, s);
+  if (m.hd == 64)
+    return dtype ? attn_impl<bf16, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, s)
+                 : attn_impl<float, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dflash

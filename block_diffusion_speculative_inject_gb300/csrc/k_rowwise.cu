@@ -1,0 +1,267 @@
+// Row-wise kernels of the draft step: block embedding, RMSNorm, q/k head norm + RoPE,
+// the injection epilogue (k-norm + RoPE + paged-cache write), SwiGLU, greedy verify and
+// the KV export. All are HBM/latency-bound elementwise passes; one warp per row or per
+// (row, head), 16-byte aligned rows, fp32 arithmetic and one rounding per stored value.
+#include "kernels.h"
+
+namespace dflash {
+
+constexpr int PAGE = 64;
+
+__device__ __forceinline__ size_t pool_index(int page, int l, int kv, int h, int off, int L,
+                                             int nkv, int hd) {
+  return ((((size_t)page * L + l) * 2 + kv) * nkv + h) * (size_t)(PAGE * hd) + (size_t)off * hd;
+}
+
+// ------------------------------------------------------------------------- embedding
+// Block rows of request b: row 0 is the anchor token, rows 1..K the mask token; each is
+// the shared embedding row times input_embedding_scale ("DFlash 2 块扩散投机解码技术详解"
+// §2.2; "DFlash：把串行 Draft 变成并行“填空”" §4).
+template <typename T>
+__global__ void k_embed(int H, int Q, int V, const int32_t *anchors, int mask_id, float scale,
+                        const T *embed, T *x, int *err) {
+  int r = blockIdx.x;
+  int b = r / Q, j = r % Q;
+  int tok = j == 0 ? anchors[b] : mask_id;
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) raise_err(err, DEV_ERR_TOKEN);
+    tok = 0;
+  }
+  const T *src = embed + (size_t)tok * H;
+  T *dst = x + (size_t)r * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = from_f<T>(to_f(src[i]) * scale);
+}
+
+cudaError_t launch_embed(int dtype, const ModelDims &m, int B, const int32_t *anchors,
+                         int mask_id, const void *embed, void *x, int *err, cudaStream_t s) {
+  dim3 g(B * m.Q());
+  if (dtype) k_embed<bf16><<<g, 256, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
+                                             (const bf16 *)embed, (bf16 *)x, err);
+  else k_embed<float><<<g, 256, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
+                                        (const float *)embed, (float *)x, err);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- RMSNorm
+// y = x * rsqrt(mean(x^2) + eps) * w, one warp per row.
+template <typename T>
+__global__ void k_rmsnorm(int rows, int H, const T *in, int ld_in, T *out, int ld_out,
+                          const T *w, float eps, int skip_k) {
+  int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  int src = skip_k > 0 ? (r / skip_k) * (skip_k + 1) + r % skip_k + 1 : r;
+  const T *xi = in + (size_t)src * ld_in;
+  float ss = 0.f;
+  for (int i = lane; i < H; i += 32) {
+    float v = to_f(xi[i]);
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  float rs = rsqrtf(ss / (float)H + eps);
+  T *yo = out + (size_t)r * ld_out;
+  for (int i = lane; i < H; i += 32) yo[i] = from_f<T>(to_f(xi[i]) * rs * to_f(w[i]));
+}
+
+cudaError_t launch_rmsnorm(int dtype, int rows, int H, const void *in, int ld_in, void *out,
+                           int ld_out, const void *w, float eps, int skip_anchor_k,
+                           cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  dim3 g((rows + 7) / 8);
+  if (dtype) k_rmsnorm<bf16><<<g, 256, 0, s>>>(rows, H, (const bf16 *)in, ld_in, (bf16 *)out,
+                                               ld_out, (const bf16 *)w, eps, skip_anchor_k);
+  else k_rmsnorm<float><<<g, 256, 0, s>>>(rows, H, (const float *)in, ld_in, (float *)out,
+                                          ld_out, (const float *)w, eps, skip_anchor_k);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- head norm + RoPE
+// One warp rotates one head vector of hd (64 or 128) values held as hd/32 per lane:
+// lane holds i = lane + 32*t; pairs are (i, i + hd/2) so for hd = 128 lane's t=0,1
+// pair with t=2,3 and for hd = 64 t=0 pairs with t=1.
+template <typename T>
+__device__ __forceinline__ void head_norm_rope(const T *src, T *dst, const T *nw, int hd,
+                                               float eps, const float2 *rope_row, int lane) {
+  float v[4];
+  const int per = hd / 32;
+  float ss = 0.f;
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    if (t < per) {
+      v[t] = to_f(src[lane + 32 * t]);
+      ss += v[t] * v[t];
+    }
+  if (nw) {
+    ss = warp_sum(ss);
+    float rs = rsqrtf(ss / (float)hd + eps);
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (t < per) v[t] = v[t] * rs * to_f(nw[lane + 32 * t]);
+  }
+  const int hp = per / 2;  // number of first-half slots per lane
+  float o[4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    if (t < hp) {
+      int i = lane + 32 * t;
+      float2 cs = rope_row[i];
+      float x1 = v[t], x2 = v[t + hp];
+      o[t] = x1 * cs.x - x2 * cs.y;
+      o[t + hp] = x2 * cs.x + x1 * cs.y;
+    }
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    if (t < per) dst[lane + 32 * t] = from_f<T>(o[t]);
+}
+
+template <typename T>
+__global__ void k_qk_norm_rope(int rows, int Q, int nq, int nkv, int hd, int qkv_dim,
+                               T *qkv, const int32_t *ctx_len, const float2 *rope,
+                               const T *q_norm, const T *k_norm, float eps) {
+  int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  int heads = nq + nkv;
+  if (w >= rows * heads) return;
+  int r = w / heads, h = w % heads;
+  int b = r / Q, j = r % Q;
+  int pos = ctx_len[b] + j;
+  T *p = qkv + (size_t)r * qkv_dim + (size_t)h * hd;   // q heads then k heads are contiguous
+  const T *nw = h < nq ? q_norm : k_norm;
+  head_norm_rope<T>(p, p, nw, hd, eps, rope + (size_t)pos * (hd / 2), lane);
+}
+
+cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, void *qkv,
+                                const int32_t *ctx_len, const float2 *rope,
+                                const void *q_norm, const void *k_norm, cudaStream_t s) {
+  int rows = B * m.Q();
+  int warps = rows * (m.nq + m.nkv);
+  dim3 g((warps + 7) / 8);
+  const void *qn = m.qk_norm ? q_norm : nullptr, *kn = m.qk_norm ? k_norm : nullptr;
+  if (dtype) k_qk_norm_rope<bf16><<<g, 256, 0, s>>>(rows, m.Q(), m.nq, m.nkv, m.hd, m.qkv_dim(),
+                                                    (bf16 *)qkv, ctx_len, rope, (const bf16 *)qn,
+                                                    (const bf16 *)kn, m.eps);
+  else k_qk_norm_rope<float><<<g, 256, 0, s>>>(rows, m.Q(), m.nq, m.nkv, m.hd, m.qkv_dim(),
+                                               (float *)qkv, ctx_len, rope, (const float *)qn,
+                                               (const float *)kn, m.eps);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- injection epilogue
+// Row t of the layer-batched K/V projection of g goes, in every layer, through the per-head
+// k-norm and RoPE at its position and into its page slot; V is stored as projected
+// ("DFlash：块扩散 + KV 注入" §四: projection then norm + RoPE post-processing;
+// "DFlash：把串行 Draft 变成并行“填空”" §5.1).
+struct KNormPtrs { const void *p[16]; };
+
+template <typename T>
+__global__ void k_inject_kv(int T_rows, int L, int nkv, int hd, const T *kv, const int32_t *slot,
+                            const int32_t *pos, const float2 *rope, KNormPtrs kn, int qk_norm,
+                            float eps, T *pool) {
+  int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (w >= T_rows * L * nkv) return;
+  int t = w / (L * nkv), rem = w % (L * nkv);
+  int l = rem / nkv, h = rem % nkv;
+  int kv_dim = nkv * hd;
+  int sl = slot[t];
+  int page = sl / PAGE, off = sl % PAGE;
+  const T *src_k = kv + (size_t)t * (L * 2 * kv_dim) + (size_t)l * 2 * kv_dim + (size_t)h * hd;
+  const T *src_v = src_k + kv_dim;
+  T *dk = pool + pool_index(page, l, 0, h, off, L, nkv, hd);
+  T *dv = pool + pool_index(page, l, 1, h, off, L, nkv, hd);
+  const T *nw = qk_norm ? (const T *)kn.p[l] : nullptr;
+  head_norm_rope<T>(src_k, dk, nw, hd, eps, rope + (size_t)pos[t] * (hd / 2), lane);
+  for (int i = lane; i < hd; i += 32) dv[i] = src_v[i];
+}
+
+cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const void *kv,
+                             const int32_t *slot, const int32_t *pos, const float2 *rope,
+                             const void *const *k_norms, void *pool, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  KNormPtrs kn{};
+  for (int l = 0; l < m.L && l < 16; ++l) kn.p[l] = k_norms[l];
+  long warps = (long)T * m.L * m.nkv;
+  dim3 g((unsigned)((warps + 7) / 8));
+  if (dtype) k_inject_kv<bf16><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, (const bf16 *)kv, slot, pos,
+                                                 rope, kn, m.qk_norm, m.eps, (bf16 *)pool);
+  else k_inject_kv<float><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, (const float *)kv, slot, pos,
+                                            rope, kn, m.qk_norm, m.eps, (float *)pool);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- SwiGLU
+// gu rows hold [gate (I) | up (I)], both already rounded GEMM outputs; h = silu(g) * u.
+template <typename T>
+__global__ void k_swiglu(long n, int I, const T *gu, T *h) {
+  long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  long r = i / I, c = i % I;
+  float g = to_f(gu[r * 2 * I + c]), u = to_f(gu[r * 2 * I + I + c]);
+  h[i] = from_f<T>(g / (1.f + expf(-g)) * u);
+}
+
+cudaError_t launch_swiglu(int dtype, int rows, int I, const void *gu, void *h, cudaStream_t s) {
+  long n = (long)rows * I;
+  if (n == 0) return cudaSuccess;
+  dim3 g((unsigned)((n + 255) / 256));
+  if (dtype) k_swiglu<bf16><<<g, 256, 0, s>>>(n, I, (const bf16 *)gu, (bf16 *)h);
+  else k_swiglu<float><<<g, 256, 0, s>>>(n, I, (const float *)gu, (float *)h);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- greedy verify
+// a = number of leading j < K with draft[j] == target[j]; emit draft[0..a-1] then target[a]
+// ("DFlash 2 块扩散投机解码技术详解" §2.3; at most K+1 tokens: "DFlash：把串行 Draft 变成并行“填空”" §2).
+__global__ void k_verify(int n, int K, const int32_t *draft, const int32_t *target,
+                         int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= n) return;
+  const int32_t *d = draft + (size_t)b * K;
+  const int32_t *t = target + (size_t)b * (K + 1);
+  int a = 0;
+  while (a < K && d[a] == t[a]) ++a;
+  int32_t *o = out_tokens + (size_t)b * (K + 1);
+  for (int j = 0; j <= K; ++j) o[j] = j < a ? d[j] : (j == a ? t[a] : -1);
+  accept_len[b] = a;
+  next_anchor[b] = t[a];
+}
+
+cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *target,
+                          int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
+                          cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_verify<<<(n + 127) / 128, 128, 0, s>>>(n, K, draft, target, accept_len, out_tokens,
+                                           next_anchor);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- KV export
+template <typename T>
+__global__ void k_export_kv(int L, int nkv, int hd, int layer, int pos0, int n,
+                            const int32_t *pages, const T *pool, T *k_out, T *v_out) {
+  long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  long total = (long)n * nkv * hd;
+  if (i >= total) return;
+  int d = i % hd;
+  int h = (i / hd) % nkv;
+  int t = i / ((long)hd * nkv);
+  int p = pos0 + t;
+  int page = pages[p / PAGE], off = p % PAGE;
+  k_out[i] = pool[pool_index(page, layer, 0, h, off, L, nkv, hd) + d];
+  v_out[i] = pool[pool_index(page, layer, 1, h, off, L, nkv, hd) + d];
+}
+
+cudaError_t launch_export_kv(int dtype, const ModelDims &m, int layer, int pos0, int n,
+                             const int32_t *pages, const void *pool, void *k_out, void *v_out,
+                             cudaStream_t s) {
+  long total = (long)n * m.nkv * m.hd;
+  if (total == 0) return cudaSuccess;
+  dim3 g((unsigned)((total + 255) / 256));
+  if (dtype) k_export_kv<bf16><<<g, 256, 0, s>>>(m.L, m.nkv, m.hd, layer, pos0, n, pages,
+                                                 (const bf16 *)pool, (bf16 *)k_out, (bf16 *)v_out);
+  else k_export_kv<float><<<g, 256, 0, s>>>(m.L, m.nkv, m.hd, layer, pos0, n, pages,
+                                            (const float *)pool, (float *)k_out, (float *)v_out);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -1,0 +1,205 @@
+/*
+ * dflash.h — C ABI of the DFlash batched draft step on one GB300 (sm_103a).
+ *
+ * The library runs the hot path of DFlash block-diffusion speculative decoding:
+ *   1. KV injection: target hidden states of n_feat target layers are concatenated,
+ *      projected by fc and RMSNorm into the fused feature g, then put through every
+ *      draft layer's K/V projection (+ per-head k-norm) and RoPE and written to the
+ *      paged draft KV cache.
+ *        ("LLM的推理加速-DFlash", 关键创新 Step 1-3; "DFlash 2 块扩散投机解码技术详解" §2.2;
+ *         "DFlash：块扩散 + KV 注入" §四; "DFlash：把串行 Draft 变成并行“填空”" §5.1, §5.6)
+ *   2. One parallel forward of the query block [anchor, MASK x K] (embedding rows times
+ *      input_embedding_scale) through the draft decoder layers, attending without a mask
+ *      over the injected context K/V followed by the block's own K/V.
+ *        ("DFlash 2 块扩散投机解码技术详解" §2.1-2.2; "DFlash：把串行 Draft 变成并行“填空”"
+ *         §4-4.4, §5.3; "LLM的推理加速-DFlash", 关键创新 Step 3)
+ *   3. The LM head with per-position argmax and top-k for the K mask rows only (the
+ *      anchor row yields no candidate).
+ *        ("DFlash：把串行 Draft 变成并行“填空”" §4.3; "DFlash 2 块扩散投机解码技术详解" §2.2)
+ *   4. Greedy verification: the longest prefix of drafts equal to the target tokens,
+ *      then one target token (correction or bonus); at most K+1 tokens per round.
+ *        ("DFlash 2 块扩散投机解码技术详解" §2.3; "DFlash：把串行 Draft 变成并行“填空”" §2;
+ *         "LLM的推理加速-DFlash", 核心推理伪代码)
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses on the device the context was created
+ *     on; host pointers are ordinary host memory read before the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls only enqueue work on it and never synchronise the device. All calls on
+ *     one context must be issued in one stream order (one stream, or streams the
+ *     caller orders with events); the context is not thread-safe.
+ *   - Weight matrices are row-major [out_features, in_features] (the nn.Linear layout),
+ *     norm weights are vectors; all have the storage type of `dtype` (fp32 or bf16).
+ *     The caller owns weights and every input/output buffer and keeps the weights
+ *     alive and unchanged while the context exists. The library owns the paged KV
+ *     pool, its page tables, scratch and pinned staging, all allocated in
+ *     dflash_create and freed in dflash_destroy.
+ *   - Every call returns a dflash_status. On an error no request state changes (pages
+ *     are planned on the host before anything is launched); dflash_last_error()
+ *     gives the reason. Device-side checks (out-of-range token ids, exhausted waits)
+ *     latch a flag that the next call reports as DFLASH_ERR_DEVICE.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = -1,     /* a NULL/misaligned pointer, a size out of range */
+  DFLASH_ERR_OUT_OF_PAGES = -2,    /* the paged KV pool cannot hold the injection   */
+  DFLASH_ERR_UNKNOWN_REQUEST = -3, /* req_id was never injected or was released     */
+  DFLASH_ERR_CUDA = -4,            /* a CUDA runtime/driver call failed             */
+  DFLASH_ERR_DEVICE = -5,          /* a device-side check latched an error flag     */
+  DFLASH_ERR_UNSUPPORTED = -6      /* a shape the kernels do not handle             */
+} dflash_status;
+
+typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
+
+/* Draft-model shape and context limits. Requirements (checked by dflash_validate_config):
+ * hidden, intermediate, n_q_heads*head_dim and n_kv_heads*head_dim multiples of 128;
+ * target_hidden a multiple of 64; head_dim 64 or 128; n_q_heads a multiple of
+ * n_kv_heads with n_q_heads/n_kv_heads <= 8; 1 <= block_k <= 31; 1 <= topk <= 32;
+ * page_size == 64; vocab >= topk; mask_token_id in [0, vocab). */
+typedef struct {
+  int32_t hidden;            /* H: draft hidden size                                   */
+  int32_t n_layers;          /* L: draft decoder layers                                */
+  int32_t n_q_heads;         /* nq                                                     */
+  int32_t n_kv_heads;        /* nkv (GQA: q head h reads kv head h / (nq/nkv))         */
+  int32_t head_dim;          /* hd                                                     */
+  int32_t intermediate;      /* I: SwiGLU width                                        */
+  int32_t vocab;             /* V                                                      */
+  int32_t n_feat;            /* number of target layers whose hidden states are fused  */
+  int32_t target_hidden;     /* H_t: width of each target hidden state                 */
+  int32_t block_k;           /* K mask positions; the query block has K+1 rows         */
+  int32_t topk;              /* k of the per-position top-k                            */
+  int32_t mask_token_id;     /* embedding row used for every mask position             */
+  int32_t qk_norm;           /* 1: per-head RMSNorm (q_norm/k_norm) before RoPE        */
+  int32_t max_batch;         /* most requests in one call                              */
+  int32_t max_requests;      /* most live requests                                     */
+  int32_t max_pages;         /* pages in the KV pool                                   */
+  int32_t page_size;         /* tokens per page; must be 64                            */
+  int32_t max_positions;     /* longest context + K + 1 (RoPE table length)            */
+  int32_t max_inject_rows;   /* rows per internal injection chunk (scratch sizing)     */
+  float rms_eps;             /* RMSNorm epsilon                                        */
+  float rope_theta;          /* RoPE base                                              */
+  float input_embedding_scale; /* multiplies the block's embedding rows                */
+  dflash_dtype dtype;        /* storage / GEMM operand type                            */
+} dflash_config;
+
+/* One draft decoder layer (pre-norm, Qwen3-style). All [out, in] row-major. */
+typedef struct {
+  const void *in_norm;   /* [H]                 */
+  const void *wq;        /* [nq*hd, H]          */
+  const void *wk;        /* [nkv*hd, H]         */
+  const void *wv;        /* [nkv*hd, H]         */
+  const void *q_norm;    /* [hd] (unused when qk_norm == 0, may be NULL) */
+  const void *k_norm;    /* [hd] (unused when qk_norm == 0, may be NULL) */
+  const void *wo;        /* [H, nq*hd]          */
+  const void *post_norm; /* [H]                 */
+  const void *w_gate;    /* [I, H]              */
+  const void *w_up;      /* [I, H]              */
+  const void *w_down;    /* [H, I]              */
+} dflash_layer_weights;
+
+typedef struct {
+  const void *embed;       /* [V, H] shared token embedding                          */
+  const void *lm_head;     /* [V, H] shared LM head (may equal embed)                */
+  const void *fc;          /* [H, n_feat*H_t]; input column block f holds feature f  */
+  const void *fc_norm;     /* [H] RMSNorm after fc                                   */
+  const void *final_norm;  /* [H] RMSNorm before the LM head                         */
+  const dflash_layer_weights *layers; /* host array of n_layers entries (copied)     */
+} dflash_weights;
+
+typedef struct dflash_ctx dflash_ctx;
+
+/* Checks a configuration on the host only (no CUDA call). Writes a reason into msg
+ * (if msg != NULL and msg_len > 0) when the status is not DFLASH_OK. */
+dflash_status dflash_validate_config(const dflash_config *cfg, char *msg, int32_t msg_len);
+
+/* Creates a context on `device`: validates cfg, checks weight pointers (non-NULL,
+ * 16-byte aligned), allocates the KV pool (max_pages x n_layers x 2 x nkv x 64 x hd
+ * elements), scratch and staging. *out is set only on DFLASH_OK. */
+dflash_status dflash_create(const dflash_config *cfg, const dflash_weights *w,
+                            int32_t device, dflash_ctx **out);
+
+/* Frees everything the context owns (after synchronising its device). NULL is a no-op. */
+void dflash_destroy(dflash_ctx *ctx);
+
+/* KV injection ("LLM的推理加速-DFlash" 关键创新 Step 2-3; "DFlash：把串行 Draft 变成并行“填空”"
+ * §4.1, §5.1): appends n_new[b] positions to request req_ids[b] for b < n_req.
+ *   req_ids [n_req] host: request ids (any int32); an unknown id registers a request.
+ *   n_new   [n_req] host: rows per request, >= 0.
+ *   reset   1: drop each request's existing context first (prefill); 0: append.
+ *   feats   host array of n_feat DEVICE pointers; feats[f] is [sum(n_new), H_t]
+ *           row-major (16-byte aligned), rows grouped by request in req_ids order.
+ * Position p of a request gets K = RoPE(k_norm(g Wk^T), p) and V = g Wv^T in every
+ * layer, g = RMSNorm(concat_f(h_f) W_fc^T). Errors: OUT_OF_PAGES / INVALID_ARG with
+ * no state change. Rows are processed in chunks of max_inject_rows. */
+dflash_status dflash_inject_context(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                    const int32_t *req_ids, const int32_t *n_new,
+                                    int32_t reset, const void *const *feats);
+
+/* One draft step for n_req live requests ("DFlash：把串行 Draft 变成并行“填空”" §4-4.4):
+ *   req_ids  [n_req] host.
+ *   anchors  [n_req] int32 DEVICE: the last verified token of each request.
+ *   argmax   [n_req, K] int32 DEVICE (required): per mask position, lowest index on ties.
+ *   topk_idx [n_req, K, topk] int32 DEVICE or NULL; topk_val the fp32 logits, sorted
+ *            descending (ties: lower index first); both or neither.
+ *   logits   [n_req, K, V] fp32 DEVICE or NULL: full logits (for inspection).
+ * Block row j of request b sits at position ctx_len_b + j (row 0 is the anchor). The
+ * block's own K/V are not added to the cache. */
+dflash_status dflash_draft_step(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                const int32_t *req_ids, const int32_t *anchors,
+                                int32_t *argmax, int32_t *topk_idx, float *topk_val,
+                                float *logits);
+
+/* Greedy verification ("DFlash 2 块扩散投机解码技术详解" §2.3): for each of n_req rows,
+ *   draft  [n_req, K] int32 DEVICE, target [n_req, K+1] int32 DEVICE (the target's token
+ *   after the anchor and after each draft), outputs (DEVICE):
+ *   accept_len [n_req] = number of leading j < K with draft[j] == target[j] (= a),
+ *   out_tokens [n_req, K+1] = draft[0..a-1], target[a], then -1 padding,
+ *   next_anchor [n_req] = target[a].
+ * The next injection for the request is a + 1 positions (the anchor and the accepted
+ * drafts). n_req may exceed max_batch. */
+dflash_status dflash_verify_greedy(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                   const int32_t *draft, const int32_t *target,
+                                   int32_t *accept_len, int32_t *out_tokens,
+                                   int32_t *next_anchor);
+
+/* Forgets a request and returns its pages to the pool (host only). Work already
+ * enqueued that reads those pages must precede any later call in stream order. */
+dflash_status dflash_release(dflash_ctx *ctx, int32_t req_id);
+
+/* Shortens a request's context to new_len <= its length (host only; frees whole pages
+ * past the new end). Used by schedulers that roll a request back. */
+dflash_status dflash_truncate(dflash_ctx *ctx, int32_t req_id, int32_t new_len);
+
+/* Context length of a live request (host only). */
+dflash_status dflash_context_len(const dflash_ctx *ctx, int32_t req_id, int32_t *len);
+
+/* Copies positions [pos0, pos0+n) of one layer's cached K and V of a request into
+ * k_out / v_out, each [n, nkv, hd] DEVICE buffers of the storage type (inspection). */
+dflash_status dflash_export_kv(dflash_ctx *ctx, void *stream, int32_t req_id, int32_t layer,
+                               int32_t pos0, int32_t n, void *k_out, void *v_out);
+
+/* Free pages in the pool (host only). */
+int32_t dflash_free_pages(const dflash_ctx *ctx);
+
+/* Text of the last error on this context ("" if none). Valid until the next call. */
+const char *dflash_last_error(const dflash_ctx *ctx);
+
+/* Static name of a status code. */
+const char *dflash_status_string(dflash_status s);
+
+/* Number of kernel launches this context has issued so far (all calls). */
+int64_t dflash_launch_count(const dflash_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */

@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle, on the same
+seeded inputs, element by element at small sizes and on whole steps of the workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import get_config
+from synth import inputs as S
+
+from harness import Pair, check_argmax, check_logits, check_topk, to_np, LOGIT_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_diffusion_speculative_inject_gb300 import build
+    build.build()
+
+
+def _limits(**kw):
+    from block_diffusion_speculative_inject_gb300 import Limits
+    return Limits(**kw)
+
+
+# ----------------------------------------------------------------------------- verify
+def test_verify_greedy_bit_exact_random_and_edges():
+    from block_diffusion_speculative_inject_gb300 import Context
+    cfg = get_config("mini_bf16", n_layers=1)
+    pair = Pair(cfg, _limits(max_batch=4, max_pages=4, max_positions=128, max_inject_rows=16))
+    K, V = cfg.block_k, 7    # tiny alphabet -> many matches
+    g = torch.Generator().manual_seed(5)
+    B = 1000                 # verification is not bounded by max_batch
+    draft = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    target = torch.randint(0, V, (B, K + 1), generator=g, dtype=torch.int32)
+    copy = torch.rand((B, K), generator=g) < 0.8
+    target[:, :K] = torch.where(copy, draft, target[:, :K])
+    target[0, :K] = draft[0]                  # all accepted -> bonus
+    target[1, 0] = (draft[1, 0] + 1) % V      # first rejected
+    acc, out, nxt = pair.ctx.verify(draft.cuda(), target.cuda())
+    wa, wo, wn = O.verify_greedy(draft.numpy(), target.numpy())
+    np.testing.assert_array_equal(acc.cpu().numpy(), wa)
+    np.testing.assert_array_equal(out.cpu().numpy(), wo)
+    np.testing.assert_array_equal(nxt.cpu().numpy(), wn)
+    assert acc[0].item() == K and acc[1].item() == 0
+    assert int(acc.max()) <= K
+
+
+# ----------------------------------------------------------------------------- whole steps
+def _run_steps(cfg, limits, ctx_lens, steps, seed=0, check_kv=True):
+    pair = Pair(cfg, limits, seed=seed)
+    B = len(ctx_lens)
+    reqs = list(range(10, 10 + B))
+    pair.inject(reqs, ctx_lens, "prefill", reset=True)
+    tol = LOGIT_TOL[cfg.dtype]
+    if check_kv:
+        for i, r in enumerate(reqs):
+            for l in range(cfg.n_layers):
+                k, v = pair.ctx.export_kv(r, l, 0, ctx_lens[i])
+                wk, wv = pair.orc.cache[r]["K"][l], pair.orc.cache[r]["V"][l]
+                kv_tol = 1e-4 if cfg.dtype == "f32" else 3e-2
+                np.testing.assert_allclose(to_np(k), wk, atol=kv_tol, rtol=0)
+                np.testing.assert_allclose(to_np(v), wv, atol=kv_tol, rtol=0)
+                if cfg.dtype == "bf16":   # rounding flips are rare
+                    assert np.mean(to_np(k) == wk) > 0.99 and np.mean(to_np(v) == wv) > 0.99
+    anchors = S.make_anchors(cfg, B, seed, 0)
+    for step in range(steps):
+        out = pair.ctx.draft(reqs, anchors.cuda(), want_logits=True)
+        lg = to_np(out["logits"])
+        am = out["argmax"].cpu().numpy()
+        ti, tv = out["topk_idx"].cpu().numpy(), to_np(out["topk_val"])
+        oam = np.zeros((B, cfg.block_k), dtype=np.int64)
+        for i, r in enumerate(reqs):
+            w_am, w_idx, w_val, w_lg = pair.orc.draft(r, int(anchors[i]))
+            oam[i] = w_am
+            check_logits(cfg, lg[i], w_lg, f"step {step} req {r}")
+            check_argmax(am[i], w_lg, f"step {step} req {r}")
+            check_topk(ti[i], tv[i], w_lg, cfg.topk, tol, f"step {step} req {r}")
+            assert np.all(am[i] == ti[i][:, 0])
+        # the synthetic target follows the oracle's argmax; both verifies see the same ids
+        target = S.make_targets(cfg, torch.from_numpy(oam), seed, step)
+        acc, toks, nxt = pair.ctx.verify(out["argmax"], target.cuda())
+        wa, wo, wn = O.verify_greedy(am, target.numpy())
+        np.testing.assert_array_equal(acc.cpu().numpy(), wa)
+        np.testing.assert_array_equal(toks.cpu().numpy(), wo)
+        np.testing.assert_array_equal(nxt.cpu().numpy(), wn)
+        # next round: inject the anchor + accepted drafts (a + 1 positions)
+        n_new = (acc.cpu() + 1).tolist()
+        pair.inject(reqs, n_new, ("step", step))
+        for i, r in enumerate(reqs):
+            assert pair.ctx.context_len(r) == pair.orc.context_len(r)
+        anchors = nxt.cpu()
+    return pair
+
+
+def test_tiny_f32_steps():
+    cfg = get_config("tiny_f32")
+    _run_steps(cfg, _limits(max_batch=1, max_pages=8, max_positions=256, max_inject_rows=64),
+               [64], steps=3)
+
+
+def test_mini_bf16_ragged_batch_steps():
+    cfg = get_config("mini_bf16")
+    _run_steps(cfg, _limits(max_batch=4, max_pages=32, max_positions=512, max_inject_rows=100),
+               [50, 173, 300], steps=3)
+
+
+def test_mini_bf16_empty_context_and_page_edges():
+    cfg = get_config("mini_bf16", n_layers=1)
+    _run_steps(cfg, _limits(max_batch=4, max_pages=16, max_positions=512, max_inject_rows=64),
+               [1, 63, 64, 65], steps=2)
+
+
+# ----------------------------------------------------------------------------- invariants on the GPU
+def test_incremental_injection_bit_identical_to_one_shot():
+    cfg = get_config("mini_bf16")
+    w = S.make_weights(cfg, 3)
+    lim = _limits(max_batch=2, max_pages=16, max_positions=512, max_inject_rows=40)
+    a = Pair(cfg, lim, seed=3, weights=w)
+    b = Pair(cfg, lim, seed=3, weights=w)
+    n = 150
+    feats = S.make_features(cfg, n, 3, "ctx")
+    fg = [f.cuda() for f in feats]
+    a.ctx.inject([1], [n], fg, reset=True)
+    g = torch.Generator().manual_seed(4)
+    s = 0
+    while s < n:
+        m = min(int(torch.randint(1, 17, (1,), generator=g)), n - s)
+        b.ctx.inject([1], [m], [f[s:s + m].contiguous() for f in fg])
+        s += m
+    for l in range(cfg.n_layers):
+        ka, va = a.ctx.export_kv(1, l, 0, n)
+        kb, vb = b.ctx.export_kv(1, l, 0, n)
+        assert torch.equal(ka, kb) and torch.equal(va, vb)
+
+
+def test_results_independent_of_batch_composition():
+    cfg = get_config("mini_bf16")
+    w = S.make_weights(cfg, 6)
+    lim = _limits(max_batch=4, max_pages=32, max_positions=512, max_inject_rows=128)
+    p = Pair(cfg, lim, seed=6, weights=w)
+    lens = [120, 37, 260]
+    p.inject([1, 2, 3], lens, "prefill", reset=True)
+    anchors = torch.tensor([5, 17, 99], dtype=torch.int32).cuda()
+    full = p.ctx.draft([1, 2, 3], anchors, want_logits=True)
+    solo = p.ctx.draft([2], anchors[1:2].contiguous(), want_logits=True)
+    perm = p.ctx.draft([3, 1], anchors[[2, 0]].contiguous(), want_logits=True)
+    assert torch.equal(full["logits"][1], solo["logits"][0])
+    assert torch.equal(full["logits"][2], perm["logits"][0])
+    assert torch.equal(full["logits"][0], perm["logits"][1])
+    assert torch.equal(full["topk_idx"][1], solo["topk_idx"][0])
+
+
+def test_host_errors_change_no_state():
+    from block_diffusion_speculative_inject_gb300 import DFlashError
+    cfg = get_config("mini_bf16", n_layers=1)
+    p = Pair(cfg, _limits(max_batch=2, max_pages=3, max_positions=256, max_inject_rows=64))
+    p.inject([1], [100], "a", reset=True)             # 2 pages
+    free = p.ctx.free_pages()
+    feats = [f.cuda() for f in S.make_features(cfg, 130, 0, "b")]
+    with pytest.raises(DFlashError) as e:              # needs 3 more pages, 1 free
+        p.ctx.inject([2], [130], feats)
+    assert e.value.status == -2
+    assert p.ctx.free_pages() == free and p.ctx.context_len(1) == 100
+    with pytest.raises(DFlashError) as e:
+        p.ctx.draft([7], torch.zeros(1, dtype=torch.int32).cuda())
+    assert e.value.status == -3
+    with pytest.raises(DFlashError) as e:              # duplicate request in one call
+        p.ctx.draft([1, 1], torch.zeros(2, dtype=torch.int32).cuda())
+    assert e.value.status == -1
+    with pytest.raises(DFlashError) as e:              # beyond max_positions
+        p.ctx.inject([1], [200], [f[:1] for f in feats])
+    assert e.value.status == -1 and p.ctx.context_len(1) == 100
+    # a bad anchor id is caught on the device and reported by the next call
+    p.ctx.draft([1], torch.tensor([10 ** 6], dtype=torch.int32).cuda())
+    torch.cuda.synchronize()
+    with pytest.raises(DFlashError) as e:
+        p.ctx.draft([1], torch.zeros(1, dtype=torch.int32).cuda())
+    assert e.value.status == -5
+    p.ctx.draft([1], torch.zeros(1, dtype=torch.int32).cuda())   # flag cleared
+    # truncate / release return pages
+    p.ctx.truncate(1, 10)
+    assert p.ctx.free_pages() == free + 1
+    p.ctx.release(1)
+    assert p.ctx.free_pages() == 3
+
+
+# ----------------------------------------------------------------------------- full-size workload
+@pytest.mark.slow
+def test_q8b_b1_full_size_step():
+    """Qwen3-8B-shaped draft, batch 1, context 2048, K=15: two whole steps vs the oracle."""
+    cfg = get_config("q8b_b1")
+    _run_steps(cfg, _limits(max_batch=1, max_pages=40, max_positions=2304, max_inject_rows=2048),
+               [2048], steps=2, check_kv=False)
