@@ -30,12 +30,13 @@ Readings where the pages leave a step open (each is also listed in the design no
   * Block K/V are never written to the cache; after a verify the caller injects the
     anchor plus the accepted drafts (a + 1 positions).
   * RMSNorm: y = x / sqrt(mean(x^2) + eps) * w.
-  * Storage rounding ("contract points"): every stored activation is rounded to the
-    storage type (bf16, round-to-nearest-even, or fp32): the fc output, g, every GEMM
-    output (q, k, v, o-proj, gate, up, down, context K/V), normed activations, the
-    residual stream after each add, the SwiGLU product, the attention output and the
-    roped q/k. Logits are not rounded (they stay fp64 here, fp32 on the GPU); argmax
-    and top-k are decided on the logits rounded to fp32, ties to the lowest index.
+  * Precision: the stored operands of the method — weights, the target hidden states
+    and the context K/V cache — have the storage type (bf16 or fp32); the cache is
+    rounded to it (round-to-nearest-even) when written. Every other value (the fused
+    feature g, the residual stream, normed activations, q/k/v, attention, SwiGLU, the
+    final hidden rows, logits) is an activation carried at full precision: fp64 here,
+    fp32 (or an exact bf16 hi+lo pair as a tensor-core operand) on the GPU. Argmax and
+    top-k are decided on the logits rounded to fp32, ties to the lowest index.
   * top-k: k values sorted descending, indices tie-broken by lowest index.
 
 Parity status: every function here is pinned by the CPU tests (brute force, closed
@@ -79,7 +80,7 @@ def f32_round(x):
 
 
 def round_to(dtype):
-    """The storage rounding used at every contract point for the given storage dtype."""
+    """Rounding to the storage type (applied where the KV cache is written)."""
     if dtype == "bf16":
         return bf16_round
     if dtype == "f32":
@@ -147,27 +148,27 @@ class OracleDraft:
     def __init__(self, cfg, weights):
         self.cfg = cfg
         self.w = weights
-        self.r = round_to(cfg.dtype)
+        self.r = round_to(cfg.dtype)   # storage rounding of the KV cache
         self.cache = {}   # req -> {"K": [L arrays [n, nkv, hd]], "V": [...]}
 
     # -- context fusion and injection ([P1] Step 2-3, [P2] §2.2, [P3] §四, [P4] §5.1)
     def fuse(self, feats):
         """g = RMSNorm(concat_f(h_f) @ W_fc^T) for rows of n_feat hidden-state arrays."""
-        c, r = self.cfg, self.r
+        c = self.cfg
         cat = np.concatenate([_f64(f) for f in feats], axis=1)           # [n, n_feat*H_t]
-        fc_out = r(cat @ _f64(self.w["fc"]).T)                          # [n, H]
-        return r(rmsnorm(fc_out, self.w["fc_norm"], c.rms_eps))
+        fc_out = cat @ _f64(self.w["fc"]).T                             # [n, H]
+        return rmsnorm(fc_out, self.w["fc_norm"], c.rms_eps)
 
     def project_kv(self, g, pos, layer):
         """Context K/V of one draft layer for fused rows g at positions pos."""
         c, r, lw = self.cfg, self.r, self.w["layers"][layer]
         n = g.shape[0]
-        k = r(g @ _f64(lw["wk"]).T).reshape(n, c.n_kv_heads, c.head_dim)
-        v = r(g @ _f64(lw["wv"]).T).reshape(n, c.n_kv_heads, c.head_dim)
+        k = (g @ _f64(lw["wk"]).T).reshape(n, c.n_kv_heads, c.head_dim)
+        v = (g @ _f64(lw["wv"]).T).reshape(n, c.n_kv_heads, c.head_dim)
         if c.qk_norm:
             k = rmsnorm(k, lw["k_norm"], c.rms_eps)
-        k = r(rope(k, pos, c.rope_theta))
-        return k, v
+        # the cache stores K and V in the storage type
+        return r(rope(k, pos, c.rope_theta)), r(v)
 
     def inject(self, req, feats, reset=False):
         """Append the K/V of newly accepted positions (rows of feats) to req's cache."""
@@ -202,18 +203,18 @@ class OracleDraft:
 
     def layer(self, x, l, ctx_k, ctx_v, pos):
         """One pre-norm decoder layer over the block rows x [K+1, H]."""
-        c, r, lw = self.cfg, self.r, self.w["layers"][l]
+        c, lw = self.cfg, self.w["layers"][l]
         nq, nkv, hd = c.n_q_heads, c.n_kv_heads, c.head_dim
         q_rows = x.shape[0]
-        xn = r(rmsnorm(x, lw["in_norm"], c.rms_eps))
-        q = r(xn @ _f64(lw["wq"]).T).reshape(q_rows, nq, hd)
-        k = r(xn @ _f64(lw["wk"]).T).reshape(q_rows, nkv, hd)
-        v = r(xn @ _f64(lw["wv"]).T).reshape(q_rows, nkv, hd)
+        xn = rmsnorm(x, lw["in_norm"], c.rms_eps)
+        q = (xn @ _f64(lw["wq"]).T).reshape(q_rows, nq, hd)
+        k = (xn @ _f64(lw["wk"]).T).reshape(q_rows, nkv, hd)
+        v = (xn @ _f64(lw["wv"]).T).reshape(q_rows, nkv, hd)
         if c.qk_norm:
             q = rmsnorm(q, lw["q_norm"], c.rms_eps)
             k = rmsnorm(k, lw["k_norm"], c.rms_eps)
-        q = r(rope(q, pos, c.rope_theta))
-        k = r(rope(k, pos, c.rope_theta))
+        q = rope(q, pos, c.rope_theta)
+        k = rope(k, pos, c.rope_theta)
         # context K/V first, then the block's own K/V; no mask inside the block
         keys = np.concatenate([ctx_k, k], axis=0)         # [n_ctx + K + 1, nkv, hd]
         vals = np.concatenate([ctx_v, v], axis=0)
@@ -223,27 +224,24 @@ class OracleDraft:
             kvh = h // group
             s = (q[:, h, :] @ keys[:, kvh, :].T) / np.sqrt(hd)   # [K+1, n_keys]
             o[:, h, :] = softmax(s, axis=-1) @ vals[:, kvh, :]
-        o = r(o.reshape(q_rows, nq * hd))
-        x = r(x + r(o @ _f64(lw["wo"]).T))
-        xn2 = r(rmsnorm(x, lw["post_norm"], c.rms_eps))
-        gate = r(xn2 @ _f64(lw["w_gate"]).T)
-        up = r(xn2 @ _f64(lw["w_up"]).T)
-        hmid = r(silu(gate) * up)
-        x = r(x + r(hmid @ _f64(lw["w_down"]).T))
-        return x
+        o = o.reshape(q_rows, nq * hd)
+        x = x + o @ _f64(lw["wo"]).T
+        xn2 = rmsnorm(x, lw["post_norm"], c.rms_eps)
+        hmid = silu(xn2 @ _f64(lw["w_gate"]).T) * (xn2 @ _f64(lw["w_up"]).T)
+        return x + hmid @ _f64(lw["w_down"]).T
 
     def hidden(self, req, anchor):
         """Final-normed hidden rows of the K mask positions, [K, H]."""
-        c, r = self.cfg, self.r
+        c = self.cfg
         ent = self.cache[req]
         n_ctx = ent["K"][0].shape[0]
         toks = self.block_tokens(anchor)
-        x = r(_f64(self.w["embed"][toks]) * c.input_embedding_scale)
+        x = _f64(self.w["embed"][toks]) * c.input_embedding_scale
         pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
         for l in range(c.n_layers):
             x = self.layer(x, l, ent["K"][l], ent["V"][l], pos)
         # the anchor row yields no candidate ([P4] §4.3): only the K mask rows go on
-        return r(rmsnorm(x[1:], self.w["final_norm"], c.rms_eps))
+        return rmsnorm(x[1:], self.w["final_norm"], c.rms_eps)
 
     def logits(self, req, anchor, chunk=16384):
         """fp64 logits [K, V] of the K mask positions (LM head in vocabulary chunks)."""

@@ -460,3 +460,18 @@ def test_verify_sample_monte_carlo_matches_exact_law():
     # the first emitted token follows p(. | prefix) exactly; 5 sigma tolerance
     f = np.array([float(x) for x in first_exact])
     assert np.all(np.abs(counts / n - f) < 5 * np.sqrt(f * (1 - f) / n) + 1e-3)
+
+
+@pytest.mark.parametrize("dtype,rnd", [("bf16", O.bf16_round), ("f32", O.f32_round)])
+def test_cache_is_stored_in_the_storage_type_and_activations_are_not(dtype, rnd):
+    """The KV cache lands on the storage grid; g and the logits are carried unrounded."""
+    c = _cfg(dtype=dtype)
+    w = _weights(c, seed=31)
+    od = O.OracleDraft(c, w)
+    fe = _feats(c, 20, 32)
+    od.inject(0, fe)
+    for l in range(c.n_layers):
+        np.testing.assert_array_equal(rnd(od.cache[0]["K"][l]), od.cache[0]["K"][l])
+        np.testing.assert_array_equal(rnd(od.cache[0]["V"][l]), od.cache[0]["V"][l])
+    g = od.fuse(fe)
+    assert np.any(O.bf16_round(g) != g) and np.any(O.f32_round(g) != g)
