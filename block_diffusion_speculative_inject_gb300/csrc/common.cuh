@@ -38,16 +38,35 @@ __device__ __forceinline__ void raise_err(int *flag, int code) {
   if (flag) *(volatile int *)flag = code;
 }
 
+// ---------------------------------------------------------------- activation operands
+// Activations are fp32. Where an activation is the X operand of a GEMM it is written as
+// an "operand": fp32 for fp32 weights, or for bf16 weights an exact pair of bf16 planes
+// hi = bf16(v), lo = bf16(v - hi), so a bf16 tensor-core product W.hi + W.lo carries the
+// activation to ~2^-17 relative precision.
+struct OpOut {
+  void *hi;   // fp32 [rows, ld] when lo == nullptr, else bf16 [rows, ld]
+  void *lo;   // bf16 [rows, ld] or nullptr
+};
+
+__device__ __forceinline__ void write_op(const OpOut &o, size_t idx, float v) {
+  if (o.lo) {
+    bf16 h = __float2bfloat16_rn(v);
+    ((bf16 *)o.hi)[idx] = h;
+    ((bf16 *)o.lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+  } else {
+    ((float *)o.hi)[idx] = v;
+  }
+}
+
 // ---------------------------------------------------------------- GEMM description
-// Y[M, N] = epilogue( X[M, K] . W[N, K]^T ), X and W of the storage type.
-// X may be split along K into segments with separate base pointers (the fc fusion reads
-// the n_feat feature tensors in place); W may be split along N into segments (e.g. the
-// q/k/v or the per-layer k/v weights) each [rows, K] row-major with row stride K.
+// Y[M, N] = epilogue( X[M, K] . W[N, K]^T ) with fp32 output. W has the storage type.
+// X is fp32, bf16, or a bf16 hi/lo pair (x_lo non-null). X may be split along K into
+// segments with separate base pointers (the fc fusion reads the n_feat feature tensors in
+// place); W may be split along N into segments (the q/k/v weights, the per-layer k/v
+// weights, gate/up) each [rows, K] row-major with row stride K.
 enum GemmEpi : int {
-  EPI_STORE = 0,   // Y = round(acc)                                 (storage type)
-  EPI_RESID = 1,   // Y = round(R + round(acc))   (R may alias Y)     (storage type)
-  EPI_F32 = 2,     // Yf = acc                                       (fp32)
-  EPI_SWIGLU = 3,  // W = [gate; up] halves: Y[:, n] = round(silu(round(g)) * round(u)), N = 2*I
+  EPI_STORE = 0,   // Y = acc
+  EPI_RESID = 1,   // Y = R + acc   (R may alias Y)
 };
 
 constexpr int GEMM_MAX_XSEG = 8;
@@ -55,17 +74,19 @@ constexpr int GEMM_MAX_WSEG = 16;
 
 struct GemmDesc {
   int M, N, K;
+  int x_bf16;                    // 1: X planes are bf16, 0: fp32
   int n_xseg;
   const void *x[GEMM_MAX_XSEG];
+  const void *x_lo[GEMM_MAX_XSEG];   // lo plane (bf16 pair) or nullptr
   int x_k0[GEMM_MAX_XSEG + 1];   // K offset where segment s starts; x_k0[n_xseg] = K
   int ldx[GEMM_MAX_XSEG];        // row stride (elements) of each X segment
   int n_wseg;
   const void *w[GEMM_MAX_WSEG];
   int w_n0[GEMM_MAX_WSEG + 1];   // N offset where segment s starts; w_n0[n_wseg] = N
   int epi;
-  void *y;                       // output [M, ldy] (storage type, or fp32 for EPI_F32)
+  float *y;                      // output [M, ldy] fp32
   int ldy;
-  const void *resid;             // EPI_RESID input [M, ldy]
+  const float *resid;            // EPI_RESID input [M, ldy]
 };
 
 }  // namespace dflash

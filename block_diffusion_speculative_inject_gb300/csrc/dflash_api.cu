@@ -54,12 +54,15 @@ struct dflash_ctx {
   int max_pages_per_req = 0;
   float2 *rope = nullptr;
 
-  // draft scratch
-  void *x = nullptr, *xn = nullptr, *qkv = nullptr, *ao = nullptr, *gu = nullptr,
-       *hmid = nullptr, *xf = nullptr;
+  // draft scratch: fp32 activations; xn, ao, hmid, xf, g are GEMM operands (fp32, or a
+  // bf16 hi plane followed by a bf16 lo plane of the same row count)
+  float *x = nullptr, *qkv = nullptr, *gu = nullptr;
+  void *xn = nullptr, *ao = nullptr, *hmid = nullptr, *xf = nullptr;
   float *logits = nullptr, *part_o = nullptr, *part_ml = nullptr;
+  int rows_max = 0, rows_k_max = 0;
   // injection scratch
-  void *fc_out = nullptr, *g = nullptr, *kvproj = nullptr;
+  float *fc_out = nullptr, *kvproj = nullptr;
+  void *g = nullptr;
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -147,20 +150,31 @@ static dflash_status run_gemm(dflash_ctx *c, const GemmDesc &d, cudaStream_t s) 
   return DFLASH_OK;
 }
 
-static GemmDesc gemm_desc(int M, int N, int K, const void *x, int ldx, int epi, void *y, int ldy) {
+static GemmDesc gemm_desc(int M, int N, int K, int epi, float *y, int ldy) {
   GemmDesc d{};
   d.M = M;
   d.N = N;
   d.K = K;
-  d.n_xseg = 1;
-  d.x[0] = x;
-  d.x_k0[0] = 0;
-  d.x_k0[1] = K;
-  d.ldx[0] = ldx;
   d.epi = epi;
   d.y = y;
   d.ldy = ldy;
   return d;
+}
+
+// Operand view of a scratch buffer with `rows` x `ld` elements per plane.
+static OpOut op_of(const dflash_ctx *c, void *base, size_t plane_elems) {
+  if (c->dtype == DFLASH_BF16) return OpOut{base, (bf16 *)base + plane_elems};
+  return OpOut{base, nullptr};
+}
+
+static void set_x(const dflash_ctx *c, GemmDesc &d, const OpOut &o, int ld) {
+  d.x_bf16 = c->dtype == DFLASH_BF16;
+  d.n_xseg = 1;
+  d.x[0] = o.hi;
+  d.x_lo[0] = o.lo;
+  d.x_k0[0] = 0;
+  d.x_k0[1] = d.K;
+  d.ldx[0] = ld;
 }
 
 static void add_wseg(GemmDesc &d, const void *w, int rows) {
@@ -281,24 +295,27 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   const int R = cfg->max_batch * m.Q();
   const int RK = cfg->max_batch * m.K;
   const int C = cfg->max_inject_rows;
+  c->rows_max = R;
+  c->rows_k_max = RK;
+  const size_t f4 = sizeof(float);   // an operand element takes 4 bytes (fp32, or bf16 hi + lo)
   c->page_elems = (size_t)m.L * 2 * m.nkv * kPage * m.hd;
   c->max_pages_per_req = (cfg->max_positions + kPage - 1) / kPage;
   struct Alloc { void **p; size_t bytes; } allocs[] = {
       {&c->pool, (size_t)cfg->max_pages * c->page_elems * es},
       {(void **)&c->rope, (size_t)cfg->max_positions * (m.hd / 2) * sizeof(float2)},
-      {&c->x, (size_t)R * m.H * es},
-      {&c->xn, (size_t)R * m.H * es},
-      {&c->qkv, (size_t)R * m.qkv_dim() * es},
-      {&c->ao, (size_t)R * m.q_dim() * es},
-      {&c->gu, (size_t)R * 2 * m.I * es},
-      {&c->hmid, (size_t)R * m.I * es},
-      {&c->xf, (size_t)RK * m.H * es},
-      {(void **)&c->logits, (size_t)RK * m.V * sizeof(float)},
-      {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * sizeof(float)},
-      {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * sizeof(float)},
-      {&c->fc_out, (size_t)C * m.H * es},
-      {&c->g, (size_t)C * m.H * es},
-      {&c->kvproj, (size_t)C * m.L * 2 * m.kv_dim() * es},
+      {(void **)&c->x, (size_t)R * m.H * f4},
+      {&c->xn, (size_t)R * m.H * f4},
+      {(void **)&c->qkv, (size_t)R * m.qkv_dim() * f4},
+      {&c->ao, (size_t)R * m.q_dim() * f4},
+      {(void **)&c->gu, (size_t)R * 2 * m.I * f4},
+      {&c->hmid, (size_t)R * m.I * f4},
+      {&c->xf, (size_t)RK * m.H * f4},
+      {(void **)&c->logits, (size_t)RK * m.V * f4},
+      {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * f4},
+      {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * f4},
+      {(void **)&c->fc_out, (size_t)C * m.H * f4},
+      {&c->g, (size_t)C * m.H * f4},
+      {(void **)&c->kvproj, (size_t)C * m.L * 2 * m.kv_dim() * f4},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -479,8 +496,8 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     const int32_t *dslot = nullptr;
     if ((st = stage_upload(c, s, buf.data(), buf.size() * 4, &dslot)) != DFLASH_OK) return st;
     // fc over the n_feat feature tensors read in place (K segments)
-    GemmDesc d{};
-    d.M = n; d.N = m.H; d.K = F; d.epi = EPI_STORE; d.y = c->fc_out; d.ldy = m.H;
+    GemmDesc d = gemm_desc(n, m.H, F, EPI_STORE, c->fc_out, m.H);
+    d.x_bf16 = c->dtype == DFLASH_BF16;   // the features are exact storage-type values
     d.n_xseg = m.n_feat;
     for (int f = 0; f < m.n_feat; ++f) {
       d.x[f] = (const char *)feats[f] + (size_t)r0 * m.Ht * c->esz;
@@ -490,10 +507,12 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     d.x_k0[m.n_feat] = F;
     add_wseg(d, c->w.fc, m.H);
     if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
-    CK(c, launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, c->g, m.H, c->w.fc_norm, m.eps, 0, s));
+    OpOut g = op_of(c, c->g, (size_t)C * m.H);
+    CK(c, launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, g, m.H, c->w.fc_norm, m.eps, 0, s));
     c->launches++;
     // every layer's [Wk; Wv] in one GEMM
-    GemmDesc e = gemm_desc(n, kvw, m.H, c->g, m.H, EPI_STORE, c->kvproj, kvw);
+    GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, c->kvproj, kvw);
+    set_x(c, e, g, m.H);
     for (int l = 0; l < m.L; ++l) {
       add_wseg(e, c->layers[l].wk, m.kv_dim());
       add_wseg(e, c->layers[l].wv, m.kv_dim());
@@ -561,44 +580,53 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   DraftBatch bt{dd, dd + B, dd + 2 * B, dd + 3 * B, dd + 4 * B + 1, B, max_split};
 
   const int R = B * Q;
+  const OpOut xn = op_of(c, c->xn, (size_t)c->rows_max * m.H);
+  const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
+  const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
+  const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
   CK(c, launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x, c->err_d, s));
   c->launches++;
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
-    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, c->xn, m.H, lw.in_norm, m.eps, 0, s));
+    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s));
     c->launches++;
-    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, c->xn, m.H, EPI_STORE, c->qkv, m.qkv_dim());
+    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, c->qkv, m.qkv_dim());
+    set_x(c, d, xn, m.H);
     add_wseg(d, lw.wq, m.q_dim());
     add_wseg(d, lw.wk, m.kv_dim());
     add_wseg(d, lw.wv, m.kv_dim());
     if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
     CK(c, launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm, lw.k_norm, s));
     c->launches++;
-    CK(c, launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, c->ao, s));
+    CK(c, launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao, s));
     c->launches += 2;
-    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), c->ao, m.q_dim(), EPI_RESID, c->x, m.H);
+    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
+    set_x(c, o, ao, m.q_dim());
     o.resid = c->x;
     add_wseg(o, lw.wo, m.H);
     if ((st = run_gemm(c, o, s)) != DFLASH_OK) return st;
-    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, c->xn, m.H, lw.post_norm, m.eps, 0, s));
+    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s));
     c->launches++;
-    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, c->xn, m.H, EPI_STORE, c->gu, 2 * m.I);
+    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, c->gu, 2 * m.I);
+    set_x(c, gu, xn, m.H);
     add_wseg(gu, lw.w_gate, m.I);
     add_wseg(gu, lw.w_up, m.I);
     if ((st = run_gemm(c, gu, s)) != DFLASH_OK) return st;
-    CK(c, launch_swiglu(c->dtype, R, m.I, c->gu, c->hmid, s));
+    CK(c, launch_swiglu(R, m.I, c->gu, hm, s));
     c->launches++;
-    GemmDesc dn = gemm_desc(R, m.H, m.I, c->hmid, m.I, EPI_RESID, c->x, m.H);
+    GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_RESID, c->x, m.H);
+    set_x(c, dn, hm, m.I);
     dn.resid = c->x;
     add_wseg(dn, lw.w_down, m.H);
     if ((st = run_gemm(c, dn, s)) != DFLASH_OK) return st;
   }
   // final norm on the K mask rows only (the anchor row yields no candidate)
   const int RK = B * m.K;
-  CK(c, launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, c->xf, m.H, c->w.final_norm, m.eps, m.K, s));
+  CK(c, launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s));
   c->launches++;
   float *lg = logits ? logits : c->logits;
-  GemmDesc lm = gemm_desc(RK, m.V, m.H, c->xf, m.H, EPI_F32, lg, m.V);
+  GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
+  set_x(c, lm, xf, m.H);
   add_wseg(lm, c->w.lm_head, m.V);
   if ((st = run_gemm(c, lm, s)) != DFLASH_OK) return st;
   CK(c, launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s));

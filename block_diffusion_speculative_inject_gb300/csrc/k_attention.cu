@@ -17,7 +17,7 @@ constexpr int AT_PAGE = 64;
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(256) k_attn_split(
-    int L, int nq, int nkv, int Q, int layer, const T *qkv, const T *pool,
+    int L, int nq, int nkv, int Q, int layer, const float *qkv, const T *pool,
     const int32_t *ctx_len, const int32_t *n_split, const int32_t *split_len,
     const int32_t *page_off, const int32_t *pages, int max_split, float scale, float *part_o,
     float *part_ml) {
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) k_attn_split(
   for (int i = tid; i < R * HD; i += 256) {
     int r = i / HD, d = i % HD;
     int g = r / Q, j = r % Q;
-    qs[i] = to_f(qkv[(row0 + j) * qkv_dim + (size_t)(kvh * G + g) * HD + d]);
+    qs[i] = qkv[(row0 + j) * qkv_dim + (size_t)(kvh * G + g) * HD + d];
   }
 
   constexpr int DPL = HD / 32;                 // dims per lane in the PV accumulator
@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(256) k_attn_split(
           vval = to_f(pool[base + (size_t)nkv * AT_PAGE * HD]);
         } else {
           size_t r = row0 + (key - n_ctx);
-          kval = to_f(qkv[r * qkv_dim + (size_t)nq * HD + (size_t)kvh * HD + d]);
-          vval = to_f(qkv[r * qkv_dim + (size_t)nq * HD + kv_dim + (size_t)kvh * HD + d]);
+          kval = qkv[r * qkv_dim + (size_t)nq * HD + (size_t)kvh * HD + d];
+          vval = qkv[r * qkv_dim + (size_t)nq * HD + kv_dim + (size_t)kvh * HD + d];
         }
       }
       ks[kk * (HD + 1) + d] = kval;
@@ -122,9 +122,9 @@ __global__ void __launch_bounds__(256) k_attn_split(
 }
 
 // o[b*Q + j, h*HD + d] = sum_s acc_s * exp(m_s - M) / sum_s l_s * exp(m_s - M), in split order.
-template <typename T, int HD>
+template <int HD>
 __global__ void k_attn_combine(int nq, int Q, const int32_t *n_split, int max_split,
-                               const float *part_o, const float *part_ml, T *o) {
+                               const float *part_o, const float *part_ml, OpOut o) {
   int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   int b = blockIdx.y;
@@ -143,14 +143,14 @@ __global__ void k_attn_combine(int nq, int Q, const int32_t *n_split, int max_sp
     for (int d = 0; d < HD / 32; ++d) acc[d] += part_o[(base + s) * HD + lane + 32 * d] * c;
   }
   float inv = 1.f / Lsum;
-  T *dst = o + ((size_t)b * Q + j) * (nq * HD) + (size_t)h * HD;
+  size_t dst = ((size_t)b * Q + j) * (nq * HD) + (size_t)h * HD;
 #pragma unroll
-  for (int d = 0; d < HD / 32; ++d) dst[lane + 32 * d] = from_f<T>(acc[d] * inv);
+  for (int d = 0; d < HD / 32; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
 }
 
 template <typename T, int HD>
-static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer, const void *qkv,
-                             const void *pool, float *part_o, float *part_ml, void *o,
+static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer, const float *qkv,
+                             const void *pool, float *part_o, float *part_ml, OpOut o,
                              cudaStream_t s) {
   size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k_attn_split<T, HD>,
@@ -158,19 +158,18 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
   if (e != cudaSuccess) return e;
   dim3 g(bt.max_split, m.nkv, bt.B);
   k_attn_split<T, HD><<<g, 256, smem, s>>>(
-      m.L, m.nq, m.nkv, m.Q(), layer, (const T *)qkv, (const T *)pool, bt.ctx_len, bt.n_split,
+      m.L, m.nq, m.nkv, m.Q(), layer, qkv, (const T *)pool, bt.ctx_len, bt.n_split,
       bt.split_len, bt.page_off, bt.pages, bt.max_split, 1.f / sqrtf((float)HD), part_o, part_ml);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2((m.Q() * m.nq + 7) / 8, bt.B);
-  k_attn_combine<T, HD><<<g2, 256, 0, s>>>(m.nq, m.Q(), bt.n_split, bt.max_split, part_o, part_ml,
-                                            (T *)o);
+  k_attn_combine<HD><<<g2, 256, 0, s>>>(m.nq, m.Q(), bt.n_split, bt.max_split, part_o, part_ml, o);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &bt, int layer,
-                             const void *qkv, const void *pool, float *part_o, float *part_ml,
-                             void *o, cudaStream_t s) {
+                             const float *qkv, const void *pool, float *part_o, float *part_ml,
+                             OpOut o, cudaStream_t s) {
   if (bt.B <= 0) return cudaSuccess;
   if (m.hd == 128)
     return dtype ? attn_impl<bf16, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, s)

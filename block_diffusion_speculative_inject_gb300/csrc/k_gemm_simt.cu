@@ -3,12 +3,21 @@
 // This is the fp32-storage path (where tensor-core TF32 would not meet fp32 accuracy) and
 // the reference kernel the tensor-core path is checked against. Tile 32 (rows of X) x 64
 // (rows of W) x 32 (K), 256 threads, each thread 2 x 4 outputs. X may be split along K
-// into segments (the fc fusion reads each feature tensor in place); W may be split along N.
+// into segments (the fc fusion reads each feature tensor in place) and may be a bf16
+// hi/lo pair; W may be split along N.
 #include "kernels.h"
 
 namespace dflash {
 
 constexpr int SB_M = 32, SB_N = 64, SB_K = 32;
+
+template <typename T>
+__device__ __forceinline__ float load_x(const GemmDesc &d, int s, size_t idx) {
+  if (!d.x_bf16) return ((const float *)d.x[s])[idx];
+  float v = to_f(((const bf16 *)d.x[s])[idx]);
+  if (d.x_lo[s]) v += to_f(((const bf16 *)d.x_lo[s])[idx]);
+  return v;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
@@ -28,13 +37,12 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
   for (int k0 = 0; k0 < d.K; k0 += SB_K) {
     int xs_i = 0;
     while (xs_i + 1 < d.n_xseg && k0 >= d.x_k0[xs_i + 1]) ++xs_i;
-    const T *xbase = (const T *)d.x[xs_i];
     const int xk = k0 - d.x_k0[xs_i], ldx = d.ldx[xs_i];
     // X tile: 32 x 32
     for (int i = tid; i < SB_M * SB_K; i += 256) {
       int r = i / SB_K, c = i % SB_K;
       int m = m0 + r;
-      xs[c][r] = m < d.M ? to_f(xbase[(size_t)m * ldx + xk + c]) : 0.f;
+      xs[c][r] = m < d.M ? load_x<T>(d, xs_i, (size_t)m * ldx + xk + c) : 0.f;
     }
     // W tile: 64 x 32
     for (int i = tid; i < SB_N * SB_K; i += 256) {
@@ -66,21 +74,13 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
       if (n >= d.N) continue;
       float a = acc[i][j];
       size_t o = (size_t)m * d.ldy + n;
-      if (d.epi == EPI_F32) {
-        ((float *)d.y)[o] = a;
-      } else if (d.epi == EPI_RESID) {
-        float r = to_f(((const T *)d.resid)[o]);
-        ((T *)d.y)[o] = from_f<T>(r + round_st<T>(a));
-      } else {
-        ((T *)d.y)[o] = from_f<T>(a);
-      }
+      d.y[o] = d.epi == EPI_RESID ? d.resid[o] + a : a;
     }
   }
 }
 
 cudaError_t gemm_simt(int dtype, const GemmDesc &d, cudaStream_t s) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
-  if (d.epi == EPI_SWIGLU) return cudaErrorInvalidValue;   // composed by the caller
   dim3 g((d.N + SB_N - 1) / SB_N, (d.M + SB_M - 1) / SB_M);
   if (dtype) k_gemm_simt<bf16><<<g, 256, 0, s>>>(d);
   else k_gemm_simt<float><<<g, 256, 0, s>>>(d);

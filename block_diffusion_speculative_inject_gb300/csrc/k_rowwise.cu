@@ -19,7 +19,7 @@ __device__ __forceinline__ size_t pool_index(int page, int l, int kv, int h, int
 // §2.2; "DFlash：把串行 Draft 变成并行“填空”" §4).
 template <typename T>
 __global__ void k_embed(int H, int Q, int V, const int32_t *anchors, int mask_id, float scale,
-                        const T *embed, T *x, int *err) {
+                        const T *embed, float *x, int *err) {
   int r = blockIdx.x;
   int b = r / Q, j = r % Q;
   int tok = j == 0 ? anchors[b] : mask_id;
@@ -28,50 +28,47 @@ __global__ void k_embed(int H, int Q, int V, const int32_t *anchors, int mask_id
     tok = 0;
   }
   const T *src = embed + (size_t)tok * H;
-  T *dst = x + (size_t)r * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = from_f<T>(to_f(src[i]) * scale);
+  float *dst = x + (size_t)r * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = to_f(src[i]) * scale;
 }
 
 cudaError_t launch_embed(int dtype, const ModelDims &m, int B, const int32_t *anchors,
-                         int mask_id, const void *embed, void *x, int *err, cudaStream_t s) {
+                         int mask_id, const void *embed, float *x, int *err, cudaStream_t s) {
   dim3 g(B * m.Q());
   if (dtype) k_embed<bf16><<<g, 256, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
-                                             (const bf16 *)embed, (bf16 *)x, err);
+                                             (const bf16 *)embed, x, err);
   else k_embed<float><<<g, 256, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
-                                        (const float *)embed, (float *)x, err);
+                                        (const float *)embed, x, err);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------- RMSNorm
-// y = x * rsqrt(mean(x^2) + eps) * w, one warp per row.
-template <typename T>
-__global__ void k_rmsnorm(int rows, int H, const T *in, int ld_in, T *out, int ld_out,
-                          const T *w, float eps, int skip_k) {
+// y = x * rsqrt(mean(x^2) + eps) * w, one warp per row, written as a GEMM operand.
+template <typename TW>
+__global__ void k_rmsnorm(int rows, int H, const float *in, int ld_in, OpOut out, int ld_out,
+                          const TW *w, float eps, int skip_k) {
   int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   if (r >= rows) return;
   int src = skip_k > 0 ? (r / skip_k) * (skip_k + 1) + r % skip_k + 1 : r;
-  const T *xi = in + (size_t)src * ld_in;
+  const float *xi = in + (size_t)src * ld_in;
   float ss = 0.f;
-  for (int i = lane; i < H; i += 32) {
-    float v = to_f(xi[i]);
-    ss += v * v;
-  }
+  for (int i = lane; i < H; i += 32) ss += xi[i] * xi[i];
   ss = warp_sum(ss);
   float rs = rsqrtf(ss / (float)H + eps);
-  T *yo = out + (size_t)r * ld_out;
-  for (int i = lane; i < H; i += 32) yo[i] = from_f<T>(to_f(xi[i]) * rs * to_f(w[i]));
+  size_t o = (size_t)r * ld_out;
+  for (int i = lane; i < H; i += 32) write_op(out, o + i, xi[i] * rs * to_f(w[i]));
 }
 
-cudaError_t launch_rmsnorm(int dtype, int rows, int H, const void *in, int ld_in, void *out,
+cudaError_t launch_rmsnorm(int dtype, int rows, int H, const float *in, int ld_in, OpOut out,
                            int ld_out, const void *w, float eps, int skip_anchor_k,
                            cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   dim3 g((rows + 7) / 8);
-  if (dtype) k_rmsnorm<bf16><<<g, 256, 0, s>>>(rows, H, (const bf16 *)in, ld_in, (bf16 *)out,
-                                               ld_out, (const bf16 *)w, eps, skip_anchor_k);
-  else k_rmsnorm<float><<<g, 256, 0, s>>>(rows, H, (const float *)in, ld_in, (float *)out,
-                                          ld_out, (const float *)w, eps, skip_anchor_k);
+  if (dtype) k_rmsnorm<bf16><<<g, 256, 0, s>>>(rows, H, in, ld_in, out, ld_out, (const bf16 *)w,
+                                               eps, skip_anchor_k);
+  else k_rmsnorm<float><<<g, 256, 0, s>>>(rows, H, in, ld_in, out, ld_out, (const float *)w, eps,
+                                          skip_anchor_k);
   return cudaGetLastError();
 }
 
@@ -79,8 +76,8 @@ cudaError_t launch_rmsnorm(int dtype, int rows, int H, const void *in, int ld_in
 // One warp rotates one head vector of hd (64 or 128) values held as hd/32 per lane:
 // lane holds i = lane + 32*t; pairs are (i, i + hd/2) so for hd = 128 lane's t=0,1
 // pair with t=2,3 and for hd = 64 t=0 pairs with t=1.
-template <typename T>
-__device__ __forceinline__ void head_norm_rope(const T *src, T *dst, const T *nw, int hd,
+template <typename TW, typename TD>
+__device__ __forceinline__ void head_norm_rope(const float *src, TD *dst, const TW *nw, int hd,
                                                float eps, const float2 *rope_row, int lane) {
   float v[4];
   const int per = hd / 32;
@@ -88,7 +85,7 @@ __device__ __forceinline__ void head_norm_rope(const T *src, T *dst, const T *nw
 #pragma unroll
   for (int t = 0; t < 4; ++t)
     if (t < per) {
-      v[t] = to_f(src[lane + 32 * t]);
+      v[t] = src[lane + 32 * t];
       ss += v[t] * v[t];
     }
   if (nw) {
@@ -111,13 +108,13 @@ __device__ __forceinline__ void head_norm_rope(const T *src, T *dst, const T *nw
     }
 #pragma unroll
   for (int t = 0; t < 4; ++t)
-    if (t < per) dst[lane + 32 * t] = from_f<T>(o[t]);
+    if (t < per) dst[lane + 32 * t] = from_f<TD>(o[t]);
 }
 
-template <typename T>
+template <typename TW>
 __global__ void k_qk_norm_rope(int rows, int Q, int nq, int nkv, int hd, int qkv_dim,
-                               T *qkv, const int32_t *ctx_len, const float2 *rope,
-                               const T *q_norm, const T *k_norm, float eps) {
+                               float *qkv, const int32_t *ctx_len, const float2 *rope,
+                               const TW *q_norm, const TW *k_norm, float eps) {
   int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   int heads = nq + nkv;
@@ -125,12 +122,12 @@ __global__ void k_qk_norm_rope(int rows, int Q, int nq, int nkv, int hd, int qkv
   int r = w / heads, h = w % heads;
   int b = r / Q, j = r % Q;
   int pos = ctx_len[b] + j;
-  T *p = qkv + (size_t)r * qkv_dim + (size_t)h * hd;   // q heads then k heads are contiguous
-  const T *nw = h < nq ? q_norm : k_norm;
-  head_norm_rope<T>(p, p, nw, hd, eps, rope + (size_t)pos * (hd / 2), lane);
+  float *p = qkv + (size_t)r * qkv_dim + (size_t)h * hd;   // q heads then k heads are contiguous
+  const TW *nw = h < nq ? q_norm : k_norm;
+  head_norm_rope<TW, float>(p, p, nw, hd, eps, rope + (size_t)pos * (hd / 2), lane);
 }
 
-cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, void *qkv,
+cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, float *qkv,
                                 const int32_t *ctx_len, const float2 *rope,
                                 const void *q_norm, const void *k_norm, cudaStream_t s) {
   int rows = B * m.Q();
@@ -138,10 +135,10 @@ cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, void *qkv,
   dim3 g((warps + 7) / 8);
   const void *qn = m.qk_norm ? q_norm : nullptr, *kn = m.qk_norm ? k_norm : nullptr;
   if (dtype) k_qk_norm_rope<bf16><<<g, 256, 0, s>>>(rows, m.Q(), m.nq, m.nkv, m.hd, m.qkv_dim(),
-                                                    (bf16 *)qkv, ctx_len, rope, (const bf16 *)qn,
+                                                    qkv, ctx_len, rope, (const bf16 *)qn,
                                                     (const bf16 *)kn, m.eps);
   else k_qk_norm_rope<float><<<g, 256, 0, s>>>(rows, m.Q(), m.nq, m.nkv, m.hd, m.qkv_dim(),
-                                               (float *)qkv, ctx_len, rope, (const float *)qn,
+                                               qkv, ctx_len, rope, (const float *)qn,
                                                (const float *)kn, m.eps);
   return cudaGetLastError();
 }
@@ -154,7 +151,7 @@ cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, void *qkv,
 struct KNormPtrs { const void *p[16]; };
 
 template <typename T>
-__global__ void k_inject_kv(int T_rows, int L, int nkv, int hd, const T *kv, const int32_t *slot,
+__global__ void k_inject_kv(int T_rows, int L, int nkv, int hd, const float *kv, const int32_t *slot,
                             const int32_t *pos, const float2 *rope, KNormPtrs kn, int qk_norm,
                             float eps, T *pool) {
   int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -165,16 +162,16 @@ __global__ void k_inject_kv(int T_rows, int L, int nkv, int hd, const T *kv, con
   int kv_dim = nkv * hd;
   int sl = slot[t];
   int page = sl / PAGE, off = sl % PAGE;
-  const T *src_k = kv + (size_t)t * (L * 2 * kv_dim) + (size_t)l * 2 * kv_dim + (size_t)h * hd;
-  const T *src_v = src_k + kv_dim;
+  const float *src_k = kv + (size_t)t * (L * 2 * kv_dim) + (size_t)l * 2 * kv_dim + (size_t)h * hd;
+  const float *src_v = src_k + kv_dim;
   T *dk = pool + pool_index(page, l, 0, h, off, L, nkv, hd);
   T *dv = pool + pool_index(page, l, 1, h, off, L, nkv, hd);
   const T *nw = qk_norm ? (const T *)kn.p[l] : nullptr;
-  head_norm_rope<T>(src_k, dk, nw, hd, eps, rope + (size_t)pos[t] * (hd / 2), lane);
-  for (int i = lane; i < hd; i += 32) dv[i] = src_v[i];
+  head_norm_rope<T, T>(src_k, dk, nw, hd, eps, rope + (size_t)pos[t] * (hd / 2), lane);
+  for (int i = lane; i < hd; i += 32) dv[i] = from_f<T>(src_v[i]);
 }
 
-cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const void *kv,
+cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const float *kv,
                              const int32_t *slot, const int32_t *pos, const float2 *rope,
                              const void *const *k_norms, void *pool, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
@@ -182,30 +179,27 @@ cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const void *k
   for (int l = 0; l < m.L && l < 16; ++l) kn.p[l] = k_norms[l];
   long warps = (long)T * m.L * m.nkv;
   dim3 g((unsigned)((warps + 7) / 8));
-  if (dtype) k_inject_kv<bf16><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, (const bf16 *)kv, slot, pos,
-                                                 rope, kn, m.qk_norm, m.eps, (bf16 *)pool);
-  else k_inject_kv<float><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, (const float *)kv, slot, pos,
-                                            rope, kn, m.qk_norm, m.eps, (float *)pool);
+  if (dtype) k_inject_kv<bf16><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, kv, slot, pos, rope, kn,
+                                                 m.qk_norm, m.eps, (bf16 *)pool);
+  else k_inject_kv<float><<<g, 256, 0, s>>>(T, m.L, m.nkv, m.hd, kv, slot, pos, rope, kn,
+                                            m.qk_norm, m.eps, (float *)pool);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------- SwiGLU
-// gu rows hold [gate (I) | up (I)], both already rounded GEMM outputs; h = silu(g) * u.
-template <typename T>
-__global__ void k_swiglu(long n, int I, const T *gu, T *h) {
+// gu rows hold [gate (I) | up (I)] in fp32; h = silu(gate) * up as a GEMM operand.
+__global__ void k_swiglu(long n, int I, const float *gu, OpOut h) {
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   long r = i / I, c = i % I;
-  float g = to_f(gu[r * 2 * I + c]), u = to_f(gu[r * 2 * I + I + c]);
-  h[i] = from_f<T>(g / (1.f + expf(-g)) * u);
+  float g = gu[r * 2 * I + c], u = gu[r * 2 * I + I + c];
+  write_op(h, i, g / (1.f + expf(-g)) * u);
 }
 
-cudaError_t launch_swiglu(int dtype, int rows, int I, const void *gu, void *h, cudaStream_t s) {
+cudaError_t launch_swiglu(int rows, int I, const float *gu, OpOut h, cudaStream_t s) {
   long n = (long)rows * I;
   if (n == 0) return cudaSuccess;
-  dim3 g((unsigned)((n + 255) / 256));
-  if (dtype) k_swiglu<bf16><<<g, 256, 0, s>>>(n, I, (const bf16 *)gu, (bf16 *)h);
-  else k_swiglu<float><<<g, 256, 0, s>>>(n, I, (const float *)gu, (float *)h);
+  k_swiglu<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(n, I, gu, h);
   return cudaGetLastError();
 }
 

@@ -22,37 +22,40 @@ struct DraftBatch {
   int max_split;
 };
 
-// dtype: 0 = fp32, 1 = bf16 (matches dflash_dtype)
+// dtype (storage type of weights / features / cache): 0 = fp32, 1 = bf16.
 cudaError_t gemm_simt(int dtype, const GemmDesc &d, cudaStream_t s);
 
+// x[b*(K+1) + j] = embed[token] * scale, token = anchor (j = 0) or mask id; fp32 out.
 cudaError_t launch_embed(int dtype, const ModelDims &m, int B, const int32_t *anchors,
-                         int mask_id, const void *embed, void *x, int *err, cudaStream_t s);
+                         int mask_id, const void *embed, float *x, int *err, cudaStream_t s);
 
-// out row r <- rmsnorm(in row map(r)); map(r) = r, or with skip_anchor_k = K > 0 the
-// K mask rows of each (K+1)-row block: (r / K) * (K + 1) + r % K + 1.
-cudaError_t launch_rmsnorm(int dtype, int rows, int H, const void *in, int ld_in, void *out,
+// out row r <- rmsnorm(in row map(r)) as a GEMM operand; map(r) = r, or with
+// skip_anchor_k = K > 0 the K mask rows of each (K+1)-row block:
+// (r / K) * (K + 1) + r % K + 1.
+cudaError_t launch_rmsnorm(int dtype, int rows, int H, const float *in, int ld_in, OpOut out,
                            int ld_out, const void *w, float eps, int skip_anchor_k,
                            cudaStream_t s);
 
-// In place on qkv rows [B*(K+1), qkv_dim]: per-head q/k RMSNorm (if enabled) + RoPE at
-// position ctx_len[b] + j, rounded to the storage type.
-cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, void *qkv,
+// In place on fp32 qkv rows [B*(K+1), qkv_dim]: per-head q/k RMSNorm (if enabled) + RoPE
+// at position ctx_len[b] + j.
+cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, float *qkv,
                                 const int32_t *ctx_len, const float2 *rope,
                                 const void *q_norm, const void *k_norm, cudaStream_t s);
 
-// Injection epilogue: kv rows [T, L*2*kv_dim] (per layer [k | v]) -> k-norm + RoPE at
-// pos[t] -> KV pool slot[t] (page * 64 + offset) in every layer.
-cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const void *kv,
+// Injection epilogue: fp32 kv rows [T, L*2*kv_dim] (per layer [k | v]) -> k-norm + RoPE at
+// pos[t] -> KV pool slot[t] (page * 64 + offset) of every layer, in the storage type.
+cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const float *kv,
                              const int32_t *slot, const int32_t *pos, const float2 *rope,
                              const void *const *k_norms, void *pool, cudaStream_t s);
 
-cudaError_t launch_swiglu(int dtype, int rows, int I, const void *gu, void *h, cudaStream_t s);
+// h = silu(gate) * up from fp32 rows [gate (I) | up (I)], written as a GEMM operand.
+cudaError_t launch_swiglu(int rows, int I, const float *gu, OpOut h, cudaStream_t s);
 
 // Split-KV attention of the query block of each request over its paged context plus the
-// block's own K/V, then the split combine into o [B*(K+1), q_dim].
+// block's own K/V, then the split combine into the operand o [B*(K+1), q_dim].
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &b, int layer,
-                             const void *qkv, const void *pool, float *part_o, float *part_ml,
-                             void *o, cudaStream_t s);
+                             const float *qkv, const void *pool, float *part_o, float *part_ml,
+                             OpOut o, cudaStream_t s);
 
 // Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V].
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
