@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Throughput of the DFlash batched draft step on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole hot path over one batch: incremental KV injection of the
+newly accepted positions of every request, the draft forward of the query blocks with the
+LM head's argmax/top-k, and the greedy verification. Inputs (weights, features, anchors,
+target ids) are seeded synthetic tensors resident in HBM before the timed region; the
+weights (GBs) are larger than L2, so every step streams them from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config q8b_b1] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
+replicas: the step has no exchange between requests), timing is the max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synth import get_config  # noqa: E402
+from synth import inputs as S  # noqa: E402
+
+WORKLOAD_TEXT = {
+    "q8b_b1": "Qwen3-8B-shaped bf16 draft (5 layers, H 4096, 32/8 heads x 128, SwiGLU 12288, "
+              "V 151936, 5 features 20480->4096), batch 1, context 2048, K=15",
+    "q8b_b32": "Qwen3-8B-shaped bf16 draft, batch 32, ragged contexts U[512, 8192], K=15",
+    "q4b_b128": "Qwen3-4B-shaped bf16 draft, batch 128, context 1024, K=7",
+    "q27b_b8": "27B-target-shaped bf16 draft, batch 8, context 32768, K=15",
+    "mini_bf16": "small bf16 draft (parity shape)",
+    "tiny_f32": "tiny fp32 draft (parity shape)",
+}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(ws, v, device):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workload
+class Workload:
+    """Seeded inputs of one workload, resident on the device before timing."""
+
+    def __init__(self, cfg, steps, seed=0, device="cuda:0"):
+        self.cfg = cfg
+        self.device = device
+        self.B = cfg.batch
+        self.reqs = list(range(self.B))
+        self.ctx = S.make_context_lengths(cfg, seed)
+        self.n_new = [S.make_n_new(cfg, self.B, seed, s) for s in range(steps)]
+        self.anchors = [S.make_anchors(cfg, self.B, seed, s + 1) for s in range(steps)]
+        zeros = torch.zeros((self.B, cfg.block_k), dtype=torch.int32)
+        # the synthetic target stands in for the target model; its ids are drawn up front
+        self.targets = [S.make_targets(cfg, zeros, seed, s, p=0.0) for s in range(steps)]
+        self.feats = []
+        for s in range(steps):
+            parts = [S.make_features(cfg, n, seed, "step", s, r) for r, n in zip(self.reqs, self.n_new[s])]
+            self.feats.append([torch.cat([p[f] for p in parts], 0) for f in range(cfg.n_feat)])
+
+    def max_positions(self):
+        return max(self.ctx) + self.cfg.n_new_max + self.cfg.block_k + 2
+
+    def to_device(self):
+        d = self.device
+        self.anchors_d = [a.to(d) for a in self.anchors]
+        self.targets_d = [t.to(d) for t in self.targets]
+        self.feats_d = [[f.to(d) for f in fs] for fs in self.feats]
+
+    def pinned(self):
+        self.anchors_h = [a.pin_memory() for a in self.anchors]
+        self.targets_h = [t.pin_memory() for t in self.targets]
+        self.feats_h = [[f.pin_memory() for f in fs] for fs in self.feats]
+
+
+def _make_context(cfg, wl, device):
+    from block_diffusion_speculative_inject_gb300 import Context, Limits
+    pages = sum((c + cfg.n_new_max + 63) // 64 + 1 for c in wl.ctx) + 16
+    lim = Limits(max_batch=wl.B, max_requests=wl.B, max_pages=pages,
+                 max_positions=wl.max_positions(), max_inject_rows=8192)
+    w = S.make_weights(cfg, 0)
+    wg = {k: v.to(device) for k, v in w.items() if k != "layers"}
+    wg["layers"] = [{k: v.to(device) for k, v in lw.items()} for lw in w["layers"]]
+    ctx = Context(cfg, wg, lim, device=torch.device(device).index or 0)
+    return ctx, w
+
+
+def _prefill(ctx, cfg, wl):
+    for r, n in zip(wl.reqs, wl.ctx):
+        feats = [f.to(wl.device) for f in S.make_features(cfg, n, 0, "prefill", r)]
+        ctx.inject([r], [n], feats, reset=True)
+    torch.cuda.synchronize()
+
+
+def _step(ctx, wl, s, out, feats, anchors, targets):
+    """One step: bring each request back to its context length minus the new positions,
+    inject them, draft, verify."""
+    for r, c, n in zip(wl.reqs, wl.ctx, wl.n_new[s]):
+        ctx.truncate(r, c - n)
+    ctx.inject(wl.reqs, wl.n_new[s], feats)
+    ctx.draft(wl.reqs, anchors, argmax=out["argmax"], topk_idx=out["topk_idx"],
+              topk_val=out["topk_val"])
+    ctx.verify(out["argmax"], targets, out["acc"], out["toks"], out["nxt"])
+
+
+def _algorithmic(cfg, wl, steps):
+    """Algorithmic flops and HBM bytes of the timed steps (weights once per step, every
+    context K/V once per layer, features of the injected rows)."""
+    H, F, V, L = cfg.hidden, cfg.feat_dim, cfg.vocab, cfg.n_layers
+    kvw = L * 2 * cfg.kv_dim
+    Q, K = cfg.block_k + 1, cfg.block_k
+    w_bytes = 2 * (L * cfg.layer_params() + V * H + H * F + L * 0)  # layers, LM head, fc
+    flops = byts = 0.0
+    for s in range(steps):
+        n = sum(wl.n_new[s])
+        flops += 2.0 * n * (F * H + kvw * H)
+        flops += 2.0 * wl.B * Q * L * (cfg.layer_params() - 2 * H - 2 * cfg.head_dim)
+        flops += 2.0 * wl.B * K * V * H
+        flops += sum(4.0 * Q * cfg.n_q_heads * cfg.head_dim * (c + Q) * L for c in wl.ctx)
+        byts += w_bytes + sum(c * L * 2 * cfg.kv_dim * 2 for c in wl.ctx) + n * F * 2
+        byts += n * kvw * 2   # cache writes
+    return flops, byts
+
+
+def run_ours(args):
+    ws, rank, local = _dist()
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    cfg = get_config(args.config)
+    steps = args.warmup + args.steps
+    wl = Workload(cfg, steps, seed=0, device=device)
+    wl.to_device()
+    ctx, w_cpu = _make_context(cfg, wl, device)
+    _prefill(ctx, cfg, wl)
+    B, K, k = wl.B, cfg.block_k, cfg.topk
+    out = dict(argmax=torch.empty((B, K), dtype=torch.int32, device=device),
+               topk_idx=torch.empty((B, K, k), dtype=torch.int32, device=device),
+               topk_val=torch.empty((B, K, k), dtype=torch.float32, device=device),
+               acc=torch.empty((B,), dtype=torch.int32, device=device),
+               toks=torch.empty((B, K + 1), dtype=torch.int32, device=device),
+               nxt=torch.empty((B,), dtype=torch.int32, device=device))
+    stream = torch.cuda.current_stream()
+    for s in range(args.warmup):
+        _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+    torch.cuda.synchronize()
+    ctx.timing_read()            # drop anything recorded so far
+    ctx.timing_enable(True)
+    launches0 = ctx.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for s in range(args.warmup, steps):
+            _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    launches = ctx.launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+    kern = ctx.timing_read()
+    ctx.timing_enable(False)
+    ms_max = _max_over_ranks(ws, ms, device)
+
+    # end to end through host buffers: H2D of the step's inputs, D2H of its results
+    e2e = None
+    if not args.no_e2e:
+        wl.pinned()
+        host_out = dict(argmax=torch.empty((B, K), dtype=torch.int32).pin_memory(),
+                        acc=torch.empty((B,), dtype=torch.int32).pin_memory(),
+                        toks=torch.empty((B, K + 1), dtype=torch.int32).pin_memory())
+        dev_f = [torch.empty_like(f, device=device) for f in wl.feats_d[0]]
+        anc_d = torch.empty((B,), dtype=torch.int32, device=device)
+        tgt_d = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+        h2d = d2h = 0
+        _barrier(ws)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for s in range(args.warmup, steps):
+            fs = []
+            for f in wl.feats_h[s]:
+                d = torch.empty(f.shape, dtype=f.dtype, device=device)
+                d.copy_(f, non_blocking=True)
+                fs.append(d)
+                h2d += f.numel() * f.element_size()
+            anc_d.copy_(wl.anchors_h[s], non_blocking=True)
+            tgt_d.copy_(wl.targets_h[s], non_blocking=True)
+            h2d += wl.anchors_h[s].numel() * 4 + wl.targets_h[s].numel() * 4
+            _step(ctx, wl, s, out, fs, anc_d, tgt_d)
+            host_out["argmax"].copy_(out["argmax"], non_blocking=True)
+            host_out["acc"].copy_(out["acc"], non_blocking=True)
+            host_out["toks"].copy_(out["toks"], non_blocking=True)
+            d2h += (B * K + B + B * (K + 1)) * 4
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1), device)
+        e2e = {"value": ws * B * K * args.steps / (e2e_ms / 1e3), "unit": "draft tok/s",
+               "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps,
+               "ms_per_step": e2e_ms / args.steps, "host_wall_ms_per_step": wall * 1e3 / args.steps}
+        del dev_f
+
+    if rank != 0:
+        return
+    hbm, tf, tf_sus, src = _peaks()
+    gemm_cls = [c for c in kern if c.startswith("gemm_")]
+    g_ms = sum(kern[c]["ms"] for c in gemm_cls)
+    g_bytes = sum(kern[c]["bytes"] for c in gemm_cls)
+    g_flops = sum(kern[c]["flops"] for c in gemm_cls)
+    g_launch = sum(kern[c]["launches"] for c in gemm_cls)
+    total_k_ms = sum(v["ms"] for v in kern.values())
+    achieved = g_bytes / (g_ms / 1e3) / 1e9
+    roofline = {"kernel": "gemm (all weight-streaming GEMMs of the step)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                "avg_launch_us": round(g_ms * 1e3 / max(1, g_launch), 2),
+                "algorithmic_bytes_per_launch": round(g_bytes / max(1, g_launch)),
+                "tensor_tflops": round(g_flops / (g_ms / 1e3) / 1e12, 2)}
+    flops, byts = _algorithmic(cfg, wl, args.steps)
+    t_roof = max(flops / (tf * 1e12), byts / (hbm * 1e9))
+    step_roof = {"flops_per_step": flops / args.steps, "bytes_per_step": byts / args.steps,
+                 "roofline_us_per_step": t_roof * 1e6 / args.steps,
+                 "bound": "tensor" if flops / (tf * 1e12) > byts / (hbm * 1e9) else "hbm",
+                 "frac": round(t_roof / (ms / 1e3), 4)}
+    kernels = {c: {"ms_per_step": round(v["ms"] / args.steps, 4), "share": round(v["ms"] / total_k_ms, 4),
+                   "launches_per_step": v["launches"] / args.steps}
+               for c, v in sorted(kern.items(), key=lambda kv: -kv[1]["ms"])}
+    tok = ws * B * K * args.steps / (ms_max / 1e3)
+    res = {
+        "metric": "draft_tokens_per_s", "value": round(tok, 1), "unit": "draft tok/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 4),
+        "us_per_step": round(ms_max * 1e3 / args.steps, 1),
+        "steps_per_s": round(ws * args.steps / (ms_max / 1e3), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded N(0,0.02) weights, N(0,1) target hidden states, uniform ids",
+        "config": {"workload": f"{cfg.name}: {WORKLOAD_TEXT.get(cfg.name, cfg.name)}", "batch": B,
+                   "context": wl.ctx if B <= 8 else [min(wl.ctx), max(wl.ctx)], "K": K,
+                   "new_positions_per_step": f"U[1,{cfg.n_new_max}] per request",
+                   "l2": "inputs larger than L2: every step streams all weights (GBs) from HBM",
+                   "parallelism": f"{ws} independent replica(s)"},
+        "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
+        "e2e": e2e, "gpu_launches": launches,
+    }
+    res["clocks"] = clk.summary()
+    if not args.no_cpu_baseline and ws >= 1:
+        res["cpu_baseline"] = cpu_baseline(cfg, wl, w_cpu)
+    print(json.dumps(res), flush=True)
+
+
+# ----------------------------------------------------------------------------- the oracle arm
+def _oracle_setup(cfg, wl, w_cpu):
+    import numpy as np
+    import oracle as O
+    wn = {k: v.float().numpy() for k, v in w_cpu.items() if k != "layers"}
+    wn["layers"] = [{k: v.float().numpy() for k, v in lw.items()} for lw in w_cpu["layers"]]
+    orc = O.OracleDraft(cfg, wn)
+    r = wl.reqs[0]
+    orc.inject(r, [f.double().numpy() for f in S.make_features(cfg, wl.ctx[0], 0, "prefill", r)])
+    return orc, np
+
+
+def _oracle_step(orc, np, cfg, wl, s):
+    """The oracle's step for request 0 of the workload: inject, draft, verify."""
+    import oracle as O
+    r = wl.reqs[0]
+    n = wl.n_new[s][0]
+    orc.truncate(r, wl.ctx[0] - n)
+    orc.inject(r, [f[:n].double().numpy() for f in wl.feats[s]])
+    am, idx, val, lg = orc.draft(r, int(wl.anchors[s][0]))
+    O.verify_greedy(am[None], wl.targets[s][:1].numpy())
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(cfg, wl, w_cpu):
+    orc, np = _oracle_setup(cfg, wl, w_cpu)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        _oracle_step(orc, np, cfg, wl, n % len(wl.n_new))
+        n += 1
+        if time.perf_counter() - t0 > 10 or n >= 3:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(cfg.block_k / dt, 3), "unit": "draft tok/s", "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"{n} step(s) of request 0 of {cfg.name} (inject n_new + draft of K={cfg.block_k} "
+                      f"+ verify) on the fp64 numpy oracle; one request of a batch of {wl.B}"}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    cfg = get_config(args.config)
+    steps = args.warmup + args.steps
+    wl = Workload(cfg, steps, seed=0, device="cpu")
+    w_cpu = S.make_weights(cfg, 0)
+    orc, np = _oracle_setup(cfg, wl, w_cpu)
+    for s in range(args.warmup):
+        _oracle_step(orc, np, cfg, wl, s)
+    t0 = time.perf_counter()
+    for s in range(args.warmup, steps):
+        _oracle_step(orc, np, cfg, wl, s)
+    dt = time.perf_counter() - t0
+    v = cfg.block_k * args.steps / dt
+    res = {"impl": "reference", "metric": "draft_tokens_per_s", "value": round(v, 3),
+           "unit": "draft tok/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt * 1e3 / args.steps, 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: seeded N(0,0.02) weights, N(0,1) target hidden states, uniform ids",
+           "config": {"workload": f"{cfg.name}: {WORKLOAD_TEXT.get(cfg.name, cfg.name)}",
+                      "sample": "request 0 of the batch per step"},
+           "cpu_baseline": {"value": round(v, 3), "unit": "draft tok/s", "cores": _cores(),
+                            "kind": "oracle", "sample": f"request 0 of {cfg.name} per step"},
+           "e2e": {"value": round(v, 3), "unit": "draft tok/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="q8b_b1")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        from __graft_entry__ import build
+        build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -189,6 +189,24 @@ class Context:
     def launch_count(self):
         return self.lib.dflash_launch_count(self.h)
 
+    def timing_enable(self, on=True):
+        self._check(self.lib.dflash_timing_enable(self.h, 1 if on else 0))
+
+    def timing_read(self):
+        """{class: dict(ms, launches, bytes, flops)} accumulated since the last read."""
+        n = self.lib.dflash_timing_classes()
+        ms = (ctypes.c_double * n)()
+        la = (ctypes.c_int64 * n)()
+        by = (ctypes.c_double * n)()
+        fl = (ctypes.c_double * n)()
+        self._check(self.lib.dflash_timing_read(self.h, ms, la, by, fl, n))
+        out = {}
+        for i in range(n):
+            if la[i]:
+                out[self.lib.dflash_timing_class_name(i).decode()] = dict(
+                    ms=ms[i], launches=la[i], bytes=by[i], flops=fl[i])
+        return out
+
 
 # ----------------------------------------------------------------- C-named functions
 def dflash_create(cfg, weights, limits: Limits, device=0):

@@ -52,6 +52,11 @@ SIGNATURES = {
     "dflash_last_error": (ctypes.c_char_p, [_P]),
     "dflash_status_string": (ctypes.c_char_p, [_I32]),
     "dflash_launch_count": (ctypes.c_int64, [_P]),
+    "dflash_timing_enable": (_I32, [_P, _I32]),
+    "dflash_timing_classes": (_I32, []),
+    "dflash_timing_class_name": (ctypes.c_char_p, [_I32]),
+    "dflash_timing_read": (_I32, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _I32]),
 }
 
 _lib = None

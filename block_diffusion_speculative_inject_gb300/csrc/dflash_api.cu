@@ -35,6 +35,22 @@ struct Req {
 };
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Kernel classes of the timing records.
+enum KCls : int {
+  K_GEMM_FC, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_LMHEAD,
+  K_ATTN, K_RMSNORM, K_ROPE, K_INJECT_KV, K_SWIGLU, K_EMBED, K_TOPK, K_VERIFY, K_EXPORT, K_NUM
+};
+const char *kClsName[K_NUM] = {"gemm_fc", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup",
+                               "gemm_down", "gemm_lmhead", "attention", "rmsnorm", "qk_norm_rope",
+                               "inject_kv", "swiglu", "embed", "topk", "verify", "export_kv"};
+
+struct TimeRec {
+  int cls;
+  cudaEvent_t a, b;
+  double bytes, flops;
+  int launches;
+};
 }  // namespace
 
 struct dflash_ctx {
@@ -72,6 +88,10 @@ struct dflash_ctx {
   TcGemm *tc = nullptr;   // tensor-core GEMM plans (bf16 only)
   std::string last_error;
   int64_t launches = 0;
+
+  bool timing = false;
+  std::vector<TimeRec> recs;
+  std::vector<cudaEvent_t> spare_events;
 };
 
 // ------------------------------------------------------------------------------ helpers
@@ -120,6 +140,37 @@ static dflash_status check_device_flag(dflash_ctx *c) {
   return DFLASH_OK;
 }
 
+static cudaEvent_t take_event(dflash_ctx *c) {
+  if (!c->spare_events.empty()) {
+    cudaEvent_t e = c->spare_events.back();
+    c->spare_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs one launch (or a fixed group of launches) of kernel class `cls`; with timing on it
+// is bracketed by events on its stream and tagged with its algorithmic bytes and flops.
+template <typename F>
+static cudaError_t timed(dflash_ctx *c, int cls, cudaStream_t s, double bytes, double flops,
+                         int n_launch, F &&launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (c->timing) {
+    a = take_event(c);
+    b = take_event(c);
+    cudaEventRecord(a, s);
+  }
+  cudaError_t e = launch();
+  c->launches += n_launch;
+  if (c->timing) {
+    cudaEventRecord(b, s);
+    c->recs.push_back(TimeRec{cls, a, b, bytes, flops, n_launch});
+  }
+  return e;
+}
+
 static dflash_status stage_upload(dflash_ctx *c, cudaStream_t s, const void *src, size_t bytes,
                                   const int32_t **dev_out) {
   if (bytes > c->stage_cap)
@@ -136,17 +187,19 @@ static dflash_status stage_upload(dflash_ctx *c, cudaStream_t s, const void *src
   return DFLASH_OK;
 }
 
-static dflash_status run_gemm(dflash_ctx *c, const GemmDesc &d, cudaStream_t s) {
+static dflash_status run_gemm(dflash_ctx *c, int cls, const GemmDesc &d, cudaStream_t s) {
+  const double xsz = (d.x_bf16 && !d.x_lo[0]) ? 2.0 : 4.0;
+  const double bytes = (double)d.N * d.K * c->esz + (double)d.M * d.K * xsz +
+                       (double)d.M * d.N * 4.0 * (d.epi == EPI_RESID ? 2 : 1);
+  const double flops = 2.0 * d.M * d.N * d.K;
   if (c->tc && c->dtype == DFLASH_BF16) {
-    int n = 0;
-    cudaError_t e = tc_gemm_run(c->tc, d, s, &n);
+    int n = tc_gemm_launches(c->tc, d);
+    cudaError_t e = timed(c, cls, s, bytes, flops, n, [&] { return tc_gemm_run(c->tc, d, s); });
     if (e != cudaSuccess)
       return set_err(c, DFLASH_ERR_CUDA, "tensor-core GEMM launch failed: %s", cudaGetErrorString(e));
-    c->launches += n;
     return DFLASH_OK;
   }
-  CK(c, gemm_simt(c->dtype, d, s));
-  c->launches += 1;
+  CK(c, timed(c, cls, s, bytes, flops, 1, [&] { return gemm_simt(c->dtype, d, s); }));
   return DFLASH_OK;
 }
 
@@ -245,6 +298,11 @@ static void free_all(dflash_ctx *c) {
   }
   if (c->err_h) cudaFreeHost(c->err_h);
   if (c->tc) tc_gemm_destroy(c->tc);
+  for (const TimeRec &r : c->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : c->spare_events) cudaEventDestroy(e);
 }
 
 extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_weights *w,
@@ -506,10 +564,11 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     }
     d.x_k0[m.n_feat] = F;
     add_wseg(d, c->w.fc, m.H);
-    if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
+    if ((st = run_gemm(c, K_GEMM_FC, d, s)) != DFLASH_OK) return st;
     OpOut g = op_of(c, c->g, (size_t)C * m.H);
-    CK(c, launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, g, m.H, c->w.fc_norm, m.eps, 0, s));
-    c->launches++;
+    CK(c, timed(c, K_RMSNORM, s, 8.0 * n * m.H, 4.0 * n * m.H, 1, [&] {
+         return launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, g, m.H, c->w.fc_norm, m.eps, 0, s);
+       }));
     // every layer's [Wk; Wv] in one GEMM
     GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, c->kvproj, kvw);
     set_x(c, e, g, m.H);
@@ -517,10 +576,11 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
       add_wseg(e, c->layers[l].wk, m.kv_dim());
       add_wseg(e, c->layers[l].wv, m.kv_dim());
     }
-    if ((st = run_gemm(c, e, s)) != DFLASH_OK) return st;
-    CK(c, launch_inject_kv(c->dtype, m, n, c->kvproj, dslot, dslot + n, c->rope, knorm.data(),
-                           c->pool, s));
-    c->launches++;
+    if ((st = run_gemm(c, K_GEMM_KV, e, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_INJECT_KV, s, (double)n * kvw * (4.0 + c->esz), 8.0 * n * kvw, 1, [&] {
+         return launch_inject_kv(c->dtype, m, n, c->kvproj, dslot, dslot + n, c->rope,
+                                 knorm.data(), c->pool, s);
+       }));
   }
   return DFLASH_OK;
 }
@@ -572,6 +632,15 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   desc[4 * B] = off;
   for (int b = 0; b < B; ++b) desc.insert(desc.end(), rq[b]->pages.begin(), rq[b]->pages.end());
 
+  // algorithmic work of one layer's attention: read every context K/V once, 4 flops per
+  // (query row, head, dim, key) for scores and the weighted sum
+  double attn_bytes = 0, attn_flops = 0;
+  for (int b = 0; b < B; ++b) {
+    double S = (double)rq[b]->len + Q;
+    attn_bytes += (double)rq[b]->len * 2 * m.kv_dim() * c->esz + (double)Q * (m.q_dim() + 2 * m.kv_dim()) * 4 +
+                  (double)Q * m.q_dim() * 4;
+    attn_flops += 4.0 * Q * m.nq * m.hd * S;
+  }
   DeviceGuard guard(c->device);
   if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
   cudaStream_t s = (cudaStream_t)stream;
@@ -584,53 +653,62 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
   const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
   const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
-  CK(c, launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x, c->err_d, s));
-  c->launches++;
+  CK(c, timed(c, K_EMBED, s, (double)R * m.H * (c->esz + 4), (double)R * m.H, 1, [&] {
+       return launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x,
+                           c->err_d, s);
+     }));
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
-    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s));
-    c->launches++;
+    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
+         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s);
+       }));
     GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, c->qkv, m.qkv_dim());
     set_x(c, d, xn, m.H);
     add_wseg(d, lw.wq, m.q_dim());
     add_wseg(d, lw.wk, m.kv_dim());
     add_wseg(d, lw.wv, m.kv_dim());
-    if ((st = run_gemm(c, d, s)) != DFLASH_OK) return st;
-    CK(c, launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm, lw.k_norm, s));
-    c->launches++;
-    CK(c, launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao, s));
-    c->launches += 2;
+    if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_ROPE, s, 8.0 * R * (m.nq + m.nkv) * m.hd, 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
+         return launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
+                                    lw.k_norm, s);
+       }));
+    CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, 2, [&] {
+         return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao, s);
+       }));
     GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
     set_x(c, o, ao, m.q_dim());
     o.resid = c->x;
     add_wseg(o, lw.wo, m.H);
-    if ((st = run_gemm(c, o, s)) != DFLASH_OK) return st;
-    CK(c, launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s));
-    c->launches++;
+    if ((st = run_gemm(c, K_GEMM_O, o, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
+         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s);
+       }));
     GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, c->gu, 2 * m.I);
     set_x(c, gu, xn, m.H);
     add_wseg(gu, lw.w_gate, m.I);
     add_wseg(gu, lw.w_up, m.I);
-    if ((st = run_gemm(c, gu, s)) != DFLASH_OK) return st;
-    CK(c, launch_swiglu(R, m.I, c->gu, hm, s));
-    c->launches++;
+    if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_SWIGLU, s, 12.0 * R * m.I, 5.0 * R * m.I, 1,
+                [&] { return launch_swiglu(R, m.I, c->gu, hm, s); }));
     GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_RESID, c->x, m.H);
     set_x(c, dn, hm, m.I);
     dn.resid = c->x;
     add_wseg(dn, lw.w_down, m.H);
-    if ((st = run_gemm(c, dn, s)) != DFLASH_OK) return st;
+    if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
   }
   // final norm on the K mask rows only (the anchor row yields no candidate)
   const int RK = B * m.K;
-  CK(c, launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s));
-  c->launches++;
+  CK(c, timed(c, K_RMSNORM, s, 8.0 * RK * m.H, 4.0 * RK * m.H, 1, [&] {
+       return launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s);
+     }));
   float *lg = logits ? logits : c->logits;
   GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
   set_x(c, lm, xf, m.H);
   add_wseg(lm, c->w.lm_head, m.V);
-  if ((st = run_gemm(c, lm, s)) != DFLASH_OK) return st;
-  CK(c, launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s));
-  c->launches++;
+  if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+  CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
+       return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s);
+     }));
   return DFLASH_OK;
 }
 
@@ -648,9 +726,11 @@ extern "C" dflash_status dflash_verify_greedy(dflash_ctx *c, void *stream, int32
     return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
   DeviceGuard guard(c->device);
   if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
-  CK(c, launch_verify(n_req, c->m.K, draft, target, accept_len, out_tokens, next_anchor,
-                      (cudaStream_t)stream));
-  c->launches++;
+  CK(c, timed(c, K_VERIFY, (cudaStream_t)stream, 4.0 * n_req * (3 * c->m.K + 4), (double)n_req * c->m.K, 1,
+              [&] {
+                return launch_verify(n_req, c->m.K, draft, target, accept_len, out_tokens,
+                                     next_anchor, (cudaStream_t)stream);
+              }));
   return DFLASH_OK;
 }
 
@@ -671,7 +751,45 @@ extern "C" dflash_status dflash_export_kv(dflash_ctx *c, void *stream, int32_t r
   cudaStream_t s = (cudaStream_t)stream;
   const int32_t *dp = nullptr;
   if ((st = stage_upload(c, s, q.pages.data(), q.pages.size() * 4, &dp)) != DFLASH_OK) return st;
-  CK(c, launch_export_kv(c->dtype, c->m, layer, pos0, n, dp, c->pool, k_out, v_out, s));
-  c->launches++;
+  CK(c, timed(c, K_EXPORT, s, 4.0 * n * c->m.kv_dim() * c->esz, 0.0, 1, [&] {
+       return launch_export_kv(c->dtype, c->m, layer, pos0, n, dp, c->pool, k_out, v_out, s);
+     }));
   return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------------------ timing
+extern "C" dflash_status dflash_timing_enable(dflash_ctx *c, int32_t enable) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  c->timing = enable != 0;
+  return DFLASH_OK;
+}
+
+extern "C" int32_t dflash_timing_classes(void) { return K_NUM; }
+
+extern "C" const char *dflash_timing_class_name(int32_t cls) {
+  return (cls >= 0 && cls < K_NUM) ? kClsName[cls] : "";
+}
+
+extern "C" dflash_status dflash_timing_read(dflash_ctx *c, double *ms, int64_t *launches,
+                                            double *bytes, double *flops, int32_t n) {
+  if (!c || n < 0) return DFLASH_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  dflash_status st = DFLASH_OK;
+  for (const TimeRec &r : c->recs) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+    if (e != cudaSuccess && st == DFLASH_OK)
+      st = set_err(c, DFLASH_ERR_CUDA, "timing event: %s", cudaGetErrorString(e));
+    if (r.cls < n) {
+      if (ms) ms[r.cls] += t;
+      if (launches) launches[r.cls] += r.launches;
+      if (bytes) bytes[r.cls] += r.bytes;
+      if (flops) flops[r.cls] += r.flops;
+    }
+    c->spare_events.push_back(r.a);
+    c->spare_events.push_back(r.b);
+  }
+  c->recs.clear();
+  return st;
 }

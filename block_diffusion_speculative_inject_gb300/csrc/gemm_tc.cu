@@ -5,5 +5,6 @@ namespace dflash {
 struct TcGemm { int dummy; };
 cudaError_t tc_gemm_create(TcGemm **out, int, int) { *out = nullptr; return cudaSuccess; }
 void tc_gemm_destroy(TcGemm *t) { delete t; }
-cudaError_t tc_gemm_run(TcGemm *, const GemmDesc &, cudaStream_t, int *) { return cudaErrorNotSupported; }
+int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 0; }
+cudaError_t tc_gemm_run(TcGemm *, const GemmDesc &, cudaStream_t) { return cudaErrorNotSupported; }
 }  // namespace dflash

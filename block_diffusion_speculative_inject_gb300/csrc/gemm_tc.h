@@ -10,7 +10,9 @@ struct TcGemm;
 // nullptr, in which case callers use the FFMA GEMM.
 cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms);
 void tc_gemm_destroy(TcGemm *t);
-// Runs Y = epilogue(X . W^T) for bf16 X, W; *launches receives the kernel count.
-cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s, int *launches);
+// Number of kernel launches tc_gemm_run issues for this GEMM.
+int tc_gemm_launches(const TcGemm *t, const GemmDesc &d);
+// Runs Y = epilogue(X . W^T) for bf16 W and a bf16 (or bf16 hi/lo pair) X.
+cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s);
 
 }  // namespace dflash

@@ -199,6 +199,18 @@ const char *dflash_status_string(dflash_status s);
 /* Number of kernel launches this context has issued so far (all calls). */
 int64_t dflash_launch_count(const dflash_ctx *ctx);
 
+/* Kernel timing (tracing). With timing enabled every kernel launch is bracketed by CUDA
+ * events on its stream and tagged with a kernel class and its algorithmic bytes and
+ * flops. dflash_timing_read synchronises on the recorded events, adds the elapsed time
+ * per class into ms[i] (milliseconds), launches[i], bytes[i], flops[i] for
+ * i < min(n, dflash_timing_classes()) (any of the arrays may be NULL), then clears the
+ * records. Enabling adds two event records per launch. */
+dflash_status dflash_timing_enable(dflash_ctx *ctx, int32_t enable);
+int32_t dflash_timing_classes(void);
+const char *dflash_timing_class_name(int32_t cls);
+dflash_status dflash_timing_read(dflash_ctx *ctx, double *ms, int64_t *launches, double *bytes,
+                                 double *flops, int32_t n);
+
 #ifdef __cplusplus
 }
 #endif
