@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <unordered_map>
@@ -412,8 +413,10 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
     return fail(DFLASH_ERR_CUDA);
   *c->err_h = 0;
 
-  if (c->dtype == DFLASH_BF16) {
-    cudaError_t e = tc_gemm_create(&c->tc, device, c->num_sms);
+  // bf16 weights use the tensor-core GEMM; DFLASH_FORCE_FFMA=1 (diagnostics) keeps the FFMA one
+  const char *force_ffma = getenv("DFLASH_FORCE_FFMA");
+  if (c->dtype == DFLASH_BF16 && !(force_ffma && force_ffma[0] == '1')) {
+    cudaError_t e = tc_gemm_create(&c->tc, device, c->num_sms, c->err_d);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA);
   }
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(DFLASH_ERR_CUDA);

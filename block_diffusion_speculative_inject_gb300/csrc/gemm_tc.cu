@@ -1,10 +1,488 @@
-// Tensor-core GEMM (placeholder until the tcgen05 kernel lands): disabled.
+// Tensor-core GEMM on sm_103a: tcgen05.mma with the accumulator in TMEM, operands staged
+// in shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle), an mbarrier pipeline.
+//
+//   Y[m, n] = sum_k X[m, k] * W[n, k]      (W: bf16 weights [N, K]; X: bf16 activations)
+//
+// The draft step multiplies few token rows (16 at batch 1) by large weight matrices, so
+// the product is computed transposed ("swap AB"): a CTA owns 128 weight rows (the UMMA M
+// dimension) and BN token rows (the UMMA N dimension, 16..128), and streams its weight
+// slab through the pipeline once. When X is an exact bf16 hi/lo pair (an fp32 activation),
+// both planes are multiplied by the same staged weight tile and accumulate into the same
+// TMEM columns, so the weights are read from HBM once. Small grids are split along K
+// (split-K) so every SM streams weights; the fp32 partials are summed in a fixed order by
+// a second kernel that also applies the epilogue.
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 owns the TMEM allocation and
+// its lane 0 issues the MMAs, warps 2-5 (one per 32-lane TMEM quarter) run the epilogue.
+// Every mbarrier wait is bounded in time; on expiry the kernel raises the device error
+// flag, drains its own TMA loads and frees its TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <tuple>
+#include <vector>
+
 #include "gemm_tc.h"
 
 namespace dflash {
-struct TcGemm { int dummy; };
-cudaError_t tc_gemm_create(TcGemm **out, int, int) { *out = nullptr; return cudaSuccess; }
-void tc_gemm_destroy(TcGemm *t) { delete t; }
-int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 0; }
-cudaError_t tc_gemm_run(TcGemm *, const GemmDesc &, cudaStream_t) { return cudaErrorNotSupported; }
+
+constexpr int TC_BM = 128;            // weight rows per tile (UMMA M)
+constexpr int TC_BK = 64;             // K per pipeline stage: 64 bf16 = one 128-byte row
+constexpr int TC_MAX_WSEG = 16;
+constexpr int TC_MAX_XMAP = 8;
+constexpr int TC_THREADS = 192;
+constexpr unsigned long long TC_WAIT_NS = 2000000000ull;   // 2 s bound on any wait
+
+struct TcParams {
+  CUtensorMap wmap[TC_MAX_WSEG];      // one per weight segment, box {64, 128}
+  CUtensorMap xmap[TC_MAX_XMAP];      // X segments (box {64, BN}); split: [0] hi, [1] lo
+  int n_wseg;
+  int w_n0[TC_MAX_WSEG + 1];
+  int n_xseg;
+  int x_k0[TC_MAX_XMAP + 1];
+  int split;                          // X is a hi/lo pair
+  int M, N, K;
+  int kb_total, kb_per, S;
+  int stages;
+  int epi;
+  float *y;
+  int ldy;
+  const float *resid;
+  float *ws;                          // [S][M][N] partials when S > 1
+  int *err;
+};
+
+// ------------------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false when the CTA was aborted or the wait ran out of time (which aborts).
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort_flag,
+                                          int *err) {
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > TC_WAIT_NS) {
+      *abort_flag = 1;
+      raise_err(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle layout: rows of
+// 128 bytes, 8-row atoms 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+template <int BN>
+constexpr int tmem_cols() {
+  return BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+}
+
+// ------------------------------------------------------------------------- the kernel
+template <int BN>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+  constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+  const uint32_t stage_bytes = A_BYTES + B_BYTES * (p.split ? 2 : 1);
+  const int stages = p.stages;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t tiles = (raw + 1023u) & ~1023u;           // 1024-byte aligned tile base
+  uint8_t *gen_tiles = smem_raw + (tiles - raw);
+  uint64_t *bars = (uint64_t *)(gen_tiles + (size_t)stages * stage_bytes);
+  const uint32_t full0 = smem_u32(bars);                   // full[s]  = full0 + 8 s
+  const uint32_t empty0 = full0 + 8u * stages;             // empty[s] = empty0 + 8 s
+  const uint32_t accf = empty0 + 8u * stages;
+  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * stages + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
+  const int kb0 = split * p.kb_per;
+  const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(accf, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols<BN>());
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0 && nkb > 0) {
+    // ---------------- TMA producer
+    int ws = 0;
+    while (ws + 1 < p.n_wseg && n0 >= p.w_n0[ws + 1]) ++ws;
+    const CUtensorMap *wm = &p.wmap[ws];
+    const int wrow = n0 - p.w_n0[ws];
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % stages, u = i / stages;
+      if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err)) break;
+      const uint32_t st = tiles + (uint32_t)s * stage_bytes;
+      const uint32_t fb = full0 + 8u * s;
+      mbar_expect_tx(fb, stage_bytes);
+      const int k = (kb0 + i) * TC_BK;
+      tma_load_2d(st, wm, k, wrow, fb);
+      if (p.split) {
+        tma_load_2d(st + A_BYTES, &p.xmap[0], k, m0, fb);
+        tma_load_2d(st + A_BYTES + B_BYTES, &p.xmap[1], k, m0, fb);
+      } else {
+        int xs = 0;
+        while (xs + 1 < p.n_xseg && k >= p.x_k0[xs + 1]) ++xs;
+        tma_load_2d(st + A_BYTES, &p.xmap[xs], k - p.x_k0[xs], m0, fb);
+      }
+      issued = i + 1;
+    }
+    // drain: every load this thread issued has landed before the CTA may exit
+    for (int s = 0; s < stages && s < issued; ++s) {
+      const int last = s + stages * ((issued - 1 - s) / stages);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(full0 + 8u * s, (last / stages) & 1) && global_ns() - t0 < TC_WAIT_NS) {
+      }
+    }
+  } else if (warp == 1 && lane == 0 && nkb > 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(TC_BM, BN);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % stages, u = i / stages;
+      if (!mbar_wait(full0 + 8u * s, u & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t a = tiles + (uint32_t)s * stage_bytes;
+      const uint32_t b = a + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; ++kk)
+        umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+      if (p.split) {
+#pragma unroll
+        for (int kk = 0; kk < TC_BK / 16; ++kk)
+          umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + B_BYTES + kk * 32), idesc, 1u);
+      }
+      umma_commit(empty0 + 8u * s);       // frees the stage once these MMAs have read it
+    }
+    umma_commit(accf);                    // accumulator complete (all MMAs issued above)
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> global
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err);
+    tc_fence_after();
+    const int n = n0 + q * 32 + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+      tmem_ld_wait();
+      if (!ok || n >= p.N) continue;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = m0 + c0 + j;
+        if (m >= p.M) break;
+        const float v = __uint_as_float(r[j]);
+        if (p.S > 1) {
+          p.ws[((size_t)split * p.M + m) * p.N + n] = v;
+        } else {
+          const size_t o = (size_t)m * p.ldy + n;
+          p.y[o] = p.epi == EPI_RESID ? p.resid[o] + v : v;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols<BN>());
+  }
+}
+
+// Sum of the S split-K partials in split order, then the epilogue.
+__global__ void k_splitk_reduce(int M, int N, int S, const float *__restrict__ ws, int epi,
+                                float *y, int ldy, const float *resid) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long)M * N) return;
+  const int m = (int)(i / N), n = (int)(i % N);
+  float a = 0.f;
+  for (int s = 0; s < S; ++s) a += ws[((size_t)s * M + m) * N + n];
+  const size_t o = (size_t)m * ldy + n;
+  y[o] = epi == EPI_RESID ? resid[o] + a : a;
+}
+
+// ------------------------------------------------------------------------- host side
+struct TcGemm {
+  int device = 0, num_sms = 0;
+  int *err = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
+  float *ws = nullptr;
+  size_t ws_bytes = 0;
+  bool attr_set[4] = {false, false, false, false};
+};
+
+cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag) {
+  *out = nullptr;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+  TcGemm *t = new TcGemm();
+  t->device = device;
+  t->num_sms = num_sms;
+  t->encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  t->err = err_flag;
+  *out = t;
+  return cudaSuccess;
+}
+
+void tc_gemm_destroy(TcGemm *t) {
+  if (!t) return;
+  if (t->ws) cudaFree(t->ws);
+  delete t;
+}
+
+// bf16 2-D tensor map over a row-major [rows, cols] matrix with row stride ld (elements),
+// box {64, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool get_map(TcGemm *t, const void *ptr, long rows, long cols, long ld, int box_rows,
+                    CUtensorMap *out) {
+  auto key = std::make_tuple(ptr, rows, cols, ld, box_rows);
+  auto it = t->maps.find(key);
+  if (it != t->maps.end()) {
+    *out = it->second;
+    return true;
+  }
+  CUtensorMap m;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = t->encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (t->maps.size() > 4096) t->maps.clear();
+  t->maps.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+struct Plan {
+  int bn, t_tiles, n_tiles, kb, kb_per, S, stages;
+  size_t smem;
+};
+
+static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
+  Plan p{};
+  p.bn = d.M <= 16 ? 16 : d.M <= 32 ? 32 : d.M <= 64 ? 64 : 128;
+  p.t_tiles = (d.M + p.bn - 1) / p.bn;
+  p.n_tiles = (d.N + TC_BM - 1) / TC_BM;
+  p.kb = d.K / TC_BK;
+  const int base = p.t_tiles * p.n_tiles;
+  const int target = 2 * t->num_sms;
+  int S = (target + base - 1) / base;
+  S = std::max(1, std::min(S, std::min(32, p.kb / 4)));
+  p.kb_per = (p.kb + S - 1) / S;
+  p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
+  const bool split = d.x_lo[0] != nullptr;
+  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * (split ? 2 : 1);
+  const size_t budget = p.bn <= 32 ? 100 * 1024 : 200 * 1024;
+  p.stages = (int)std::max<size_t>(2, std::min<size_t>(8, budget / stage));
+  p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 1) + 16;
+  return p;
+}
+
+int tc_gemm_launches(const TcGemm *t, const GemmDesc &d) {
+  return plan_for(t, d).S > 1 ? 2 : 1;
+}
+
+template <int BN>
+static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan &pl, cudaStream_t s) {
+  if (!t->attr_set[slot]) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    t->attr_set[slot] = true;
+  }
+  dim3 grid(pl.t_tiles, pl.n_tiles, pl.S);
+  k_gemm_tc<BN><<<grid, TC_THREADS, pl.smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
+  if (d.M <= 0 || d.N <= 0) return cudaSuccess;
+  if (!d.x_bf16 || d.K % TC_BK || d.n_wseg > TC_MAX_WSEG || d.n_xseg > TC_MAX_XMAP ||
+      (d.x_lo[0] && d.n_xseg != 1))
+    return cudaErrorInvalidValue;
+  const Plan pl = plan_for(t, d);
+  TcParams p;   // kernel parameters (copied at launch)
+  memset(&p, 0, sizeof(p));
+  p.n_wseg = d.n_wseg;
+  for (int i = 0; i < d.n_wseg; ++i) {
+    const long rows = d.w_n0[i + 1] - d.w_n0[i];
+    if (!get_map(t, d.w[i], rows, d.K, d.K, TC_BM, &p.wmap[i])) return cudaErrorInvalidValue;
+    p.w_n0[i] = d.w_n0[i];
+  }
+  p.w_n0[d.n_wseg] = d.w_n0[d.n_wseg];
+  p.split = d.x_lo[0] != nullptr;
+  p.n_xseg = d.n_xseg;
+  if (p.split) {
+    if (!get_map(t, d.x[0], d.M, d.K, d.ldx[0], pl.bn, &p.xmap[0]) ||
+        !get_map(t, d.x_lo[0], d.M, d.K, d.ldx[0], pl.bn, &p.xmap[1]))
+      return cudaErrorInvalidValue;
+    p.x_k0[0] = 0;
+    p.x_k0[1] = d.K;
+  } else {
+    for (int i = 0; i < d.n_xseg; ++i) {
+      const long cols = d.x_k0[i + 1] - d.x_k0[i];
+      if (cols % TC_BK) return cudaErrorInvalidValue;
+      if (!get_map(t, d.x[i], d.M, cols, d.ldx[i], pl.bn, &p.xmap[i])) return cudaErrorInvalidValue;
+      p.x_k0[i] = d.x_k0[i];
+    }
+    p.x_k0[d.n_xseg] = d.x_k0[d.n_xseg];
+  }
+  p.M = d.M;
+  p.N = d.N;
+  p.K = d.K;
+  p.kb_total = pl.kb;
+  p.kb_per = pl.kb_per;
+  p.S = pl.S;
+  p.stages = pl.stages;
+  p.epi = d.epi;
+  p.y = d.y;
+  p.ldy = d.ldy;
+  p.resid = d.resid;
+  p.err = t->err;
+  if (pl.S > 1) {
+    const size_t need = (size_t)pl.S * d.M * d.N * sizeof(float);
+    if (need > t->ws_bytes) {
+      if (t->ws) cudaFree(t->ws);
+      t->ws = nullptr;
+      t->ws_bytes = 0;
+      cudaError_t e = cudaMalloc(&t->ws, need);
+      if (e != cudaSuccess) return e;
+      t->ws_bytes = need;
+    }
+    p.ws = t->ws;
+  }
+  cudaError_t e;
+  switch (pl.bn) {
+    case 16: e = launch_bn<16>(t, 0, p, pl, s); break;
+    case 32: e = launch_bn<32>(t, 1, p, pl, s); break;
+    case 64: e = launch_bn<64>(t, 2, p, pl, s); break;
+    default: e = launch_bn<128>(t, 3, p, pl, s); break;
+  }
+  if (e != cudaSuccess || pl.S == 1) return e;
+  const long n = (long)d.M * d.N;
+  k_splitk_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d.M, d.N, pl.S, t->ws, d.epi, d.y,
+                                                               d.ldy, d.resid);
+  return cudaGetLastError();
+}
+
 }  // namespace dflash

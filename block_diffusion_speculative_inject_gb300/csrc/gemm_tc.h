@@ -6,9 +6,9 @@ namespace dflash {
 
 struct TcGemm;
 
-// Creates the per-context GEMM state (driver entry points, SM count). *out may be set to
-// nullptr, in which case callers use the FFMA GEMM.
-cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms);
+// Creates the per-context GEMM state (driver entry point for tensor maps, SM count, the
+// device error flag its bounded waits raise).
+cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag);
 void tc_gemm_destroy(TcGemm *t);
 // Number of kernel launches tc_gemm_run issues for this GEMM.
 int tc_gemm_launches(const TcGemm *t, const GemmDesc &d);

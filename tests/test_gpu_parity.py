@@ -113,7 +113,7 @@ def test_mini_bf16_empty_context_and_page_edges():
 
 
 # ----------------------------------------------------------------------------- invariants on the GPU
-def test_incremental_injection_bit_identical_to_one_shot():
+def test_incremental_injection_equals_one_shot():
     cfg = get_config("mini_bf16")
     w = S.make_weights(cfg, 3)
     lim = _limits(max_batch=2, max_pages=16, max_positions=512, max_inject_rows=40)
@@ -129,13 +129,21 @@ def test_incremental_injection_bit_identical_to_one_shot():
         m = min(int(torch.randint(1, 17, (1,), generator=g)), n - s)
         b.ctx.inject([1], [m], [f[s:s + m].contiguous() for f in fg])
         s += m
+    # The GEMM's split-K factor follows the row count of each call, so the fp32 sums differ in
+    # order between chunkings; the stored bf16 K/V then agree except for rare rounding flips
+    # of one unit in the last place.
     for l in range(cfg.n_layers):
-        ka, va = a.ctx.export_kv(1, l, 0, n)
-        kb, vb = b.ctx.export_kv(1, l, 0, n)
-        assert torch.equal(ka, kb) and torch.equal(va, vb)
+        for x, y in zip(a.ctx.export_kv(1, l, 0, n), b.ctx.export_kv(1, l, 0, n)):
+            x, y = x.float(), y.float()
+            assert torch.mean((x == y).float()).item() > 0.999
+            ulp = torch.abs(x) * 2.0 ** -7 + 1e-30
+            assert torch.all(torch.abs(x - y) <= ulp + 1e-6)
 
 
 def test_results_independent_of_batch_composition():
+    """A request's logits do not depend on which other requests share the step. The split-K
+    factor of a GEMM depends on the batch's row count, so agreement is to fp32 summation
+    order (well inside the oracle tolerance), and the argmax must not move."""
     cfg = get_config("mini_bf16")
     w = S.make_weights(cfg, 6)
     lim = _limits(max_batch=4, max_pages=32, max_positions=512, max_inject_rows=128)
@@ -146,10 +154,36 @@ def test_results_independent_of_batch_composition():
     full = p.ctx.draft([1, 2, 3], anchors, want_logits=True)
     solo = p.ctx.draft([2], anchors[1:2].contiguous(), want_logits=True)
     perm = p.ctx.draft([3, 1], anchors[[2, 0]].contiguous(), want_logits=True)
-    assert torch.equal(full["logits"][1], solo["logits"][0])
-    assert torch.equal(full["logits"][2], perm["logits"][0])
-    assert torch.equal(full["logits"][0], perm["logits"][1])
-    assert torch.equal(full["topk_idx"][1], solo["topk_idx"][0])
+    for a, b in [(full["logits"][1], solo["logits"][0]), (full["logits"][2], perm["logits"][0]),
+                 (full["logits"][0], perm["logits"][1])]:
+        assert torch.max(torch.abs(a - b)).item() < 1e-4
+    assert torch.equal(full["argmax"][1], solo["argmax"][0])
+    assert torch.equal(full["argmax"][2], perm["argmax"][0])
+    assert torch.equal(full["argmax"][0], perm["argmax"][1])
+
+
+def test_tensor_core_gemm_matches_ffma_gemm(monkeypatch):
+    """The tcgen05 path and the FFMA path of the same bf16 context agree closely, over a
+    batch whose 144 block rows span two token tiles, a ragged vocabulary and split-K."""
+    cfg = get_config("mini_bf16")
+    w = S.make_weights(cfg, 8)
+    lim = _limits(max_batch=9, max_pages=64, max_positions=512, max_inject_rows=700)
+    lens = [50 + 29 * i for i in range(9)]
+    outs = []
+    for force in ("0", "1"):
+        monkeypatch.setenv("DFLASH_FORCE_FFMA", force)
+        p = Pair(cfg, lim, seed=8, weights=w)
+        p.inject(list(range(9)), lens, "prefill", reset=True)
+        anchors = torch.arange(9, dtype=torch.int32).cuda() * 7
+        o = p.ctx.draft(list(range(9)), anchors, want_logits=True)
+        k, v = p.ctx.export_kv(4, 1, 0, lens[4])
+        outs.append((o["logits"].cpu(), o["argmax"].cpu(), k.float().cpu(), v.float().cpu()))
+        p.ctx.close()
+    (lt, at, kt, vt), (lf, af, kf, vf) = outs
+    assert torch.max(torch.abs(lt - lf)).item() < 1e-3
+    assert torch.mean((at == af).float()).item() > 0.99
+    assert torch.max(torch.abs(kt - kf)).item() < 3e-2 and torch.mean((kt == kf).float()).item() > 0.99
+    assert torch.max(torch.abs(vt - vf)).item() < 3e-2 and torch.mean((vt == vf).float()).item() > 0.99
 
 
 def test_host_errors_change_no_state():
