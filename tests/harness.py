@@ -11,6 +11,11 @@ from synth import inputs as S
 # candidates in question is below 1e-3.
 LOGIT_TOL = {"bf16": 2e-2, "f32": 1e-4}
 TIE_GAP = 1e-3
+# Top-k ranks below the first: a swap of two candidates is accepted when the oracle separates
+# them by less than this. bf16 weights with bf16 hi/lo activation operands put the logits
+# within ~1.7e-3 (max abs, Qwen3-8B shape) of the fp64 oracle, so neighbours closer than a
+# few times that may legitimately trade places.
+TOPK_GAP = {"bf16": 5e-3, "f32": 1e-4}
 
 
 def to_np(t):
@@ -74,9 +79,9 @@ def check_argmax(got, logits_oracle, what=""):
             f"{what} row {j}: argmax {got[j]} vs oracle {want[j]} (gap {top - l32[j, got[j]]:.3g})"
 
 
-def check_topk(got_idx, got_val, logits_oracle, k, tol, what=""):
+def check_topk(got_idx, got_val, logits_oracle, k, tol, what="", gap=TIE_GAP):
     """Values match the oracle's sorted top-k within tol; indices equal the oracle's except
-    inside runs of near-ties (gap < TIE_GAP), where they must be valid near-tied members."""
+    inside runs of near-ties (oracle gap < `gap`), where they must be valid near-tied members."""
     l32 = O.f32_round(logits_oracle)
     want_idx, want_val = O.topk_desc(l32, k)
     np.testing.assert_allclose(got_val, want_val, atol=tol, rtol=0, err_msg=what)
@@ -85,6 +90,6 @@ def check_topk(got_idx, got_val, logits_oracle, k, tol, what=""):
         for r in range(k):
             if got_idx[j, r] == want_idx[j, r]:
                 continue
-            # a swap is allowed only among candidates the oracle ranks within TIE_GAP
-            assert abs(l32[j, got_idx[j, r]] - want_val[j, r]) < TIE_GAP, \
+            # a swap is allowed only among candidates the oracle ranks within `gap`
+            assert abs(l32[j, got_idx[j, r]] - want_val[j, r]) < gap, \
                 f"{what} row {j} rank {r}: {got_idx[j, r]} vs {want_idx[j, r]}"

@@ -8,7 +8,7 @@ import oracle as O
 from synth import get_config
 from synth import inputs as S
 
-from harness import Pair, check_argmax, check_logits, check_topk, to_np, LOGIT_TOL
+from harness import Pair, check_argmax, check_logits, check_topk, to_np, LOGIT_TOL, TOPK_GAP
 
 pytestmark = pytest.mark.gpu
 
@@ -76,7 +76,7 @@ def _run_steps(cfg, limits, ctx_lens, steps, seed=0, check_kv=True):
             oam[i] = w_am
             check_logits(cfg, lg[i], w_lg, f"step {step} req {r}")
             check_argmax(am[i], w_lg, f"step {step} req {r}")
-            check_topk(ti[i], tv[i], w_lg, cfg.topk, tol, f"step {step} req {r}")
+            check_topk(ti[i], tv[i], w_lg, cfg.topk, tol, f"step {step} req {r}", TOPK_GAP[cfg.dtype])
             assert np.all(am[i] == ti[i][:, 0])
         # the synthetic target follows the oracle's argmax; both verifies see the same ids
         target = S.make_targets(cfg, torch.from_numpy(oam), seed, step)
