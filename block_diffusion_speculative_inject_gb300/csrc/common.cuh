@@ -67,6 +67,8 @@ __device__ __forceinline__ void write_op(const OpOut &o, size_t idx, float v) {
 enum GemmEpi : int {
   EPI_STORE = 0,   // Y = acc
   EPI_RESID = 1,   // Y = R + acc   (R may alias Y)
+  EPI_TOPK = 2,    // per 128-row weight tile and token: the tile's top-k (value, index)
+                   // into cand[tile][m][k]; Y = acc as well when y != nullptr
 };
 
 constexpr int GEMM_MAX_XSEG = 8;
@@ -87,6 +89,8 @@ struct GemmDesc {
   float *y;                      // output [M, ldy] fp32
   int ldy;
   const float *resid;            // EPI_RESID input [M, ldy]
+  int topk;                      // EPI_TOPK: k
+  int2 *cand;                    // EPI_TOPK: [ceil(N/128)][M][k] (float bits, index)
 };
 
 }  // namespace dflash

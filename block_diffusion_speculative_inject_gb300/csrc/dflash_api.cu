@@ -76,6 +76,7 @@ struct dflash_ctx {
   float *x = nullptr, *qkv = nullptr, *gu = nullptr;
   void *xn = nullptr, *ao = nullptr, *hmid = nullptr, *xf = nullptr;
   float *logits = nullptr, *part_o = nullptr, *part_ml = nullptr;
+  int2 *cand = nullptr;    // LM-head per-tile top-k candidates [V/128][rows][topk]
   int rows_max = 0, rows_k_max = 0;
   // injection scratch
   float *fc_out = nullptr, *kvproj = nullptr;
@@ -246,7 +247,8 @@ extern "C" dflash_status dflash_validate_config(const dflash_config *c, char *ms
   };
   if (!c) return bad(DFLASH_ERR_INVALID_ARG, "config is NULL");
   if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return bad(DFLASH_ERR_INVALID_ARG, "dtype");
-  if (c->hidden <= 0 || c->hidden % 128) return bad(DFLASH_ERR_UNSUPPORTED, "hidden must be a positive multiple of 128");
+  if (c->hidden <= 0 || c->hidden % 128 || c->hidden > 8192)
+    return bad(DFLASH_ERR_UNSUPPORTED, "hidden must be a multiple of 128 in [128, 8192]");
   if (c->intermediate <= 0 || c->intermediate % 128) return bad(DFLASH_ERR_UNSUPPORTED, "intermediate must be a positive multiple of 128");
   if (c->head_dim != 64 && c->head_dim != 128) return bad(DFLASH_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
@@ -288,7 +290,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 
 // ------------------------------------------------------------------------------ create / destroy
 static void free_all(dflash_ctx *c) {
-  void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits,
+  void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj};
   for (void *p : dev)
     if (p) cudaFree(p);
@@ -370,6 +372,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {&c->hmid, (size_t)R * m.I * f4},
       {&c->xf, (size_t)RK * m.H * f4},
       {(void **)&c->logits, (size_t)RK * m.V * f4},
+      {(void **)&c->cand, (size_t)((m.V + 127) / 128) * RK * m.topk * sizeof(int2)},
       {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * f4},
       {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * f4},
       {(void **)&c->fc_out, (size_t)C * m.H * f4},
@@ -704,14 +707,29 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   CK(c, timed(c, K_RMSNORM, s, 8.0 * RK * m.H, 4.0 * RK * m.H, 1, [&] {
        return launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s);
      }));
-  float *lg = logits ? logits : c->logits;
-  GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
-  set_x(c, lm, xf, m.H);
-  add_wseg(lm, c->w.lm_head, m.V);
-  if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
-  CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
-       return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s);
-     }));
+  if (c->tc) {
+    // tensor-core LM head: per-tile top-k in the GEMM epilogue, then a cross-tile merge;
+    // full logits are written only when the caller asks for them
+    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_TOPK, logits, m.V);
+    set_x(c, lm, xf, m.H);
+    add_wseg(lm, c->w.lm_head, m.V);
+    lm.topk = m.topk;
+    lm.cand = c->cand;
+    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+    const int tiles = (m.V + 127) / 128;
+    CK(c, timed(c, K_TOPK, s, 8.0 * tiles * RK * m.topk, 1.0 * tiles * RK * m.topk, 1, [&] {
+         return launch_topk_merge(tiles, RK, m.topk, c->cand, argmax, topk_idx, topk_val, s);
+       }));
+  } else {
+    float *lg = logits ? logits : c->logits;
+    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
+    set_x(c, lm, xf, m.H);
+    add_wseg(lm, c->w.lm_head, m.V);
+    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
+         return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s);
+       }));
+  }
   return DFLASH_OK;
 }
 

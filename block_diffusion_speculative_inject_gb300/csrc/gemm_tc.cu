@@ -52,6 +52,8 @@ struct TcParams {
   int ldy;
   const float *resid;
   float *ws;                          // [S][M][N] partials when S > 1
+  int topk;                           // EPI_TOPK
+  int2 *cand;                         // EPI_TOPK: [n_tiles][M][topk]
   int *err;
 };
 
@@ -274,11 +276,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err);
     tc_fence_after();
     const int n = n0 + q * 32 + lane;
+    // the top-k epilogue stages the tile [BN tokens][128 rows] in the (now idle) stage memory
+    float *tile = (float *)gen_tiles;
+    constexpr int TP = TC_BM + 1;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       uint32_t r[16];
       tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
       tmem_ld_wait();
+      if (p.epi == EPI_TOPK) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c0 + j;
+          const bool valid = ok && n < p.N && m < p.M;
+          const float v = __uint_as_float(r[j]);
+          tile[(c0 + j) * TP + q * 32 + lane] = valid ? v : -INFINITY;
+          if (valid && p.y) p.y[(size_t)m * p.ldy + n] = v;
+        }
+        continue;
+      }
       if (!ok || n >= p.N) continue;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -290,6 +306,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
         } else {
           const size_t o = (size_t)m * p.ldy + n;
           p.y[o] = p.epi == EPI_RESID ? p.resid[o] + v : v;
+        }
+      }
+    }
+    if (p.epi == EPI_TOPK) {
+      // per token: the tile's best topk (value desc, lower index first) by warp arg-max rounds
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int c = warp - 2; c < BN; c += 4) {
+        const int m = m0 + c;
+        if (m >= p.M || !ok) continue;
+        float v[4];
+        int id[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[j] = tile[c * TP + lane + 32 * j];
+          id[j] = n0 + lane + 32 * j;
+        }
+        int2 *out = p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk;
+        for (int rr = 0; rr < p.topk; ++rr) {
+          float bv = v[0];
+          int bi = id[0];
+#pragma unroll
+          for (int j = 1; j < 4; ++j)
+            if (v[j] > bv || (v[j] == bv && id[j] < bi)) {
+              bv = v[j];
+              bi = id[j];
+            }
+          float wv = bv;
+          int wi = bi;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+            if (ov > wv || (ov == wv && oi < wi)) {
+              wv = ov;
+              wi = oi;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (id[j] == wi) {      // the winner leaves the race
+              v[j] = -INFINITY;
+              id[j] = 0x7fffffff;
+            }
+          if (lane == 0) out[rr] = make_int2(__float_as_int(wv), wi);
         }
       }
     }
@@ -388,6 +448,7 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   const int target = 2 * t->num_sms;
   int S = (target + base - 1) / base;
   S = std::max(1, std::min(S, std::min(32, p.kb / 4)));
+  if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
   p.kb_per = (p.kb + S - 1) / S;
   p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
   const bool split = d.x_lo[0] != nullptr;
@@ -417,6 +478,7 @@ static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan 
 
 cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
+  if (d.epi == EPI_TOPK && (d.topk < 1 || d.topk > 32 || !d.cand)) return cudaErrorInvalidValue;
   if (!d.x_bf16 || d.K % TC_BK || d.n_wseg > TC_MAX_WSEG || d.n_xseg > TC_MAX_XMAP ||
       (d.x_lo[0] && d.n_xseg != 1))
     return cudaErrorInvalidValue;
@@ -455,6 +517,8 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.S = pl.S;
   p.stages = pl.stages;
   p.epi = d.epi;
+  p.topk = d.topk;
+  p.cand = d.cand;
   p.y = d.y;
   p.ldy = d.ldy;
   p.resid = d.resid;

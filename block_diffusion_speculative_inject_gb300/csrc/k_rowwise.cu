@@ -43,32 +43,62 @@ cudaError_t launch_embed(int dtype, const ModelDims &m, int B, const int32_t *an
 }
 
 // ------------------------------------------------------------------------- RMSNorm
-// y = x * rsqrt(mean(x^2) + eps) * w, one warp per row, written as a GEMM operand.
+// y = x * rsqrt(mean(x^2) + eps) * w, written as a GEMM operand. One 128-thread CTA per row:
+// the row is read once with float4 loads into registers (H <= 8192), reduced across the
+// block, scaled and written.
+constexpr int RN_THREADS = 128;
+constexpr int RN_VEC = 16;   // float4 per thread: H <= 128 * 4 * 16 = 8192
+
 template <typename TW>
-__global__ void k_rmsnorm(int rows, int H, const float *in, int ld_in, OpOut out, int ld_out,
-                          const TW *w, float eps, int skip_k) {
-  int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(RN_THREADS) k_rmsnorm(int rows, int H, const float *in, int ld_in,
+                                                        OpOut out, int ld_out, const TW *w,
+                                                        float eps, int skip_k) {
+  __shared__ float red[RN_THREADS / 32];
+  const int r = blockIdx.x;
   if (r >= rows) return;
-  int src = skip_k > 0 ? (r / skip_k) * (skip_k + 1) + r % skip_k + 1 : r;
-  const float *xi = in + (size_t)src * ld_in;
+  const int src = skip_k > 0 ? (r / skip_k) * (skip_k + 1) + r % skip_k + 1 : r;
+  const float4 *xi = (const float4 *)(in + (size_t)src * ld_in);
+  const int n4 = H / 4;
+  float4 v[RN_VEC];
   float ss = 0.f;
-  for (int i = lane; i < H; i += 32) ss += xi[i] * xi[i];
+#pragma unroll
+  for (int t = 0; t < RN_VEC; ++t) {
+    const int i = threadIdx.x + t * RN_THREADS;
+    if (i < n4) {
+      v[t] = xi[i];
+      ss += v[t].x * v[t].x + v[t].y * v[t].y + v[t].z * v[t].z + v[t].w * v[t].w;
+    }
+  }
   ss = warp_sum(ss);
-  float rs = rsqrtf(ss / (float)H + eps);
-  size_t o = (size_t)r * ld_out;
-  for (int i = lane; i < H; i += 32) write_op(out, o + i, xi[i] * rs * to_f(w[i]));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < RN_THREADS / 32; ++i) tot += red[i];
+  const float rs = rsqrtf(tot / (float)H + eps);
+  const size_t o = (size_t)r * ld_out;
+#pragma unroll
+  for (int t = 0; t < RN_VEC; ++t) {
+    const int i = threadIdx.x + t * RN_THREADS;
+    if (i < n4) {
+      const int e = 4 * i;
+      write_op(out, o + e + 0, v[t].x * rs * to_f(w[e + 0]));
+      write_op(out, o + e + 1, v[t].y * rs * to_f(w[e + 1]));
+      write_op(out, o + e + 2, v[t].z * rs * to_f(w[e + 2]));
+      write_op(out, o + e + 3, v[t].w * rs * to_f(w[e + 3]));
+    }
+  }
 }
 
 cudaError_t launch_rmsnorm(int dtype, int rows, int H, const float *in, int ld_in, OpOut out,
                            int ld_out, const void *w, float eps, int skip_anchor_k,
                            cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  dim3 g((rows + 7) / 8);
-  if (dtype) k_rmsnorm<bf16><<<g, 256, 0, s>>>(rows, H, in, ld_in, out, ld_out, (const bf16 *)w,
-                                               eps, skip_anchor_k);
-  else k_rmsnorm<float><<<g, 256, 0, s>>>(rows, H, in, ld_in, out, ld_out, (const float *)w, eps,
-                                          skip_anchor_k);
+  if (H % 4 || H > RN_THREADS * 4 * RN_VEC || ld_in % 4) return cudaErrorInvalidValue;
+  if (dtype) k_rmsnorm<bf16><<<rows, RN_THREADS, 0, s>>>(rows, H, in, ld_in, out, ld_out,
+                                                        (const bf16 *)w, eps, skip_anchor_k);
+  else k_rmsnorm<float><<<rows, RN_THREADS, 0, s>>>(rows, H, in, ld_in, out, ld_out,
+                                                   (const float *)w, eps, skip_anchor_k);
   return cudaGetLastError();
 }
 

@@ -1,7 +1,10 @@
-// Row-wise top-k over fp32 logits: values descending, equal values ordered by the lower
-// vocabulary index; the argmax is the first entry. One CTA per row: every thread keeps a
-// sorted register list of its best TK candidates over a strided slice of the row, then
-// the block merges the 256 sorted lists by k rounds of a block-wide "best head" pick.
+// Top-k selection (values descending, equal values ordered by the lower vocabulary index;
+// the argmax is the first entry). Two entry points share one block-wide selector:
+//   launch_topk        a row of fp32 logits [V] per CTA (the FFMA path);
+//   launch_topk_merge  the per-tile candidates written by the tensor-core LM-head GEMM
+//                      epilogue, [tiles][rows][k] (value, index) per row, merged per CTA.
+// Each thread keeps a sorted register list of its best TK candidates over a strided slice,
+// then the block merges the 256 sorted lists by k rounds of a block-wide best-head pick.
 #include "kernels.h"
 
 namespace dflash {
@@ -13,14 +16,13 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const float *logits,
-                                                          int32_t *argmax, int32_t *topk_idx,
-                                                          float *topk_val) {
+template <typename Get>
+__device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argmax_out,
+                                           int32_t *idx_out, float *val_out) {
   __shared__ float hv[TK_THREADS];
   __shared__ int hi[TK_THREADS];
   __shared__ int ht[TK_THREADS];
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const float *x = logits + (size_t)row * V;
+  const int tid = threadIdx.x;
   float lv[TK];
   int li[TK];
 #pragma unroll
@@ -28,24 +30,24 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
     lv[q] = -INFINITY;
     li[q] = 0x7fffffff;
   }
-  for (int i = tid; i < V; i += TK_THREADS) {
-    float v = x[i];
-    if (!better(v, i, lv[TK - 1], li[TK - 1])) continue;
-    // insertion into the sorted list (unrolled, registers only)
+  for (int i = tid; i < n; i += TK_THREADS) {
+    float v;
+    int id;
+    get(i, v, id);
+    if (!better(v, id, lv[TK - 1], li[TK - 1])) continue;
     float cv = v;
-    int ci = i;
+    int ci = id;
 #pragma unroll
-    for (int q = 0; q < TK; ++q) {
-      bool b = better(cv, ci, lv[q], li[q]);
-      float tv = lv[q];
-      int ti = li[q];
+    for (int q = 0; q < TK; ++q) {   // insertion into the sorted list (registers only)
+      const bool b = better(cv, ci, lv[q], li[q]);
+      const float tv = lv[q];
+      const int ti = li[q];
       lv[q] = b ? cv : lv[q];
       li[q] = b ? ci : li[q];
       cv = b ? tv : cv;
       ci = b ? ti : ci;
     }
   }
-  // merge: each round every thread offers its current head; the block best is emitted
   int head = 0;
   for (int r = 0; r < k; ++r) {
     float myv = -INFINITY;
@@ -68,18 +70,43 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
       }
       __syncthreads();
     }
-    float bv = hv[0];
-    int bi = hi[0], bt = ht[0];
+    const float bv = hv[0];
+    const int bi = hi[0], bt = ht[0];
     __syncthreads();
     if (tid == bt) ++head;
     if (tid == 0) {
-      if (r == 0) argmax[row] = bi;
-      if (topk_idx) {
-        topk_idx[(size_t)row * k + r] = bi;
-        topk_val[(size_t)row * k + r] = bv;
+      if (r == 0) *argmax_out = bi;
+      if (idx_out) {
+        idx_out[r] = bi;
+        val_out[r] = bv;
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const float *logits,
+                                                          int32_t *argmax, int32_t *topk_idx,
+                                                          float *topk_val) {
+  const int row = blockIdx.x;
+  const float *x = logits + (size_t)row * V;
+  block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; }, argmax + row,
+             topk_idx ? topk_idx + (size_t)row * k : nullptr,
+             topk_val ? topk_val + (size_t)row * k : nullptr);
+}
+
+__global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
+                                                           const int2 *cand, int32_t *argmax,
+                                                           int32_t *topk_idx, float *topk_val) {
+  const int row = blockIdx.x;
+  block_topk(tiles * k, k,
+             [&](int i, float &v, int &id) {
+               const int t = i / k, j = i % k;
+               const int2 c = cand[((size_t)t * rows + row) * k + j];
+               v = __int_as_float(c.x);
+               id = c.y;
+             },
+             argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
+             topk_val ? topk_val + (size_t)row * k : nullptr);
 }
 
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
@@ -87,6 +114,14 @@ cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *ar
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
   k_topk_rows<<<rows, TK_THREADS, 0, s>>>(V, k, logits, argmax, topk_idx, topk_val);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
+                              int32_t *topk_idx, float *topk_val, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (k < 1 || k > TK) return cudaErrorInvalidValue;
+  k_topk_merge<<<rows, TK_THREADS, 0, s>>>(tiles, rows, k, cand, argmax, topk_idx, topk_val);
   return cudaGetLastError();
 }
 

@@ -61,6 +61,10 @@ cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &b,
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
                         int32_t *topk_idx, float *topk_val, cudaStream_t s);
 
+// Merge of the per-tile candidates [tiles][rows][k] of the tensor-core LM-head epilogue.
+cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
+                              int32_t *topk_idx, float *topk_val, cudaStream_t s);
+
 cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *target,
                           int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
                           cudaStream_t s);

@@ -61,7 +61,7 @@ typedef enum {
 typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
 
 /* Draft-model shape and context limits. Requirements (checked by dflash_validate_config):
- * hidden, intermediate, n_q_heads*head_dim and n_kv_heads*head_dim multiples of 128;
+ * hidden (<= 8192), intermediate, n_q_heads*head_dim and n_kv_heads*head_dim multiples of 128;
  * target_hidden a multiple of 64; head_dim 64 or 128; n_q_heads a multiple of
  * n_kv_heads with n_q_heads/n_kv_heads <= 8; 1 <= block_k <= 31; 1 <= topk <= 32;
  * page_size == 64; vocab >= topk; mask_token_id in [0, vocab). */
