@@ -38,6 +38,17 @@ __device__ __forceinline__ void raise_err(int *flag, int code) {
   if (flag) *(volatile int *)flag = code;
 }
 
+// ---------------------------------------------------------------- paged KV pool
+// A page holds 64 positions of every layer: [L][K|V][nkv][block], one block per (layer,
+// K or V, kv head) of 64 x hd values. K blocks are position-major [64][hd] (hd contiguous);
+// V blocks are stored transposed, [hd][64] (positions contiguous), so that both attention
+// products read their operands K-major.
+constexpr int KV_PAGE = 64;
+__host__ __device__ __forceinline__ size_t kv_block(int page, int l, int kv, int h, int L, int nkv,
+                                                    int hd) {
+  return ((((size_t)page * L + l) * 2 + kv) * nkv + h) * (size_t)(KV_PAGE * hd);
+}
+
 // ---------------------------------------------------------------- activation operands
 // Activations are fp32. Where an activation is the X operand of a GEMM it is written as
 // an "operand": fp32 for fp32 weights, or for bf16 weights an exact pair of bf16 planes

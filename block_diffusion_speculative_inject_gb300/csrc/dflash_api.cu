@@ -88,6 +88,7 @@ struct dflash_ctx {
   int *err_h = nullptr, *err_d = nullptr;
 
   TcGemm *tc = nullptr;   // tensor-core GEMM plans (bf16 only)
+  AttnMaps amaps{};       // tensor maps over the KV pool for the tensor-core attention
   std::string last_error;
   int64_t launches = 0;
 
@@ -397,6 +398,9 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       return fail(DFLASH_ERR_CUDA);
   }
 
+  // every cache slot starts finite (masked positions of a page still meet a zero weight)
+  if (cudaMemset(c->pool, 0, (size_t)cfg->max_pages * c->page_elems * es) != cudaSuccess)
+    return fail(DFLASH_ERR_CUDA);
   c->free_pages.reserve(cfg->max_pages);
   for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
 
@@ -421,6 +425,13 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   if (c->dtype == DFLASH_BF16 && !(force_ffma && force_ffma[0] == '1')) {
     cudaError_t e = tc_gemm_create(&c->tc, device, c->num_sms, c->err_d);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA);
+    if (m.hd == 128) {
+      // K blocks as rows of hd values, V blocks ([hd][64]) as rows of 64 positions
+      const unsigned long long blocks = (unsigned long long)cfg->max_pages * m.L * 2 * m.nkv;
+      c->amaps.valid = tc_encode_2d(c->tc, c->pool, blocks * kPage, m.hd, m.hd, 64, 64, &c->amaps.k) &&
+                       tc_encode_2d(c->tc, c->pool, blocks * m.hd, kPage, kPage, 64, 128, &c->amaps.v);
+      c->amaps.err = c->err_d;
+    }
   }
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(DFLASH_ERR_CUDA);
   *out = c;
@@ -592,11 +603,19 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
 }
 
 // ------------------------------------------------------------------------------ draft step
-static void plan_splits(int S, int *n_split, int *split_len) {
-  int ns = std::min(kMaxSplit, std::max(1, (S + 511) / 512));
-  int len = round_up((S + ns - 1) / ns, 32);
-  *n_split = ns;
-  *split_len = len;
+// Context splits of one request: whole pages, about `target` splits (enough CTAs over the
+// batch's kv heads to fill the GPU), at most kMaxSplit, none for an empty context.
+static void plan_splits(int ctx_len, int target, int *n_split, int *split_len) {
+  const int pages = (ctx_len + kPage - 1) / kPage;
+  if (pages == 0) {
+    *n_split = 0;
+    *split_len = kPage;
+    return;
+  }
+  int ns = std::max(1, std::min(std::min(target, kMaxSplit), pages));
+  const int per = (pages + ns - 1) / ns;       // pages per split
+  *n_split = (pages + per - 1) / per;          // every split non-empty
+  *split_len = per * kPage;
 }
 
 extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t n_req,
@@ -616,7 +635,8 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   std::vector<int32_t> desc(4 * B + 1);
   std::vector<const Req *> rq(B);
   std::unordered_set<int32_t> seen;
-  int max_split = 1;
+  int max_split = 0;
+  const int target = std::max(1, (2 * c->num_sms + B * m.nkv - 1) / (B * m.nkv));
   for (int b = 0; b < B; ++b) {
     if (!seen.insert(req_ids[b]).second)
       return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d appears twice", req_ids[b]);
@@ -624,7 +644,7 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
     if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_ids[b]);
     rq[b] = &it->second;
     int ns, sl;
-    plan_splits(rq[b]->len + Q, &ns, &sl);
+    plan_splits(rq[b]->len, target, &ns, &sl);
     desc[b] = rq[b]->len;
     desc[B + b] = ns;
     desc[2 * B + b] = sl;
@@ -679,7 +699,8 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
                                     lw.k_norm, s);
        }));
     CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, 2, [&] {
-         return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao, s);
+         return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
+                                 c->amaps.valid ? &c->amaps : nullptr, s);
        }));
     GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
     set_x(c, o, ao, m.q_dim());

@@ -10,6 +10,11 @@ struct TcGemm;
 // device error flag its bounded waits raise).
 cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag);
 void tc_gemm_destroy(TcGemm *t);
+// bf16 2-D tensor map over a row-major [rows, cols] matrix with row stride ld elements,
+// box {box_cols, box_rows}, 128-byte swizzle. False if the driver rejects it.
+bool tc_encode_2d(TcGemm *t, const void *ptr, unsigned long long rows, unsigned long long cols,
+                  unsigned long long ld, unsigned box_cols, unsigned box_rows, void *map_out);
+
 // Number of kernel launches tc_gemm_run issues for this GEMM.
 int tc_gemm_launches(const TcGemm *t, const GemmDesc &d);
 // Runs Y = epilogue(X . W^T) for bf16 W and a bf16 (or bf16 hi/lo pair) X.

@@ -3,10 +3,13 @@
 // Per request b the keys are [context positions 0..ctx_len-1 (paged cache) ; the block's
 // own K+1 keys], with no mask anywhere ("LLM的推理加速-DFlash" 关键创新 Step 3: target
 // features first, block keys after; "DFlash：把串行 Draft 变成并行“填空”" §5.3: non-causal).
-// One CTA handles (split s, kv head, request b): its rows are the G = nq/nkv query heads
-// sharing that kv head times the K+1 block rows; the key range of split s is
-// [s*split_len, min((s+1)*split_len, ctx_len + K + 1)). Partial results (unnormalised
-// accumulator, running max, running sum) are combined across splits in a fixed order.
+// A split CTA handles (split s, kv head, request b): its rows are the G = nq/nkv query heads
+// sharing that kv head times the K+1 block rows, its keys the context range
+// [s*split_len, min((s+1)*split_len, ctx_len)) (page aligned). It writes an unnormalised
+// accumulator, the running max and the running sum, with scores in log2 units
+// (q.k * log2(e) / sqrt(hd)). The combine kernel adds the block's own K+1 keys (fp32, from
+// the q/k/v rows) and merges the splits in a fixed order. Splits run on the tensor cores
+// (k_attention_tc.cu) for bf16 caches with head_dim 128, on the FFMA cores otherwise.
 #include "kernels.h"
 
 namespace dflash {
@@ -30,9 +33,8 @@ __global__ void __launch_bounds__(256) k_attn_split(
   const int G = nq / nkv, R = G * Q;
   const int qkv_dim = (nq + 2 * nkv) * HD;
   const int n_ctx = ctx_len[b];
-  const int S = n_ctx + Q;
   const int k_begin = s * split_len[b];
-  const int k_end = min(k_begin + split_len[b], S);
+  const int k_end = min(k_begin + split_len[b], n_ctx);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t row0 = (size_t)b * Q;
   const int32_t *pg = pages + page_off[b];
@@ -54,7 +56,6 @@ __global__ void __launch_bounds__(256) k_attn_split(
     for (int d = 0; d < DPL; ++d) acc[i][d] = 0.f;
   }
 
-  const int kv_dim = nkv * HD;
   for (int t0 = k_begin; t0 < k_end; t0 += AT_KT) {
     __syncthreads();
     for (int i = tid; i < AT_KT * HD; i += 256) {
@@ -62,17 +63,9 @@ __global__ void __launch_bounds__(256) k_attn_split(
       int key = t0 + kk;
       float kval = 0.f, vval = 0.f;
       if (key < k_end) {
-        if (key < n_ctx) {
-          int page = pg[key / AT_PAGE], off = key % AT_PAGE;
-          size_t base = ((((size_t)page * L + layer) * 2) * nkv + kvh) * (size_t)(AT_PAGE * HD) +
-                        (size_t)off * HD + d;
-          kval = to_f(pool[base]);
-          vval = to_f(pool[base + (size_t)nkv * AT_PAGE * HD]);
-        } else {
-          size_t r = row0 + (key - n_ctx);
-          kval = qkv[r * qkv_dim + (size_t)nq * HD + (size_t)kvh * HD + d];
-          vval = qkv[r * qkv_dim + (size_t)nq * HD + kv_dim + (size_t)kvh * HD + d];
-        }
+        int page = pg[key / AT_PAGE], off = key % AT_PAGE;
+        kval = to_f(pool[kv_block(page, layer, 0, kvh, L, nkv, HD) + (size_t)off * HD + d]);
+        vval = to_f(pool[kv_block(page, layer, 1, kvh, L, nkv, HD) + (size_t)d * AT_PAGE + off]);
       }
       ks[kk * (HD + 1) + d] = kval;
       vs[kk * HD + d] = vval;
@@ -91,8 +84,8 @@ __global__ void __launch_bounds__(256) k_attn_split(
       sc = valid ? sc * scale : -INFINITY;
       float mt = warp_max(sc);
       float m_new = fmaxf(m_run[i], mt);
-      float p = valid ? expf(sc - m_new) : 0.f;
-      float corr = expf(m_run[i] - m_new);      // exp(-inf) = 0 on the first tile
+      float p = valid ? exp2f(sc - m_new) : 0.f;
+      float corr = exp2f(m_run[i] - m_new);     // exp2(-inf) = 0 on the first tile
       l_run[i] = l_run[i] * corr + warp_sum(p);
       m_run[i] = m_new;
 #pragma unroll
@@ -121,62 +114,98 @@ __global__ void __launch_bounds__(256) k_attn_split(
   }
 }
 
-// o[b*Q + j, h*HD + d] = sum_s acc_s * exp(m_s - M) / sum_s l_s * exp(m_s - M), in split order.
+// Per (request b, block row j, q head h), one warp: scores against the block's own K+1
+// keys (fp32 q/k/v rows), then the merge with the context splits, in split order:
+//   o = (sum_s acc_s 2^(m_s - M) + sum_kk 2^(s_kk - M) v_kk) / (sum_s l_s 2^(m_s - M) + sum_kk 2^(s_kk - M))
 template <int HD>
-__global__ void k_attn_combine(int nq, int Q, const int32_t *n_split, int max_split,
-                               const float *part_o, const float *part_ml, OpOut o) {
-  int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  int lane = threadIdx.x & 31;
-  int b = blockIdx.y;
+__global__ void k_attn_combine(int nq, int nkv, int Q, const int32_t *n_split, int max_split,
+                               const float *part_o, const float *part_ml, const float *qkv,
+                               float scale_log2, OpOut o) {
+  constexpr int DPL = HD / 32;
+  const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
   if (w >= Q * nq) return;
-  int j = w / nq, h = w % nq;
-  size_t base = (((size_t)b * Q + j) * nq + h) * max_split;
-  int ns = n_split[b];
+  const int j = w / nq, h = w % nq;
+  const int G = nq / nkv, kvh = h / G;
+  const int qkv_dim = (nq + 2 * nkv) * HD;
+  const size_t row = (size_t)b * Q + j;
+  float q[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) q[d] = qkv[row * qkv_dim + (size_t)h * HD + lane + 32 * d] * scale_log2;
+  const float *kblk = qkv + (size_t)b * Q * qkv_dim + (size_t)nq * HD + (size_t)kvh * HD;
+  const float *vblk = kblk + (size_t)nkv * HD;
+  const size_t base = (((size_t)b * Q + j) * nq + h) * max_split;
+  const int ns = n_split[b];
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
+  for (int kk = 0; kk < Q; ++kk) {
+    float t = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) t += q[d] * kblk[(size_t)kk * qkv_dim + lane + 32 * d];
+    M = fmaxf(M, warp_sum(t));
+  }
   float Lsum = 0.f;
-  float acc[HD / 32] = {};
+  float acc[DPL] = {};
   for (int s = 0; s < ns; ++s) {
-    float c = expf(part_ml[(base + s) * 2] - M);
+    const float c = exp2f(part_ml[(base + s) * 2] - M);
     Lsum += part_ml[(base + s) * 2 + 1] * c;
 #pragma unroll
-    for (int d = 0; d < HD / 32; ++d) acc[d] += part_o[(base + s) * HD + lane + 32 * d] * c;
+    for (int d = 0; d < DPL; ++d) acc[d] += part_o[(base + s) * HD + lane + 32 * d] * c;
   }
-  float inv = 1.f / Lsum;
-  size_t dst = ((size_t)b * Q + j) * (nq * HD) + (size_t)h * HD;
+  for (int kk = 0; kk < Q; ++kk) {
+    float t = 0.f;
 #pragma unroll
-  for (int d = 0; d < HD / 32; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
+    for (int d = 0; d < DPL; ++d) t += q[d] * kblk[(size_t)kk * qkv_dim + lane + 32 * d];
+    const float p = exp2f(warp_sum(t) - M);
+    Lsum += p;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] += p * vblk[(size_t)kk * qkv_dim + lane + 32 * d];
+  }
+  const float inv = 1.f / Lsum;
+  const size_t dst = row * (nq * HD) + (size_t)h * HD;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
 }
 
 template <typename T, int HD>
 static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer, const float *qkv,
                              const void *pool, float *part_o, float *part_ml, OpOut o,
-                             cudaStream_t s) {
-  size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(k_attn_split<T, HD>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 g(bt.max_split, m.nkv, bt.B);
-  k_attn_split<T, HD><<<g, 256, smem, s>>>(
-      m.L, m.nq, m.nkv, m.Q(), layer, qkv, (const T *)pool, bt.ctx_len, bt.n_split,
-      bt.split_len, bt.page_off, bt.pages, bt.max_split, 1.f / sqrtf((float)HD), part_o, part_ml);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+                             const AttnMaps *maps, cudaStream_t s) {
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  cudaError_t e = cudaSuccess;
+  if (bt.max_split > 0) {
+    if (maps && maps->valid && HD == 128 && sizeof(T) == 2) {
+      e = launch_attn_split_tc(m, bt, layer, qkv, maps, scale_log2, part_o, part_ml, s);
+    } else {
+      size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
+      e = cudaFuncSetAttribute(k_attn_split<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+      dim3 g(bt.max_split, m.nkv, bt.B);
+      k_attn_split<T, HD><<<g, 256, smem, s>>>(
+          m.L, m.nq, m.nkv, m.Q(), layer, qkv, (const T *)pool, bt.ctx_len, bt.n_split,
+          bt.split_len, bt.page_off, bt.pages, bt.max_split, scale_log2, part_o, part_ml);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+  }
   dim3 g2((m.Q() * m.nq + 7) / 8, bt.B);
-  k_attn_combine<HD><<<g2, 256, 0, s>>>(m.nq, m.Q(), bt.n_split, bt.max_split, part_o, part_ml, o);
+  k_attn_combine<HD><<<g2, 256, 0, s>>>(m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split, part_o,
+                                        part_ml, qkv, scale_log2, o);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &bt, int layer,
                              const float *qkv, const void *pool, float *part_o, float *part_ml,
-                             OpOut o, cudaStream_t s) {
+                             OpOut o, const AttnMaps *maps, cudaStream_t s) {
   if (bt.B <= 0) return cudaSuccess;
   if (m.hd == 128)
-    return dtype ? attn_impl<bf16, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, s)
-                 : attn_impl<float, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, s);
+    return dtype ? attn_impl<bf16, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, maps, s)
+                 : attn_impl<float, 128>(m, bt, layer, qkv, pool, part_o, part_ml, o, maps, s);
   if (m.hd == 64)
-    return dtype ? attn_impl<bf16, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, s)
-                 : attn_impl<float, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, s);
+    return dtype ? attn_impl<bf16, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, maps, s)
+                 : attn_impl<float, 64>(m, bt, layer, qkv, pool, part_o, part_ml, o, maps, s);
   return cudaErrorInvalidValue;
 }
 

@@ -6,12 +6,7 @@
 
 namespace dflash {
 
-constexpr int PAGE = 64;
-
-__device__ __forceinline__ size_t pool_index(int page, int l, int kv, int h, int off, int L,
-                                             int nkv, int hd) {
-  return ((((size_t)page * L + l) * 2 + kv) * nkv + h) * (size_t)(PAGE * hd) + (size_t)off * hd;
-}
+constexpr int PAGE = KV_PAGE;
 
 // ------------------------------------------------------------------------- embedding
 // Block rows of request b: row 0 is the anchor token, rows 1..K the mask token; each is
@@ -194,11 +189,11 @@ __global__ void k_inject_kv(int T_rows, int L, int nkv, int hd, const float *kv,
   int page = sl / PAGE, off = sl % PAGE;
   const float *src_k = kv + (size_t)t * (L * 2 * kv_dim) + (size_t)l * 2 * kv_dim + (size_t)h * hd;
   const float *src_v = src_k + kv_dim;
-  T *dk = pool + pool_index(page, l, 0, h, off, L, nkv, hd);
-  T *dv = pool + pool_index(page, l, 1, h, off, L, nkv, hd);
+  T *dk = pool + kv_block(page, l, 0, h, L, nkv, hd) + (size_t)off * hd;
+  T *dv = pool + kv_block(page, l, 1, h, L, nkv, hd) + off;     // transposed: [hd][64]
   const T *nw = qk_norm ? (const T *)kn.p[l] : nullptr;
   head_norm_rope<T, T>(src_k, dk, nw, hd, eps, rope + (size_t)pos[t] * (hd / 2), lane);
-  for (int i = lane; i < hd; i += 32) dv[i] = from_f<T>(src_v[i]);
+  for (int i = lane; i < hd; i += 32) dv[(size_t)i * PAGE] = from_f<T>(src_v[i]);
 }
 
 cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const float *kv,
@@ -271,8 +266,8 @@ __global__ void k_export_kv(int L, int nkv, int hd, int layer, int pos0, int n,
   int t = i / ((long)hd * nkv);
   int p = pos0 + t;
   int page = pages[p / PAGE], off = p % PAGE;
-  k_out[i] = pool[pool_index(page, layer, 0, h, off, L, nkv, hd) + d];
-  v_out[i] = pool[pool_index(page, layer, 1, h, off, L, nkv, hd) + d];
+  k_out[i] = pool[kv_block(page, layer, 0, h, L, nkv, hd) + (size_t)off * hd + d];
+  v_out[i] = pool[kv_block(page, layer, 1, h, L, nkv, hd) + (size_t)d * PAGE + off];
 }
 
 cudaError_t launch_export_kv(int dtype, const ModelDims &m, int layer, int pos0, int n,

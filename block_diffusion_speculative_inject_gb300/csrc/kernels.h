@@ -1,5 +1,7 @@
 // Internal launchers of libdflash (not part of the C ABI).
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace dflash {
@@ -51,11 +53,24 @@ cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const float *
 // h = silu(gate) * up from fp32 rows [gate (I) | up (I)], written as a GEMM operand.
 cudaError_t launch_swiglu(int rows, int I, const float *gu, OpOut h, cudaStream_t s);
 
+// Tensor maps over the KV pool for the tensor-core attention: K blocks viewed as rows of hd
+// values (box 64 x 64), V blocks ([hd][64]) as rows of 64 positions (box 64 x 128).
+struct AttnMaps {
+  CUtensorMap k, v;
+  bool valid;
+  int *err;      // device error flag raised by expired waits
+};
+
 // Split-KV attention of the query block of each request over its paged context plus the
 // block's own K/V, then the split combine into the operand o [B*(K+1), q_dim].
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &b, int layer,
                              const float *qkv, const void *pool, float *part_o, float *part_ml,
-                             OpOut o, cudaStream_t s);
+                             OpOut o, const AttnMaps *maps, cudaStream_t s);
+
+// The tensor-core split kernel (bf16 cache, head_dim 128).
+cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &b, int layer,
+                                 const float *qkv, const AttnMaps *maps, float scale_log2,
+                                 float *part_o, float *part_ml, cudaStream_t s);
 
 // Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V].
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
