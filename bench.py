@@ -230,24 +230,36 @@ def run_ours(args):
     for s in range(args.warmup):
         _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
     torch.cuda.synchronize()
-    ctx.timing_read()            # drop anything recorded so far
-    ctx.timing_enable(True)
     launches0 = ctx.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(ws)
     torch.cuda.synchronize()
     with Clocks(local) as clk:
+        t0 = time.perf_counter()
         e0.record(stream)
         for s in range(args.warmup, steps):
             _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
         e1.record(stream)
+        host_enqueue = time.perf_counter() - t0
         torch.cuda.synchronize()
     _barrier(ws)
     launches = ctx.launch_count() - launches0
     ms = e0.elapsed_time(e1)
+    ms_max = _max_over_ranks(ws, ms, device)
+
+    # per-kernel breakdown: the same steps again with CUDA events around every launch (the
+    # events add a little time, so the headline number above is taken without them)
+    ctx.timing_read()
+    ctx.timing_enable(True)
+    kb0, kb1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kb0.record(stream)
+    for s in range(args.warmup, steps):
+        _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+    kb1.record(stream)
+    torch.cuda.synchronize()
     kern = ctx.timing_read()
     ctx.timing_enable(False)
-    ms_max = _max_over_ranks(ws, ms, device)
+    ms_events = kb0.elapsed_time(kb1)
 
     # end to end through host buffers: H2D of the step's inputs, D2H of its results
     e2e = None
@@ -330,6 +342,8 @@ def run_ours(args):
                    "parallelism": f"{ws} independent replica(s)"},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches,
+        "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / args.steps, 4),
+        "ms_per_step_with_kernel_events": round(ms_events / args.steps, 4),
     }
     res["clocks"] = clk.summary()
     if not args.no_cpu_baseline and ws >= 1:

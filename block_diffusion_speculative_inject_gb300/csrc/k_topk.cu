@@ -94,19 +94,65 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
              topk_val ? topk_val + (size_t)row * k : nullptr);
 }
 
+// Merge of per-tile sorted candidate lists. The k-th best of the tiles' first candidates is
+// a lower bound T of the row's k-th best value (those k tiles each hold a value >= T), so
+// only candidates >= T can be in the result: they are gathered in one parallel pass and
+// selected exactly. (If more than MERGE_CAP candidates tie at or above T, every candidate
+// is scanned instead.)
+constexpr int MERGE_CAP = 1024;
+
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
                                                            const int2 *cand, int32_t *argmax,
                                                            int32_t *topk_idx, float *topk_val) {
+  __shared__ int2 pool[MERGE_CAP];
+  __shared__ int n_pool;
+  __shared__ float thr_val[32];
+  __shared__ int thr_idx[32];
+  __shared__ int dummy;
   const int row = blockIdx.x;
-  block_topk(tiles * k, k,
+  auto at = [&](int t, int j) { return cand[((size_t)t * rows + row) * k + j]; };
+  // 1) lower bound: k-th best of the tiles' first candidates
+  const int kk = min(k, tiles);
+  block_topk(tiles, kk,
              [&](int i, float &v, int &id) {
-               const int t = i / k, j = i % k;
-               const int2 c = cand[((size_t)t * rows + row) * k + j];
+               const int2 c = at(i, 0);
                v = __int_as_float(c.x);
                id = c.y;
              },
-             argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
-             topk_val ? topk_val + (size_t)row * k : nullptr);
+             &dummy, thr_idx, thr_val);
+  if (threadIdx.x == 0) n_pool = 0;
+  __syncthreads();
+  const float T = thr_val[kk - 1];
+  // 2) gather every candidate >= T
+  const int n = tiles * k;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < n; i += TK_THREADS) {
+    const int2 c = at(i / k, i % k);
+    if (__int_as_float(c.x) >= T) {
+      const int slot = atomicAdd(&n_pool, 1);
+      if (slot < MERGE_CAP) pool[slot] = c;
+    }
+  }
+  __syncthreads();
+  const int np = n_pool;
+  int32_t *oi = topk_idx ? topk_idx + (size_t)row * k : nullptr;
+  float *ov = topk_val ? topk_val + (size_t)row * k : nullptr;
+  if (np <= MERGE_CAP) {
+    block_topk(np, k,
+               [&](int i, float &v, int &id) {
+                 v = __int_as_float(pool[i].x);
+                 id = pool[i].y;
+               },
+               argmax + row, oi, ov);
+  } else {
+    block_topk(n, k,
+               [&](int i, float &v, int &id) {
+                 const int2 c = at(i / k, i % k);
+                 v = __int_as_float(c.x);
+                 id = c.y;
+               },
+               argmax + row, oi, ov);
+  }
 }
 
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
