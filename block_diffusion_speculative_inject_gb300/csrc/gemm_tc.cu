@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   const uint32_t accf = empty0 + 8u * stages;
   uint32_t *tmem_slot = (uint32_t *)(bars + 2 * stages + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  volatile int *is_last = (volatile int *)(tmem_slot + 2);   // split-K: this CTA reduces
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
@@ -200,17 +201,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     }
     if (p.S > 1 && p.epi != EPI_TOPK) {
       // split-K: the last CTA of this output tile to arrive sums the partials in split order
-      __shared__ int is_last;
       __threadfence();
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (threadIdx.x == 64) {
         int *ctr = p.counters + blockIdx.y * gridDim.x + blockIdx.x;
         const int prev = atomicAdd(ctr, 1);
-        is_last = prev == p.S - 1;
-        if (is_last) *ctr = 0;              // ready for the next launch
+        *is_last = prev == p.S - 1;
+        if (prev == p.S - 1) *ctr = 0;      // ready for the next launch
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (is_last && ok && n < p.N) {
+      if (*is_last && ok && n < p.N) {
         __threadfence();
         for (int c = 0; c < BN; ++c) {
           const int m = m0 + c;
