@@ -46,6 +46,14 @@ const char *kClsName[K_NUM] = {"gemm_fc", "gemm_kv", "gemm_qkv", "gemm_o", "gemm
                                "gemm_down", "gemm_lmhead", "attention", "rmsnorm", "qk_norm_rope",
                                "inject_kv", "swiglu", "embed", "topk", "verify", "export_kv"};
 
+struct DraftGraph {
+  long long key;
+  int seen;
+  int gen;
+  int n_launch;
+  cudaGraphExec_t exec;
+};
+
 struct TimeRec {
   int cls;
   cudaEvent_t a, b;
@@ -91,6 +99,12 @@ struct dflash_ctx {
   AttnMaps amaps{};       // tensor maps over the KV pool for the tensor-core attention
   std::string last_error;
   int64_t launches = 0;
+
+  // CUDA graphs of the layer stack, keyed by batch size and split plan
+  bool graphs_enabled = true;
+  cudaStream_t cap_stream = nullptr;
+  int32_t *desc_fixed = nullptr;   // device descriptor read by captured kernels
+  std::vector<DraftGraph> graphs;
 
   bool timing = false;
   std::vector<TimeRec> recs;
@@ -187,6 +201,22 @@ static dflash_status stage_upload(dflash_ctx *c, cudaStream_t s, const void *src
   CK(c, cudaEventRecord(st.ev, s));
   st.used = true;
   *dev_out = (const int32_t *)st.d;
+  return DFLASH_OK;
+}
+
+// Like stage_upload, into a caller-chosen device buffer.
+static dflash_status stage_upload_to(dflash_ctx *c, cudaStream_t s, const void *src, size_t bytes,
+                                     int32_t *dst) {
+  if (bytes > c->stage_cap)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "descriptor of %zu bytes exceeds staging %zu", bytes,
+                   c->stage_cap);
+  Stage &st = c->ring[c->ring_next];
+  c->ring_next = (c->ring_next + 1) % (int)c->ring.size();
+  if (st.used) CK(c, cudaEventSynchronize(st.ev));
+  memcpy(st.h, src, bytes);
+  CK(c, cudaMemcpyAsync(dst, st.h, bytes, cudaMemcpyHostToDevice, s));
+  CK(c, cudaEventRecord(st.ev, s));
+  st.used = true;
   return DFLASH_OK;
 }
 
@@ -307,6 +337,10 @@ static void free_all(dflash_ctx *c) {
     cudaEventDestroy(r.b);
   }
   for (cudaEvent_t e : c->spare_events) cudaEventDestroy(e);
+  for (auto &g : c->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (c->desc_fixed) cudaFree(c->desc_fixed);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
 }
 
 extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_weights *w,
@@ -414,6 +448,13 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
         cudaMalloc(&s.d, c->stage_cap) != cudaSuccess ||
         cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) != cudaSuccess)
       return fail(DFLASH_ERR_CUDA);
+  }
+  if (cudaMalloc(&c->desc_fixed, c->stage_cap) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return fail(DFLASH_ERR_CUDA);
+  {
+    const char *ng = getenv("DFLASH_NO_GRAPHS");
+    c->graphs_enabled = !(ng && ng[0] == '1');
   }
   if (cudaHostAlloc((void **)&c->err_h, sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer((void **)&c->err_d, c->err_h, 0) != cudaSuccess)
@@ -618,6 +659,137 @@ static void plan_splits(int ctx_len, int target, int *n_split, int *split_len) {
   *split_len = per * kPage;
 }
 
+// The layer stack of the draft step plus the final norm and the LM-head GEMM: every launch
+// between the embedding and the top-k selection. It touches only library buffers and the
+// device descriptor `bt`, so it can be captured once per (batch, split plan) and replayed.
+static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, double attn_bytes,
+                                  double attn_flops, float *logits, cudaStream_t s) {
+  const ModelDims &m = c->m;
+  dflash_status st;
+  const int R = B * m.Q();
+  const OpOut xn = op_of(c, c->xn, (size_t)c->rows_max * m.H);
+  const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
+  const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
+  const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
+  for (int l = 0; l < m.L; ++l) {
+    const dflash_layer_weights &lw = c->layers[l];
+    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
+         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s);
+       }));
+    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, c->qkv, m.qkv_dim());
+    set_x(c, d, xn, m.H);
+    add_wseg(d, lw.wq, m.q_dim());
+    add_wseg(d, lw.wk, m.kv_dim());
+    add_wseg(d, lw.wv, m.kv_dim());
+    if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_ROPE, s, 8.0 * R * (m.nq + m.nkv) * m.hd, 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
+         return launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
+                                    lw.k_norm, s);
+       }));
+    CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, bt.max_split > 0 ? 2 : 1, [&] {
+         return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
+                                 c->amaps.valid ? &c->amaps : nullptr, s);
+       }));
+    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
+    set_x(c, o, ao, m.q_dim());
+    o.resid = c->x;
+    add_wseg(o, lw.wo, m.H);
+    if ((st = run_gemm(c, K_GEMM_O, o, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
+         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s);
+       }));
+    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, c->gu, 2 * m.I);
+    set_x(c, gu, xn, m.H);
+    add_wseg(gu, lw.w_gate, m.I);
+    add_wseg(gu, lw.w_up, m.I);
+    if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_SWIGLU, s, 12.0 * R * m.I, 5.0 * R * m.I, 1,
+                [&] { return launch_swiglu(R, m.I, c->gu, hm, s); }));
+    GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_RESID, c->x, m.H);
+    set_x(c, dn, hm, m.I);
+    dn.resid = c->x;
+    add_wseg(dn, lw.w_down, m.H);
+    if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
+  }
+  // final norm on the K mask rows only (the anchor row yields no candidate)
+  const int RK = B * m.K;
+  CK(c, timed(c, K_RMSNORM, s, 8.0 * RK * m.H, 4.0 * RK * m.H, 1, [&] {
+       return launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s);
+     }));
+  if (c->tc) {
+    // tensor-core LM head: per-tile top-k in the GEMM epilogue (merged afterwards); full
+    // logits are written only when the caller asks for them
+    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_TOPK, logits, m.V);
+    set_x(c, lm, xf, m.H);
+    add_wseg(lm, c->w.lm_head, m.V);
+    lm.topk = m.topk;
+    lm.cand = c->cand;
+    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+  } else {
+    float *lg = logits ? logits : c->logits;
+    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
+    set_x(c, lm, xf, m.H);
+    add_wseg(lm, c->w.lm_head, m.V);
+    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+  }
+  return DFLASH_OK;
+}
+
+// Replays (or, on the second sighting of this batch size and split plan, captures) the
+// layer stack as a CUDA graph. Capture runs on the library's own stream (captures never
+// execute); the graph is launched on the caller's stream.
+static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt, cudaStream_t s) {
+  const long long key = ((long long)B << 8) | bt.max_split;
+  const int gen = tc_gemm_generation(c->tc);
+  for (auto &g : c->graphs) {
+    if (g.key != key) continue;
+    if (g.exec && g.gen == gen) {
+      CK(c, cudaGraphLaunch(g.exec, s));
+      c->launches += g.n_launch;
+      return DFLASH_OK;
+    }
+    if (g.exec) {                       // a GEMM workspace moved since the capture
+      cudaGraphExecDestroy(g.exec);
+      g.exec = nullptr;
+    }
+    if (g.seen++ < 1) break;            // run eagerly until the plan has been seen twice
+    const int64_t l0 = c->launches;
+    CK(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    dflash_status st = draft_layers(c, B, bt, 0, 0, nullptr, c->cap_stream);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+    c->launches = l0;
+    if (st != DFLASH_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return st;
+    }
+    if (e != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+    size_t n_nodes = 0;
+    cudaGraphGetNodes(graph, nullptr, &n_nodes);
+    e = cudaGraphInstantiate(&g.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+      g.exec = nullptr;
+      return set_err(c, DFLASH_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    }
+    g.gen = gen;
+    g.n_launch = (int)n_nodes;
+    CK(c, cudaGraphLaunch(g.exec, s));
+    c->launches += g.n_launch;
+    return DFLASH_OK;
+  }
+  bool found = false;
+  for (auto &g : c->graphs) found |= g.key == key;
+  if (!found) {
+    if (c->graphs.size() >= 16) {
+      if (c->graphs.front().exec) cudaGraphExecDestroy(c->graphs.front().exec);
+      c->graphs.erase(c->graphs.begin());
+    }
+    c->graphs.push_back(DraftGraph{key, 1, gen, 0, nullptr});
+  }
+  return draft_layers(c, B, bt, 0, 0, nullptr, s);
+}
+
 extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t n_req,
                                            const int32_t *req_ids, const int32_t *anchors,
                                            int32_t *argmax, int32_t *topk_idx, float *topk_val,
@@ -670,83 +842,34 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   DeviceGuard guard(c->device);
   if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
   cudaStream_t s = (cudaStream_t)stream;
+  const int RK = B * m.K;
+  const bool use_graph = c->tc && !logits && !c->timing && c->graphs_enabled;
   const int32_t *dd = nullptr;
-  if ((st = stage_upload(c, s, desc.data(), desc.size() * 4, &dd)) != DFLASH_OK) return st;
+  if (use_graph) {
+    // the descriptor goes to a fixed device buffer that the captured kernels read
+    if ((st = stage_upload_to(c, s, desc.data(), desc.size() * 4, c->desc_fixed)) != DFLASH_OK) return st;
+    dd = c->desc_fixed;
+  } else if ((st = stage_upload(c, s, desc.data(), desc.size() * 4, &dd)) != DFLASH_OK) {
+    return st;
+  }
   DraftBatch bt{dd, dd + B, dd + 2 * B, dd + 3 * B, dd + 4 * B + 1, B, max_split};
 
-  const int R = B * Q;
-  const OpOut xn = op_of(c, c->xn, (size_t)c->rows_max * m.H);
-  const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
-  const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
-  const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
-  CK(c, timed(c, K_EMBED, s, (double)R * m.H * (c->esz + 4), (double)R * m.H, 1, [&] {
+  CK(c, timed(c, K_EMBED, s, (double)B * Q * m.H * (c->esz + 4), (double)B * Q * m.H, 1, [&] {
        return launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x,
                            c->err_d, s);
      }));
-  for (int l = 0; l < m.L; ++l) {
-    const dflash_layer_weights &lw = c->layers[l];
-    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
-         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s);
-       }));
-    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, c->qkv, m.qkv_dim());
-    set_x(c, d, xn, m.H);
-    add_wseg(d, lw.wq, m.q_dim());
-    add_wseg(d, lw.wk, m.kv_dim());
-    add_wseg(d, lw.wv, m.kv_dim());
-    if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_ROPE, s, 8.0 * R * (m.nq + m.nkv) * m.hd, 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
-         return launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
-                                    lw.k_norm, s);
-       }));
-    CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, 2, [&] {
-         return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
-                                 c->amaps.valid ? &c->amaps : nullptr, s);
-       }));
-    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
-    set_x(c, o, ao, m.q_dim());
-    o.resid = c->x;
-    add_wseg(o, lw.wo, m.H);
-    if ((st = run_gemm(c, K_GEMM_O, o, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
-         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s);
-       }));
-    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, c->gu, 2 * m.I);
-    set_x(c, gu, xn, m.H);
-    add_wseg(gu, lw.w_gate, m.I);
-    add_wseg(gu, lw.w_up, m.I);
-    if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_SWIGLU, s, 12.0 * R * m.I, 5.0 * R * m.I, 1,
-                [&] { return launch_swiglu(R, m.I, c->gu, hm, s); }));
-    GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_RESID, c->x, m.H);
-    set_x(c, dn, hm, m.I);
-    dn.resid = c->x;
-    add_wseg(dn, lw.w_down, m.H);
-    if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
+  if (use_graph) {
+    if ((st = run_layers_graph(c, B, bt, s)) != DFLASH_OK) return st;
+  } else if ((st = draft_layers(c, B, bt, attn_bytes, attn_flops, logits, s)) != DFLASH_OK) {
+    return st;
   }
-  // final norm on the K mask rows only (the anchor row yields no candidate)
-  const int RK = B * m.K;
-  CK(c, timed(c, K_RMSNORM, s, 8.0 * RK * m.H, 4.0 * RK * m.H, 1, [&] {
-       return launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s);
-     }));
   if (c->tc) {
-    // tensor-core LM head: per-tile top-k in the GEMM epilogue, then a cross-tile merge;
-    // full logits are written only when the caller asks for them
-    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_TOPK, logits, m.V);
-    set_x(c, lm, xf, m.H);
-    add_wseg(lm, c->w.lm_head, m.V);
-    lm.topk = m.topk;
-    lm.cand = c->cand;
-    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
     const int tiles = (m.V + 127) / 128;
     CK(c, timed(c, K_TOPK, s, 8.0 * tiles * RK * m.topk, 1.0 * tiles * RK * m.topk, 1, [&] {
          return launch_topk_merge(tiles, RK, m.topk, c->cand, argmax, topk_idx, topk_val, s);
        }));
   } else {
     float *lg = logits ? logits : c->logits;
-    GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_STORE, lg, m.V);
-    set_x(c, lm, xf, m.H);
-    add_wseg(lm, c->w.lm_head, m.V);
-    if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
     CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
          return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s);
        }));

@@ -9,9 +9,8 @@
 // slab through the pipeline once. When X is an exact bf16 hi/lo pair (an fp32 activation),
 // both planes are multiplied by the same staged weight tile and accumulate into the same
 // TMEM columns, so the weights are read from HBM once. Small grids are split along K
-// (split-K) so every SM streams weights; each split writes fp32 partials and the last CTA
-// of an output tile to arrive (an atomic counter per tile) sums them in split order and
-// applies the epilogue, so the result does not depend on arrival order.
+// (split-K) so every SM streams weights; the fp32 partials are summed in a fixed order by
+// a second kernel that also applies the epilogue.
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 owns the TMEM allocation and
 // its lane 0 issues the MMAs, warps 2-5 (one per 32-lane TMEM quarter) run the epilogue.
@@ -55,7 +54,6 @@ struct TcParams {
   float *ws;                          // [S][M][N] partials when S > 1
   int topk;                           // EPI_TOPK
   int2 *cand;                         // EPI_TOPK: [n_tiles][M][topk]
-  int *counters;                      // split-K arrival counters, one per output tile
   int *err;
 };
 
@@ -82,7 +80,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   const uint32_t accf = empty0 + 8u * stages;
   uint32_t *tmem_slot = (uint32_t *)(bars + 2 * stages + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
-  volatile int *is_last = (volatile int *)(tmem_slot + 2);   // split-K: this CTA reduces
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
@@ -199,29 +196,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
         }
       }
     }
-    if (p.S > 1 && p.epi != EPI_TOPK) {
-      // split-K: the last CTA of this output tile to arrive sums the partials in split order
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (threadIdx.x == 64) {
-        int *ctr = p.counters + blockIdx.y * gridDim.x + blockIdx.x;
-        const int prev = atomicAdd(ctr, 1);
-        *is_last = prev == p.S - 1;
-        if (prev == p.S - 1) *ctr = 0;      // ready for the next launch
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (*is_last && ok && n < p.N) {
-        __threadfence();
-        for (int c = 0; c < BN; ++c) {
-          const int m = m0 + c;
-          if (m >= p.M) break;
-          float a = 0.f;
-          for (int sp = 0; sp < p.S; ++sp) a += __ldcg(p.ws + ((size_t)sp * p.M + m) * p.N + n);
-          const size_t o = (size_t)m * p.ldy + n;
-          p.y[o] = p.epi == EPI_RESID ? p.resid[o] + a : a;
-        }
-      }
-    }
     if (p.epi == EPI_TOPK) {
       // per token: the tile's best topk (value desc, lower index first) by warp arg-max rounds
       asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -275,17 +249,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   }
 }
 
-// ------------------------------------------------------------------------- host side
-constexpr int TC_MAX_TILES = 1 << 16;
+// Sum of the S split-K partials in split order, then the epilogue.
+__global__ void k_splitk_reduce(int M, int N, int S, const float *__restrict__ ws, int epi,
+                                float *y, int ldy, const float *resid) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long)M * N) return;
+  const int m = (int)(i / N), n = (int)(i % N);
+  float a = 0.f;
+  for (int s = 0; s < S; ++s) a += ws[((size_t)s * M + m) * N + n];
+  const size_t o = (size_t)m * ldy + n;
+  y[o] = epi == EPI_RESID ? resid[o] + a : a;
+}
 
+// ------------------------------------------------------------------------- host side
 struct TcGemm {
   int device = 0, num_sms = 0;
   int *err = nullptr;
-  int *counters = nullptr;        // [TC_MAX_TILES] split-K arrival counters, kept at zero
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
   float *ws = nullptr;
   size_t ws_bytes = 0;
+  int generation = 0;
   bool attr_set[4] = {false, false, false, false};
 };
 
@@ -301,12 +285,6 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
   t->num_sms = num_sms;
   t->encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
   t->err = err_flag;
-  if (cudaMalloc(&t->counters, TC_MAX_TILES * sizeof(int)) != cudaSuccess ||
-      cudaMemset(t->counters, 0, TC_MAX_TILES * sizeof(int)) != cudaSuccess) {
-    if (t->counters) cudaFree(t->counters);
-    delete t;
-    return cudaErrorMemoryAllocation;
-  }
   *out = t;
   return cudaSuccess;
 }
@@ -314,7 +292,6 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
 void tc_gemm_destroy(TcGemm *t) {
   if (!t) return;
   if (t->ws) cudaFree(t->ws);
-  if (t->counters) cudaFree(t->counters);
   delete t;
 }
 
@@ -383,7 +360,11 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   return p;
 }
 
-int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 1; }
+int tc_gemm_generation(const TcGemm *t) { return t ? t->generation : 0; }
+
+int tc_gemm_launches(const TcGemm *t, const GemmDesc &d) {
+  return plan_for(t, d).S > 1 ? 2 : 1;
+}
 
 template <int BN>
 static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan &pl, cudaStream_t s) {
@@ -445,8 +426,6 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.ldy = d.ldy;
   p.resid = d.resid;
   p.err = t->err;
-  p.counters = t->counters;
-  if (pl.t_tiles * pl.n_tiles > TC_MAX_TILES) return cudaErrorInvalidValue;
   if (pl.S > 1) {
     const size_t need = (size_t)pl.S * d.M * d.N * sizeof(float);
     if (need > t->ws_bytes) {
@@ -456,6 +435,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
       cudaError_t e = cudaMalloc(&t->ws, need);
       if (e != cudaSuccess) return e;
       t->ws_bytes = need;
+      ++t->generation;
     }
     p.ws = t->ws;
   }
@@ -466,7 +446,11 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     case 64: e = launch_bn<64>(t, 2, p, pl, s); break;
     default: e = launch_bn<128>(t, 3, p, pl, s); break;
   }
-  return e;
+  if (e != cudaSuccess || pl.S == 1) return e;
+  const long n = (long)d.M * d.N;
+  k_splitk_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d.M, d.N, pl.S, t->ws, d.epi, d.y,
+                                                               d.ldy, d.resid);
+  return cudaGetLastError();
 }
 
 }  // namespace dflash

@@ -15,6 +15,10 @@ void tc_gemm_destroy(TcGemm *t);
 bool tc_encode_2d(TcGemm *t, const void *ptr, unsigned long long rows, unsigned long long cols,
                   unsigned long long ld, unsigned box_cols, unsigned box_rows, void *map_out);
 
+// Incremented whenever an internal buffer (split-K workspace) is reallocated; captured
+// graphs that used the old buffer must be re-captured.
+int tc_gemm_generation(const TcGemm *t);
+
 // Number of kernel launches tc_gemm_run issues for this GEMM.
 int tc_gemm_launches(const TcGemm *t, const GemmDesc &d);
 // Runs Y = epilogue(X . W^T) for bf16 W and a bf16 (or bf16 hi/lo pair) X.

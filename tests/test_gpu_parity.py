@@ -227,3 +227,27 @@ def test_q8b_b1_full_size_step():
     cfg = get_config("q8b_b1")
     _run_steps(cfg, _limits(max_batch=1, max_pages=40, max_positions=2304, max_inject_rows=2048),
                [2048], steps=2, check_kv=False)
+
+
+def test_graph_replay_matches_eager(monkeypatch):
+    """The draft step replayed from a captured CUDA graph gives the same argmax / top-k bits as
+    the eagerly launched step, across repeated steps with changing context lengths."""
+    cfg = get_config("mini_bf16")
+    w = S.make_weights(cfg, 9)
+    lim = _limits(max_batch=3, max_pages=48, max_positions=1024, max_inject_rows=400)
+    results = []
+    for no_graphs in ("1", "0"):
+        monkeypatch.setenv("DFLASH_NO_GRAPHS", no_graphs)
+        p = Pair(cfg, lim, seed=9, weights=w)
+        p.inject([1, 2, 3], [120, 250, 64], "prefill", reset=True)
+        outs = []
+        for step in range(5):
+            anchors = S.make_anchors(cfg, 3, 9, step).cuda()
+            o = p.ctx.draft([1, 2, 3], anchors)
+            outs.append((o["argmax"].cpu(), o["topk_idx"].cpu(), o["topk_val"].cpu()))
+            n_new = [1 + (step + i) % 5 for i in range(3)]
+            p.inject([1, 2, 3], n_new, ("g", step))
+        results.append(outs)
+        p.ctx.close()
+    for (a1, i1, v1), (a2, i2, v2) in zip(*results):
+        assert torch.equal(a1, a2) and torch.equal(i1, i2) and torch.equal(v1, v2)
