@@ -116,22 +116,24 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       src = p.qkv + ((size_t)b * p.Q + j) * qkv_dim + (size_t)(kvh * G + g) * 128;
     }
 #pragma unroll 1
-    for (int c = 0; c < 16; ++c) {
-      float v[8];
-      if (src) {
-        const float4 a = *(const float4 *)(src + 8 * c), d = *(const float4 *)(src + 8 * c + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = d.x; v[5] = d.y; v[6] = d.z; v[7] = d.w;
+    for (int c4 = 0; c4 < 16; c4 += 4) {            // 4 chunks of 8 values per round trip
+      float4 raw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        raw[i] = src ? *(const float4 *)(src + 8 * c4 + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int cc4 = 0; cc4 < 4; ++cc4) {
+        const int c = c4 + cc4;
+        const float4 a = raw[2 * cc4], d = raw[2 * cc4 + 1];
+        float v[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] *= p.scale_log2;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        uint4 hi, lo;
+        split8(v, hi, lo);
+        const int half = c >> 3, cc = c & 7;
+        *(uint4 *)(gbase + (0 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = hi;
+        *(uint4 *)(gbase + (1 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = lo;
       }
-      uint4 hi, lo;
-      split8(v, hi, lo);
-      const int half = c >> 3, cc = c & 7;
-      *(uint4 *)(gbase + (0 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = hi;
-      *(uint4 *)(gbase + (1 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = lo;
     }
     fence_proxy_async_smem();
   }

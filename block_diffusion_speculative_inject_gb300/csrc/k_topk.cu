@@ -19,9 +19,6 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 template <typename Get>
 __device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argmax_out,
                                            int32_t *idx_out, float *val_out) {
-  __shared__ float hv[TK_THREADS];
-  __shared__ int hi[TK_THREADS];
-  __shared__ int ht[TK_THREADS];
   const int tid = threadIdx.x;
   float lv[TK];
   int li[TK];
@@ -48,39 +45,66 @@ __device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argma
       ci = b ? ti : ci;
     }
   }
+  // merge: each round every thread offers its current head; warps reduce by shuffles, the
+  // eight warp winners through shared memory; the owner of the block winner advances
+  __shared__ float wv_s[TK_THREADS / 32];
+  __shared__ int wi_s[TK_THREADS / 32], wt_s[TK_THREADS / 32];
+  __shared__ int win_t;
+  const int lane = tid & 31, warp = tid >> 5;
   int head = 0;
   for (int r = 0; r < k; ++r) {
-    float myv = -INFINITY;
-    int myi = 0x7fffffff;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
 #pragma unroll
     for (int q = 0; q < TK; ++q)
       if (q == head) {
-        myv = lv[q];
-        myi = li[q];
+        bv = lv[q];
+        bi = li[q];
       }
-    hv[tid] = myv;
-    hi[tid] = myi;
-    ht[tid] = tid;
-    __syncthreads();
-    for (int st = TK_THREADS / 2; st > 0; st >>= 1) {
-      if (tid < st && better(hv[tid + st], hi[tid + st], hv[tid], hi[tid])) {
-        hv[tid] = hv[tid + st];
-        hi[tid] = hi[tid + st];
-        ht[tid] = ht[tid + st];
-      }
-      __syncthreads();
-    }
-    const float bv = hv[0];
-    const int bi = hi[0], bt = ht[0];
-    __syncthreads();
-    if (tid == bt) ++head;
-    if (tid == 0) {
-      if (r == 0) *argmax_out = bi;
-      if (idx_out) {
-        idx_out[r] = bi;
-        val_out[r] = bv;
+    int bt = tid;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+        bt = ot;
       }
     }
+    if (lane == 0) {
+      wv_s[warp] = bv;
+      wi_s[warp] = bi;
+      wt_s[warp] = bt;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < TK_THREADS / 32 ? wv_s[lane] : -INFINITY;
+      int i = lane < TK_THREADS / 32 ? wi_s[lane] : 0x7fffffff;
+      int t = lane < TK_THREADS / 32 ? wt_s[lane] : 0;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, t, o);
+        if (better(ov, oi, v, i)) {
+          v = ov;
+          i = oi;
+          t = ot;
+        }
+      }
+      if (lane == 0) {
+        win_t = t;
+        if (r == 0) *argmax_out = i;
+        if (idx_out) {
+          idx_out[r] = i;
+          val_out[r] = v;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == win_t) ++head;
   }
 }
 
