@@ -114,21 +114,26 @@ __global__ void __launch_bounds__(256) k_attn_split(
   }
 }
 
-// One CTA per (kv head, request b) over its R = G (K+1) rows (one warp per row at a time):
-// the block's own K+1 keys and values (fp32 q/k/v rows) are staged in shared memory, each
-// lane scores one block key, the context splits' (max, sum) are read one per lane, and the
-// merged output is accumulated with each lane owning hd/32 dimensions:
+// One CTA per (kv head, request b, chunk of 8 rows), one warp per row (rows are the G query
+// heads of the kv head times the K+1 block rows). The block's own K+1 keys and values (fp32
+// q/k/v rows) are staged in shared memory; each lane scores one block key against the warp's
+// q row (also staged), the context splits' (max, sum) are read one per lane, and the merged
+// output is accumulated with each lane owning hd/32 dimensions:
 //   o = (sum_s acc_s 2^(m_s - M) + sum_kk 2^(s_kk - M) v_kk) / (sum_s l_s 2^(m_s - M) + sum_kk 2^(s_kk - M))
 // The order of every sum is fixed.
+constexpr int CB_ROWS = 8;
+
 template <int HD>
-__global__ void __launch_bounds__(256) k_attn_combine(int nq, int nkv, int Q, const int32_t *n_split,
-                                                      int max_split, const float *part_o,
-                                                      const float *part_ml, const float *qkv,
-                                                      float scale_log2, OpOut o) {
+__global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, int Q,
+                                                               const int32_t *n_split, int max_split,
+                                                               const float *part_o,
+                                                               const float *part_ml, const float *qkv,
+                                                               float scale_log2, OpOut o) {
   constexpr int DPL = HD / 32;
   constexpr int KP = HD + 1;                       // padded row: lane-per-key reads are conflict free
   __shared__ float ks[32 * KP];
   __shared__ float vs[32 * HD];
+  __shared__ float qs[CB_ROWS][HD];
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int G = nq / nkv, R = G * Q;
   const int qkv_dim = (nq + 2 * nkv) * HD;
@@ -139,46 +144,49 @@ __global__ void __launch_bounds__(256) k_attn_combine(int nq, int nkv, int Q, co
     ks[kk * KP + d] = row[(size_t)kvh * HD + d];
     vs[kk * HD + d] = row[(size_t)nkv * HD + (size_t)kvh * HD + d];
   }
-  __syncthreads();
-  const int ns = n_split[b];
-  for (int r = warp; r < R; r += blockDim.x / 32) {
-    const int g = r / Q, j = r % Q, h = kvh * G + g;
-    const size_t row = (size_t)b * Q + j;
-    const float *qr = qkv + row * qkv_dim + (size_t)h * HD;
-    // block-key score of lane kk (q read as a broadcast, k from padded shared memory)
-    float sk = -INFINITY;
-    if (lane < Q) {
-      float t = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < HD; ++d) t = fmaf(__ldg(qr + d), ks[lane * KP + d], t);
-      sk = t * scale_log2;
-    }
-    const size_t base = (row * nq + h) * max_split;
-    float ms = -INFINITY, ls = 0.f;
-    if (lane < ns) {
-      ms = part_ml[(base + lane) * 2];
-      ls = part_ml[(base + lane) * 2 + 1];
-    }
-    const float M = warp_max(fmaxf(sk, ms));
-    const float pk = lane < Q ? exp2f(sk - M) : 0.f;
-    const float cs = lane < ns ? exp2f(ms - M) : 0.f;
-    const float Lsum = warp_sum(pk + cs * ls);
-    float acc[DPL] = {};
-    for (int sp = 0; sp < ns; ++sp) {
-      const float c = __shfl_sync(0xffffffffu, cs, sp);
+  const int r = blockIdx.z * CB_ROWS + warp;
+  const int g = r / Q, j = r % Q, h = kvh * G + g;
+  const size_t row = (size_t)b * Q + j;
+  if (r < R) {
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) acc[d] = fmaf(c, part_o[(base + sp) * HD + lane + 32 * d], acc[d]);
-    }
-    for (int kk = 0; kk < Q; ++kk) {
-      const float p = __shfl_sync(0xffffffffu, pk, kk);
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) acc[d] = fmaf(p, vs[kk * HD + lane + 32 * d], acc[d]);
-    }
-    const float inv = 1.f / Lsum;
-    const size_t dst = row * (nq * HD) + (size_t)h * HD;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
+    for (int d = 0; d < DPL; ++d) qs[warp][lane + 32 * d] = qkv[row * qkv_dim + (size_t)h * HD + lane + 32 * d];
   }
+  __syncthreads();
+  if (r >= R) return;
+  const int ns = n_split[b];
+  const size_t base = (row * nq + h) * max_split;
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < ns) {
+    ms = part_ml[(base + lane) * 2];
+    ls = part_ml[(base + lane) * 2 + 1];
+  }
+  float sk = -INFINITY;
+  if (lane < Q) {
+    float t = 0.f;
+#pragma unroll 16
+    for (int d = 0; d < HD; ++d) t = fmaf(qs[warp][d], ks[lane * KP + d], t);
+    sk = t * scale_log2;
+  }
+  const float M = warp_max(fmaxf(sk, ms));
+  const float pk = lane < Q ? exp2f(sk - M) : 0.f;
+  const float cs = lane < ns ? exp2f(ms - M) : 0.f;
+  const float Lsum = warp_sum(pk + cs * ls);
+  float acc[DPL] = {};
+#pragma unroll 4
+  for (int sp = 0; sp < ns; ++sp) {
+    const float c = __shfl_sync(0xffffffffu, cs, sp);
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(c, part_o[(base + sp) * HD + lane + 32 * d], acc[d]);
+  }
+  for (int kk = 0; kk < Q; ++kk) {
+    const float p = __shfl_sync(0xffffffffu, pk, kk);
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(p, vs[kk * HD + lane + 32 * d], acc[d]);
+  }
+  const float inv = 1.f / Lsum;
+  const size_t dst = row * (nq * HD) + (size_t)h * HD;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
 }
 
 template <typename T, int HD>
@@ -203,8 +211,9 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
     }
     if (e != cudaSuccess) return e;
   }
-  dim3 g2(m.nkv, bt.B);
-  k_attn_combine<HD><<<g2, 256, 0, s>>>(m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split, part_o,
+  const int R = (m.nq / m.nkv) * m.Q();
+  dim3 g2(m.nkv, bt.B, (R + CB_ROWS - 1) / CB_ROWS);
+  k_attn_combine<HD><<<g2, 32 * CB_ROWS, 0, s>>>(m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split, part_o,
                                         part_ml, qkv, scale_log2, o);
   return cudaGetLastError();
 }
