@@ -102,6 +102,8 @@ struct GemmDesc {
   const float *resid;            // EPI_RESID input [M, ldy]
   int topk;                      // EPI_TOPK: k
   int2 *cand;                    // EPI_TOPK: [ceil(N/128)][M][k] (float bits, index)
+  float *part;                   // partials mode: write the split-K partials [S][M][N] here
+                                 // (S = 1: the plain product) instead of Y; a post-op sums them
 };
 
 }  // namespace dflash

@@ -100,6 +100,13 @@ struct dflash_ctx {
   std::string last_error;
   int64_t launches = 0;
 
+  // GEMM partials [S][M][N] consumed by the post-op kernels; grows on demand (never during
+  // a graph capture); ws_gen counts reallocations so stale graphs are re-captured
+  float *ws = nullptr;
+  size_t ws_floats = 0;
+  int ws_gen = 0;
+  bool capturing = false;
+
   // CUDA graphs of the layer stack, keyed by batch size and split plan
   bool graphs_enabled = true;
   cudaStream_t cap_stream = nullptr;
@@ -236,6 +243,25 @@ static dflash_status run_gemm(dflash_ctx *c, int cls, const GemmDesc &d, cudaStr
   return DFLASH_OK;
 }
 
+// Runs a GEMM in partials mode into the context workspace; *S receives the split count the
+// post-op must sum.
+static dflash_status gemm_ws(dflash_ctx *c, int cls, GemmDesc d, cudaStream_t s, int *S) {
+  const int splits = (c->tc && c->dtype == DFLASH_BF16) ? tc_gemm_splits(c->tc, d) : 1;
+  const size_t need = (size_t)splits * d.M * d.N;
+  if (need > c->ws_floats) {
+    if (c->capturing) return set_err(c, DFLASH_ERR_CUDA, "workspace would grow during a graph capture");
+    if (c->ws) cudaFree(c->ws);
+    c->ws = nullptr;
+    c->ws_floats = 0;
+    CK(c, cudaMalloc(&c->ws, need * sizeof(float)));
+    c->ws_floats = need;
+    ++c->ws_gen;
+  }
+  d.part = c->ws;
+  *S = splits;
+  return run_gemm(c, cls, d, s);
+}
+
 static GemmDesc gemm_desc(int M, int N, int K, int epi, float *y, int ldy) {
   GemmDesc d{};
   d.M = M;
@@ -339,6 +365,7 @@ static void free_all(dflash_ctx *c) {
   for (cudaEvent_t e : c->spare_events) cudaEventDestroy(e);
   for (auto &g : c->graphs)
     if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (c->ws) cudaFree(c->ws);
   if (c->desc_fixed) cudaFree(c->desc_fixed);
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
 }
@@ -611,8 +638,8 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     buf.insert(buf.end(), pos.begin() + r0, pos.begin() + r0 + n);
     const int32_t *dslot = nullptr;
     if ((st = stage_upload(c, s, buf.data(), buf.size() * 4, &dslot)) != DFLASH_OK) return st;
-    // fc over the n_feat feature tensors read in place (K segments)
-    GemmDesc d = gemm_desc(n, m.H, F, EPI_STORE, c->fc_out, m.H);
+    // fc over the n_feat feature tensors read in place (K segments), then RMSNorm -> g
+    GemmDesc d = gemm_desc(n, m.H, F, EPI_STORE, nullptr, m.H);
     d.x_bf16 = c->dtype == DFLASH_BF16;   // the features are exact storage-type values
     d.n_xseg = m.n_feat;
     for (int f = 0; f < m.n_feat; ++f) {
@@ -622,22 +649,23 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     }
     d.x_k0[m.n_feat] = F;
     add_wseg(d, c->w.fc, m.H);
-    if ((st = run_gemm(c, K_GEMM_FC, d, s)) != DFLASH_OK) return st;
+    int S = 1;
+    if ((st = gemm_ws(c, K_GEMM_FC, d, s, &S)) != DFLASH_OK) return st;
     OpOut g = op_of(c, c->g, (size_t)C * m.H);
-    CK(c, timed(c, K_RMSNORM, s, 8.0 * n * m.H, 4.0 * n * m.H, 1, [&] {
-         return launch_rmsnorm(c->dtype, n, m.H, c->fc_out, m.H, g, m.H, c->w.fc_norm, m.eps, 0, s);
+    CK(c, timed(c, K_RMSNORM, s, 4.0 * n * m.H * (S + 1), 4.0 * n * m.H, 1, [&] {
+         return launch_post_norm(c->dtype, n, m.H, c->ws, S, nullptr, g, c->w.fc_norm, m.eps, 0, s);
        }));
-    // every layer's [Wk; Wv] in one GEMM
-    GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, c->kvproj, kvw);
+    // every layer's [Wk; Wv] in one GEMM, then k-norm + RoPE + paged write
+    GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, nullptr, kvw);
     set_x(c, e, g, m.H);
     for (int l = 0; l < m.L; ++l) {
       add_wseg(e, c->layers[l].wk, m.kv_dim());
       add_wseg(e, c->layers[l].wv, m.kv_dim());
     }
-    if ((st = run_gemm(c, K_GEMM_KV, e, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_INJECT_KV, s, (double)n * kvw * (4.0 + c->esz), 8.0 * n * kvw, 1, [&] {
-         return launch_inject_kv(c->dtype, m, n, c->kvproj, dslot, dslot + n, c->rope,
-                                 knorm.data(), c->pool, s);
+    if ((st = gemm_ws(c, K_GEMM_KV, e, s, &S)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_INJECT_KV, s, (double)n * kvw * (4.0 * S + c->esz), 8.0 * n * kvw, 1, [&] {
+         return launch_post_kv(c->dtype, m, n, c->ws, S, dslot, dslot + n, c->rope, knorm.data(),
+                               c->pool, s);
        }));
   }
   return DFLASH_OK;
@@ -666,56 +694,58 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
                                   double attn_flops, float *logits, cudaStream_t s) {
   const ModelDims &m = c->m;
   dflash_status st;
-  const int R = B * m.Q();
+  const int R = B * m.Q(), RK = B * m.K;
   const OpOut xn = op_of(c, c->xn, (size_t)c->rows_max * m.H);
   const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
   const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
   const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
+  int S = 1;
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
-    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
-         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.in_norm, m.eps, 0, s);
-       }));
-    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, c->qkv, m.qkv_dim());
+    // q/k/v projection; post-op: per-head q/k norm + RoPE
+    GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, nullptr, m.qkv_dim());
     set_x(c, d, xn, m.H);
     add_wseg(d, lw.wq, m.q_dim());
     add_wseg(d, lw.wk, m.kv_dim());
     add_wseg(d, lw.wv, m.kv_dim());
-    if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_ROPE, s, 8.0 * R * (m.nq + m.nkv) * m.hd, 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
-         return launch_qk_norm_rope(c->dtype, m, B, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
-                                    lw.k_norm, s);
+    if ((st = gemm_ws(c, K_GEMM_QKV, d, s, &S)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_ROPE, s, 4.0 * R * m.qkv_dim() * (S + 1), 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
+         return launch_post_qkv(c->dtype, m, B, c->ws, S, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
+                                lw.k_norm, s);
        }));
     CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, bt.max_split > 0 ? 2 : 1, [&] {
          return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
                                  c->amaps.valid ? &c->amaps : nullptr, s);
        }));
-    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_RESID, c->x, m.H);
+    // output projection; post-op: residual add + post-attention norm
+    GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_STORE, nullptr, m.H);
     set_x(c, o, ao, m.q_dim());
-    o.resid = c->x;
     add_wseg(o, lw.wo, m.H);
-    if ((st = run_gemm(c, K_GEMM_O, o, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_RMSNORM, s, 8.0 * R * m.H, 4.0 * R * m.H, 1, [&] {
-         return launch_rmsnorm(c->dtype, R, m.H, c->x, m.H, xn, m.H, lw.post_norm, m.eps, 0, s);
+    if ((st = gemm_ws(c, K_GEMM_O, o, s, &S)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
+         return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, xn, lw.post_norm, m.eps, 0, s);
        }));
-    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, c->gu, 2 * m.I);
+    // gate/up projection; post-op: SwiGLU
+    GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, nullptr, 2 * m.I);
     set_x(c, gu, xn, m.H);
     add_wseg(gu, lw.w_gate, m.I);
     add_wseg(gu, lw.w_up, m.I);
-    if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_SWIGLU, s, 12.0 * R * m.I, 5.0 * R * m.I, 1,
-                [&] { return launch_swiglu(R, m.I, c->gu, hm, s); }));
-    GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_RESID, c->x, m.H);
+    if ((st = gemm_ws(c, K_GEMM_GATEUP, gu, s, &S)) != DFLASH_OK) return st;
+    CK(c, timed(c, K_SWIGLU, s, 4.0 * R * m.I * (2 * S + 1), 5.0 * R * m.I, 1,
+                [&] { return launch_post_swiglu(R, m.I, c->ws, S, hm, s); }));
+    // down projection; post-op: residual add + the next layer's input norm, or after the
+    // last layer the final norm of the K mask rows (the anchor row yields no candidate)
+    GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_STORE, nullptr, m.H);
     set_x(c, dn, hm, m.I);
-    dn.resid = c->x;
     add_wseg(dn, lw.w_down, m.H);
-    if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
+    if ((st = gemm_ws(c, K_GEMM_DOWN, dn, s, &S)) != DFLASH_OK) return st;
+    const bool last = l + 1 == m.L;
+    const void *nw = last ? c->w.final_norm : c->layers[l + 1].in_norm;
+    CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
+         return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, last ? xf : xn, nw, m.eps,
+                                 last ? m.K : 0, s);
+       }));
   }
-  // final norm on the K mask rows only (the anchor row yields no candidate)
-  const int RK = B * m.K;
-  CK(c, timed(c, K_RMSNORM, s, 8.0 * RK * m.H, 4.0 * RK * m.H, 1, [&] {
-       return launch_rmsnorm(c->dtype, RK, m.H, c->x, m.H, xf, m.H, c->w.final_norm, m.eps, m.K, s);
-     }));
   if (c->tc) {
     // tensor-core LM head: per-tile top-k in the GEMM epilogue (merged afterwards); full
     // logits are written only when the caller asks for them
@@ -740,7 +770,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
 // execute); the graph is launched on the caller's stream.
 static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt, cudaStream_t s) {
   const long long key = ((long long)B << 8) | bt.max_split;
-  const int gen = tc_gemm_generation(c->tc);
+  const int gen = tc_gemm_generation(c->tc) * 4096 + c->ws_gen;
   for (auto &g : c->graphs) {
     if (g.key != key) continue;
     if (g.exec && g.gen == gen) {
@@ -755,7 +785,9 @@ static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt
     if (g.seen++ < 1) break;            // run eagerly until the plan has been seen twice
     const int64_t l0 = c->launches;
     CK(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    c->capturing = true;
     dflash_status st = draft_layers(c, B, bt, 0, 0, nullptr, c->cap_stream);
+    c->capturing = false;
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
     c->launches = l0;
@@ -854,9 +886,11 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   }
   DraftBatch bt{dd, dd + B, dd + 2 * B, dd + 3 * B, dd + 4 * B + 1, B, max_split};
 
-  CK(c, timed(c, K_EMBED, s, (double)B * Q * m.H * (c->esz + 4), (double)B * Q * m.H, 1, [&] {
-       return launch_embed(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x,
-                           c->err_d, s);
+  // block embedding [anchor, mask x K] x scale, fused with the first layer's input norm
+  const OpOut xn0 = op_of(c, c->xn, (size_t)c->rows_max * m.H);
+  CK(c, timed(c, K_EMBED, s, (double)B * Q * m.H * (c->esz + 8), (double)B * Q * m.H * 4, 1, [&] {
+       return launch_embed_norm(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x,
+                                xn0, c->layers[0].in_norm, c->err_d, s);
      }));
   if (use_graph) {
     if ((st = run_layers_graph(c, B, bt, s)) != DFLASH_OK) return st;

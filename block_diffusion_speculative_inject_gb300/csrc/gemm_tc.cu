@@ -362,8 +362,10 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
 
 int tc_gemm_generation(const TcGemm *t) { return t ? t->generation : 0; }
 
+int tc_gemm_splits(const TcGemm *t, const GemmDesc &d) { return plan_for(t, d).S; }
+
 int tc_gemm_launches(const TcGemm *t, const GemmDesc &d) {
-  return plan_for(t, d).S > 1 ? 2 : 1;
+  return (plan_for(t, d).S > 1 && !d.part) ? 2 : 1;
 }
 
 template <int BN>
@@ -426,7 +428,15 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.ldy = d.ldy;
   p.resid = d.resid;
   p.err = t->err;
-  if (pl.S > 1) {
+  if (d.part) {
+    // partials mode: the caller's buffer holds [S][M][N]; with S == 1 it is the product itself
+    if (pl.S == 1) {
+      p.y = d.part;
+      p.ldy = d.N;
+      p.epi = EPI_STORE;
+    }
+    p.ws = d.part;
+  } else if (pl.S > 1) {
     const size_t need = (size_t)pl.S * d.M * d.N * sizeof(float);
     if (need > t->ws_bytes) {
       if (t->ws) cudaFree(t->ws);
@@ -446,7 +456,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     case 64: e = launch_bn<64>(t, 2, p, pl, s); break;
     default: e = launch_bn<128>(t, 3, p, pl, s); break;
   }
-  if (e != cudaSuccess || pl.S == 1) return e;
+  if (e != cudaSuccess || pl.S == 1 || d.part) return e;
   const long n = (long)d.M * d.N;
   k_splitk_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d.M, d.N, pl.S, t->ws, d.epi, d.y,
                                                                d.ldy, d.resid);

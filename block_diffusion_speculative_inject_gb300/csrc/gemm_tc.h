@@ -19,6 +19,9 @@ bool tc_encode_2d(TcGemm *t, const void *ptr, unsigned long long rows, unsigned 
 // graphs that used the old buffer must be re-captured.
 int tc_gemm_generation(const TcGemm *t);
 
+// Split-K factor the GEMM will use, and the floats its partials need in partials mode.
+int tc_gemm_splits(const TcGemm *t, const GemmDesc &d);
+
 // Number of kernel launches tc_gemm_run issues for this GEMM.
 int tc_gemm_launches(const TcGemm *t, const GemmDesc &d);
 // Runs Y = epilogue(X . W^T) for bf16 W and a bf16 (or bf16 hi/lo pair) X.

@@ -79,8 +79,14 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
   }
 }
 
-cudaError_t gemm_simt(int dtype, const GemmDesc &d, cudaStream_t s) {
-  if (d.M <= 0 || d.N <= 0) return cudaSuccess;
+cudaError_t gemm_simt(int dtype, const GemmDesc &d_in, cudaStream_t s) {
+  if (d_in.M <= 0 || d_in.N <= 0) return cudaSuccess;
+  GemmDesc d = d_in;
+  if (d.part) {                 // partials mode: one split, the product itself
+    d.y = d.part;
+    d.ldy = d.N;
+    d.epi = EPI_STORE;
+  }
   dim3 g((d.N + SB_N - 1) / SB_N, (d.M + SB_M - 1) / SB_M);
   if (dtype) k_gemm_simt<bf16><<<g, 256, 0, s>>>(d);
   else k_gemm_simt<float><<<g, 256, 0, s>>>(d);

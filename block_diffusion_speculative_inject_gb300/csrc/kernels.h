@@ -80,6 +80,20 @@ cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *ar
 cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
                               int32_t *topk_idx, float *topk_val, cudaStream_t s);
 
+// GEMM post-ops over split-K partials ws[S][M][N] (see k_post.cu).
+cudaError_t launch_post_qkv(int dtype, const ModelDims &m, int B, const float *ws, int S, float *qkv,
+                            const int32_t *ctx_len, const float2 *rope, const void *q_norm,
+                            const void *k_norm, cudaStream_t s);
+cudaError_t launch_post_norm(int dtype, int M, int H, const float *ws, int S, float *x, OpOut out,
+                             const void *w, float eps, int out_skip_k, cudaStream_t s);
+cudaError_t launch_post_swiglu(int M, int I, const float *ws, int S, OpOut h, cudaStream_t s);
+cudaError_t launch_post_kv(int dtype, const ModelDims &m, int T, const float *ws, int S,
+                           const int32_t *slot, const int32_t *pos, const float2 *rope,
+                           const void *const *k_norms, void *pool, cudaStream_t s);
+cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_t *anchors, int mask_id,
+                              const void *embed, float *x, OpOut out, const void *w, int *err,
+                              cudaStream_t s);
+
 cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *target,
                           int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
                           cudaStream_t s);
