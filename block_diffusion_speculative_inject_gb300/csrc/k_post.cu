@@ -12,8 +12,20 @@ namespace dflash {
 
 __device__ __forceinline__ float psum(const float *__restrict__ ws, int S, int M, int N, int m,
                                       int n) {
+  // four independent loads in flight per round trip; the sum keeps split order
   float a = 0.f;
-  for (int s = 0; s < S; ++s) a += __ldg(ws + ((size_t)s * M + m) * N + n);
+  int s = 0;
+  for (; s + 4 <= S; s += 4) {
+    const float v0 = __ldg(ws + ((size_t)(s + 0) * M + m) * N + n);
+    const float v1 = __ldg(ws + ((size_t)(s + 1) * M + m) * N + n);
+    const float v2 = __ldg(ws + ((size_t)(s + 2) * M + m) * N + n);
+    const float v3 = __ldg(ws + ((size_t)(s + 3) * M + m) * N + n);
+    a += v0;
+    a += v1;
+    a += v2;
+    a += v3;
+  }
+  for (; s < S; ++s) a += __ldg(ws + ((size_t)s * M + m) * N + n);
   return a;
 }
 
@@ -101,19 +113,32 @@ __global__ void __launch_bounds__(PN_THREADS) k_post_norm(int M, int S, const fl
   const int m = blockIdx.x;
   const int n4 = H / 4;
   float4 v[PN_VEC];
+  // residual first, then the partials split by split (all of a split's loads in flight)
+#pragma unroll
+  for (int t = 0; t < PN_VEC; ++t) {
+    const int i = threadIdx.x + t * PN_THREADS;
+    v[t] = (x && i < n4) ? ((const float4 *)(x + (size_t)m * H))[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s = 0; s < S; ++s) {
+    const float4 *src = (const float4 *)(ws + ((size_t)s * M + m) * H);
+    float4 p[PN_VEC];
+#pragma unroll
+    for (int t = 0; t < PN_VEC; ++t) {
+      const int i = threadIdx.x + t * PN_THREADS;
+      p[t] = i < n4 ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int t = 0; t < PN_VEC; ++t) {
+      v[t].x += p[t].x; v[t].y += p[t].y; v[t].z += p[t].z; v[t].w += p[t].w;
+    }
+  }
   float ss = 0.f;
 #pragma unroll
   for (int t = 0; t < PN_VEC; ++t) {
     const int i = threadIdx.x + t * PN_THREADS;
     if (i < n4) {
-      float4 a = x ? ((const float4 *)(x + (size_t)m * H))[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < S; ++s) {
-        const float4 p = __ldg((const float4 *)(ws + ((size_t)s * M + m) * H) + i);
-        a.x += p.x; a.y += p.y; a.z += p.z; a.w += p.w;
-      }
-      v[t] = a;
-      if (x) ((float4 *)(x + (size_t)m * H))[i] = a;
-      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+      if (x) ((float4 *)(x + (size_t)m * H))[i] = v[t];
+      ss += v[t].x * v[t].x + v[t].y * v[t].y + v[t].z * v[t].z + v[t].w * v[t].w;
     }
   }
   int orow = m;
