@@ -9,8 +9,10 @@
 // slab through the pipeline once. When X is an exact bf16 hi/lo pair (an fp32 activation),
 // both planes are multiplied by the same staged weight tile and accumulate into the same
 // TMEM columns, so the weights are read from HBM once. Small grids are split along K
-// (split-K) so every SM streams weights; the fp32 partials are summed in a fixed order by
-// a second kernel that also applies the epilogue.
+// (split-K, S <= 8) so every SM streams weights; the S CTAs of one output tile form a
+// thread-block cluster, stage their fp32 partial tiles in their own shared memory, and the
+// cluster's rank-0 CTA sums them through distributed shared memory in rank order and
+// applies the epilogue — no partials go through HBM and the sum order is fixed.
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 owns the TMEM allocation and
 // its lane 0 issues the MMAs, warps 2-5 (one per 32-lane TMEM quarter) run the epilogue.
@@ -51,7 +53,6 @@ struct TcParams {
   float *y;
   int ldy;
   const float *resid;
-  float *ws;                          // [S][M][N] partials when S > 1
   int topk;                           // EPI_TOPK
   int2 *cand;                         // EPI_TOPK: [n_tiles][M][topk]
   int *err;
@@ -182,18 +183,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
         }
         continue;
       }
+      if (p.S > 1) {
+        // split-K: stage this CTA's partial tile [BN][128] for the cluster's reduction
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tile[(c0 + j) * TC_BM + q * 32 + lane] = ok ? __uint_as_float(r[j]) : 0.f;
+        continue;
+      }
       if (!ok || n >= p.N) continue;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = m0 + c0 + j;
         if (m >= p.M) break;
         const float v = __uint_as_float(r[j]);
-        if (p.S > 1) {
-          p.ws[((size_t)split * p.M + m) * p.N + n] = v;
-        } else {
-          const size_t o = (size_t)m * p.ldy + n;
-          p.y[o] = p.epi == EPI_RESID ? p.resid[o] + v : v;
-        }
+        const size_t o = (size_t)m * p.ldy + n;
+        p.y[o] = p.epi == EPI_RESID ? p.resid[o] + v : v;
       }
     }
     if (p.epi == EPI_TOPK) {
@@ -243,22 +246,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  if (p.S > 1) {
+    // every split's partial tile is staged; rank 0 sums them in rank order
+    cluster_sync_all();
+    if (cluster_ctarank() == 0 && warp >= 2) {
+      const int q = warp & 3;
+      const int n = n0 + q * 32 + lane;
+      const uint32_t base = smem_u32(gen_tiles);
+      for (int c = 0; c < BN; ++c) {
+        const int m = m0 + c;
+        if (m >= p.M) break;
+        const uint32_t off = base + (uint32_t)((c * TC_BM + q * 32 + lane) * 4);
+        float a = 0.f;
+        for (int rk = 0; rk < p.S; ++rk) a += dsmem_ld(dsmem_addr(off, (uint32_t)rk));
+        if (n < p.N) {
+          const size_t o = (size_t)m * p.ldy + n;
+          p.y[o] = p.epi == EPI_RESID ? p.resid[o] + a : a;
+        }
+      }
+    }
+    cluster_sync_all();               // peers keep their shared memory until rank 0 is done
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols<BN>());
   }
-}
-
-// Sum of the S split-K partials in split order, then the epilogue.
-__global__ void k_splitk_reduce(int M, int N, int S, const float *__restrict__ ws, int epi,
-                                float *y, int ldy, const float *resid) {
-  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long)M * N) return;
-  const int m = (int)(i / N), n = (int)(i % N);
-  float a = 0.f;
-  for (int s = 0; s < S; ++s) a += ws[((size_t)s * M + m) * N + n];
-  const size_t o = (size_t)m * ldy + n;
-  y[o] = epi == EPI_RESID ? resid[o] + a : a;
 }
 
 // ------------------------------------------------------------------------- host side
@@ -267,8 +279,6 @@ struct TcGemm {
   int *err = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
-  float *ws = nullptr;
-  size_t ws_bytes = 0;
   int generation = 0;
   bool attr_set[4] = {false, false, false, false};
 };
@@ -291,7 +301,6 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
 
 void tc_gemm_destroy(TcGemm *t) {
   if (!t) return;
-  if (t->ws) cudaFree(t->ws);
   delete t;
 }
 
@@ -348,7 +357,7 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   const int base = p.t_tiles * p.n_tiles;
   const int target = 2 * t->num_sms;
   int S = (target + base - 1) / base;
-  S = std::max(1, std::min(S, std::min(32, p.kb / 4)));
+  S = std::max(1, std::min(S, std::min(8, p.kb / 4)));    // a portable cluster holds 8 CTAs
   if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
   p.kb_per = (p.kb + S - 1) / S;
   p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
@@ -362,11 +371,9 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
 
 int tc_gemm_generation(const TcGemm *t) { return t ? t->generation : 0; }
 
-int tc_gemm_splits(const TcGemm *t, const GemmDesc &d) { return plan_for(t, d).S; }
+int tc_gemm_splits(const TcGemm *, const GemmDesc &) { return 1; }   // reduced in-cluster
 
-int tc_gemm_launches(const TcGemm *t, const GemmDesc &d) {
-  return (plan_for(t, d).S > 1 && !d.part) ? 2 : 1;
-}
+int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 1; }
 
 template <int BN>
 static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan &pl, cudaStream_t s) {
@@ -376,9 +383,19 @@ static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan 
     if (e != cudaSuccess) return e;
     t->attr_set[slot] = true;
   }
-  dim3 grid(pl.t_tiles, pl.n_tiles, pl.S);
-  k_gemm_tc<BN><<<grid, TC_THREADS, pl.smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.t_tiles, pl.n_tiles, pl.S);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = pl.S;      // the S splits of one output tile
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, p);
 }
 
 cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
@@ -429,25 +446,10 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.resid = d.resid;
   p.err = t->err;
   if (d.part) {
-    // partials mode: the caller's buffer holds [S][M][N]; with S == 1 it is the product itself
-    if (pl.S == 1) {
-      p.y = d.part;
-      p.ldy = d.N;
-      p.epi = EPI_STORE;
-    }
-    p.ws = d.part;
-  } else if (pl.S > 1) {
-    const size_t need = (size_t)pl.S * d.M * d.N * sizeof(float);
-    if (need > t->ws_bytes) {
-      if (t->ws) cudaFree(t->ws);
-      t->ws = nullptr;
-      t->ws_bytes = 0;
-      cudaError_t e = cudaMalloc(&t->ws, need);
-      if (e != cudaSuccess) return e;
-      t->ws_bytes = need;
-      ++t->generation;
-    }
-    p.ws = t->ws;
+    // partials mode: the (already reduced) product goes to the caller's buffer [M][N]
+    p.y = d.part;
+    p.ldy = d.N;
+    p.epi = EPI_STORE;
   }
   cudaError_t e;
   switch (pl.bn) {
@@ -456,11 +458,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     case 64: e = launch_bn<64>(t, 2, p, pl, s); break;
     default: e = launch_bn<128>(t, 3, p, pl, s); break;
   }
-  if (e != cudaSuccess || pl.S == 1 || d.part) return e;
-  const long n = (long)d.M * d.N;
-  k_splitk_reduce<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d.M, d.N, pl.S, t->ws, d.epi, d.y,
-                                                               d.ldy, d.resid);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dflash
