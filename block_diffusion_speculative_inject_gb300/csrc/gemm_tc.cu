@@ -10,9 +10,10 @@
 // both planes are multiplied by the same staged weight tile and accumulate into the same
 // TMEM columns, so the weights are read from HBM once. Small grids are split along K
 // (split-K, S <= 8) so every SM streams weights; the S CTAs of one output tile form a
-// thread-block cluster, stage their fp32 partial tiles in their own shared memory, and the
-// cluster's rank-0 CTA sums them through distributed shared memory in rank order and
-// applies the epilogue — no partials go through HBM and the sum order is fixed.
+// thread-block cluster, stage their fp32 partial tiles in their own shared memory, and each
+// rank sums a share of the tile's columns over all ranks through distributed shared memory,
+// in rank order, and applies the epilogue — no partials go through HBM and the sum order
+// is fixed.
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA loads, warp 1 owns the TMEM allocation and
 // its lane 0 issues the MMAs, warps 2-5 (one per 32-lane TMEM quarter) run the epilogue.
@@ -247,25 +248,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (p.S > 1) {
-    // every split's partial tile is staged; rank 0 sums them in rank order
+    // every split's partial tile is staged; rank r sums columns r, r + S, ... over all
+    // ranks, in rank order
     cluster_sync_all();
-    if (cluster_ctarank() == 0 && warp >= 2) {
+    if (warp >= 2) {
       const int q = warp & 3;
       const int n = n0 + q * 32 + lane;
       const uint32_t base = smem_u32(gen_tiles);
-      for (int c = 0; c < BN; ++c) {
+      for (int c = (int)cluster_ctarank(); c < BN; c += p.S) {
         const int m = m0 + c;
         if (m >= p.M) break;
         const uint32_t off = base + (uint32_t)((c * TC_BM + q * 32 + lane) * 4);
+        float v[8];
+#pragma unroll
+        for (int rk = 0; rk < 8; ++rk) v[rk] = rk < p.S ? dsmem_ld(dsmem_addr(off, (uint32_t)rk)) : 0.f;
         float a = 0.f;
-        for (int rk = 0; rk < p.S; ++rk) a += dsmem_ld(dsmem_addr(off, (uint32_t)rk));
+#pragma unroll
+        for (int rk = 0; rk < 8; ++rk) a += v[rk];
         if (n < p.N) {
           const size_t o = (size_t)m * p.ldy + n;
           p.y[o] = p.epi == EPI_RESID ? p.resid[o] + a : a;
         }
       }
     }
-    cluster_sync_all();               // peers keep their shared memory until rank 0 is done
+    cluster_sync_all();               // peers keep their shared memory until all are done
   }
   if (warp == 1) {
     tc_fence_after();
