@@ -68,6 +68,7 @@ constexpr int tmem_cols() {
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_trigger();
   constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
   constexpr uint32_t B_BYTES = BN * TC_BK * 2;
   const uint32_t stage_bytes = A_BYTES + B_BYTES * (p.split ? 2 : 1);
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (!(warp == 0 && lane == 0 && nkb > 0)) pdl_wait();   // the producer waits after its prefetch
 
   if (warp == 0 && lane == 0 && nkb > 0) {
     // ---------------- TMA producer
@@ -112,15 +114,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     while (ws + 1 < p.n_wseg && n0 >= p.w_n0[ws + 1]) ++ws;
     const CUtensorMap *wm = &p.wmap[ws];
     const int wrow = n0 - p.w_n0[ws];
+    // the first stages' weight tiles do not depend on the previous kernel: start streaming
+    // them before waiting for it
+    const int pre = min(stages, nkb);
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t fb = full0 + 8u * i;
+      mbar_expect_tx(fb, stage_bytes);
+      tma_load_2d(tiles + (uint32_t)i * stage_bytes, wm, (kb0 + i) * TC_BK, wrow, fb);
+    }
+    pdl_wait();
     int issued = 0;
     for (int i = 0; i < nkb; ++i) {
       const int s = i % stages, u = i / stages;
-      if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err)) break;
       const uint32_t st = tiles + (uint32_t)s * stage_bytes;
       const uint32_t fb = full0 + 8u * s;
-      mbar_expect_tx(fb, stage_bytes);
       const int k = (kb0 + i) * TC_BK;
-      tma_load_2d(st, wm, k, wrow, fb);
+      if (i >= pre) {
+        if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(fb, stage_bytes);
+        tma_load_2d(st, wm, k, wrow, fb);
+      }
       if (p.split) {
         tma_load_2d(st + A_BYTES, &p.xmap[0], k, m0, fb);
         tma_load_2d(st + A_BYTES + B_BYTES, &p.xmap[1], k, m0, fb);
@@ -131,6 +144,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
       }
       issued = i + 1;
     }
+    if (issued < pre) issued = pre;
     // drain: every load this thread issued has landed before the CTA may exit
     for (int s = 0; s < stages && s < issued; ++s) {
       const int last = s + stages * ((issued - 1 - s) / stages);
@@ -394,13 +408,15 @@ static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan 
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = pl.S;      // the S splits of one output tile
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, p);
 }
 

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) k_attn_split(
     const int32_t *ctx_len, const int32_t *n_split, const int32_t *split_len,
     const int32_t *page_off, const int32_t *pages, int max_split, float scale, float *part_o,
     float *part_ml) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float sm[];
   float *qs = sm;                              // [R][HD]
   float *ks = qs + AT_MAXR * HD;               // [KT][HD+1]
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
                                                                const float *part_o,
                                                                const float *part_ml, const float *qkv,
                                                                float scale_log2, OpOut o) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int DPL = HD / 32;
   constexpr int KP = HD + 1;                       // padded row: lane-per-key reads are conflict free
   __shared__ float ks[32 * KP];
@@ -204,18 +208,16 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
                                (int)smem);
       if (e != cudaSuccess) return e;
       dim3 g(bt.max_split, m.nkv, bt.B);
-      k_attn_split<T, HD><<<g, 256, smem, s>>>(
-          m.L, m.nq, m.nkv, m.Q(), layer, qkv, (const T *)pool, bt.ctx_len, bt.n_split,
-          bt.split_len, bt.page_off, bt.pages, bt.max_split, scale_log2, part_o, part_ml);
-      e = cudaGetLastError();
+      e = launch_pdl(k_attn_split<T, HD>, g, dim3(256), smem, s, m.L, m.nq, m.nkv, m.Q(), layer, qkv,
+                     (const T *)pool, bt.ctx_len, bt.n_split, bt.split_len, bt.page_off, bt.pages,
+                     bt.max_split, scale_log2, part_o, part_ml);
     }
     if (e != cudaSuccess) return e;
   }
   const int R = (m.nq / m.nkv) * m.Q();
   dim3 g2(m.nkv, bt.B, (R + CB_ROWS - 1) / CB_ROWS);
-  k_attn_combine<HD><<<g2, 32 * CB_ROWS, 0, s>>>(m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split, part_o,
-                                        part_ml, qkv, scale_log2, o);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_combine<HD>, g2, dim3(32 * CB_ROWS), 0, s, m.nq, m.nkv, m.Q(), bt.n_split,
+                    bt.max_split, (const float *)part_o, (const float *)part_ml, qkv, scale_log2, o);
 }
 
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &bt, int layer,

@@ -67,8 +67,9 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4 &hi, uint4 &lo
 
 __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid_constant__ AttnTcParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_trigger();
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int ns = p.n_split[b];
+  const int ns = p.n_split[b];                           // descriptor: staged before the chain
   if (s >= ns) return;                                   // uniform for the CTA
   const int n_ctx = p.ctx_len[b];
   const int k_begin = s * p.split_len[b];
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     tmem_alloc(smem_u32(tmem_slot), AT_TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();                                            // q comes from the previous kernel
   if (warp >= 2) {
     // Q rows (scaled, split into hi/lo) in the 128-byte-swizzled K-major layout
     const int r = threadIdx.x - 64;
@@ -325,8 +327,7 @@ cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &bt, int l
   p.part_ml = part_ml;
   p.err = maps->err;
   dim3 g(bt.max_split, m.nkv, bt.B);
-  k_attn_split_tc<<<g, AT_TC_THREADS, AT_TC_SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_split_tc, g, dim3(AT_TC_THREADS), AT_TC_SMEM, s, p);
 }
 
 }  // namespace dflash

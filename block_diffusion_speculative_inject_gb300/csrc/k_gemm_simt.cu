@@ -21,6 +21,8 @@ __device__ __forceinline__ float load_x(const GemmDesc &d, int s, size_t idx) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float xs[SB_K][SB_M + 1];
   __shared__ float ws[SB_K][SB_N + 1];
   const int m0 = blockIdx.y * SB_M, n0 = blockIdx.x * SB_N;
@@ -88,9 +90,8 @@ cudaError_t gemm_simt(int dtype, const GemmDesc &d_in, cudaStream_t s) {
     d.epi = EPI_STORE;
   }
   dim3 g((d.N + SB_N - 1) / SB_N, (d.M + SB_M - 1) / SB_M);
-  if (dtype) k_gemm_simt<bf16><<<g, 256, 0, s>>>(d);
-  else k_gemm_simt<float><<<g, 256, 0, s>>>(d);
-  return cudaGetLastError();
+  if (dtype) return launch_pdl(k_gemm_simt<bf16>, g, dim3(256), 0, s, d);
+  return launch_pdl(k_gemm_simt<float>, g, dim3(256), 0, s, d);
 }
 
 }  // namespace dflash

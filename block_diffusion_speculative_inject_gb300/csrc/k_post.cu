@@ -62,6 +62,8 @@ template <typename TW>
 __global__ void k_post_qkv(int M, int S, const float *ws, int Q, int nq, int nkv, int hd,
                            float *qkv, const int32_t *ctx_len, const float2 *rope, const TW *q_norm,
                            const TW *k_norm, float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const int heads = nq + 2 * nkv;
@@ -90,11 +92,11 @@ cudaError_t launch_post_qkv(int dtype, const ModelDims &m, int B, const float *w
   const int warps = rows * (m.nq + 2 * m.nkv);
   dim3 g((warps + 7) / 8);
   const void *qn = m.qk_norm ? q_norm : nullptr, *kn = m.qk_norm ? k_norm : nullptr;
-  if (dtype) k_post_qkv<bf16><<<g, 256, 0, s>>>(rows, S, ws, m.Q(), m.nq, m.nkv, m.hd, qkv, ctx_len,
-                                                rope, (const bf16 *)qn, (const bf16 *)kn, m.eps);
-  else k_post_qkv<float><<<g, 256, 0, s>>>(rows, S, ws, m.Q(), m.nq, m.nkv, m.hd, qkv, ctx_len, rope,
-                                           (const float *)qn, (const float *)kn, m.eps);
-  return cudaGetLastError();
+  if (dtype)
+    return launch_pdl(k_post_qkv<bf16>, g, dim3(256), 0, s, rows, S, ws, m.Q(), m.nq, m.nkv, m.hd, qkv,
+                      ctx_len, rope, (const bf16 *)qn, (const bf16 *)kn, m.eps);
+  return launch_pdl(k_post_qkv<float>, g, dim3(256), 0, s, rows, S, ws, m.Q(), m.nq, m.nkv, m.hd, qkv,
+                    ctx_len, rope, (const float *)qn, (const float *)kn, m.eps);
 }
 
 // ------------------------------------------------------------------------- residual + RMSNorm
@@ -109,6 +111,8 @@ template <typename TW>
 __global__ void __launch_bounds__(PN_THREADS) k_post_norm(int M, int S, const float *ws, int H,
                                                           float *x, OpOut out, const TW *w,
                                                           float eps, int out_skip_k) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[PN_THREADS / 32];
   const int m = blockIdx.x;
   const int n4 = H / 4;
@@ -172,13 +176,17 @@ cudaError_t launch_post_norm(int dtype, int M, int H, const float *ws, int S, fl
                              const void *w, float eps, int out_skip_k, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (H % 4 || H > PN_THREADS * 4 * PN_VEC) return cudaErrorInvalidValue;
-  if (dtype) k_post_norm<bf16><<<M, PN_THREADS, 0, s>>>(M, S, ws, H, x, out, (const bf16 *)w, eps, out_skip_k);
-  else k_post_norm<float><<<M, PN_THREADS, 0, s>>>(M, S, ws, H, x, out, (const float *)w, eps, out_skip_k);
-  return cudaGetLastError();
+  if (dtype)
+    return launch_pdl(k_post_norm<bf16>, dim3(M), dim3(PN_THREADS), 0, s, M, S, ws, H, x, out,
+                      (const bf16 *)w, eps, out_skip_k);
+  return launch_pdl(k_post_norm<float>, dim3(M), dim3(PN_THREADS), 0, s, M, S, ws, H, x, out,
+                    (const float *)w, eps, out_skip_k);
 }
 
 // ------------------------------------------------------------------------- SwiGLU
 __global__ void k_post_swiglu(int M, int S, const float *ws, int I, OpOut h) {
+  pdl_wait();
+  pdl_trigger();
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)M * I) return;
   const int m = (int)(i / I), c = (int)(i % I);
@@ -189,8 +197,7 @@ __global__ void k_post_swiglu(int M, int S, const float *ws, int I, OpOut h) {
 cudaError_t launch_post_swiglu(int M, int I, const float *ws, int S, OpOut h, cudaStream_t s) {
   const long n = (long)M * I;
   if (n == 0) return cudaSuccess;
-  k_post_swiglu<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(M, S, ws, I, h);
-  return cudaGetLastError();
+  return launch_pdl(k_post_swiglu, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, M, S, ws, I, h);
 }
 
 // ------------------------------------------------------------------------- injection into the cache
@@ -200,6 +207,8 @@ template <typename T>
 __global__ void k_post_kv(int Trows, int S, const float *ws, int L, int nkv, int hd,
                           const int32_t *slot, const int32_t *pos, const float2 *rope, KNorms kn,
                           int qk_norm, float eps, T *pool) {
+  pdl_wait();
+  pdl_trigger();
   const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (w >= Trows * L * nkv) return;
@@ -235,11 +244,11 @@ cudaError_t launch_post_kv(int dtype, const ModelDims &m, int T, const float *ws
   for (int l = 0; l < m.L && l < 16; ++l) kn.p[l] = k_norms[l];
   const long warps = (long)T * m.L * m.nkv;
   dim3 g((unsigned)((warps + 7) / 8));
-  if (dtype) k_post_kv<bf16><<<g, 256, 0, s>>>(T, S, ws, m.L, m.nkv, m.hd, slot, pos, rope, kn,
-                                               m.qk_norm, m.eps, (bf16 *)pool);
-  else k_post_kv<float><<<g, 256, 0, s>>>(T, S, ws, m.L, m.nkv, m.hd, slot, pos, rope, kn, m.qk_norm,
-                                          m.eps, (float *)pool);
-  return cudaGetLastError();
+  if (dtype)
+    return launch_pdl(k_post_kv<bf16>, g, dim3(256), 0, s, T, S, ws, m.L, m.nkv, m.hd, slot, pos, rope,
+                      kn, m.qk_norm, m.eps, (bf16 *)pool);
+  return launch_pdl(k_post_kv<float>, g, dim3(256), 0, s, T, S, ws, m.L, m.nkv, m.hd, slot, pos, rope,
+                    kn, m.qk_norm, m.eps, (float *)pool);
 }
 
 // ------------------------------------------------------------------------- embedding + first norm
@@ -250,6 +259,8 @@ __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, 
                                                            int mask_id, float scale, const TW *embed,
                                                            float *x, OpOut out, const TW *w, float eps,
                                                            int *err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[PN_THREADS / 32];
   const int r = blockIdx.x, b = r / Q, j = r % Q;
   int tok = j == 0 ? anchors[b] : mask_id;
@@ -288,13 +299,11 @@ cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_
                               cudaStream_t s) {
   if (m.H > 4 * PN_VEC * PN_THREADS) return cudaErrorInvalidValue;
   dim3 g(B * m.Q());
-  if (dtype) k_embed_norm<bf16><<<g, PN_THREADS, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
-                                                        (const bf16 *)embed, x, out, (const bf16 *)w,
-                                                        m.eps, err);
-  else k_embed_norm<float><<<g, PN_THREADS, 0, s>>>(m.H, m.Q(), m.V, anchors, mask_id, m.emb_scale,
-                                                   (const float *)embed, x, out, (const float *)w,
-                                                   m.eps, err);
-  return cudaGetLastError();
+  if (dtype)
+    return launch_pdl(k_embed_norm<bf16>, g, dim3(PN_THREADS), 0, s, m.H, m.Q(), m.V, anchors, mask_id,
+                      m.emb_scale, (const bf16 *)embed, x, out, (const bf16 *)w, m.eps, err);
+  return launch_pdl(k_embed_norm<float>, g, dim3(PN_THREADS), 0, s, m.H, m.Q(), m.V, anchors, mask_id,
+                    m.emb_scale, (const float *)embed, x, out, (const float *)w, m.eps, err);
 }
 
 }  // namespace dflash

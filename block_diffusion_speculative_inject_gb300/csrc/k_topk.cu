@@ -111,6 +111,8 @@ __device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argma
 __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x;
   const float *x = logits + (size_t)row * V;
   block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; }, argmax + row,
@@ -128,6 +130,8 @@ constexpr int MERGE_CAP = 1024;
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
                                                            const int2 *cand, int32_t *argmax,
                                                            int32_t *topk_idx, float *topk_val) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int2 pool[MERGE_CAP];
   __shared__ int n_pool;
   __shared__ float thr_val[32];
@@ -183,16 +187,16 @@ cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *ar
                         int32_t *topk_idx, float *topk_val, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
-  k_topk_rows<<<rows, TK_THREADS, 0, s>>>(V, k, logits, argmax, topk_idx, topk_val);
-  return cudaGetLastError();
+  return launch_pdl(k_topk_rows, dim3(rows), dim3(TK_THREADS), 0, s, V, k, logits, argmax, topk_idx,
+                    topk_val);
 }
 
 cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
                               int32_t *topk_idx, float *topk_val, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
-  k_topk_merge<<<rows, TK_THREADS, 0, s>>>(tiles, rows, k, cand, argmax, topk_idx, topk_val);
-  return cudaGetLastError();
+  return launch_pdl(k_topk_merge, dim3(rows), dim3(TK_THREADS), 0, s, tiles, rows, k, cand, argmax,
+                    topk_idx, topk_val);
 }
 
 }  // namespace dflash

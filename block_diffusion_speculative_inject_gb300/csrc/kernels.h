@@ -27,32 +27,6 @@ struct DraftBatch {
 // dtype (storage type of weights / features / cache): 0 = fp32, 1 = bf16.
 cudaError_t gemm_simt(int dtype, const GemmDesc &d, cudaStream_t s);
 
-// x[b*(K+1) + j] = embed[token] * scale, token = anchor (j = 0) or mask id; fp32 out.
-cudaError_t launch_embed(int dtype, const ModelDims &m, int B, const int32_t *anchors,
-                         int mask_id, const void *embed, float *x, int *err, cudaStream_t s);
-
-// out row r <- rmsnorm(in row map(r)) as a GEMM operand; map(r) = r, or with
-// skip_anchor_k = K > 0 the K mask rows of each (K+1)-row block:
-// (r / K) * (K + 1) + r % K + 1.
-cudaError_t launch_rmsnorm(int dtype, int rows, int H, const float *in, int ld_in, OpOut out,
-                           int ld_out, const void *w, float eps, int skip_anchor_k,
-                           cudaStream_t s);
-
-// In place on fp32 qkv rows [B*(K+1), qkv_dim]: per-head q/k RMSNorm (if enabled) + RoPE
-// at position ctx_len[b] + j.
-cudaError_t launch_qk_norm_rope(int dtype, const ModelDims &m, int B, float *qkv,
-                                const int32_t *ctx_len, const float2 *rope,
-                                const void *q_norm, const void *k_norm, cudaStream_t s);
-
-// Injection epilogue: fp32 kv rows [T, L*2*kv_dim] (per layer [k | v]) -> k-norm + RoPE at
-// pos[t] -> KV pool slot[t] (page * 64 + offset) of every layer, in the storage type.
-cudaError_t launch_inject_kv(int dtype, const ModelDims &m, int T, const float *kv,
-                             const int32_t *slot, const int32_t *pos, const float2 *rope,
-                             const void *const *k_norms, void *pool, cudaStream_t s);
-
-// h = silu(gate) * up from fp32 rows [gate (I) | up (I)], written as a GEMM operand.
-cudaError_t launch_swiglu(int rows, int I, const float *gu, OpOut h, cudaStream_t s);
-
 // Tensor maps over the KV pool for the tensor-core attention: K blocks viewed as rows of hd
 // values (box 64 x 64), V blocks ([hd][64]) as rows of 64 positions (box 64 x 128).
 struct AttnMaps {
