@@ -375,8 +375,9 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   p.n_tiles = (d.N + TC_BM - 1) / TC_BM;
   p.kb = d.K / TC_BK;
   const int base = p.t_tiles * p.n_tiles;
-  const int target = 2 * t->num_sms;
-  int S = (target + base - 1) / base;
+  // as many splits as fit the grid into one wave of resident CTAs (two per SM at small BN)
+  const int slots = (p.bn <= 32 ? 2 : 1) * t->num_sms;
+  int S = std::max(1, slots / base);
   S = std::max(1, std::min(S, std::min(8, p.kb / 4)));    // a portable cluster holds 8 CTAs
   if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
   p.kb_per = (p.kb + S - 1) / S;

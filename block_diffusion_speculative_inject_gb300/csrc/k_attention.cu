@@ -142,11 +142,30 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
   const int G = nq / nkv, R = G * Q;
   const int qkv_dim = (nq + 2 * nkv) * HD;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < Q * HD; i += blockDim.x) {
-    const int kk = i / HD, d = i % HD;
-    const float *row = qkv + ((size_t)b * Q + kk) * qkv_dim + (size_t)nq * HD;
-    ks[kk * KP + d] = row[(size_t)kvh * HD + d];
-    vs[kk * HD + d] = row[(size_t)nkv * HD + (size_t)kvh * HD + d];
+  {
+    // block keys and values: float4 loads, all issued before any store
+    constexpr int V4 = HD / 4;
+    float4 kv4[4], vv4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = tid + u * 32 * CB_ROWS;   // float4 index over [Q][HD/4]
+      const int kk = i / V4, d4 = i % V4;
+      const bool in = kk < Q;
+      const float4 *row = (const float4 *)(qkv + ((size_t)b * Q + (in ? kk : 0)) * qkv_dim + (size_t)nq * HD);
+      kv4[u] = in ? row[(size_t)kvh * V4 + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      vv4[u] = in ? row[(size_t)(nkv + kvh) * V4 + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = tid + u * 32 * CB_ROWS;
+      const int kk = i / V4, d4 = i % V4;
+      if (kk < Q) {
+        const float4 a = kv4[u], v = vv4[u];
+        ks[kk * KP + 4 * d4 + 0] = a.x; ks[kk * KP + 4 * d4 + 1] = a.y;
+        ks[kk * KP + 4 * d4 + 2] = a.z; ks[kk * KP + 4 * d4 + 3] = a.w;
+        *(float4 *)&vs[kk * HD + 4 * d4] = v;
+      }
+    }
   }
   const int r = blockIdx.z * CB_ROWS + warp;
   const int g = r / Q, j = r % Q, h = kvh * G + g;

@@ -117,25 +117,20 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       const int g = r / p.Q, j = r % p.Q;
       src = p.qkv + ((size_t)b * p.Q + j) * qkv_dim + (size_t)(kvh * G + g) * 128;
     }
-#pragma unroll 1
-    for (int c4 = 0; c4 < 16; c4 += 4) {            // 4 chunks of 8 values per round trip
-      float4 raw[8];
+    float4 raw[32];                                  // the whole row in one round trip
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        raw[i] = src ? *(const float4 *)(src + 8 * c4 + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 32; ++i) raw[i] = src ? *(const float4 *)(src + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int cc4 = 0; cc4 < 4; ++cc4) {
-        const int c = c4 + cc4;
-        const float4 a = raw[2 * cc4], d = raw[2 * cc4 + 1];
-        float v[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
+    for (int c = 0; c < 16; ++c) {
+      const float4 a = raw[2 * c], d = raw[2 * c + 1];
+      float v[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] *= p.scale_log2;
-        uint4 hi, lo;
-        split8(v, hi, lo);
-        const int half = c >> 3, cc = c & 7;
-        *(uint4 *)(gbase + (0 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = hi;
-        *(uint4 *)(gbase + (1 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = lo;
-      }
+      for (int i = 0; i < 8; ++i) v[i] *= p.scale_log2;
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      const int half = c >> 3, cc = c & 7;
+      *(uint4 *)(gbase + (0 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = hi;
+      *(uint4 *)(gbase + (1 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = lo;
     }
     fence_proxy_async_smem();
   }

@@ -268,14 +268,19 @@ __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, 
     if (threadIdx.x == 0) raise_err(err, DEV_ERR_TOKEN);
     tok = 0;
   }
-  const TW *src = embed + (size_t)tok * H;
+  const TW *__restrict__ src = embed + (size_t)tok * H;
   float vals[4 * PN_VEC];
+  // all loads first (the row is read once), then the stores
+#pragma unroll
+  for (int t = 0; t < 4 * PN_VEC; ++t) {
+    const int i = threadIdx.x + t * PN_THREADS;
+    vals[t] = i < H ? to_f(src[i]) * scale : 0.f;
+  }
   float ss = 0.f;
 #pragma unroll
   for (int t = 0; t < 4 * PN_VEC; ++t) {
     const int i = threadIdx.x + t * PN_THREADS;
     if (i < H) {
-      vals[t] = to_f(src[i]) * scale;
       x[(size_t)r * H + i] = vals[t];
       ss += vals[t] * vals[t];
     }
