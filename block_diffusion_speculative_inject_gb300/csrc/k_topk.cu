@@ -120,11 +120,11 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
              topk_val ? topk_val + (size_t)row * k : nullptr);
 }
 
-// Merge of per-tile sorted candidate lists. The k-th best of the tiles' first candidates is
-// a lower bound T of the row's k-th best value (those k tiles each hold a value >= T), so
-// only candidates >= T can be in the result: they are gathered in one parallel pass and
-// selected exactly. (If more than MERGE_CAP candidates tie at or above T, every candidate
-// is scanned instead.)
+// Merge of per-tile sorted candidate lists. With at least k tiles, the k-th best of the
+// tiles' first candidates is a lower bound T of the row's k-th best value (those k tiles
+// each hold a value >= T), so only candidates >= T can be in the result: they are gathered
+// in one parallel pass and selected exactly. (If more than MERGE_CAP candidates tie at or
+// above T, every candidate is scanned instead; with fewer than k tiles all are ranked.)
 constexpr int MERGE_CAP = 1024;
 
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
@@ -139,8 +139,20 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
   __shared__ int dummy;
   const int row = blockIdx.x;
   auto at = [&](int t, int j) { return cand[((size_t)t * rows + row) * k + j]; };
+  if (tiles < k) {
+    // the bound below needs k tiles; with fewer there are at most k*k candidates: rank all
+    block_topk(tiles * k, k,
+               [&](int i, float &v, int &id) {
+                 const int2 c = at(i / k, i % k);
+                 v = __int_as_float(c.x);
+                 id = c.y;
+               },
+               argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
+               topk_val ? topk_val + (size_t)row * k : nullptr);
+    return;
+  }
   // 1) lower bound: k-th best of the tiles' first candidates
-  const int kk = min(k, tiles);
+  const int kk = k;
   block_topk(tiles, kk,
              [&](int i, float &v, int &id) {
                const int2 c = at(i, 0);
