@@ -52,6 +52,7 @@ SIGNATURES = {
     "dflash_last_error": (ctypes.c_char_p, [_P]),
     "dflash_status_string": (ctypes.c_char_p, [_I32]),
     "dflash_launch_count": (ctypes.c_int64, [_P]),
+    "dflash_topk_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_char_p, _I32]),
     "dflash_timing_enable": (_I32, [_P, _I32]),
     "dflash_timing_classes": (_I32, []),
     "dflash_timing_class_name": (ctypes.c_char_p, [_I32]),

@@ -5,6 +5,10 @@
 //                      epilogue, [tiles][rows][k] (value, index) per row, merged per CTA.
 // Each thread keeps a sorted register list of its best TK candidates over a strided slice,
 // then the block merges the 256 sorted lists by k rounds of a block-wide best-head pick.
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/dflash.h"
 #include "kernels.h"
 
 namespace dflash {
@@ -211,4 +215,83 @@ cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int3
                     topk_idx, topk_val);
 }
 
+// ------------------------------------------------------------------------- no-allocation variant
+// dflash_topk_noalloc (declared in dflash.h) ranks rows of fp32 logits like the LM-head path:
+// per-chunk candidates first, then the same cross-chunk merge. Its candidates live in the
+// file-scope device array below instead of memory the caller or a context allocates, for
+// callers that must not touch the CUDA allocator (code recorded into a CUDA graph, runtimes
+// that own a fixed device-memory budget). The array is shared by every call in the process
+// and keeps the last call's contents.
+constexpr int NA_CHUNK = 4096;                      // logits per candidate chunk
+constexpr long NA_MAX_CAND = 1L << 19;              // 4 MiB of (value, index) candidates
+static __device__ __align__(256) int2 g_topk_scratch[NA_MAX_CAND];
+
+__global__ void __launch_bounds__(TK_THREADS) k_topk_chunks(int V, int k, int chunks, int rows,
+                                                            const float *logits, int2 *cand) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int32_t idx[32];
+  __shared__ float val[32];
+  __shared__ int32_t first;
+  const int chunk = blockIdx.x, row = blockIdx.y;
+  const int v0 = chunk * NA_CHUNK, n = min(NA_CHUNK, V - v0);
+  const float *x = logits + (size_t)row * V + v0;
+  block_topk(n, k, [&](int i, float &v, int &id) { v = x[i]; id = v0 + i; }, &first, idx, val);
+  __syncthreads();
+  if (threadIdx.x < k)
+    cand[((size_t)chunk * rows + row) * k + threadIdx.x] = make_int2(__float_as_int(val[threadIdx.x]), idx[threadIdx.x]);
+}
+
+namespace {
+std::mutex g_na_mu;
+int2 *g_na_ptr[128] = {};    // device address of g_topk_scratch, per device, set up once
+}  // namespace
+
 }  // namespace dflash
+
+using namespace dflash;
+
+extern "C" dflash_status dflash_topk_noalloc(void *stream, int32_t rows, int32_t vocab, int32_t k,
+                                             const float *logits, int32_t *argmax,
+                                             int32_t *topk_idx, float *topk_val, char *msg,
+                                             int32_t msg_len) {
+  auto fail = [&](dflash_status st, const char *why) {
+    if (msg && msg_len > 0) snprintf(msg, (size_t)msg_len, "%s", why);
+    return st;
+  };
+  if (msg && msg_len > 0) msg[0] = 0;
+  if (rows < 0 || vocab < 1 || k < 1 || k > TK || k > vocab)
+    return fail(DFLASH_ERR_INVALID_ARG, "need rows >= 0 and 1 <= k <= min(32, vocab)");
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !argmax || ((topk_idx == nullptr) != (topk_val == nullptr)))
+    return fail(DFLASH_ERR_INVALID_ARG, "logits and argmax are required; topk_idx/topk_val both or neither");
+  const long chunks = (vocab + NA_CHUNK - 1) / NA_CHUNK;
+  if ((long)rows * chunks * k > NA_MAX_CAND) {
+    char why[200];
+    snprintf(why, sizeof why, "rows * ceil(vocab/%d) * k = %ld exceeds the fixed scratch of %ld candidates",
+             NA_CHUNK, (long)rows * chunks * k, NA_MAX_CAND);
+    return fail(DFLASH_ERR_INVALID_ARG, why);
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+    return fail(DFLASH_ERR_CUDA, "no current CUDA device");
+  int2 *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (!g_na_ptr[dev]) {
+      // once per device: the host-side symbol is only a stand-in, the kernels need the
+      // device address of this device's copy of the array
+      int2 *ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_topk_scratch);
+      if (e != cudaSuccess || !ptr) return fail(DFLASH_ERR_CUDA, "cudaGetSymbolAddress of the top-k scratch failed");
+      g_na_ptr[dev] = ptr;
+    }
+    scratch = g_na_ptr[dev];
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_pdl(k_topk_chunks, dim3((unsigned)chunks, (unsigned)rows), dim3(TK_THREADS), 0, s,
+                             (int)vocab, (int)k, (int)chunks, (int)rows, logits, scratch);
+  if (e == cudaSuccess) e = launch_topk_merge((int)chunks, rows, k, scratch, argmax, topk_idx, topk_val, s);
+  if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, cudaGetErrorString(e));
+  return DFLASH_OK;
+}

@@ -211,6 +211,24 @@ const char *dflash_timing_class_name(int32_t cls);
 dflash_status dflash_timing_read(dflash_ctx *ctx, double *ms, int64_t *launches, double *bytes,
                                  double *flops, int32_t n);
 
+/* Top-k of fp32 logits that allocates nothing (no counterpart on the pages: a service of
+ * this library). Same result as the top-k of dflash_draft_step (values descending, ties to
+ * the lower index, argmax = first), computed as per-chunk candidates plus a merge, with the
+ * candidates in a fixed 4 MiB device array compiled into the library instead of memory from
+ * cudaMalloc. It is meant for callers that cannot call the CUDA allocator: code being
+ * recorded into a CUDA graph, or runtimes that own a fixed device-memory budget.
+ *   logits [rows, vocab] fp32 DEVICE; argmax [rows] int32 DEVICE; topk_idx [rows, k] int32
+ *   and topk_val [rows, k] fp32 DEVICE or both NULL; 1 <= k <= min(32, vocab);
+ *   rows * ceil(vocab / 4096) * k must not exceed 524288 (else DFLASH_ERR_INVALID_ARG).
+ *   msg (optional, msg_len bytes) receives the reason of an error.
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress); make it before any stream capture. Every call, from any thread
+ * or stream, uses the same array: calls that overlap on the GPU race and must be ordered
+ * by the caller. No slot is read before the call writes it, so nothing needs clearing. */
+dflash_status dflash_topk_noalloc(void *stream, int32_t rows, int32_t vocab, int32_t k,
+                                  const float *logits, int32_t *argmax, int32_t *topk_idx,
+                                  float *topk_val, char *msg, int32_t msg_len);
+
 #ifdef __cplusplus
 }
 #endif
