@@ -1,0 +1,98 @@
+"""Full-size parity on the batched workloads: the CUDA library runs the whole batch, the oracle
+recomputes a seeded sample of requests (per-request results do not depend on the rest of
+the batch). Sampled requests get the same synthetic features on both sides; the others get
+device-drawn features that only the GPU sees."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import get_config
+from synth import inputs as S
+
+from harness import TOPK_GAP, LOGIT_TOL, check_argmax, check_logits, check_topk, to_np, weights_cuda, weights_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_diffusion_speculative_inject_gb300 import build
+    build.build()
+
+
+def _device_feats(cfg, n, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    return [torch.randn((n, cfg.target_hidden), generator=g, device="cuda").to(dt) for _ in range(cfg.n_feat)]
+
+
+def _run(cfg_name, sample, steps, ctx_override=None):
+    from block_diffusion_speculative_inject_gb300 import Context, Limits
+    cfg = get_config(cfg_name)
+    B = cfg.batch
+    ctx_lens = ctx_override or S.make_context_lengths(cfg, 0)
+    w = S.make_weights(cfg, 0)
+    pages = sum((c + 64 * (steps + 2)) // 64 + 2 for c in ctx_lens)
+    ctx = Context(cfg, weights_cuda(w), Limits(max_batch=B, max_requests=B, max_pages=pages,
+                                               max_positions=max(ctx_lens) + 64 * (steps + 2),
+                                               max_inject_rows=8192))
+    orc = O.OracleDraft(cfg, weights_np(w))
+    del w
+    reqs = list(range(B))
+
+    def inject(n_new, tag, reset=False):
+        parts = []
+        for r, n in zip(reqs, n_new):
+            if r in sample:
+                f = S.make_features(cfg, n, 0, tag, r)
+                orc.inject(r, [to_np(x).astype(np.float64) for x in f], reset=reset)
+                parts.append([x.cuda() for x in f])
+            else:
+                parts.append(_device_feats(cfg, n, zlib.crc32(repr((tag, r)).encode())))
+        feats = [torch.cat([p[f] for p in parts], 0).contiguous() for f in range(cfg.n_feat)]
+        ctx.inject(reqs, n_new, feats, reset=reset)
+
+    inject(ctx_lens, "prefill", reset=True)
+    anchors = S.make_anchors(cfg, B, 0, 0)
+    tol = LOGIT_TOL[cfg.dtype]
+    for step in range(steps):
+        out = ctx.draft(reqs, anchors.cuda(), want_logits=True)
+        am = out["argmax"].cpu().numpy()
+        ti, tv = out["topk_idx"].cpu().numpy(), to_np(out["topk_val"])
+        oam = am.copy()
+        for r in sample:
+            w_am, w_idx, w_val, w_lg = orc.draft(r, int(anchors[r]))
+            lg = to_np(out["logits"][r])
+            check_logits(cfg, lg, w_lg, f"{cfg_name} step {step} req {r}")
+            check_argmax(am[r], w_lg, f"{cfg_name} step {step} req {r}")
+            check_topk(ti[r], tv[r], w_lg, cfg.topk, tol, f"{cfg_name} step {step} req {r}", TOPK_GAP[cfg.dtype])
+            oam[r] = w_am
+        target = S.make_targets(cfg, torch.from_numpy(oam), 0, step)
+        acc, toks, nxt = ctx.verify(out["argmax"], target.cuda())
+        wa, wo, wn = O.verify_greedy(am, target.numpy())
+        np.testing.assert_array_equal(acc.cpu().numpy(), wa)
+        np.testing.assert_array_equal(toks.cpu().numpy(), wo)
+        np.testing.assert_array_equal(nxt.cpu().numpy(), wn)
+        inject((acc.cpu() + 1).tolist(), ("step", step))
+        anchors = nxt.cpu()
+        for r in sample:
+            assert ctx.context_len(r) == orc.context_len(r)
+    ctx.close()
+
+
+def test_q8b_b32_ragged_batch():
+    """Qwen3-8B-shaped draft, 32 requests with contexts U[512, 8192], K=15; requests 3 and 17."""
+    _run("q8b_b32", sample=(3, 17), steps=2)
+
+
+def test_q4b_b128_large_batch():
+    """Qwen3-4B-shaped draft, 128 requests of context 1024, K=7; requests 0 and 101."""
+    _run("q4b_b128", sample=(0, 101), steps=2)
+
+
+def test_q27b_b8_long_context():
+    """27B-target-shaped draft, 8 requests of context 32768, K=15; request 5."""
+    _run("q27b_b8", sample=(5,), steps=2)
