@@ -127,7 +127,14 @@ class Clocks:
 
 # ----------------------------------------------------------------------------- workload
 class Workload:
-    """Seeded inputs of one workload, resident on the device before timing."""
+    """Seeded inputs of one workload, resident on the device before timing.
+
+    Steady workloads (fixed context lengths) draw the newly accepted positions of every step
+    up front: a step truncates each request to its context length minus those positions and
+    injects them, so every draft runs at the configured length. Verify-driven workloads (the
+    long-context one) inject the anchor plus the accepted drafts of the previous verify, with
+    target ids that follow the draft argmax with probability accept_p; their contexts grow.
+    """
 
     def __init__(self, cfg, steps, seed=0, device="cuda:0"):
         self.cfg = cfg
@@ -135,23 +142,29 @@ class Workload:
         self.B = cfg.batch
         self.reqs = list(range(self.B))
         self.ctx = S.make_context_lengths(cfg, seed)
+        self.driven = cfg.verify_driven
         self.n_new = [S.make_n_new(cfg, self.B, seed, s) for s in range(steps)]
         self.anchors = [S.make_anchors(cfg, self.B, seed, s + 1) for s in range(steps)]
         zeros = torch.zeros((self.B, cfg.block_k), dtype=torch.int32)
         # the synthetic target stands in for the target model; its ids are drawn up front
         self.targets = [S.make_targets(cfg, zeros, seed, s, p=0.0) for s in range(steps)]
+        g = torch.Generator().manual_seed(seed + 1)
+        self.coin = [torch.rand((self.B, cfg.block_k), generator=g) < cfg.accept_p for _ in range(steps)]
         self.feats = []
         for s in range(steps):
-            parts = [S.make_features(cfg, n, seed, "step", s, r) for r, n in zip(self.reqs, self.n_new[s])]
+            rows = [cfg.n_new_max] * self.B if self.driven else self.n_new[s]
+            parts = [S.make_features(cfg, n, seed, "step", s, r) for r, n in zip(self.reqs, rows)]
             self.feats.append([torch.cat([p[f] for p in parts], 0) for f in range(cfg.n_feat)])
 
-    def max_positions(self):
-        return max(self.ctx) + self.cfg.n_new_max + self.cfg.block_k + 2
+    def max_positions(self, steps):
+        grow = (steps + 2) * (self.cfg.n_new_max) if self.driven else self.cfg.n_new_max
+        return max(self.ctx) + grow + self.cfg.block_k + 2
 
     def to_device(self):
         d = self.device
         self.anchors_d = [a.to(d) for a in self.anchors]
         self.targets_d = [t.to(d) for t in self.targets]
+        self.coin_d = [c.to(d) for c in self.coin]
         self.feats_d = [[f.to(d) for f in fs] for fs in self.feats]
 
     def pinned(self):
@@ -160,11 +173,12 @@ class Workload:
         self.feats_h = [[f.pin_memory() for f in fs] for fs in self.feats]
 
 
-def _make_context(cfg, wl, device):
+def _make_context(cfg, wl, device, steps):
     from block_diffusion_speculative_inject_gb300 import Context, Limits
-    pages = sum((c + cfg.n_new_max + 63) // 64 + 1 for c in wl.ctx) + 16
-    lim = Limits(max_batch=wl.B, max_requests=wl.B, max_pages=pages,
-                 max_positions=wl.max_positions(), max_inject_rows=8192)
+    maxpos = wl.max_positions(steps)
+    pages = sum((min(maxpos, c + (maxpos - max(wl.ctx))) + 63) // 64 + 1 for c in wl.ctx) + 16
+    lim = Limits(max_batch=wl.B, max_requests=wl.B, max_pages=pages, max_positions=maxpos,
+                 max_inject_rows=8192)
     w = S.make_weights(cfg, 0)
     wg = {k: v.to(device) for k, v in w.items() if k != "layers"}
     wg["layers"] = [{k: v.to(device) for k, v in lw.items()} for lw in w["layers"]]
@@ -173,39 +187,77 @@ def _make_context(cfg, wl, device):
 
 
 def _prefill(ctx, cfg, wl):
+    """Whole-context injection of every request (untimed). Features come from a seeded device
+    generator: N(0, 1) like the timed steps' features, without a CPU round trip."""
+    g = torch.Generator(device=wl.device).manual_seed(12345)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     for r, n in zip(wl.reqs, wl.ctx):
-        feats = [f.to(wl.device) for f in S.make_features(cfg, n, 0, "prefill", r)]
+        feats = [torch.randn((n, cfg.target_hidden), generator=g, device=wl.device).to(dt)
+                 for _ in range(cfg.n_feat)]
         ctx.inject([r], [n], feats, reset=True)
     torch.cuda.synchronize()
 
 
-def _step(ctx, wl, s, out, feats, anchors, targets):
-    """One step: bring each request back to its context length minus the new positions,
-    inject them, draft, verify."""
-    for r, c, n in zip(wl.reqs, wl.ctx, wl.n_new[s]):
-        ctx.truncate(r, c - n)
-    ctx.inject(wl.reqs, wl.n_new[s], feats)
-    ctx.draft(wl.reqs, anchors, argmax=out["argmax"], topk_idx=out["topk_idx"],
-              topk_val=out["topk_val"])
-    ctx.verify(out["argmax"], targets, out["acc"], out["toks"], out["nxt"])
+class StepLoop:
+    """Runs steps of the workload; records the context lengths and injected counts so the
+    algorithmic work of the timed steps can be computed."""
+
+    def __init__(self, ctx, cfg, wl, device):
+        self.ctx, self.cfg, self.wl, self.device = ctx, cfg, wl, device
+        B, K, k = wl.B, cfg.block_k, cfg.topk
+        self.out = dict(argmax=torch.empty((B, K), dtype=torch.int32, device=device),
+                        topk_idx=torch.empty((B, K, k), dtype=torch.int32, device=device),
+                        topk_val=torch.empty((B, K, k), dtype=torch.float32, device=device),
+                        acc=torch.empty((B,), dtype=torch.int32, device=device),
+                        toks=torch.empty((B, K + 1), dtype=torch.int32, device=device),
+                        nxt=torch.empty((B,), dtype=torch.int32, device=device))
+        self.anchor = wl.anchors_d[0].clone()
+        self.lens = list(wl.ctx)
+        self.records = []
+
+    def step(self, s, feats=None, anchors=None, targets=None):
+        ctx, wl, out = self.ctx, self.wl, self.out
+        feats = wl.feats_d[s] if feats is None else feats
+        if not wl.driven:
+            for r, c, n in zip(wl.reqs, wl.ctx, wl.n_new[s]):
+                ctx.truncate(r, c - n)
+            ctx.inject(wl.reqs, wl.n_new[s], feats)
+            ctx.draft(wl.reqs, wl.anchors_d[s] if anchors is None else anchors, argmax=out["argmax"],
+                      topk_idx=out["topk_idx"], topk_val=out["topk_val"])
+            ctx.verify(out["argmax"], wl.targets_d[s] if targets is None else targets,
+                       out["acc"], out["toks"], out["nxt"])
+            self.records.append((list(wl.ctx), sum(wl.n_new[s])))
+            return
+        # verify-driven: draft, verify against targets following the argmax, inject a + 1
+        ctx.draft(wl.reqs, self.anchor, argmax=out["argmax"], topk_idx=out["topk_idx"],
+                  topk_val=out["topk_val"])
+        rnd = wl.targets_d[s] if targets is None else targets
+        tgt = torch.cat([torch.where(wl.coin_d[s], out["argmax"], rnd[:, :-1]), rnd[:, -1:]], 1)
+        ctx.verify(out["argmax"], tgt, out["acc"], out["toks"], out["nxt"])
+        n_new = (out["acc"] + 1).tolist()                     # the scheduler reads a + 1
+        rows = torch.tensor([r * self.cfg.n_new_max + i for r, n in enumerate(n_new) for i in range(n)],
+                            device=self.device)
+        ctx.inject(wl.reqs, n_new, [f.index_select(0, rows) for f in feats])
+        self.records.append((list(self.lens), sum(n_new)))
+        self.lens = [c + n for c, n in zip(self.lens, n_new)]
+        self.anchor.copy_(out["nxt"])
 
 
-def _algorithmic(cfg, wl, steps):
-    """Algorithmic flops and HBM bytes of the timed steps (weights once per step, every
-    context K/V once per layer, features of the injected rows)."""
+def _algorithmic(cfg, records):
+    """Algorithmic flops and HBM bytes of the recorded steps (weights once per step, every
+    context K/V once per layer, features of the injected rows, cache writes)."""
     H, F, V, L = cfg.hidden, cfg.feat_dim, cfg.vocab, cfg.n_layers
     kvw = L * 2 * cfg.kv_dim
     Q, K = cfg.block_k + 1, cfg.block_k
-    w_bytes = 2 * (L * cfg.layer_params() + V * H + H * F + L * 0)  # layers, LM head, fc
+    w_bytes = 2 * (L * cfg.layer_params() + V * H + H * F)  # layers, LM head, fc
     flops = byts = 0.0
-    for s in range(steps):
-        n = sum(wl.n_new[s])
+    for lens, n in records:
+        B = len(lens)
         flops += 2.0 * n * (F * H + kvw * H)
-        flops += 2.0 * wl.B * Q * L * (cfg.layer_params() - 2 * H - 2 * cfg.head_dim)
-        flops += 2.0 * wl.B * K * V * H
-        flops += sum(4.0 * Q * cfg.n_q_heads * cfg.head_dim * (c + Q) * L for c in wl.ctx)
-        byts += w_bytes + sum(c * L * 2 * cfg.kv_dim * 2 for c in wl.ctx) + n * F * 2
-        byts += n * kvw * 2   # cache writes
+        flops += 2.0 * B * Q * L * (cfg.layer_params() - 2 * H - 2 * cfg.head_dim)
+        flops += 2.0 * B * K * V * H
+        flops += sum(4.0 * Q * cfg.n_q_heads * cfg.head_dim * (c + Q) * L for c in lens)
+        byts += w_bytes + sum(c * L * 2 * cfg.kv_dim * 2 for c in lens) + n * F * 2 + n * kvw * 2
     return flops, byts
 
 
@@ -214,31 +266,29 @@ def run_ours(args):
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     cfg = get_config(args.config)
-    steps = args.warmup + args.steps
-    wl = Workload(cfg, steps, seed=0, device=device)
+    W, K_ = args.warmup, args.steps
+    n_steps = W + (3 * K_ if cfg.verify_driven else K_)      # driven runs never revisit a step
+    wl = Workload(cfg, n_steps, seed=0, device=device)
     wl.to_device()
-    ctx, w_cpu = _make_context(cfg, wl, device)
+    ctx, w_cpu = _make_context(cfg, wl, device, n_steps)
     _prefill(ctx, cfg, wl)
-    B, K, k = wl.B, cfg.block_k, cfg.topk
-    out = dict(argmax=torch.empty((B, K), dtype=torch.int32, device=device),
-               topk_idx=torch.empty((B, K, k), dtype=torch.int32, device=device),
-               topk_val=torch.empty((B, K, k), dtype=torch.float32, device=device),
-               acc=torch.empty((B,), dtype=torch.int32, device=device),
-               toks=torch.empty((B, K + 1), dtype=torch.int32, device=device),
-               nxt=torch.empty((B,), dtype=torch.int32, device=device))
+    loop = StepLoop(ctx, cfg, wl, device)
+    B, K = wl.B, cfg.block_k
     stream = torch.cuda.current_stream()
-    for s in range(args.warmup):
-        _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+    for s in range(W):
+        loop.step(s)
     torch.cuda.synchronize()
+    loop.records.clear()
     launches0 = ctx.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(ws)
     torch.cuda.synchronize()
+    timed = list(range(W, W + K_))
     with Clocks(local) as clk:
         t0 = time.perf_counter()
         e0.record(stream)
-        for s in range(args.warmup, steps):
-            _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+        for s in timed:
+            loop.step(s)
         e1.record(stream)
         host_enqueue = time.perf_counter() - t0
         torch.cuda.synchronize()
@@ -246,15 +296,17 @@ def run_ours(args):
     launches = ctx.launch_count() - launches0
     ms = e0.elapsed_time(e1)
     ms_max = _max_over_ranks(ws, ms, device)
+    records = list(loop.records)
 
-    # per-kernel breakdown: the same steps again with CUDA events around every launch (the
-    # events add a little time, so the headline number above is taken without them)
+    # per-kernel breakdown: steps again with CUDA events around every launch (the events add
+    # a little time, so the headline number above is taken without them)
+    again = timed if not cfg.verify_driven else list(range(W + K_, W + 2 * K_))
     ctx.timing_read()
     ctx.timing_enable(True)
     kb0, kb1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     kb0.record(stream)
-    for s in range(args.warmup, steps):
-        _step(ctx, wl, s, out, wl.feats_d[s], wl.anchors_d[s], wl.targets_d[s])
+    for s in again:
+        loop.step(s)
     kb1.record(stream)
     torch.cuda.synchronize()
     kern = ctx.timing_read()
@@ -268,15 +320,15 @@ def run_ours(args):
         host_out = dict(argmax=torch.empty((B, K), dtype=torch.int32).pin_memory(),
                         acc=torch.empty((B,), dtype=torch.int32).pin_memory(),
                         toks=torch.empty((B, K + 1), dtype=torch.int32).pin_memory())
-        dev_f = [torch.empty_like(f, device=device) for f in wl.feats_d[0]]
         anc_d = torch.empty((B,), dtype=torch.int32, device=device)
         tgt_d = torch.empty((B, K + 1), dtype=torch.int32, device=device)
         h2d = d2h = 0
+        e2e_steps = timed if not cfg.verify_driven else list(range(W + 2 * K_, W + 3 * K_))
         _barrier(ws)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e0.record(stream)
-        for s in range(args.warmup, steps):
+        for s in e2e_steps:
             fs = []
             for f in wl.feats_h[s]:
                 d = torch.empty(f.shape, dtype=f.dtype, device=device)
@@ -286,19 +338,18 @@ def run_ours(args):
             anc_d.copy_(wl.anchors_h[s], non_blocking=True)
             tgt_d.copy_(wl.targets_h[s], non_blocking=True)
             h2d += wl.anchors_h[s].numel() * 4 + wl.targets_h[s].numel() * 4
-            _step(ctx, wl, s, out, fs, anc_d, tgt_d)
-            host_out["argmax"].copy_(out["argmax"], non_blocking=True)
-            host_out["acc"].copy_(out["acc"], non_blocking=True)
-            host_out["toks"].copy_(out["toks"], non_blocking=True)
+            loop.step(s, feats=fs, anchors=anc_d, targets=tgt_d)
+            host_out["argmax"].copy_(loop.out["argmax"], non_blocking=True)
+            host_out["acc"].copy_(loop.out["acc"], non_blocking=True)
+            host_out["toks"].copy_(loop.out["toks"], non_blocking=True)
             d2h += (B * K + B + B * (K + 1)) * 4
         e1.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1), device)
-        e2e = {"value": ws * B * K * args.steps / (e2e_ms / 1e3), "unit": "draft tok/s",
-               "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps,
-               "ms_per_step": e2e_ms / args.steps, "host_wall_ms_per_step": wall * 1e3 / args.steps}
-        del dev_f
+        e2e = {"value": round(ws * B * K * K_ / (e2e_ms / 1e3), 1), "unit": "draft tok/s",
+               "h2d_bytes_per_step": h2d // K_, "d2h_bytes_per_step": d2h // K_,
+               "ms_per_step": round(e2e_ms / K_, 4), "host_wall_ms_per_step": round(wall * 1e3 / K_, 4)}
 
     if rank != 0:
         return
@@ -310,43 +361,48 @@ def run_ours(args):
     g_launch = sum(kern[c]["launches"] for c in gemm_cls)
     total_k_ms = sum(v["ms"] for v in kern.values())
     achieved = g_bytes / (g_ms / 1e3) / 1e9
-    roofline = {"kernel": "gemm (all weight-streaming GEMMs of the step)", "bound": "hbm",
+    roofline = {"kernel": "k_gemm_tc (all weight-streaming GEMMs of the step)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": None,
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
                 "avg_launch_us": round(g_ms * 1e3 / max(1, g_launch), 2),
                 "algorithmic_bytes_per_launch": round(g_bytes / max(1, g_launch)),
-                "tensor_tflops": round(g_flops / (g_ms / 1e3) / 1e12, 2)}
-    flops, byts = _algorithmic(cfg, wl, args.steps)
+                "tensor_tflops": round(g_flops / (g_ms / 1e3) / 1e12, 2),
+                "timing": "CUDA events around each launch in a separate pass over the same steps"}
+    flops, byts = _algorithmic(cfg, records)
     t_roof = max(flops / (tf * 1e12), byts / (hbm * 1e9))
-    step_roof = {"flops_per_step": flops / args.steps, "bytes_per_step": byts / args.steps,
-                 "roofline_us_per_step": t_roof * 1e6 / args.steps,
+    step_roof = {"flops_per_step": flops / K_, "bytes_per_step": byts / K_,
+                 "roofline_us_per_step": t_roof * 1e6 / K_,
                  "bound": "tensor" if flops / (tf * 1e12) > byts / (hbm * 1e9) else "hbm",
                  "frac": round(t_roof / (ms / 1e3), 4)}
-    kernels = {c: {"ms_per_step": round(v["ms"] / args.steps, 4), "share": round(v["ms"] / total_k_ms, 4),
-                   "launches_per_step": v["launches"] / args.steps}
+    kernels = {c: {"ms_per_step": round(v["ms"] / len(again), 4), "share": round(v["ms"] / total_k_ms, 4),
+                   "launches_per_step": v["launches"] / len(again)}
                for c, v in sorted(kern.items(), key=lambda kv: -kv[1]["ms"])}
-    tok = ws * B * K * args.steps / (ms_max / 1e3)
+    tok = ws * B * K * K_ / (ms_max / 1e3)
+    lens = records[0][0] if records else wl.ctx
     res = {
         "metric": "draft_tokens_per_s", "value": round(tok, 1), "unit": "draft tok/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_max / args.steps, 4),
-        "us_per_step": round(ms_max * 1e3 / args.steps, 1),
-        "steps_per_s": round(ws * args.steps / (ms_max / 1e3), 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "n_gpus": ws, "steps": K_, "warmup": W,
+        "ms_per_step": round(ms_max / K_, 4),
+        "us_per_step": round(ms_max * 1e3 / K_, 1),
+        "steps_per_s": round(ws * K_ / (ms_max / 1e3), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic: seeded N(0,0.02) weights, N(0,1) target hidden states, uniform ids",
         "config": {"workload": f"{cfg.name}: {WORKLOAD_TEXT.get(cfg.name, cfg.name)}", "batch": B,
-                   "context": wl.ctx if B <= 8 else [min(wl.ctx), max(wl.ctx)], "K": K,
-                   "new_positions_per_step": f"U[1,{cfg.n_new_max}] per request",
+                   "context": lens if B <= 8 else [min(lens), max(lens)], "K": K,
+                   "new_positions_per_step": ("accept_len + 1 from the verify (targets follow the "
+                                              f"argmax with p={cfg.accept_p})") if cfg.verify_driven
+                   else f"U[1,{cfg.n_new_max}] per request",
                    "l2": "inputs larger than L2: every step streams all weights (GBs) from HBM",
                    "parallelism": f"{ws} independent replica(s)"},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches,
-        "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / args.steps, 4),
-        "ms_per_step_with_kernel_events": round(ms_events / args.steps, 4),
+        "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / K_, 4),
+        "ms_per_step_with_kernel_events": round(ms_events / len(again), 4),
     }
     res["clocks"] = clk.summary()
-    if not args.no_cpu_baseline and ws >= 1:
+    if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(cfg, wl, w_cpu)
     print(json.dumps(res), flush=True)
 
