@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
 // ------------------------------------------------------------------------- host side
 struct TcGemm {
   int device = 0, num_sms = 0;
-  int ctas_per_sm = 2;            // resident GEMM CTAs per SM the split-K plan assumes
   int *err = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
@@ -375,19 +374,20 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   p.t_tiles = (d.M + p.bn - 1) / p.bn;
   p.n_tiles = (d.N + TC_BM - 1) / TC_BM;
   p.kb = d.K / TC_BK;
+  const bool split = d.x_lo[0] != nullptr;
+  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * (split ? 2 : 1);
+  // Few token rows: a short pipeline and many resident CTAs per SM stream weights fastest
+  // (measured); more token rows: a longer pipeline in a CTA of its own.
+  p.stages = p.bn <= 32 ? 3 : (int)std::max<size_t>(2, std::min<size_t>(8, (200 * 1024) / stage));
+  p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 1) + 16;
+  const int per_sm = std::max(1, std::min(4, (int)((228 * 1024) / (p.smem + 1024))));
+  // split K into as many parts as keep the grid within one wave of resident CTAs
   const int base = p.t_tiles * p.n_tiles;
-  // as many splits as fit the grid into one wave of resident CTAs (two per SM at small BN)
-  const int slots = t->ctas_per_sm * t->num_sms;
-  int S = std::max(1, slots / base);
+  int S = std::max(1, (per_sm * t->num_sms) / base);
   S = std::max(1, std::min(S, std::min(8, p.kb / 4)));    // a portable cluster holds 8 CTAs
   if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
   p.kb_per = (p.kb + S - 1) / S;
   p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
-  const bool split = d.x_lo[0] != nullptr;
-  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * (split ? 2 : 1);
-  const size_t budget = p.bn <= 32 ? 100 * 1024 : 200 * 1024;   // two CTAs per SM at small BN
-  p.stages = (int)std::max<size_t>(2, std::min<size_t>(8, budget / stage));
-  p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 1) + 16;
   return p;
 }
 
