@@ -687,6 +687,11 @@ static void plan_splits(int ctx_len, int target, int *n_split, int *split_len) {
   *split_len = per * kPage;
 }
 
+// The LM head ranks candidates inside the tensor-core GEMM epilogue while the token tile is
+// narrow (at most 32 rows: a few selection rounds per warp); wider tiles write the fp32
+// logits and rank them row by row, which is cheaper than 32+ rounds per warp per tile.
+static bool fused_topk(const dflash_ctx *c, int rows) { return c->tc && rows <= 32; }
+
 // The layer stack of the draft step plus the final norm and the LM-head GEMM: every launch
 // between the embedding and the top-k selection. It touches only library buffers and the
 // device descriptor `bt`, so it can be captured once per (batch, split plan) and replayed.
@@ -746,7 +751,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
                                  last ? m.K : 0, s);
        }));
   }
-  if (c->tc) {
+  if (fused_topk(c, RK)) {
     // tensor-core LM head: per-tile top-k in the GEMM epilogue (merged afterwards); full
     // logits are written only when the caller asks for them
     GemmDesc lm = gemm_desc(RK, m.V, m.H, EPI_TOPK, logits, m.V);
@@ -897,7 +902,7 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   } else if ((st = draft_layers(c, B, bt, attn_bytes, attn_flops, logits, s)) != DFLASH_OK) {
     return st;
   }
-  if (c->tc) {
+  if (fused_topk(c, RK)) {
     const int tiles = (m.V + 127) / 128;
     CK(c, timed(c, K_TOPK, s, 8.0 * tiles * RK * m.topk, 1.0 * tiles * RK * m.topk, 1, [&] {
          return launch_topk_merge(tiles, RK, m.topk, c->cand, argmax, topk_idx, topk_val, s);

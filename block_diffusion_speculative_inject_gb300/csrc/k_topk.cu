@@ -20,35 +20,53 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-template <typename Get>
-__device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argmax_out,
-                                           int32_t *idx_out, float *val_out) {
-  const int tid = threadIdx.x;
-  float lv[TK];
-  int li[TK];
+__device__ __forceinline__ void list_init(float (&lv)[TK], int (&li)[TK]) {
 #pragma unroll
   for (int q = 0; q < TK; ++q) {
     lv[q] = -INFINITY;
     li[q] = 0x7fffffff;
   }
-  for (int i = tid; i < n; i += TK_THREADS) {
+}
+
+// Insertion into a thread's sorted register list (unrolled: registers only).
+__device__ __forceinline__ void list_insert(float (&lv)[TK], int (&li)[TK], float v, int id) {
+  if (!better(v, id, lv[TK - 1], li[TK - 1])) return;
+  float cv = v;
+  int ci = id;
+#pragma unroll
+  for (int q = 0; q < TK; ++q) {
+    const bool b = better(cv, ci, lv[q], li[q]);
+    const float tv = lv[q];
+    const int ti = li[q];
+    lv[q] = b ? cv : lv[q];
+    li[q] = b ? ci : li[q];
+    cv = b ? tv : cv;
+    ci = b ? ti : ci;
+  }
+}
+
+__device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int k, int32_t *argmax_out,
+                                            int32_t *idx_out, float *val_out);
+
+template <typename Get>
+__device__ __forceinline__ void block_topk(int n, int k, Get get, int32_t *argmax_out,
+                                           int32_t *idx_out, float *val_out) {
+  float lv[TK];
+  int li[TK];
+  list_init(lv, li);
+  for (int i = threadIdx.x; i < n; i += TK_THREADS) {
     float v;
     int id;
     get(i, v, id);
-    if (!better(v, id, lv[TK - 1], li[TK - 1])) continue;
-    float cv = v;
-    int ci = id;
-#pragma unroll
-    for (int q = 0; q < TK; ++q) {   // insertion into the sorted list (registers only)
-      const bool b = better(cv, ci, lv[q], li[q]);
-      const float tv = lv[q];
-      const int ti = li[q];
-      lv[q] = b ? cv : lv[q];
-      li[q] = b ? ci : li[q];
-      cv = b ? tv : cv;
-      ci = b ? ti : ci;
-    }
+    list_insert(lv, li, v, id);
   }
+  block_merge(lv, li, k, argmax_out, idx_out, val_out);
+}
+
+// Block-wide merge of the threads' sorted lists into the k best (value desc, index asc).
+__device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int k, int32_t *argmax_out,
+                                            int32_t *idx_out, float *val_out) {
+  const int tid = threadIdx.x;
   // merge: each round every thread offers its current head; warps reduce by shuffles, the
   // eight warp winners through shared memory; the owner of the block winner advances
   __shared__ float wv_s[TK_THREADS / 32];
@@ -119,9 +137,34 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
   pdl_trigger();
   const int row = blockIdx.x;
   const float *x = logits + (size_t)row * V;
-  block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; }, argmax + row,
-             topk_idx ? topk_idx + (size_t)row * k : nullptr,
-             topk_val ? topk_val + (size_t)row * k : nullptr);
+  float lv[TK];
+  int li[TK];
+  list_init(lv, li);
+  if ((V & 3) == 0) {
+    // 8 float4 per thread in flight per round, then the (mostly rejected) insertions
+    const float4 *x4 = (const float4 *)x;
+    const int n4 = V / 4;
+    for (int b = 0; b < n4; b += TK_THREADS * 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = b + threadIdx.x + j * TK_THREADS;
+        v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
+        list_insert(lv, li, v[j].x, i);
+        list_insert(lv, li, v[j].y, i + 1);
+        list_insert(lv, li, v[j].z, i + 2);
+        list_insert(lv, li, v[j].w, i + 3);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < V; i += TK_THREADS) list_insert(lv, li, x[i], i);
+  }
+  block_merge(lv, li, k, argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
+              topk_val ? topk_val + (size_t)row * k : nullptr);
 }
 
 // Merge of per-tile sorted candidate lists. With at least k tiles, the k-th best of the
