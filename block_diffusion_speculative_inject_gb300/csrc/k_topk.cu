@@ -130,39 +130,69 @@ __device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int 
   }
 }
 
+// Two passes over the row: (1) every thread's maximum; the k-th best of those maxima is a
+// lower bound T of the row's k-th best value (k threads each hold a value >= T); (2) only
+// values >= T enter the threads' lists, so almost no insertions happen.
 __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float thr_v[TK];
+  __shared__ int thr_i[TK];
+  __shared__ int dummy;
   const int row = blockIdx.x;
   const float *x = logits + (size_t)row * V;
+  const bool vec = (V & 3) == 0;
+  const int n4 = V / 4;
+  const float4 *x4 = (const float4 *)x;
   float lv[TK];
   int li[TK];
-  list_init(lv, li);
-  if ((V & 3) == 0) {
-    // 8 float4 per thread in flight per round, then the (mostly rejected) insertions
-    const float4 *x4 = (const float4 *)x;
-    const int n4 = V / 4;
-    for (int b = 0; b < n4; b += TK_THREADS * 8) {
-      float4 v[8];
+  // pass 1: per-thread maximum (index of the first occurrence)
+  float mv = -INFINITY;
+  int mi = 0x7fffffff;
+  auto scan = [&](auto &&visit) {
+    if (vec) {
+      for (int b = 0; b < n4; b += TK_THREADS * 8) {
+        float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = b + threadIdx.x + j * TK_THREADS;
-        v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
+        for (int j = 0; j < 8; ++j) {
+          const int i = b + threadIdx.x + j * TK_THREADS;
+          v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
-        list_insert(lv, li, v[j].x, i);
-        list_insert(lv, li, v[j].y, i + 1);
-        list_insert(lv, li, v[j].z, i + 2);
-        list_insert(lv, li, v[j].w, i + 3);
+        for (int j = 0; j < 8; ++j) {
+          const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
+          if (i < V) {
+            visit(v[j].x, i);
+            visit(v[j].y, i + 1);
+            visit(v[j].z, i + 2);
+            visit(v[j].w, i + 3);
+          }
+        }
       }
+    } else {
+      for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
     }
-  } else {
-    for (int i = threadIdx.x; i < V; i += TK_THREADS) list_insert(lv, li, x[i], i);
-  }
+  };
+  scan([&](float v, int i) {
+    if (better(v, i, mv, mi)) {
+      mv = v;
+      mi = i;
+    }
+  });
+  list_init(lv, li);
+  lv[0] = mv;
+  li[0] = mi;
+  const int kk = k;
+  block_merge(lv, li, kk, &dummy, thr_i, thr_v);
+  __syncthreads();
+  const float T = thr_v[kk - 1];
+  // pass 2: exact selection among the values >= T
+  list_init(lv, li);
+  scan([&](float v, int i) {
+    if (v >= T) list_insert(lv, li, v, i);
+  });
   block_merge(lv, li, k, argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
               topk_val ? topk_val + (size_t)row * k : nullptr);
 }
