@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <string>
 #include <unordered_map>
 #include <unordered_set>
@@ -109,6 +110,7 @@ struct dflash_ctx {
 
   // CUDA graphs of the layer stack, keyed by batch size and split plan
   bool graphs_enabled = true;
+  double split_overhead = 2.0;             // attention split planner: CTA overhead in pages
   cudaStream_t cap_stream = nullptr;
   int32_t *desc_fixed = nullptr;   // device descriptor read by captured kernels
   std::vector<DraftGraph> graphs;
@@ -482,6 +484,9 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   {
     const char *ng = getenv("DFLASH_NO_GRAPHS");
     c->graphs_enabled = !(ng && ng[0] == '1');
+    // per-CTA cost of the attention split kernel beyond its pages, in pages (tuning override)
+    const char *so = getenv("DFLASH_SPLIT_OVERHEAD");
+    if (so && so[0]) c->split_overhead = std::max(0.0, atof(so));
   }
   if (cudaHostAlloc((void **)&c->err_h, sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer((void **)&c->err_d, c->err_h, 0) != cudaSuccess)
@@ -672,19 +677,53 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
 }
 
 // ------------------------------------------------------------------------------ draft step
-// Context splits of one request: whole pages, about `target` splits (enough CTAs over the
-// batch's kv heads to fill the GPU), at most kMaxSplit, none for an empty context.
-static void plan_splits(int ctx_len, int target, int *n_split, int *split_len) {
-  const int pages = (ctx_len + kPage - 1) / kPage;
-  if (pages == 0) {
-    *n_split = 0;
-    *split_len = kPage;
-    return;
+// Context splits of a batch. Every request's context is cut into chunks of P whole pages
+// (its last chunk shorter), so long contexts get more splits than short ones. The CTA of a
+// (split, kv head, request) costs its pages plus a fixed setup and epilogue overhead, and
+// the block scheduler hands CTAs to free SMs in launch order (split fastest, request
+// slowest): the layer's attention time is the makespan of that list schedule on `slots`
+// resident CTAs. P is the candidate, from the longest context cut into 1..kMaxSplit
+// chunks, with the smallest simulated makespan; a finer cut must win by 2% to be taken.
+static void plan_splits(const std::vector<int> &pages, int nkv, int slots, double ovh,
+                        std::vector<int> &n_split, std::vector<int> &split_len) {
+  const int B = (int)pages.size();
+  int maxp = 0;
+  for (int b = 0; b < B; ++b) maxp = std::max(maxp, pages[b]);
+  n_split.assign(B, 0);
+  split_len.assign(B, kPage);
+  if (maxp == 0) return;
+  int best_P = maxp, prev_P = -1;
+  double best = 0;
+  std::vector<double> heap;
+  for (int k = 1; k <= kMaxSplit; ++k) {
+    const int P = (maxp + k - 1) / k;
+    if (P == prev_P) continue;
+    prev_P = P;
+    long n_cta = 0;
+    for (int b = 0; b < B; ++b) n_cta += (long)nkv * ((pages[b] + P - 1) / P);
+    if (k > 1 && n_cta > 8L * slots) break;      // finer cuts only add CTAs from here
+    heap.assign(slots, 0.0);                     // min-heap of slot free times
+    double span = 0;
+    for (int b = 0; b < B; ++b) {
+      const int ns = (pages[b] + P - 1) / P;
+      for (int h = 0; h < nkv; ++h)
+        for (int sp = 0; sp < ns; ++sp) {
+          std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
+          const double t = heap.back() + std::min(P, pages[b] - sp * P) + ovh;
+          heap.back() = t;
+          std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+          span = std::max(span, t);
+        }
+    }
+    if (k == 1 || span < 0.98 * best) {
+      best = span;
+      best_P = P;
+    }
   }
-  int ns = std::max(1, std::min(std::min(target, kMaxSplit), pages));
-  const int per = (pages + ns - 1) / ns;       // pages per split
-  *n_split = (pages + per - 1) / per;          // every split non-empty
-  *split_len = per * kPage;
+  for (int b = 0; b < B; ++b) {
+    n_split[b] = (pages[b] + best_P - 1) / best_P;
+    split_len[b] = best_P * kPage;
+  }
 }
 
 // The LM head ranks candidates inside the tensor-core GEMM epilogue while the token tile is
@@ -845,19 +884,23 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   std::vector<const Req *> rq(B);
   std::unordered_set<int32_t> seen;
   int max_split = 0;
-  const int target = std::max(1, (2 * c->num_sms + B * m.nkv - 1) / (B * m.nkv));
+  std::vector<int> pages(B), ns, sl;
   for (int b = 0; b < B; ++b) {
     if (!seen.insert(req_ids[b]).second)
       return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d appears twice", req_ids[b]);
     auto it = c->reqs.find(req_ids[b]);
     if (it == c->reqs.end()) return set_err(c, DFLASH_ERR_UNKNOWN_REQUEST, "unknown request %d", req_ids[b]);
     rq[b] = &it->second;
-    int ns, sl;
-    plan_splits(rq[b]->len, target, &ns, &sl);
+    pages[b] = (rq[b]->len + kPage - 1) / kPage;
+  }
+  // the tensor-core split kernel runs one CTA per SM, the FFMA one two
+  const bool attn_tc = c->amaps.valid;
+  plan_splits(pages, m.nkv, (attn_tc ? 1 : 2) * c->num_sms, c->split_overhead, ns, sl);
+  for (int b = 0; b < B; ++b) {
     desc[b] = rq[b]->len;
-    desc[B + b] = ns;
-    desc[2 * B + b] = sl;
-    max_split = std::max(max_split, ns);
+    desc[B + b] = ns[b];
+    desc[2 * B + b] = sl[b];
+    max_split = std::max(max_split, ns[b]);
   }
   int off = 0;
   for (int b = 0; b < B; ++b) {

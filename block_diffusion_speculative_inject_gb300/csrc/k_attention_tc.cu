@@ -14,9 +14,10 @@
 // kernel with the other splits and the block's own keys.
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA (K page: two boxes of 64 x 64, V page: one
-// box of 64 x 128) into a 3-stage ring; warp 1 owns TMEM (S at column 0, O at column 128)
+// box of 64 x 128) into a 3-stage ring; warp 1 owns TMEM (S at columns 0 and 64, O at 128)
 // and its lane 0 issues the MMAs; warps 2-5 fill Q, run the softmax (TMEM lane quarter
-// warp % 4) and write the partials. All waits are bounded in time.
+// warp % 4) and write the partials. The S of the next tile is computed into a second TMEM
+// buffer while the softmax of the current one runs. All waits are bounded in time.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -85,10 +86,11 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   uint64_t *bars = (uint64_t *)(gbase + AQ_BYTES + AP_BYTES + AT_TC_STAGES * A_STAGE);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * AT_TC_STAGES;
-  const uint32_t s_full = empty0 + 8u * AT_TC_STAGES;
-  const uint32_t p_full = s_full + 8u;
-  const uint32_t o_full = p_full + 8u;
-  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * AT_TC_STAGES + 3);
+  const uint32_t s_full0 = empty0 + 8u * AT_TC_STAGES;   // S buffer b ready: s_full0 + 8 b
+  const uint32_t p_full = s_full0 + 16u;                   // P of the current tile written
+  const uint32_t pv_done = p_full + 8u;                    // P.V of a tile retired
+  const uint32_t o_full = pv_done + 8u;                    // all P.V retired
+  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * AT_TC_STAGES + 5);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,8 +99,10 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       mbar_init(full0 + 8u * i, 1);
       mbar_init(empty0 + 8u * i, 1);
     }
-    mbar_init(s_full, 1);
+    mbar_init(s_full0, 1);
+    mbar_init(s_full0 + 8u, 1);
     mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
     mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -165,33 +169,42 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: S of tile i+1 is computed while the softmax of tile i
+    // runs (two S buffers in TMEM), then P.V of tile i
     constexpr uint32_t idS = idesc_bf16(128, 64);
     constexpr uint32_t idO = idesc_bf16(128, 128);
-    for (int i = 0; i < n_tiles; ++i) {
+    auto issue_s = [&](int i) {
       const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
-      if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err)) return false;
       tc_fence_after();
-      const uint32_t kst = st0 + (uint32_t)stg * A_STAGE, vst = kst + AK_BYTES;
+      const uint32_t kst = st0 + (uint32_t)stg * A_STAGE;
+      const uint32_t dS = tmem + (uint32_t)((i & 1) * 64);
 #pragma unroll
       for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
           for (int pl = 0; pl < 2; ++pl)
-            umma_bf16(tmem, sw128_desc(qs + (pl * 2 + half) * AQ_SUB + kk * 32),
-                      sw128_desc(kst + half * AK_SUB + kk * 32), idS,
-                      (half | kk | pl) ? 1u : 0u);
-      umma_commit(s_full);
+            umma_bf16(dS, sw128_desc(qs + (pl * 2 + half) * AQ_SUB + kk * 32),
+                      sw128_desc(kst + half * AK_SUB + kk * 32), idS, (half | kk | pl) ? 1u : 0u);
+      umma_commit(s_full0 + 8u * (i & 1));
+      return true;
+    };
+    bool go = n_tiles > 0 && issue_s(0);
+    for (int i = 0; go && i < n_tiles; ++i) {
+      if (i + 1 < n_tiles && !issue_s(i + 1)) break;
       if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) break;
       tc_fence_after();
+      const int stg = i % AT_TC_STAGES;
+      const uint32_t vst = st0 + (uint32_t)stg * A_STAGE + AK_BYTES;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
           umma_bf16(tmem + AT_TMEM_O, sw128_desc(ps + pl * AP_SUB + kk * 32),
                     sw128_desc(vst + kk * 32), idO, (i | kk | pl) ? 1u : 0u);
-      umma_commit(empty0 + 8u * stg);
+      umma_commit(empty0 + 8u * stg);      // K and V of this tile are no longer read
+      umma_commit(pv_done);
     }
     umma_commit(o_full);
   } else if (warp >= 2) {
@@ -202,14 +215,14 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < n_tiles && ok; ++i) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, i & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full0 + 8u * (i & 1), (i >> 1) & 1, abort_flag, p.err));
       tc_fence_after();
       const int nvalid = min(64, k_end - (k_begin + 64 * i));
       float sc[64];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) {
         uint32_t t[16];
-        tmem_ld16(lane_base + c0, t);
+        tmem_ld16(lane_base + (uint32_t)((i & 1) * 64) + c0, t);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) sc[c0 + j] = c0 + j < nvalid ? __uint_as_float(t[j]) : -INFINITY;
@@ -217,10 +230,15 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) mt = fmaxf(mt, sc[c]);
+      if (i > 0) {
+        // P.V of the previous tile must have retired: O is stable and the P buffer is free
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (i == 0) {
         m_used = mt;
       } else if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
-        // the previous tile's P.V has completed (MMAs retire in order before this S)
         const float m_new = fmaxf(m_used, mt);
         const float corr = exp2f(m_used - m_new);
 #pragma unroll 1
