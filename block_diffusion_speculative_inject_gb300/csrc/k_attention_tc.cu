@@ -3,39 +3,45 @@
 // One CTA = (split s, kv head, request b). Its rows are the G query heads of the kv head
 // times the K+1 block rows (R = G (K+1) <= 128, padded to the UMMA M of 128); its keys are
 // the context positions of split s, one 64-position page per tile. Per tile:
-//   S[128 rows, 64 keys]  = Q . K_tile^T          (tcgen05, A = Q in smem, B = K page)
-//   P = 2^(S - m)         (one thread per row: max, exp2, row sum; P written to smem)
-//   O[128 rows, 128 hd]  += P . V_tile            (tcgen05, A = P, B = V page stored [hd][64])
+//   S[128 rows, 64 keys]  = Q . K_tile^T          (tcgen05, A = Q in TMEM, B = K page in smem)
+//   P = 2^(S - m)         (two threads per row: max, exp2, row sum; P written over S in TMEM)
+//   O[128 rows, 128 hd]  += P . V_tile            (tcgen05, A = P in TMEM, B = V page [hd][64])
 // Q (fp32) and P (fp32) enter the tensor core as exact bf16 hi/lo pairs, so each product
 // is two MMAs against the same staged K or V tile; the cache K/V are exact bf16 already.
+// With both A operands in tensor memory the MMAs read only the K/V pages from shared
+// memory, and shared memory holds nothing but a 6-stage K/V ring.
 // Scores are in log2 units (log2(e)/sqrt(hd) folded into Q). The running max is updated
 // lazily: O in TMEM is rescaled only when a row's max grows by more than 8 (2^8 headroom).
 // The result per row is the unnormalised O, the max and the row sum, merged by the combine
 // kernel with the other splits and the block's own keys.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA (K page: two boxes of 64 x 64, V page: one
-// box of 64 x 128) into a 3-stage ring; warp 1 owns TMEM (S at columns 0 and 64, O at 128)
-// and its lane 0 issues the MMAs; warps 2-5 fill Q, run the softmax (TMEM lane quarter
-// warp % 4) and write the partials. The S of the next tile is computed into a second TMEM
-// buffer while the softmax of the current one runs. All waits are bounded in time.
+// TMEM (512 columns): S/P buffers at 0 and 64 (tile parity), O at 128, Q hi at 256, Q lo
+// at 320. A P buffer holds, for the 32 keys owned by each half of a row, 16 columns of hi
+// words then 16 of lo words, inside the S columns of those same keys.
+//
+// Roles (320 threads): warp 0 lane 0 issues TMA (K page: two boxes of 64 x 64, V page: one
+// box of 64 x 128); warp 1 owns TMEM and its lane 0 issues the MMAs; warps 2-9 fill Q, run
+// the softmax and write the partials. A row is shared by warps w and w + 4 (TMEM lane
+// quarter w % 4): each owns 32 of the tile's 64 keys and 64 of O's 128 columns, and the
+// pair exchanges its row maxima through shared memory once per tile. The S of the next
+// tile is computed while the softmax of the current one runs; the softmax waits for the
+// previous tile's P.V only when it rescales O. All waits are bounded in time.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
 namespace dflash {
 
-constexpr int AT_TC_THREADS = 192;
-constexpr int AT_TC_STAGES = 3;
-constexpr uint32_t AQ_SUB = 128 * 128;            // [128 rows x 64 hd] bf16
-constexpr uint32_t AQ_BYTES = 4 * AQ_SUB;         // [hi, lo] x [hd 0..63, 64..127]
-constexpr uint32_t AP_SUB = 128 * 128;            // [128 rows x 64 keys] bf16
-constexpr uint32_t AP_BYTES = 2 * AP_SUB;         // hi, lo
+constexpr int AT_TC_THREADS = 320;
+constexpr int AT_TC_STAGES = 6;
 constexpr uint32_t AK_SUB = 64 * 128;             // [64 keys x 64 hd] bf16
 constexpr uint32_t AK_BYTES = 2 * AK_SUB;
 constexpr uint32_t AV_BYTES = 128 * 128;          // [128 hd x 64 keys] bf16
 constexpr uint32_t A_STAGE = AK_BYTES + AV_BYTES;
-constexpr size_t AT_TC_SMEM = 1024 + AQ_BYTES + AP_BYTES + AT_TC_STAGES * A_STAGE + 256;
-constexpr uint32_t AT_TMEM_COLS = 256;
-constexpr uint32_t AT_TMEM_O = 128;               // O accumulator column offset
+constexpr uint32_t AX_BYTES = (4 * 128 + 2 * 128 + 16) * 4;   // row-max, row-sum, status exchange
+constexpr size_t AT_TC_SMEM = 1024 + AT_TC_STAGES * A_STAGE + 256 + AX_BYTES;
+constexpr uint32_t AT_TMEM_COLS = 512;
+constexpr uint32_t AT_TMEM_O = 128;               // O accumulator
+constexpr uint32_t AT_TMEM_Q = 256;               // Q hi (64 columns), then Q lo
 
 struct AttnTcParams {
   CUtensorMap kmap, vmap;
@@ -47,23 +53,22 @@ struct AttnTcParams {
   int *err;
 };
 
-// byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile of 128-byte rows
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ void split8(const float (&v)[8], uint4 &hi, uint4 &lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bf16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-    const bf16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
-    const bf16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
-    h[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-    l[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+// barrier of the two softmax warps that share a TMEM lane quarter (ids 1..4, 64 threads)
+__device__ __forceinline__ void bar_pair(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi); two values per 32-bit word
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const bf16 h0 = __float2bfloat16_rn(a), h1 = __float2bfloat16_rn(b);
+  const bf16 l0 = __float2bfloat16_rn(a - __bfloat162float(h0));
+  const bf16 l1 = __float2bfloat16_rn(b - __bfloat162float(h1));
+  hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+  lo = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
 }
 
 __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid_constant__ AttnTcParams p) {
@@ -82,16 +87,21 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  const uint32_t qs = base, ps = base + AQ_BYTES, st0 = ps + AP_BYTES;
-  uint64_t *bars = (uint64_t *)(gbase + AQ_BYTES + AP_BYTES + AT_TC_STAGES * A_STAGE);
+  const uint32_t st0 = base;
+  uint64_t *bars = (uint64_t *)(gbase + AT_TC_STAGES * A_STAGE);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * AT_TC_STAGES;
-  const uint32_t s_full0 = empty0 + 8u * AT_TC_STAGES;   // S buffer b ready: s_full0 + 8 b
+  const uint32_t s_full0 = empty0 + 8u * AT_TC_STAGES;   // S of tile parity b ready: s_full0 + 8 b
   const uint32_t p_full = s_full0 + 16u;                   // P of the current tile written
   const uint32_t pv_done = p_full + 8u;                    // P.V of a tile retired
   const uint32_t o_full = pv_done + 8u;                    // all P.V retired
   uint32_t *tmem_slot = (uint32_t *)(bars + 2 * AT_TC_STAGES + 5);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  // exchange between the two warps of a row: maxima [parity][half][row], sums [half][row],
+  // status [parity][half][quarter]
+  float *xmax = (float *)(gbase + AT_TC_STAGES * A_STAGE + 256);
+  float *xsum = xmax + 4 * 128;
+  volatile int *xok = (volatile int *)(xsum + 2 * 128);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -101,7 +111,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     }
     mbar_init(s_full0, 1);
     mbar_init(s_full0 + 8u, 1);
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
     mbar_init(o_full, 1);
     *abort_flag = 0;
@@ -111,40 +121,15 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     tmem_alloc(smem_u32(tmem_slot), AT_TMEM_COLS);
     tmem_relinquish();
   }
-  pdl_wait();                                            // q comes from the previous kernel
-  if (warp >= 2) {
-    // Q rows (scaled, split into hi/lo) in the 128-byte-swizzled K-major layout
-    const int r = threadIdx.x - 64;
-    const int qkv_dim = (p.nq + 2 * p.nkv) * 128;
-    const float *src = nullptr;
-    if (r < R) {
-      const int g = r / p.Q, j = r % p.Q;
-      src = p.qkv + ((size_t)b * p.Q + j) * qkv_dim + (size_t)(kvh * G + g) * 128;
-    }
-    float4 raw[32];                                  // the whole row in one round trip
-#pragma unroll
-    for (int i = 0; i < 32; ++i) raw[i] = src ? *(const float4 *)(src + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float4 a = raw[2 * c], d = raw[2 * c + 1];
-      float v[8] = {a.x, a.y, a.z, a.w, d.x, d.y, d.z, d.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] *= p.scale_log2;
-      uint4 hi, lo;
-      split8(v, hi, lo);
-      const int half = c >> 3, cc = c & 7;
-      *(uint4 *)(gbase + (0 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = hi;
-      *(uint4 *)(gbase + (1 * 2 + half) * AQ_SUB + sw128_off(r, cc)) = lo;
-    }
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer. The pages were written by earlier kernels of the stream
+    // (context injection), which a programmatic launch does not order before this point.
+    pdl_wait();
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
@@ -168,131 +153,179 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
              global_ns() - t0 < TC_WAIT_NS) {
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer: S of tile i+1 is computed while the softmax of tile i
-    // runs (two S buffers in TMEM), then P.V of tile i
-    constexpr uint32_t idS = idesc_bf16(128, 64);
-    constexpr uint32_t idO = idesc_bf16(128, 128);
-    auto issue_s = [&](int i) {
-      const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
-      if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err)) return false;
-      tc_fence_after();
-      const uint32_t kst = st0 + (uint32_t)stg * A_STAGE;
-      const uint32_t dS = tmem + (uint32_t)((i & 1) * 64);
-#pragma unroll
-      for (int half = 0; half < 2; ++half)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int pl = 0; pl < 2; ++pl)
-            umma_bf16(dS, sw128_desc(qs + (pl * 2 + half) * AQ_SUB + kk * 32),
-                      sw128_desc(kst + half * AK_SUB + kk * 32), idS, (half | kk | pl) ? 1u : 0u);
-      umma_commit(s_full0 + 8u * (i & 1));
-      return true;
-    };
-    bool go = n_tiles > 0 && issue_s(0);
-    for (int i = 0; go && i < n_tiles; ++i) {
-      if (i + 1 < n_tiles && !issue_s(i + 1)) break;
-      if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) break;
-      tc_fence_after();
-      const int stg = i % AT_TC_STAGES;
-      const uint32_t vst = st0 + (uint32_t)stg * A_STAGE + AK_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
+  } else if (warp == 1) {
+    // Q rows are written to TMEM by the softmax warps after the previous kernel finished
+    __syncwarp();
+    pdl_wait();
+    asm volatile("bar.sync 5, 288;" ::: "memory");   // warps 1-9: Q is in TMEM
+    tc_fence_after();
+    if (lane == 0) {
+      // ---------------- MMA issuer: S of tile i+1 is computed while the softmax of tile i
+      // runs, then P.V of tile i
+      constexpr uint32_t idS = idesc_bf16(128, 64);
+      constexpr uint32_t idO = idesc_bf16(128, 128);
+      auto issue_s = [&](int i) {
+        const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
+        if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t kst = st0 + (uint32_t)stg * A_STAGE;
+        const uint32_t dS = tmem + (uint32_t)((i & 1) * 64);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
-          umma_bf16(tmem + AT_TMEM_O, sw128_desc(ps + pl * AP_SUB + kk * 32),
-                    sw128_desc(vst + kk * 32), idO, (i | kk | pl) ? 1u : 0u);
-      umma_commit(empty0 + 8u * stg);      // K and V of this tile are no longer read
-      umma_commit(pv_done);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)           // hd in steps of 16: 8 TMEM columns of Q
+            umma_bf16_ts(dS, tmem + AT_TMEM_Q + 64 * pl + 8 * kk,
+                         sw128_desc(kst + (kk >> 2) * AK_SUB + (kk & 3) * 32), idS, (pl | kk) ? 1u : 0u);
+        umma_commit(s_full0 + 8u * (i & 1));
+        return true;
+      };
+      bool go = n_tiles > 0 && issue_s(0);
+      for (int i = 0; go && i < n_tiles; ++i) {
+        if (i + 1 < n_tiles && !issue_s(i + 1)) break;
+        if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const int stg = i % AT_TC_STAGES;
+        const uint32_t vst = st0 + (uint32_t)stg * A_STAGE + AK_BYTES;
+        const uint32_t pbuf = tmem + (uint32_t)((i & 1) * 64);
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)           // keys in steps of 16
+            umma_bf16_ts(tmem + AT_TMEM_O, pbuf + 32 * (kk >> 1) + 16 * pl + 8 * (kk & 1),
+                         sw128_desc(vst + kk * 32), idO, (i | kk | pl) ? 1u : 0u);
+        umma_commit(empty0 + 8u * stg);      // K and V of this tile are no longer read
+        umma_commit(pv_done);
+      }
+      umma_commit(o_full);
     }
-    umma_commit(o_full);
   } else if (warp >= 2) {
-    // ---------------- softmax, one thread per row (TMEM lane)
-    const int q = warp & 3;
+    const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    pdl_wait();                                        // q comes from the previous kernel
+    {
+      // Q row r, dims [64 half, 64 half + 64): scaled, split into hi/lo words in TMEM
+      const int qkv_dim = (p.nq + 2 * p.nkv) * 128;
+      const float *src = nullptr;
+      if (r < R) {
+        const int g = r / p.Q, j = r % p.Q;
+        src = p.qkv + ((size_t)b * p.Q + j) * qkv_dim + (size_t)(kvh * G + g) * 128 + 64 * half;
+      }
+      float4 raw4[16];                                 // the half row in one round trip
+#pragma unroll
+      for (int i = 0; i < 16; ++i) raw4[i] = src ? *(const float4 *)(src + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t hw[16], lw[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 a = raw4[8 * c + i];
+          split2(a.x * p.scale_log2, a.y * p.scale_log2, hw[2 * i], lw[2 * i]);
+          split2(a.z * p.scale_log2, a.w * p.scale_log2, hw[2 * i + 1], lw[2 * i + 1]);
+        }
+        tmem_st16(lane_base + AT_TMEM_Q + 32 * half + 16 * c, hw);
+        tmem_st16(lane_base + AT_TMEM_Q + 64 + 32 * half + 16 * c, lw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    asm volatile("bar.sync 5, 288;" ::: "memory");   // warps 1-9: Q is in TMEM
+
+    // ---------------- softmax: warps w and w + 4 share the rows of lane quarter w % 4
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full0 + 8u * (i & 1), (i >> 1) & 1, abort_flag, p.err));
-      tc_fence_after();
-      const int nvalid = min(64, k_end - (k_begin + 64 * i));
-      float sc[64];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t t[16];
-        tmem_ld16(lane_base + (uint32_t)((i & 1) * 64) + c0, t);
+    for (int i = 0; i < n_tiles; ++i) {
+      const int par = i & 1;
+      // the pair runs the same number of exchanges: a failed wait is passed to the partner
+      // through the status word and both leave the loop together
+      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(s_full0 + 8u * par, (i >> 1) & 1, abort_flag, p.err));
+      const uint32_t sa = lane_base + (uint32_t)(par * 64 + half * 32);   // my 32 keys
+      float sc[32];
+      float mt = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        uint32_t t0[16], t1[16];
+        tmem_ld16(sa, t0);
+        tmem_ld16(sa + 16, t1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sc[c0 + j] = c0 + j < nvalid ? __uint_as_float(t[j]) : -INFINITY;
-      }
-      float mt = -INFINITY;
+        for (int j = 0; j < 16; ++j) {
+          sc[j] = __uint_as_float(t0[j]);
+          sc[16 + j] = __uint_as_float(t1[j]);
+        }
+        const int nvalid = min(64, k_end - (k_begin + 64 * i)) - 32 * half;
+        if (nvalid < 32) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mt = fmaxf(mt, sc[c]);
-      if (i > 0) {
-        // P.V of the previous tile must have retired: O is stable and the P buffer is free
-        ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
+          for (int c = 0; c < 32; ++c) sc[c] = c < nvalid ? sc[c] : -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mt = fmaxf(mt, sc[c]);
       }
+      xmax[(par * 2 + half) * 128 + r] = mt;
+      if (lane == 0) xok[(par * 2 + half) * 4 + q] = got ? 1 : 0;
+      bar_pair(1 + q);
+      const float mp = xmax[(par * 2 + (half ^ 1)) * 128 + r];
+      ok = got && xok[(par * 2 + (half ^ 1)) * 4 + q] != 0;
+      if (!ok) break;
+      mt = fmaxf(mt, mp);
+      // lazy max: rescale only when a row's max grows by more than 8 (the pair decides alike)
       if (i == 0) {
         m_used = mt;
       } else if (__any_sync(0xffffffffu, mt > m_used + 8.f)) {
         const float m_new = fmaxf(m_used, mt);
-        const float corr = exp2f(m_used - m_new);
+        const float corr = ex2_approx(m_used - m_new);
+        m_used = m_new;
+        // P.V of the previous tile must have retired before O is rescaled (the tile before
+        // it has: its completion preceded this tile's S)
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.err))) {
+          ok = false;                      // the partner learns of it at the next exchange
+          continue;
+        }
+        tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 16) {
+        for (int c0 = 0; c0 < 64; c0 += 16) {
           uint32_t t[16];
-          tmem_ld16(lane_base + AT_TMEM_O + c0, t);
+          tmem_ld16(lane_base + AT_TMEM_O + 64 * half + c0, t);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) t[j] = __float_as_uint(__uint_as_float(t[j]) * corr);
-          tmem_st16(lane_base + AT_TMEM_O + c0, t);
+          tmem_st16(lane_base + AT_TMEM_O + 64 * half + c0, t);
         }
-        tmem_st_wait();
         l *= corr;
-        m_used = m_new;
       }
-      float rs = 0.f;
+      uint32_t ph[16], pw[16];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        sc[c] = exp2f(sc[c] - m_used);
-        rs += sc[c];
+      for (int c = 0; c < 16; ++c) {
+        const float e0 = ex2_approx(sc[2 * c] - m_used), e1 = ex2_approx(sc[2 * c + 1] - m_used);
+        l += e0 + e1;
+        split2(e0, e1, ph[c], pw[c]);
       }
-      l += rs;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = sc[8 * cc + j];
-        uint4 hi, lo;
-        split8(v, hi, lo);
-        *(uint4 *)(gbase + AQ_BYTES + sw128_off(r, cc)) = hi;
-        *(uint4 *)(gbase + AQ_BYTES + AP_SUB + sw128_off(r, cc)) = lo;
-      }
-      fence_proxy_async_smem();
+      tmem_st16(sa, ph);                   // over this thread's own S columns
+      tmem_st16(sa + 16, pw);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
+    // row sum over both halves (one more exchange, run by both warps of the pair)
+    xsum[half * 128 + r] = l;
+    bar_pair(1 + q);
+    const float l_row = l + xsum[(half ^ 1) * 128 + r];
     ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort_flag, p.err));
     tc_fence_after();
-    if (r < R) {
-      const int g = r / p.Q, j = r % p.Q;
-      const size_t idx = (((size_t)b * p.Q + j) * p.nq + (kvh * G + g)) * p.max_split + s;
+    const int g = r / p.Q, j = r % p.Q;
+    const size_t idx = (((size_t)b * p.Q + j) * p.nq + (kvh * G + g)) * p.max_split + s;
+    if (r < R && half == 0) {
       p.part_ml[idx * 2] = ok ? m_used : -INFINITY;
-      p.part_ml[idx * 2 + 1] = ok ? l : 0.f;
+      p.part_ml[idx * 2 + 1] = ok ? l_row : 0.f;
     }
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 16) {
+    for (int c0 = 0; c0 < 64; c0 += 16) {
       uint32_t t[16];
-      tmem_ld16(lane_base + AT_TMEM_O + c0, t);
+      tmem_ld16(lane_base + AT_TMEM_O + 64 * half + c0, t);
       tmem_ld_wait();
       if (r < R) {
-        const int g = r / p.Q, j = r % p.Q;
-        const size_t idx = (((size_t)b * p.Q + j) * p.nq + (kvh * G + g)) * p.max_split + s;
-        float4 *dst = (float4 *)(p.part_o + idx * 128 + c0);
+        float4 *dst = (float4 *)(p.part_o + idx * 128 + 64 * half + c0);
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4)
           dst[j4] = ok ? make_float4(__uint_as_float(t[4 * j4]), __uint_as_float(t[4 * j4 + 1]),
