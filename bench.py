@@ -265,7 +265,7 @@ def run_ours(args):
     ws, rank, local = _dist()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    cfg = get_config(args.config)
+    cfg, over = _cfg(args)
     W, K_ = args.warmup, args.steps
     n_steps = W + (3 * K_ if cfg.verify_driven else K_)      # driven runs never revisit a step
     wl = Workload(cfg, n_steps, seed=0, device=device)
@@ -395,7 +395,8 @@ def run_ours(args):
                                               f"argmax with p={cfg.accept_p})") if cfg.verify_driven
                    else f"U[1,{cfg.n_new_max}] per request",
                    "l2": "inputs larger than L2: every step streams all weights (GBs) from HBM",
-                   "parallelism": f"{ws} independent replica(s)"},
+                   "parallelism": f"{ws} independent replica(s)",
+                   **({"overrides": over} if over else {})},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches,
         "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / K_, 4),
@@ -453,11 +454,27 @@ def cpu_baseline(cfg, wl, w_cpu):
                       f"+ verify) on the fp64 numpy oracle; one request of a batch of {wl.B}"}
 
 
+def _cfg(args):
+    """The named workload, with --set KEY=VALUE overrides of its fields (profiling cases:
+    fewer layers, a smaller vocabulary or context; such a line is not the named workload)."""
+    over = {}
+    for kv in args.set or []:
+        k, v = kv.split("=", 1)
+        for cast in (int, float):
+            try:
+                v = cast(v)
+                break
+            except ValueError:
+                pass
+        over[k] = v
+    return get_config(args.config, **over), over
+
+
 def run_reference(args):
     ws, rank, local = _dist()
     if rank != 0:
         return
-    cfg = get_config(args.config)
+    cfg, over = _cfg(args)
     steps = args.warmup + args.steps
     wl = Workload(cfg, steps, seed=0, device="cpu")
     w_cpu = S.make_weights(cfg, 0)
@@ -475,7 +492,8 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic: seeded N(0,0.02) weights, N(0,1) target hidden states, uniform ids",
            "config": {"workload": f"{cfg.name}: {WORKLOAD_TEXT.get(cfg.name, cfg.name)}",
-                      "sample": "request 0 of the batch per step"},
+                      "sample": "request 0 of the batch per step",
+                      **({"overrides": over} if over else {})},
            "cpu_baseline": {"value": round(v, 3), "unit": "draft tok/s", "cores": _cores(),
                             "kind": "oracle", "sample": f"request 0 of {cfg.name} per step"},
            "e2e": {"value": round(v, 3), "unit": "draft tok/s", "h2d_bytes_per_step": 0,
@@ -492,6 +510,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--set", action="append", metavar="KEY=VALUE",
+                    help="override a workload field (profiling cases), e.g. --set n_layers=1")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
