@@ -59,10 +59,30 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 enum : int { DEV_ERR_TOKEN = 1, DEV_ERR_BOUNDS = 2, DEV_ERR_TIMEOUT = 4 };
 
 // The flag lives in mapped pinned host memory; a plain volatile store is enough (any
-// nonzero value reports an error; the code bits are a hint).
+// nonzero value reports an error; the code bits are a hint). flag[1..3] hold the detail of
+// an expired wait: the wait site, the CTA (x | y << 10 | z << 20) and the thread;
+// flag[4..5] the progress of the CTA's other roles where the kernel tracks it.
 __device__ __forceinline__ void raise_err(int *flag, int code) {
   if (flag) *(volatile int *)flag = code;
 }
+__device__ __forceinline__ void raise_wait_err(int *flag, int site, const volatile int *aux = nullptr) {
+  if (!flag) return;
+  volatile int *f = flag;
+  if (f[1] == 0) {
+    f[1] = site;
+    f[2] = (int)(blockIdx.x | (blockIdx.y << 10) | (blockIdx.z << 20));
+    f[3] = (int)threadIdx.x;
+    f[4] = aux ? aux[0] : 0;
+    f[5] = aux ? aux[1] : 0;
+  }
+  f[0] = DEV_ERR_TIMEOUT;
+}
+// wait sites reported in flag[1]
+enum : int {
+  SITE_GEMM_EMPTY = 0x101, SITE_GEMM_FULL = 0x102, SITE_GEMM_ACC = 0x103,
+  SITE_ATT_EMPTY = 0x201, SITE_ATT_FULL = 0x202, SITE_ATT_PFULL = 0x203, SITE_ATT_SFULL = 0x204,
+  SITE_ATT_PVDONE = 0x205, SITE_ATT_OFULL = 0x206,
+};
 
 // ---------------------------------------------------------------- paged KV pool
 // A page holds 64 positions of every layer: [L][K|V][nkv][block], one block per (layer,
@@ -106,6 +126,10 @@ enum GemmEpi : int {
   EPI_RESID = 1,   // Y = R + acc   (R may alias Y)
   EPI_TOPK = 2,    // per 128-row weight tile and token: the tile's top-k (value, index)
                    // into cand[tile][m][k]; Y = acc as well when y != nullptr
+  EPI_QKV = 3,     // q/k/v projection (head_dim 128: one head per 128-row tile): q and k
+                   // heads get their RMSNorm (if q_norm/k_norm) and RoPE at ctx_len[b] + j
+  EPI_SWIGLU = 4,  // W = [gate; up] ([2I, K] as two segments of I rows): a tile holds 64 gate
+                   // and the same 64 up rows; out = silu(gate) * up as an operand [M, I]
 };
 
 constexpr int GEMM_MAX_XSEG = 8;
@@ -130,6 +154,16 @@ struct GemmDesc {
   int2 *cand;                    // EPI_TOPK: [ceil(N/128)][M][k] (float bits, index)
   float *part;                   // partials mode: write the split-K partials [S][M][N] here
                                  // (S = 1: the plain product) instead of Y; a post-op sums them
+  // EPI_QKV
+  const int32_t *ctx_len;        // per request: position of its first query row
+  const float2 *rope;            // [position][hd / 2] (cos, sin)
+  const void *q_norm, *k_norm;   // bf16 [hd] or nullptr (no q/k norm)
+  float eps;
+  int rows_per_req;              // K + 1 query rows per request
+  int q_dim, kv_dim;             // column ranges [0, q_dim) q, [q_dim, q_dim + kv_dim) k
+  // EPI_SWIGLU
+  OpOut out;                     // [M, ldo] operand planes
+  int ldo;
 };
 
 }  // namespace dflash

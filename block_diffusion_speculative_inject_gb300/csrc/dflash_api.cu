@@ -158,11 +158,17 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static dflash_status check_device_flag(dflash_ctx *c) {
   if (!c->err_h) return DFLASH_OK;
   int v = __atomic_exchange_n(c->err_h, 0, __ATOMIC_SEQ_CST);
-  if (v)
-    return set_err(c, DFLASH_ERR_DEVICE, "device-side check failed earlier (code 0x%x:%s%s%s)", v,
-                   (v & DEV_ERR_TOKEN) ? " token id out of range" : "",
+  if (v) {
+    const int site = __atomic_exchange_n(c->err_h + 1, 0, __ATOMIC_SEQ_CST);
+    const int blk = c->err_h[2], thr = c->err_h[3], a0 = c->err_h[4], a1 = c->err_h[5];
+    return set_err(c, DFLASH_ERR_DEVICE,
+                   "device-side check failed earlier (code 0x%x:%s%s%s; wait site 0x%x, block "
+                   "(%d,%d,%d), thread %d, progress %d/%d)",
+                   v, (v & DEV_ERR_TOKEN) ? " token id out of range" : "",
                    (v & DEV_ERR_BOUNDS) ? " index out of bounds" : "",
-                   (v & DEV_ERR_TIMEOUT) ? " bounded wait expired" : "");
+                   (v & DEV_ERR_TIMEOUT) ? " bounded wait expired" : "", site, blk & 1023,
+                   (blk >> 10) & 1023, blk >> 20, thr, a0, a1);
+  }
   return DFLASH_OK;
 }
 
@@ -231,8 +237,9 @@ static dflash_status stage_upload_to(dflash_ctx *c, cudaStream_t s, const void *
 
 static dflash_status run_gemm(dflash_ctx *c, int cls, const GemmDesc &d, cudaStream_t s) {
   const double xsz = (d.x_bf16 && !d.x_lo[0]) ? 2.0 : 4.0;
-  const double bytes = (double)d.N * d.K * c->esz + (double)d.M * d.K * xsz +
-                       (double)d.M * d.N * 4.0 * (d.epi == EPI_RESID ? 2 : 1);
+  const double out_bytes = d.epi == EPI_SWIGLU ? (double)d.M * (d.N / 2) * 4.0
+                                               : (double)d.M * d.N * 4.0 * (d.epi == EPI_RESID ? 2 : 1);
+  const double bytes = (double)d.N * d.K * c->esz + (double)d.M * d.K * xsz + out_bytes;
   const double flops = 2.0 * d.M * d.N * d.K;
   if (c->tc && c->dtype == DFLASH_BF16) {
     int n = tc_gemm_launches(c->tc, d);
@@ -488,10 +495,10 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
     const char *so = getenv("DFLASH_SPLIT_OVERHEAD");
     if (so && so[0]) c->split_overhead = std::max(0.0, atof(so));
   }
-  if (cudaHostAlloc((void **)&c->err_h, sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
+  if (cudaHostAlloc((void **)&c->err_h, 8 * sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer((void **)&c->err_d, c->err_h, 0) != cudaSuccess)
     return fail(DFLASH_ERR_CUDA);
-  *c->err_h = 0;
+  memset(c->err_h, 0, 8 * sizeof(int));
 
   // bf16 weights use the tensor-core GEMM; DFLASH_FORCE_FFMA=1 (diagnostics) keeps the FFMA one
   const char *force_ffma = getenv("DFLASH_FORCE_FFMA");
@@ -731,6 +738,12 @@ static void plan_splits(const std::vector<int> &pages, int nkv, int slots, doubl
 // logits and rank them row by row, which is cheaper than 32+ rounds per warp per tile.
 static bool fused_topk(const dflash_ctx *c, int rows) { return c->tc && rows <= 32; }
 
+// q/k norm + RoPE and SwiGLU run in the tensor-core GEMM epilogues when a head is one
+// 128-row weight tile; otherwise (FFMA GEMM, head_dim 64) they are separate post-ops.
+static bool fused_epilogues(const dflash_ctx *c) {
+  return c->tc && c->m.hd == 128 && c->m.q_dim() % 128 == 0 && c->m.kv_dim() % 128 == 0;
+}
+
 // The layer stack of the draft step plus the final norm and the LM-head GEMM: every launch
 // between the embedding and the top-k selection. It touches only library buffers and the
 // device descriptor `bt`, so it can be captured once per (batch, split plan) and replayed.
@@ -746,17 +759,32 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
   int S = 1;
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
-    // q/k/v projection; post-op: per-head q/k norm + RoPE
+    // q/k/v projection with per-head q/k norm + RoPE: in the tensor-core GEMM's epilogue
+    // (one 128-wide head per tile), else as a post-op
     GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, nullptr, m.qkv_dim());
     set_x(c, d, xn, m.H);
     add_wseg(d, lw.wq, m.q_dim());
     add_wseg(d, lw.wk, m.kv_dim());
     add_wseg(d, lw.wv, m.kv_dim());
-    if ((st = gemm_ws(c, K_GEMM_QKV, d, s, &S)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_ROPE, s, 4.0 * R * m.qkv_dim() * (S + 1), 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
-         return launch_post_qkv(c->dtype, m, B, c->ws, S, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
-                                lw.k_norm, s);
-       }));
+    if (fused_epilogues(c)) {
+      d.epi = EPI_QKV;
+      d.y = c->qkv;
+      d.ctx_len = bt.ctx_len;
+      d.rope = c->rope;
+      d.q_norm = m.qk_norm ? lw.q_norm : nullptr;
+      d.k_norm = m.qk_norm ? lw.k_norm : nullptr;
+      d.eps = m.eps;
+      d.rows_per_req = m.Q();
+      d.q_dim = m.q_dim();
+      d.kv_dim = m.kv_dim();
+      if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
+    } else {
+      if ((st = gemm_ws(c, K_GEMM_QKV, d, s, &S)) != DFLASH_OK) return st;
+      CK(c, timed(c, K_ROPE, s, 4.0 * R * m.qkv_dim() * (S + 1), 8.0 * R * (m.nq + m.nkv) * m.hd, 1, [&] {
+           return launch_post_qkv(c->dtype, m, B, c->ws, S, c->qkv, bt.ctx_len, c->rope, lw.q_norm,
+                                  lw.k_norm, s);
+         }));
+    }
     CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, bt.max_split > 0 ? 2 : 1, [&] {
          return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
                                  c->amaps.valid ? &c->amaps : nullptr, s);
@@ -769,14 +797,22 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
          return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, xn, lw.post_norm, m.eps, 0, s);
        }));
-    // gate/up projection; post-op: SwiGLU
+    // gate/up projection with SwiGLU: in the tensor-core GEMM's epilogue (a tile takes 64
+    // gate and the same 64 up rows), else as a post-op
     GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, nullptr, 2 * m.I);
     set_x(c, gu, xn, m.H);
     add_wseg(gu, lw.w_gate, m.I);
     add_wseg(gu, lw.w_up, m.I);
-    if ((st = gemm_ws(c, K_GEMM_GATEUP, gu, s, &S)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_SWIGLU, s, 4.0 * R * m.I * (2 * S + 1), 5.0 * R * m.I, 1,
-                [&] { return launch_post_swiglu(R, m.I, c->ws, S, hm, s); }));
+    if (fused_epilogues(c) && m.I % 64 == 0) {
+      gu.epi = EPI_SWIGLU;
+      gu.out = hm;
+      gu.ldo = m.I;
+      if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
+    } else {
+      if ((st = gemm_ws(c, K_GEMM_GATEUP, gu, s, &S)) != DFLASH_OK) return st;
+      CK(c, timed(c, K_SWIGLU, s, 4.0 * R * m.I * (2 * S + 1), 5.0 * R * m.I, 1,
+                  [&] { return launch_post_swiglu(R, m.I, c->ws, S, hm, s); }));
+    }
     // down projection; post-op: residual add + the next layer's input norm, or after the
     // last layer the final norm of the K mask rows (the anchor row yields no candidate)
     GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_STORE, nullptr, m.H);

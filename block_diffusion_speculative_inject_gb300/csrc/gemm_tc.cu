@@ -56,8 +56,17 @@ struct TcParams {
   const float *resid;
   int topk;                           // EPI_TOPK
   int2 *cand;                         // EPI_TOPK: [n_tiles][M][topk]
+  const int32_t *ctx_len;             // EPI_QKV
+  const float2 *rope;
+  const bf16 *q_norm, *k_norm;
+  float eps;
+  int rows_per_req, q_dim, kv_dim;
+  OpOut out;                          // EPI_SWIGLU
+  int ldo;
   int *err;
 };
+
+
 
 template <int BN>
 constexpr int tmem_cols() {
@@ -66,7 +75,7 @@ constexpr int tmem_cols() {
 
 // ------------------------------------------------------------------------- the kernel
 template <int BN>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
   constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
@@ -86,6 +95,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
+  const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU;
   const int kb0 = split * p.kb_per;
   const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
 
@@ -112,15 +122,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     // ---------------- TMA producer
     int ws = 0;
     while (ws + 1 < p.n_wseg && n0 >= p.w_n0[ws + 1]) ++ws;
-    const CUtensorMap *wm = &p.wmap[ws];
-    const int wrow = n0 - p.w_n0[ws];
+    const bool glu = p.epi == EPI_SWIGLU;                  // rows 0-63 gate, 64-127 up
+    const CUtensorMap *wm = &p.wmap[glu ? 0 : ws];
+    const int wrow = glu ? (int)blockIdx.y * 64 : n0 - p.w_n0[ws];
+    auto load_w = [&](uint32_t st, int k, uint32_t fb) {
+      tma_load_2d(st, wm, k, wrow, fb);
+      if (glu) tma_load_2d(st + 64 * 128, &p.wmap[1], k, wrow, fb);
+    };
     // the first stages' weight tiles do not depend on the previous kernel: start streaming
     // them before waiting for it
     const int pre = min(stages, nkb);
     for (int i = 0; i < pre; ++i) {
       const uint32_t fb = full0 + 8u * i;
       mbar_expect_tx(fb, stage_bytes);
-      tma_load_2d(tiles + (uint32_t)i * stage_bytes, wm, (kb0 + i) * TC_BK, wrow, fb);
+      load_w(tiles + (uint32_t)i * stage_bytes, (kb0 + i) * TC_BK, fb);
     }
     pdl_wait();
     int issued = 0;
@@ -130,9 +145,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
       const uint32_t fb = full0 + 8u * s;
       const int k = (kb0 + i) * TC_BK;
       if (i >= pre) {
-        if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err)) break;
+        if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err, SITE_GEMM_EMPTY)) break;
         mbar_expect_tx(fb, stage_bytes);
-        tma_load_2d(st, wm, k, wrow, fb);
+        load_w(st, k, fb);
       }
       if (p.split) {
         tma_load_2d(st + A_BYTES, &p.xmap[0], k, m0, fb);
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     constexpr uint32_t idesc = idesc_bf16(TC_BM, BN);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % stages, u = i / stages;
-      if (!mbar_wait(full0 + 8u * s, u & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(full0 + 8u * s, u & 1, abort_flag, p.err, SITE_GEMM_FULL)) break;
       tc_fence_after();
       const uint32_t a = tiles + (uint32_t)s * stage_bytes;
       const uint32_t b = a + A_BYTES;
@@ -176,7 +191,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int q = warp & 3;               // TMEM lane quarter this warp may access
-    const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err);
+    const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
     tc_fence_after();
     const int n = n0 + q * 32 + lane;
     // the top-k epilogue stages the tile [BN tokens][128 rows] in the (now idle) stage memory
@@ -198,8 +213,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
         }
         continue;
       }
-      if (p.S > 1) {
-        // split-K: stage this CTA's partial tile [BN][128] for the cluster's reduction
+      if (staged) {
+        // stage this CTA's (partial) tile [BN][128] for the split-K reduction and the
+        // per-token epilogues
 #pragma unroll
         for (int j = 0; j < 16; ++j) tile[(c0 + j) * TC_BM + q * 32 + lane] = ok ? __uint_as_float(r[j]) : 0.f;
         continue;
@@ -261,31 +277,91 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
-  if (p.S > 1) {
-    // every split's partial tile is staged; rank r sums columns r, r + S, ... over all
-    // ranks, in rank order
-    cluster_sync_all();
+  if (staged) {
+    // every split's partial tile is staged; rank r owns columns (tokens) r, r + S, ...: each
+    // epilogue warp takes one of them at a time, sums its 128 rows over all ranks in rank
+    // order (lane l: rows l, l + 32, l + 64, l + 96) and applies the epilogue
+    if (p.S > 1) cluster_sync_all();
     if (warp >= 2) {
-      const int q = warp & 3;
-      const int n = n0 + q * 32 + lane;
       const uint32_t base = smem_u32(gen_tiles);
-      for (int c = (int)cluster_ctarank(); c < BN; c += p.S) {
-        const int m = m0 + c;
-        if (m >= p.M) break;
-        const uint32_t off = base + (uint32_t)((c * TC_BM + q * 32 + lane) * 4);
-        float v[8];
+      const float *own = (const float *)gen_tiles;
+      const int part = n0 < p.q_dim ? 0 : (n0 < p.q_dim + p.kv_dim ? 1 : 2);   // EPI_QKV
+      const int rank = (int)cluster_ctarank();
+      constexpr int U = 4;                     // tokens per warp per round: loads in flight
+      for (int cb = rank + p.S * (warp - 2); cb < BN; cb += 4 * U * p.S) {
+        float a[U][4];
+        float2 cs[U][2];
+        int mu[U];
 #pragma unroll
-        for (int rk = 0; rk < 8; ++rk) v[rk] = rk < p.S ? dsmem_ld(dsmem_addr(off, (uint32_t)rk)) : 0.f;
-        float a = 0.f;
+        for (int u = 0; u < U; ++u) {
+          const int c = cb + 4 * p.S * u;
+          mu[u] = (c < BN && m0 + c < p.M) ? m0 + c : -1;
+          if (mu[u] < 0) continue;
+          if (p.S == 1) {
 #pragma unroll
-        for (int rk = 0; rk < 8; ++rk) a += v[rk];
-        if (n < p.N) {
-          const size_t o = (size_t)m * p.ldy + n;
-          p.y[o] = p.epi == EPI_RESID ? p.resid[o] + a : a;
+            for (int j = 0; j < 4; ++j) a[u][j] = own[c * TC_BM + lane + 32 * j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float v[8];
+#pragma unroll
+              for (int rk = 0; rk < 8; ++rk)
+                v[rk] = rk < p.S ? dsmem_ld(dsmem_addr(base + (uint32_t)((c * TC_BM + lane + 32 * j) * 4),
+                                                       (uint32_t)rk))
+                                 : 0.f;
+              a[u][j] = 0.f;
+#pragma unroll
+              for (int rk = 0; rk < 8; ++rk) a[u][j] += v[rk];
+            }
+          }
+          if (p.epi == EPI_QKV && part < 2) {
+            const int m = mu[u];
+            const int pos = __ldg(p.ctx_len + m / p.rows_per_req) + m % p.rows_per_req;
+            cs[u][0] = __ldg(p.rope + (size_t)pos * 64 + lane);
+            cs[u][1] = __ldg(p.rope + (size_t)pos * 64 + lane + 32);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int m = mu[u];
+          if (m < 0) continue;
+          float *x = a[u];
+          if (p.epi == EPI_SWIGLU) {
+            // rows lane, lane + 32 are gate; lane + 64, lane + 96 the matching up rows
+            const size_t o = (size_t)m * p.ldo + (size_t)blockIdx.y * 64 + lane;
+            write_op(p.out, o, x[0] / (1.f + expf(-x[0])) * x[2]);
+            write_op(p.out, o + 32, x[1] / (1.f + expf(-x[1])) * x[3]);
+            continue;
+          }
+          if (p.epi == EPI_QKV && part < 2) {
+            // one head of 128: RMSNorm (if weights), then RoPE on (l, l + 64), (l + 32, l + 96)
+            const bf16 *nw = part == 0 ? p.q_norm : p.k_norm;
+            if (nw) {
+              const float rs =
+                  rsqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]) / 128.f + p.eps);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) x[j] = x[j] * rs * __bfloat162float(nw[lane + 32 * j]);
+            }
+            const float2 c0 = cs[u][0], c1 = cs[u][1];
+            const float o0 = x[0] * c0.x - x[2] * c0.y, o2 = x[2] * c0.x + x[0] * c0.y;
+            const float o1 = x[1] * c1.x - x[3] * c1.y, o3 = x[3] * c1.x + x[1] * c1.y;
+            x[0] = o0;
+            x[1] = o1;
+            x[2] = o2;
+            x[3] = o3;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + lane + 32 * j;
+            if (n < p.N) {
+              const size_t o = (size_t)m * p.ldy + n;
+              p.y[o] = p.epi == EPI_RESID ? p.resid[o] + x[j] : x[j];
+            }
+          }
         }
       }
     }
-    cluster_sync_all();               // peers keep their shared memory until all are done
+    if (p.S > 1) cluster_sync_all();   // peers keep their shared memory until all are done
   }
   if (warp == 1) {
     tc_fence_after();
@@ -381,10 +457,11 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   p.stages = p.bn <= 32 ? 3 : (int)std::max<size_t>(2, std::min<size_t>(8, (200 * 1024) / stage));
   p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 1) + 16;
   const int per_sm = std::max(1, std::min(4, (int)((228 * 1024) / (p.smem + 1024))));
-  // split K into as many parts as keep the grid within one wave of resident CTAs
+  // split K into as many parts as keep the grid within one wave of resident CTAs (more
+  // CTAs in flight streamed faster than balancing the bytes per SM, measured)
   const int base = p.t_tiles * p.n_tiles;
-  int S = std::max(1, (per_sm * t->num_sms) / base);
-  S = std::max(1, std::min(S, std::min(8, p.kb / 4)));    // a portable cluster holds 8 CTAs
+  const int s_max = std::max(1, std::min(8, p.kb / 4));    // a portable cluster holds 8 CTAs
+  int S = std::max(1, std::min((per_sm * t->num_sms) / base, s_max));
   if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
   p.kb_per = (p.kb + S - 1) / S;
   p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
@@ -431,10 +508,17 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   const Plan pl = plan_for(t, d);
   TcParams p;   // kernel parameters (copied at launch)
   memset(&p, 0, sizeof(p));
+  if (d.epi == EPI_SWIGLU &&
+      (d.n_wseg != 2 || d.w_n0[1] * 2 != d.N || d.w_n0[1] % 64 || d.part || !d.out.lo))
+    return cudaErrorInvalidValue;
+  if (d.epi == EPI_QKV && (d.q_dim % TC_BM || d.kv_dim % TC_BM || !d.ctx_len || !d.rope || d.part ||
+                           d.rows_per_req < 1))
+    return cudaErrorInvalidValue;
   p.n_wseg = d.n_wseg;
   for (int i = 0; i < d.n_wseg; ++i) {
     const long rows = d.w_n0[i + 1] - d.w_n0[i];
-    if (!get_map(t, d.w[i], rows, d.K, d.K, TC_BM, &p.wmap[i])) return cudaErrorInvalidValue;
+    const int box = d.epi == EPI_SWIGLU ? 64 : TC_BM;        // gate/up: half tiles of each
+    if (!get_map(t, d.w[i], rows, d.K, d.K, box, &p.wmap[i])) return cudaErrorInvalidValue;
     p.w_n0[i] = d.w_n0[i];
   }
   p.w_n0[d.n_wseg] = d.w_n0[d.n_wseg];
@@ -468,6 +552,16 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.y = d.y;
   p.ldy = d.ldy;
   p.resid = d.resid;
+  p.ctx_len = d.ctx_len;
+  p.rope = d.rope;
+  p.q_norm = (const bf16 *)d.q_norm;
+  p.k_norm = (const bf16 *)d.k_norm;
+  p.eps = d.eps;
+  p.rows_per_req = d.rows_per_req;
+  p.q_dim = d.q_dim;
+  p.kv_dim = d.kv_dim;
+  p.out = d.out;
+  p.ldo = d.ldo;
   p.err = t->err;
   if (d.part) {
     // partials mode: the (already reduced) product goes to the caller's buffer [M][N]

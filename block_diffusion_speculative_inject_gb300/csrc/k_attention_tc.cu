@@ -37,7 +37,7 @@ constexpr uint32_t AK_SUB = 64 * 128;             // [64 keys x 64 hd] bf16
 constexpr uint32_t AK_BYTES = 2 * AK_SUB;
 constexpr uint32_t AV_BYTES = 128 * 128;          // [128 hd x 64 keys] bf16
 constexpr uint32_t A_STAGE = AK_BYTES + AV_BYTES;
-constexpr uint32_t AX_BYTES = (4 * 128 + 2 * 128 + 16) * 4;   // row-max, row-sum, status exchange
+constexpr uint32_t AX_BYTES = (4 * 128 + 2 * 128 + 16 + 2) * 4;   // row-max, row-sum, status, progress
 constexpr size_t AT_TC_SMEM = 1024 + AT_TC_STAGES * A_STAGE + 256 + AX_BYTES;
 constexpr uint32_t AT_TMEM_COLS = 512;
 constexpr uint32_t AT_TMEM_O = 128;               // O accumulator
@@ -91,17 +91,21 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   uint64_t *bars = (uint64_t *)(gbase + AT_TC_STAGES * A_STAGE);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * AT_TC_STAGES;
-  const uint32_t s_full0 = empty0 + 8u * AT_TC_STAGES;   // S of tile parity b ready: s_full0 + 8 b
-  const uint32_t p_full = s_full0 + 16u;                   // P of the current tile written
-  const uint32_t pv_done = p_full + 8u;                    // P.V of a tile retired
+  // Per tile parity b: S ready (s_full0 + 8 b) and P written (p_full0 + 8 b). P has its own
+  // pair: the softmax may write P of tile i + 1 before the issuer has seen P of tile i.
+  const uint32_t s_full0 = empty0 + 8u * AT_TC_STAGES;
+  const uint32_t p_full0 = s_full0 + 16u;
+  const uint32_t pv_done = p_full0 + 16u;                  // P.V of a tile retired
   const uint32_t o_full = pv_done + 8u;                    // all P.V retired
-  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * AT_TC_STAGES + 5);
+  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * AT_TC_STAGES + 6);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   // exchange between the two warps of a row: maxima [parity][half][row], sums [half][row],
   // status [parity][half][quarter]
   float *xmax = (float *)(gbase + AT_TC_STAGES * A_STAGE + 256);
   float *xsum = xmax + 4 * 128;
   volatile int *xok = (volatile int *)(xsum + 2 * 128);
+  // progress of the MMA issuer and of softmax warp 2, reported if the producer's wait expires
+  volatile int *prog = xok + 16;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -111,10 +115,12 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     }
     mbar_init(s_full0, 1);
     mbar_init(s_full0 + 8u, 1);
-    mbar_init(p_full, 8);
+    mbar_init(p_full0, 8);
+    mbar_init(p_full0 + 8u, 8);
     mbar_init(pv_done, 1);
     mbar_init(o_full, 1);
     *abort_flag = 0;
+    prog[0] = prog[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {
       const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
-      if (u > 0 && !mbar_wait(empty0 + 8u * stg, (u - 1) & 1, abort_flag, p.err)) break;
+      if (u > 0 && !mbar_wait(empty0 + 8u * stg, (u - 1) & 1, abort_flag, p.err, SITE_ATT_EMPTY, prog)) break;
       const int page = pg[(k_begin + 64 * i) / 64];
       const int blk = (page * p.L + p.layer) * 2 * p.nkv;
       const int krow = (blk + kvh) * 64;               // K view: rows of 128 values
@@ -160,13 +166,14 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     asm volatile("bar.sync 5, 288;" ::: "memory");   // warps 1-9: Q is in TMEM
     tc_fence_after();
     if (lane == 0) {
+      prog[0] = 1;
       // ---------------- MMA issuer: S of tile i+1 is computed while the softmax of tile i
       // runs, then P.V of tile i
       constexpr uint32_t idS = idesc_bf16(128, 64);
       constexpr uint32_t idO = idesc_bf16(128, 128);
       auto issue_s = [&](int i) {
         const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
-        if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err, SITE_ATT_FULL)) return false;
         tc_fence_after();
         const uint32_t kst = st0 + (uint32_t)stg * A_STAGE;
         const uint32_t dS = tmem + (uint32_t)((i & 1) * 64);
@@ -181,8 +188,11 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       };
       bool go = n_tiles > 0 && issue_s(0);
       for (int i = 0; go && i < n_tiles; ++i) {
+        prog[0] = 16 + 4 * i;
         if (i + 1 < n_tiles && !issue_s(i + 1)) break;
-        if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) break;
+        prog[0] = 16 + 4 * i + 1;
+        if (!mbar_wait(p_full0 + 8u * (i & 1), (i >> 1) & 1, abort_flag, p.err, SITE_ATT_PFULL)) break;
+        prog[0] = 16 + 4 * i + 2;
         tc_fence_after();
         const int stg = i % AT_TC_STAGES;
         const uint32_t vst = st0 + (uint32_t)stg * A_STAGE + AK_BYTES;
@@ -202,7 +212,9 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    if (warp == 2 && lane == 0) prog[1] = 1;
     pdl_wait();                                        // q comes from the previous kernel
+    if (warp == 2 && lane == 0) prog[1] = 2;
     {
       // Q row r, dims [64 half, 64 half + 64): scaled, split into hi/lo words in TMEM
       const int qkv_dim = (p.nq + 2 * p.nkv) * 128;
@@ -230,15 +242,17 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       tc_fence_before();
     }
     asm volatile("bar.sync 5, 288;" ::: "memory");   // warps 1-9: Q is in TMEM
+    if (warp == 2 && lane == 0) prog[1] = 3;
 
     // ---------------- softmax: warps w and w + 4 share the rows of lane quarter w % 4
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int par = i & 1;
+      if (warp == 2 && lane == 0) prog[1] = 16 + 8 * i;
       // the pair runs the same number of exchanges: a failed wait is passed to the partner
       // through the status word and both leave the loop together
-      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(s_full0 + 8u * par, (i >> 1) & 1, abort_flag, p.err));
+      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(s_full0 + 8u * par, (i >> 1) & 1, abort_flag, p.err, SITE_ATT_SFULL));
       const uint32_t sa = lane_base + (uint32_t)(par * 64 + half * 32);   // my 32 keys
       float sc[32];
       float mt = -INFINITY;
@@ -267,6 +281,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       const float mp = xmax[(par * 2 + (half ^ 1)) * 128 + r];
       ok = got && xok[(par * 2 + (half ^ 1)) * 4 + q] != 0;
       if (!ok) break;
+      if (warp == 2 && lane == 0) prog[1] = 16 + 8 * i + 1;
       mt = fmaxf(mt, mp);
       // lazy max: rescale only when a row's max grows by more than 8 (the pair decides alike)
       if (i == 0) {
@@ -277,7 +292,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
         m_used = m_new;
         // P.V of the previous tile must have retired before O is rescaled (the tile before
         // it has: its completion preceded this tile's S)
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (i - 1) & 1, abort_flag, p.err, SITE_ATT_PVDONE))) {
           ok = false;                      // the partner learns of it at the next exchange
           continue;
         }
@@ -305,13 +320,14 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full0 + 8u * par);
+      if (warp == 2 && lane == 0) prog[1] = 16 + 8 * i + 3;
     }
     // row sum over both halves (one more exchange, run by both warps of the pair)
     xsum[half * 128 + r] = l;
     bar_pair(1 + q);
     const float l_row = l + xsum[(half ^ 1) * 128 + r];
-    ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort_flag, p.err));
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort_flag, p.err, SITE_ATT_OFULL));
     tc_fence_after();
     const int g = r / p.Q, j = r % p.Q;
     const size_t idx = (((size_t)b * p.Q + j) * p.nq + (kvh * G + g)) * p.max_split + s;

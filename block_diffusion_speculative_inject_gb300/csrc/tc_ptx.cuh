@@ -38,9 +38,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait: false when the CTA was aborted or the wait ran out of time (which aborts).
+// Bounded wait: false when the CTA was aborted or the wait ran out of time (which aborts
+// and records `site`).
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort_flag,
-                                          int *err) {
+                                          int *err, int site, const volatile int *aux = nullptr) {
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
@@ -48,7 +49,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile 
     if (*abort_flag) return false;
     if (global_ns() - t0 > TC_WAIT_NS) {
       *abort_flag = 1;
-      raise_err(err, DEV_ERR_TIMEOUT);
+      raise_wait_err(err, site, aux);
       return false;
     }
   }
