@@ -989,7 +989,7 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   } else {
     float *lg = logits ? logits : c->logits;
     CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
-         return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, s);
+         return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, 0, s);
        }));
   }
   return DFLASH_OK;

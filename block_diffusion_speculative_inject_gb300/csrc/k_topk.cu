@@ -5,6 +5,7 @@
 //                      epilogue, [tiles][rows][k] (value, index) per row, merged per CTA.
 // Each thread keeps a sorted register list of its best TK candidates over a strided slice,
 // then the block merges the 256 sorted lists by k rounds of a block-wide best-head pick.
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -132,8 +133,9 @@ __device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int 
 
 // Two passes over the row: (1) every thread's maximum; the k-th best of those maxima is a
 // lower bound T of the row's k-th best value (k threads each hold a value >= T); (2) only
-// values >= T enter the threads' lists, so almost no insertions happen.
-__global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const float *logits,
+// values >= T enter the threads' lists, so almost no insertions happen. CTA b takes rows
+// b, b + gridDim.x, ...
+__global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
   pdl_wait();
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
   __shared__ float thr_v[TK];
   __shared__ int thr_i[TK];
   __shared__ int dummy;
-  const int row = blockIdx.x;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
   const float *x = logits + (size_t)row * V;
   const bool vec = (V & 3) == 0;
   const int n4 = V / 4;
@@ -195,12 +197,14 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_rows(int V, int k, const fl
   });
   block_merge(lv, li, k, argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
               topk_val ? topk_val + (size_t)row * k : nullptr);
+  __syncthreads();                     // thr_v / the merge scratch are reused by the next row
+  }
 }
 
-// Merge of per-tile sorted candidate lists. With at least k tiles, the k-th best of the
-// tiles' first candidates is a lower bound T of the row's k-th best value (those k tiles
-// each hold a value >= T), so only candidates >= T can be in the result: they are gathered
-// in one parallel pass and selected exactly. (If more than MERGE_CAP candidates tie at or
+// Merge of per-tile sorted candidate lists (each tile's list is its best k in order). With at
+// least k tiles, the k-th best of the tiles' first candidates is a lower bound T of the
+// row's k-th best value (those k tiles each hold a value >= T), so only candidates >= T can
+// be in the result: they are gathered in one parallel pass and selected exactly. (If more than MERGE_CAP candidates tie at or
 // above T, every candidate is scanned instead; with fewer than k tiles all are ranked.)
 constexpr int MERGE_CAP = 1024;
 
@@ -240,14 +244,17 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
   if (threadIdx.x == 0) n_pool = 0;
   __syncthreads();
   const float T = thr_val[kk - 1];
-  // 2) gather every candidate >= T
-  const int n = tiles * k;
+  // 2) gather every candidate >= T. A tile's list is sorted, so only tiles whose first
+  // candidate is >= T (about k of them) can hold one.
+  for (int t = threadIdx.x; t < tiles; t += TK_THREADS) {
+    if (__int_as_float(at(t, 0).x) < T) continue;
 #pragma unroll 4
-  for (int i = threadIdx.x; i < n; i += TK_THREADS) {
-    const int2 c = at(i / k, i % k);
-    if (__int_as_float(c.x) >= T) {
-      const int slot = atomicAdd(&n_pool, 1);
-      if (slot < MERGE_CAP) pool[slot] = c;
+    for (int j = 0; j < k; ++j) {
+      const int2 c = at(t, j);
+      if (__int_as_float(c.x) >= T) {
+        const int slot = atomicAdd(&n_pool, 1);
+        if (slot < MERGE_CAP) pool[slot] = c;
+      }
     }
   }
   __syncthreads();
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
                },
                argmax + row, oi, ov);
   } else {
-    block_topk(n, k,
+    block_topk(tiles * k, k,
                [&](int i, float &v, int &id) {
                  const int2 c = at(i / k, i % k);
                  v = __int_as_float(c.x);
@@ -273,10 +280,11 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
 }
 
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
-                        int32_t *topk_idx, float *topk_val, cudaStream_t s) {
+                        int32_t *topk_idx, float *topk_val, int max_ctas, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
-  return launch_pdl(k_topk_rows, dim3(rows), dim3(TK_THREADS), 0, s, V, k, logits, argmax, topk_idx,
+  const int g = max_ctas > 0 ? std::min(rows, max_ctas) : rows;
+  return launch_pdl(k_topk_rows, dim3(g), dim3(TK_THREADS), 0, s, rows, V, k, logits, argmax, topk_idx,
                     topk_val);
 }
 

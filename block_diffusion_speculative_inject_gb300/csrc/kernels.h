@@ -46,9 +46,10 @@ cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &b, int la
                                  const float *qkv, const AttnMaps *maps, float scale_log2,
                                  float *part_o, float *part_ml, cudaStream_t s);
 
-// Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V].
+// Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V], on at
+// most max_ctas CTAs (<= 0: one per row) that loop over the rows.
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
-                        int32_t *topk_idx, float *topk_val, cudaStream_t s);
+                        int32_t *topk_idx, float *topk_val, int max_ctas, cudaStream_t s);
 
 // Merge of the per-tile candidates [tiles][rows][k] of the tensor-core LM-head epilogue.
 cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
