@@ -132,81 +132,115 @@ __device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int 
 }
 
 // Two passes over the row: (1) every thread's maximum; the k-th best of those maxima is a
-// lower bound T of the row's k-th best value (k threads each hold a value >= T); (2) only
-// values >= T enter the threads' lists, so almost no insertions happen. CTA b takes rows
-// b, b + gridDim.x, ...
+// lower bound T of the row's k-th best value (k threads each hold a value >= T); (2) the
+// values >= T (a few more than k) are gathered in shared memory and placed by rank: a
+// value's output slot is the number of gathered values that beat it. If more than ROWS_CAP
+// values reach T (ties), the block-wide list selector ranks the row instead. CTA b takes
+// rows b, b + gridDim.x, ...
+constexpr int ROWS_CAP = 2048;
+
 __global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float thr_v[TK];
-  __shared__ int thr_i[TK];
-  __shared__ int dummy;
+  __shared__ float tmax[TK_THREADS];
+  __shared__ int2 pool[ROWS_CAP];
+  __shared__ int n_pool;
+  __shared__ float thr;
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-  const float *x = logits + (size_t)row * V;
-  const bool vec = (V & 3) == 0;
-  const int n4 = V / 4;
-  const float4 *x4 = (const float4 *)x;
-  float lv[TK];
-  int li[TK];
-  // pass 1: per-thread maximum (index of the first occurrence)
-  float mv = -INFINITY;
-  int mi = 0x7fffffff;
-  auto scan = [&](auto &&visit) {
-    if (vec) {
-      for (int b = 0; b < n4; b += TK_THREADS * 8) {
-        float4 v[8];
+    const float *x = logits + (size_t)row * V;
+    const bool vec = (V & 3) == 0;
+    const int n4 = V / 4;
+    const float4 *x4 = (const float4 *)x;
+    int32_t *oi = topk_idx ? topk_idx + (size_t)row * k : nullptr;
+    float *ov = topk_val ? topk_val + (size_t)row * k : nullptr;
+    auto scan = [&](auto &&visit) {
+      if (vec) {
+        for (int b = 0; b < n4; b += TK_THREADS * 8) {
+          float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = b + threadIdx.x + j * TK_THREADS;
-          v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          for (int j = 0; j < 8; ++j) {
+            const int i = b + threadIdx.x + j * TK_THREADS;
+            v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
+            if (i < V) {
+              visit(v[j].x, i);
+              visit(v[j].y, i + 1);
+              visit(v[j].z, i + 2);
+              visit(v[j].w, i + 3);
+            }
+          }
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
-          if (i < V) {
-            visit(v[j].x, i);
-            visit(v[j].y, i + 1);
-            visit(v[j].z, i + 2);
-            visit(v[j].w, i + 3);
+      } else {
+        for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
+      }
+    };
+    // pass 1: per-thread maximum
+    float mv = -INFINITY;
+    scan([&](float v, int) { mv = fmaxf(mv, v); });
+    tmax[threadIdx.x] = mv;
+    if (threadIdx.x == 0) n_pool = 0;
+    __syncthreads();
+    {
+      // stable rank of this thread's maximum among all; rank k - 1 is the bound
+      int rank = 0;
+      for (int j = 0; j < TK_THREADS; ++j) {
+        const float u = tmax[j];
+        rank += (u > mv) | ((u == mv) & (j < (int)threadIdx.x));
+      }
+      if (rank == k - 1) thr = mv;
+    }
+    __syncthreads();
+    const float T = thr;
+    // pass 2: gather the values >= T
+    scan([&](float v, int i) {
+      if (v >= T) {
+        const int slot = atomicAdd(&n_pool, 1);
+        if (slot < ROWS_CAP) pool[slot] = make_int2(__float_as_int(v), i);
+      }
+    });
+    __syncthreads();
+    const int np = n_pool;
+    if (np <= ROWS_CAP) {
+      for (int i = threadIdx.x; i < np; i += TK_THREADS) {
+        const int2 c = pool[i];
+        const float v = __int_as_float(c.x);
+        int rank = 0;
+        for (int j = 0; j < np; ++j) {
+          const int2 d = pool[j];
+          rank += better(__int_as_float(d.x), d.y, v, c.y);
+        }
+        if (rank < k) {
+          if (rank == 0) argmax[row] = c.y;
+          if (oi) {
+            oi[rank] = c.y;
+            ov[rank] = v;
           }
         }
       }
     } else {
-      for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
+      block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; }, argmax + row, oi, ov);
     }
-  };
-  scan([&](float v, int i) {
-    if (better(v, i, mv, mi)) {
-      mv = v;
-      mi = i;
-    }
-  });
-  list_init(lv, li);
-  lv[0] = mv;
-  li[0] = mi;
-  const int kk = k;
-  block_merge(lv, li, kk, &dummy, thr_i, thr_v);
-  __syncthreads();
-  const float T = thr_v[kk - 1];
-  // pass 2: exact selection among the values >= T
-  list_init(lv, li);
-  scan([&](float v, int i) {
-    if (v >= T) list_insert(lv, li, v, i);
-  });
-  block_merge(lv, li, k, argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
-              topk_val ? topk_val + (size_t)row * k : nullptr);
-  __syncthreads();                     // thr_v / the merge scratch are reused by the next row
+    __syncthreads();                   // the shared scratch is reused by the next row
   }
 }
 
 // Merge of per-tile sorted candidate lists (each tile's list is its best k in order). With at
 // least k tiles, the k-th best of the tiles' first candidates is a lower bound T of the
 // row's k-th best value (those k tiles each hold a value >= T), so only candidates >= T can
-// be in the result: they are gathered in one parallel pass and selected exactly. (If more than MERGE_CAP candidates tie at or
-// above T, every candidate is scanned instead; with fewer than k tiles all are ranked.)
+// be in the result, and only tiles whose first candidate is >= T (about k of them) hold
+// any. T comes from warp-level selection rounds (no block barriers); the gathered
+// candidates are placed by rank: a candidate's output slot is the number of gathered
+// candidates that beat it (value desc, index asc: a strict order, so slots are distinct).
+// (With fewer than k tiles, more than MERGE_TILES tiles, or more than MERGE_CAP gathered
+// candidates, the block-wide selector ranks every candidate instead.)
 constexpr int MERGE_CAP = 1024;
+constexpr int MERGE_PER_THREAD = 8;
+constexpr int MERGE_TILES = MERGE_PER_THREAD * TK_THREADS;
 
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
                                                            const int2 *cand, int32_t *argmax,
@@ -215,67 +249,115 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
   pdl_trigger();
   __shared__ int2 pool[MERGE_CAP];
   __shared__ int n_pool;
-  __shared__ float thr_val[32];
-  __shared__ int thr_idx[32];
-  __shared__ int dummy;
+  __shared__ float warp_best[TK_THREADS / 32][TK];
+  __shared__ float thr;
   const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto at = [&](int t, int j) { return cand[((size_t)t * rows + row) * k + j]; };
-  if (tiles < k) {
-    // the bound below needs k tiles; with fewer there are at most k*k candidates: rank all
+  int32_t *oi = topk_idx ? topk_idx + (size_t)row * k : nullptr;
+  float *ov = topk_val ? topk_val + (size_t)row * k : nullptr;
+  auto rank_all = [&]() {
     block_topk(tiles * k, k,
                [&](int i, float &v, int &id) {
                  const int2 c = at(i / k, i % k);
                  v = __int_as_float(c.x);
                  id = c.y;
                },
-               argmax + row, topk_idx ? topk_idx + (size_t)row * k : nullptr,
-               topk_val ? topk_val + (size_t)row * k : nullptr);
+               argmax + row, oi, ov);
+  };
+  if (tiles < k || tiles > MERGE_TILES) {
+    rank_all();
     return;
   }
-  // 1) lower bound: k-th best of the tiles' first candidates
-  const int kk = k;
-  block_topk(tiles, kk,
-             [&](int i, float &v, int &id) {
-               const int2 c = at(i, 0);
-               v = __int_as_float(c.x);
-               id = c.y;
-             },
-             &dummy, thr_idx, thr_val);
+  // 1) this thread's tiles' first values; per warp the k best of them by argmax rounds
+  float first[MERGE_PER_THREAD];
+#pragma unroll
+  for (int j = 0; j < MERGE_PER_THREAD; ++j) {
+    const int t = threadIdx.x + j * TK_THREADS;
+    first[j] = t < tiles ? __int_as_float(at(t, 0).x) : -INFINITY;
+  }
+  {
+    float rest[MERGE_PER_THREAD];
+#pragma unroll
+    for (int j = 0; j < MERGE_PER_THREAD; ++j) rest[j] = first[j];
+    for (int r = 0; r < k; ++r) {
+      float bv = rest[0];
+      int bj = 0;
+#pragma unroll
+      for (int j = 1; j < MERGE_PER_THREAD; ++j)
+        if (rest[j] > bv) {
+          bv = rest[j];
+          bj = j;
+        }
+      float wv = bv;
+      int wl = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov2 = __shfl_xor_sync(0xffffffffu, wv, o);
+        const int ol = __shfl_xor_sync(0xffffffffu, wl, o);
+        if (ov2 > wv || (ov2 == wv && ol < wl)) {
+          wv = ov2;
+          wl = ol;
+        }
+      }
+      if (lane == wl) {
+#pragma unroll
+        for (int j = 0; j < MERGE_PER_THREAD; ++j)
+          if (j == bj) rest[j] = -INFINITY;
+      }
+      if (lane == 0) warp_best[warp][r] = wv;
+    }
+  }
   if (threadIdx.x == 0) n_pool = 0;
   __syncthreads();
-  const float T = thr_val[kk - 1];
-  // 2) gather every candidate >= T. A tile's list is sorted, so only tiles whose first
-  // candidate is >= T (about k of them) can hold one.
-  for (int t = threadIdx.x; t < tiles; t += TK_THREADS) {
-    if (__int_as_float(at(t, 0).x) < T) continue;
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int2 c = at(t, j);
-      if (__int_as_float(c.x) >= T) {
-        const int slot = atomicAdd(&n_pool, 1);
-        if (slot < MERGE_CAP) pool[slot] = c;
-      }
+  // 2) T = the k-th best of the warps' k best values (the k-th best tile first overall)
+  const int nw = (TK_THREADS / 32) * k;
+  if (threadIdx.x < nw) {
+    const float v = warp_best[threadIdx.x / k][threadIdx.x % k];
+    int above = 0, tie_before = 0;
+    for (int i = 0; i < nw; ++i) {
+      const float u = warp_best[i / k][i % k];
+      above += u > v;
+      tie_before += (u == v) & (i < (int)threadIdx.x);
+    }
+    if (above + tie_before == k - 1) thr = v;
+  }
+  __syncthreads();
+  const float T = thr;
+  // 3) gather the candidates >= T of the tiles whose first is >= T
+#pragma unroll
+  for (int j = 0; j < MERGE_PER_THREAD; ++j) {
+    const int t = threadIdx.x + j * TK_THREADS;
+    if (t >= tiles || first[j] < T) continue;
+    for (int q = 0; q < k; ++q) {
+      const int2 c = at(t, q);
+      if (__int_as_float(c.x) < T) break;            // the tile's list is sorted
+      const int slot = atomicAdd(&n_pool, 1);
+      if (slot < MERGE_CAP) pool[slot] = c;
     }
   }
   __syncthreads();
   const int np = n_pool;
-  int32_t *oi = topk_idx ? topk_idx + (size_t)row * k : nullptr;
-  float *ov = topk_val ? topk_val + (size_t)row * k : nullptr;
-  if (np <= MERGE_CAP) {
-    block_topk(np, k,
-               [&](int i, float &v, int &id) {
-                 v = __int_as_float(pool[i].x);
-                 id = pool[i].y;
-               },
-               argmax + row, oi, ov);
-  } else {
-    block_topk(tiles * k, k,
-               [&](int i, float &v, int &id) {
-                 const int2 c = at(i / k, i % k);
-                 v = __int_as_float(c.x);
-                 id = c.y;
-               },
-               argmax + row, oi, ov);
+  if (np > MERGE_CAP) {
+    rank_all();
+    return;
+  }
+  // 4) place by rank
+  for (int i = threadIdx.x; i < np; i += TK_THREADS) {
+    const int2 c = pool[i];
+    const float v = __int_as_float(c.x);
+    int rank = 0;
+    for (int j = 0; j < np; ++j) {
+      const int2 d = pool[j];
+      rank += better(__int_as_float(d.x), d.y, v, c.y);
+    }
+    if (rank < k) {
+      if (rank == 0) argmax[row] = c.y;
+      if (oi) {
+        oi[rank] = c.y;
+        ov[rank] = v;
+      }
+    }
   }
 }
 
