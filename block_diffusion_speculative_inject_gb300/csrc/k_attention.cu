@@ -24,8 +24,8 @@ __global__ void __launch_bounds__(256) k_attn_split(
     const int32_t *ctx_len, const int32_t *n_split, const int32_t *split_len,
     const int32_t *page_off, const int32_t *pages, int max_split, float scale, float *part_o,
     float *part_ml) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   extern __shared__ float sm[];
   float *qs = sm;                              // [R][HD]
   float *ks = qs + AT_MAXR * HD;               // [KT][HD+1]
@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
                                                                const float *part_o,
                                                                const float *part_ml, const float *qkv,
                                                                float scale_log2, OpOut o) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   constexpr int DPL = HD / 32;
   constexpr int KP = HD + 1;                       // padded row: lane-per-key reads are conflict free
   __shared__ float ks[32 * KP];

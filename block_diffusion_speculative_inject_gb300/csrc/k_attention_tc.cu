@@ -76,7 +76,10 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   pdl_trigger();
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int ns = p.n_split[b];                           // descriptor: staged before the chain
-  if (s >= ns) return;                                   // uniform for the CTA
+  if (s >= ns) {                                         // uniform for the CTA
+    pdl_wait();        // this grid must not complete before its predecessor has
+    return;
+  }
   const int n_ctx = p.ctx_len[b];
   const int k_begin = s * p.split_len[b];
   const int k_end = min(k_begin + p.split_len[b], n_ctx);

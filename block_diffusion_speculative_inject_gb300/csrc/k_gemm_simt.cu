@@ -21,8 +21,8 @@ __device__ __forceinline__ float load_x(const GemmDesc &d, int s, size_t idx) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ float xs[SB_K][SB_M + 1];
   __shared__ float ws[SB_K][SB_N + 1];
   const int m0 = blockIdx.y * SB_M, n0 = blockIdx.x * SB_N;

@@ -62,8 +62,8 @@ template <typename TW>
 __global__ void k_post_qkv(int M, int S, const float *ws, int Q, int nq, int nkv, int hd,
                            float *qkv, const int32_t *ctx_len, const float2 *rope, const TW *q_norm,
                            const TW *k_norm, float eps) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const int heads = nq + 2 * nkv;
@@ -111,8 +111,8 @@ template <typename TW>
 __global__ void __launch_bounds__(PN_THREADS) k_post_norm(int M, int S, const float *ws, int H,
                                                           float *x, OpOut out, const TW *w,
                                                           float eps, int out_skip_k) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ float red[PN_THREADS / 32];
   const int m = blockIdx.x;
   const int n4 = H / 4;
@@ -185,8 +185,8 @@ cudaError_t launch_post_norm(int dtype, int M, int H, const float *ws, int S, fl
 
 // ------------------------------------------------------------------------- SwiGLU
 __global__ void k_post_swiglu(int M, int S, const float *ws, int I, OpOut h) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)M * I) return;
   const int m = (int)(i / I), c = (int)(i % I);
@@ -207,8 +207,8 @@ template <typename T>
 __global__ void k_post_kv(int Trows, int S, const float *ws, int L, int nkv, int hd,
                           const int32_t *slot, const int32_t *pos, const float2 *rope, KNorms kn,
                           int qk_norm, float eps, T *pool) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (w >= Trows * L * nkv) return;
@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, 
                                                            int mask_id, float scale, const TW *embed,
                                                            float *x, OpOut out, const TW *w, float eps,
                                                            int *err) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ float red[PN_THREADS / 32];
   const int r = blockIdx.x, b = r / Q, j = r % Q;
   int tok = j == 0 ? anchors[b] : mask_id;

@@ -11,8 +11,8 @@ constexpr int PAGE = KV_PAGE;
 // ("DFlash 2 块扩散投机解码技术详解" §2.3; at most K+1 tokens: "DFlash：把串行 Draft 变成并行“填空”" §2).
 __global__ void k_verify(int n, int K, const int32_t *draft, const int32_t *target,
                          int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= n) return;
   const int32_t *d = draft + (size_t)b * K;
@@ -37,8 +37,8 @@ cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *tar
 template <typename T>
 __global__ void k_export_kv(int L, int nkv, int hd, int layer, int pos0, int n,
                             const int32_t *pages, const T *pool, T *k_out, T *v_out) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   long total = (long)n * nkv * hd;
   if (i >= total) return;

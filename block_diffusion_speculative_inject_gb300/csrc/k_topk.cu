@@ -142,8 +142,8 @@ constexpr int ROWS_CAP = 2048;
 __global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ float tmax[TK_THREADS];
   __shared__ int2 pool[ROWS_CAP];
   __shared__ int n_pool;
@@ -245,8 +245,8 @@ constexpr int MERGE_TILES = MERGE_PER_THREAD * TK_THREADS;
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
                                                            const int2 *cand, int32_t *argmax,
                                                            int32_t *topk_idx, float *topk_val) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ int2 pool[MERGE_CAP];
   __shared__ int n_pool;
   __shared__ float warp_best[TK_THREADS / 32][TK];
@@ -391,8 +391,8 @@ static __device__ __align__(256) int2 g_topk_scratch[NA_MAX_CAND];
 
 __global__ void __launch_bounds__(TK_THREADS) k_topk_chunks(int V, int k, int chunks, int rows,
                                                             const float *logits, int2 *cand) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  pdl_trigger();
   __shared__ int32_t idx[32];
   __shared__ float val[32];
   __shared__ int32_t first;
