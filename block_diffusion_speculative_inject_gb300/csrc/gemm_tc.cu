@@ -129,6 +129,10 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       tma_load_2d(st, wm, k, wrow, fb);
       if (glu) tma_load_2d(st + 64 * 128, &p.wmap[1], k, wrow, fb);
     };
+    // the activation maps are first used after the dependency wait: fetch them now
+    tma_prefetch_map(wm);
+    if (glu) tma_prefetch_map(&p.wmap[1]);
+    for (int i = 0; i < (p.split ? 2 : p.n_xseg); ++i) tma_prefetch_map(&p.xmap[i]);
     // the first stages' weight tiles do not depend on the previous kernel: start streaming
     // them before waiting for it
     const int pre = min(stages, nkb);

@@ -124,8 +124,9 @@ __global__ void __launch_bounds__(256) k_attn_split(
 //   o = (sum_s acc_s 2^(m_s - M) + sum_kk 2^(s_kk - M) v_kk) / (sum_s l_s 2^(m_s - M) + sum_kk 2^(s_kk - M))
 // The order of every sum is fixed.
 constexpr int CB_ROWS = 8;
+constexpr int CB_MAX_SPLIT = 16;   // the host plans at most this many context splits
 
-template <int HD>
+template <int HD, int MS>   // MS >= the batch's largest split count
 __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, int Q,
                                                                const int32_t *n_split, int max_split,
                                                                const float *part_o,
@@ -170,19 +171,27 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
   const int r = blockIdx.z * CB_ROWS + warp;
   const int g = r / Q, j = r % Q, h = kvh * G + g;
   const size_t row = (size_t)b * Q + j;
+  const int ns = n_split[b];
+  const size_t base = (row * nq + h) * max_split;
+  // every load of this row (its q, the splits' (m, l) and partial outputs) is issued before
+  // any of them is used: one round trip instead of one per split
+  float ms = -INFINITY, ls = 0.f;
+  float po[MS][DPL];
   if (r < R) {
 #pragma unroll
     for (int d = 0; d < DPL; ++d) qs[warp][lane + 32 * d] = qkv[row * qkv_dim + (size_t)h * HD + lane + 32 * d];
+    if (lane < ns) {
+      ms = part_ml[(base + lane) * 2];
+      ls = part_ml[(base + lane) * 2 + 1];
+    }
+#pragma unroll
+    for (int sp = 0; sp < MS; ++sp)
+#pragma unroll
+      for (int d = 0; d < DPL; ++d)
+        po[sp][d] = sp < ns ? part_o[(base + sp) * HD + lane + 32 * d] : 0.f;
   }
   __syncthreads();
   if (r >= R) return;
-  const int ns = n_split[b];
-  const size_t base = (row * nq + h) * max_split;
-  float ms = -INFINITY, ls = 0.f;
-  if (lane < ns) {
-    ms = part_ml[(base + lane) * 2];
-    ls = part_ml[(base + lane) * 2 + 1];
-  }
   float sk = -INFINITY;
   if (lane < Q) {
     float t = 0.f;
@@ -195,11 +204,11 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
   const float cs = lane < ns ? exp2f(ms - M) : 0.f;
   const float Lsum = warp_sum(pk + cs * ls);
   float acc[DPL] = {};
-#pragma unroll 4
-  for (int sp = 0; sp < ns; ++sp) {
-    const float c = __shfl_sync(0xffffffffu, cs, sp);
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(c, part_o[(base + sp) * HD + lane + 32 * d], acc[d]);
+  for (int sp = 0; sp < MS; ++sp) {
+    const float c = __shfl_sync(0xffffffffu, cs, sp);     // 0 for sp >= ns
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(c, po[sp][d], acc[d]);
   }
   for (int kk = 0; kk < Q; ++kk) {
     const float p = __shfl_sync(0xffffffffu, pk, kk);
@@ -217,6 +226,7 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
                              const void *pool, float *part_o, float *part_ml, OpOut o,
                              const AttnMaps *maps, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  if (bt.max_split > CB_MAX_SPLIT) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   if (bt.max_split > 0) {
     if (maps && maps->valid && HD == 128 && sizeof(T) == 2) {
@@ -235,8 +245,15 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
   }
   const int R = (m.nq / m.nkv) * m.Q();
   dim3 g2(m.nkv, bt.B, (R + CB_ROWS - 1) / CB_ROWS);
-  return launch_pdl(k_attn_combine<HD>, g2, dim3(32 * CB_ROWS), 0, s, m.nq, m.nkv, m.Q(), bt.n_split,
-                    bt.max_split, (const float *)part_o, (const float *)part_ml, qkv, scale_log2, o);
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, g2, dim3(32 * CB_ROWS), 0, s, m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split,
+                      (const float *)part_o, (const float *)part_ml, qkv, scale_log2, o);
+  };
+  // register room for the partial outputs follows the largest split count
+  if (bt.max_split <= 2) return go(k_attn_combine<HD, 2>);
+  if (bt.max_split <= 4) return go(k_attn_combine<HD, 4>);
+  if (bt.max_split <= 8) return go(k_attn_combine<HD, 8>);
+  return go(k_attn_combine<HD, CB_MAX_SPLIT>);
 }
 
 cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &bt, int layer,

@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer. The pages were written by earlier kernels of the stream
     // (context injection), which a programmatic launch does not order before this point.
+    tma_prefetch_map(&p.kmap);
+    tma_prefetch_map(&p.vmap);
     pdl_wait();
     int issued = 0;
     for (int i = 0; i < n_tiles; ++i) {

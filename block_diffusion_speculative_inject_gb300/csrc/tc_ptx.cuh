@@ -62,6 +62,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(mbar)
       : "memory");
 }
+// Fetch a tensor map (kernel parameter) into the TMA unit's cache ahead of its first use.
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
