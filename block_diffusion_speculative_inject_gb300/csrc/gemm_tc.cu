@@ -73,6 +73,84 @@ constexpr int tmem_cols() {
   return BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
 }
 
+// One warp: the best k of a tile column held as 4 values per lane (value desc, lower index
+// first), by k rounds of warp arg-max; lane 0 writes (value bits, index) pairs to out.
+__device__ __forceinline__ void warp_tile_topk(float (&v)[4], int (&id)[4], int k, int lane, int2 *out) {
+  for (int rr = 0; rr < k; ++rr) {
+    float bv = v[0];
+    int bi = id[0];
+#pragma unroll
+    for (int j = 1; j < 4; ++j)
+      if (v[j] > bv || (v[j] == bv && id[j] < bi)) {
+        bv = v[j];
+        bi = id[j];
+      }
+    float wv = bv;
+    int wi = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (ov > wv || (ov == wv && oi < wi)) {
+        wv = ov;
+        wi = oi;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (id[j] == wi) {      // the winner leaves the race
+        v[j] = -INFINITY;
+        id[j] = 0x7fffffff;
+      }
+    if (lane == 0) out[rr] = make_int2(__float_as_int(wv), wi);
+  }
+}
+
+// The same for T token columns at once (column t: v[t], id[t]); the T arg-max chains of a
+// round are independent, so their shuffle latencies overlap. Columns with out[t] == nullptr
+// are skipped.
+template <int T>
+__device__ __forceinline__ void warp_tile_topk_multi(float (&v)[T][4], int (&id)[T][4], int k, int lane,
+                                                     int2 *const (&out)[T]) {
+  for (int rr = 0; rr < k; ++rr) {
+    float wv[T];
+    int wi[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      wv[t] = v[t][0];
+      wi[t] = id[t][0];
+#pragma unroll
+      for (int j = 1; j < 4; ++j)
+        if (v[t][j] > wv[t] || (v[t][j] == wv[t] && id[t][j] < wi[t])) {
+          wv[t] = v[t][j];
+          wi[t] = id[t][j];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const float ov = __shfl_xor_sync(0xffffffffu, wv[t], o);
+        const int oi = __shfl_xor_sync(0xffffffffu, wi[t], o);
+        if (ov > wv[t] || (ov == wv[t] && oi < wi[t])) {
+          wv[t] = ov;
+          wi[t] = oi;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (id[t][j] == wi[t]) {      // the winner leaves the race
+          v[t][j] = -INFINITY;
+          id[t][j] = 0x7fffffff;
+        }
+      if (lane == 0 && out[t]) out[t][rr] = make_int2(__float_as_int(wv[t]), wi[t]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------- the kernel
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant__ TcParams p) {
@@ -117,6 +195,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (!(warp == 0 && lane == 0 && nkb > 0)) pdl_wait();   // the producer waits after its prefetch
+  float2 qk_cs[4][2] = {};               // EPI_QKV epilogue warps: RoPE rows, loaded early
 
   if (warp == 0 && lane == 0 && nkb > 0) {
     // ---------------- TMA producer
@@ -195,6 +274,19 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int q = warp & 3;               // TMEM lane quarter this warp may access
+    if (p.epi == EPI_QKV && n0 < p.q_dim + p.kv_dim) {
+      // RoPE (cos, sin) of the first tokens this warp finishes, fetched while the MMAs run
+      const int rank = (int)cluster_ctarank();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = rank + p.S * (warp - 2) + 4 * p.S * u, m = m0 + c;
+        if (c < BN && m < p.M) {
+          const int pos = __ldg(p.ctx_len + m / p.rows_per_req) + m % p.rows_per_req;
+          qk_cs[u][0] = __ldg(p.rope + (size_t)pos * 64 + lane);
+          qk_cs[u][1] = __ldg(p.rope + (size_t)pos * 64 + lane + 32);
+        }
+      }
+    }
     const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
     tc_fence_after();
     const int n = n0 + q * 32 + lane;
@@ -206,7 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       uint32_t r[16];
       tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
       tmem_ld_wait();
-      if (p.epi == EPI_TOPK) {
+      if (p.epi == EPI_TOPK && p.S == 1) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c0 + j;
@@ -234,47 +326,42 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         p.y[o] = p.epi == EPI_RESID ? p.resid[o] + v : v;
       }
     }
-    if (p.epi == EPI_TOPK) {
+    if (p.epi == EPI_TOPK && p.S == 1) {
       // per token: the tile's best topk (value desc, lower index first) by warp arg-max rounds
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      for (int c = warp - 2; c < BN; c += 4) {
-        const int m = m0 + c;
-        if (m >= p.M || !ok) continue;
-        float v[4];
-        int id[4];
+      if constexpr (BN <= 32) {
+        // this warp's token columns (c = warp - 2 + 4 t), four at a time in interleaved passes
+        constexpr int T = 4;
+#pragma unroll 1
+        for (int t0 = 0; 4 * t0 < BN; t0 += T) {
+          float v[T][4];
+          int id[T][4];
+          int2 *out[T];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[j] = tile[c * TP + lane + 32 * j];
-          id[j] = n0 + lane + 32 * j;
-        }
-        int2 *out = p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk;
-        for (int rr = 0; rr < p.topk; ++rr) {
-          float bv = v[0];
-          int bi = id[0];
+          for (int t = 0; t < T; ++t) {
+            const int c = warp - 2 + 4 * (t0 + t), m = m0 + c;
+            const bool live = ok && c < BN && m < p.M;
+            out[t] = live ? p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk : nullptr;
 #pragma unroll
-          for (int j = 1; j < 4; ++j)
-            if (v[j] > bv || (v[j] == bv && id[j] < bi)) {
-              bv = v[j];
-              bi = id[j];
-            }
-          float wv = bv;
-          int wi = bi;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-            if (ov > wv || (ov == wv && oi < wi)) {
-              wv = ov;
-              wi = oi;
+            for (int j = 0; j < 4; ++j) {
+              v[t][j] = live ? tile[c * TP + lane + 32 * j] : -INFINITY;
+              id[t][j] = n0 + lane + 32 * j;
             }
           }
+          warp_tile_topk_multi<T>(v, id, p.topk, lane, out);
+        }
+      } else {
+        for (int c = warp - 2; c < BN; c += 4) {
+          const int m = m0 + c;
+          if (m >= p.M || !ok) continue;
+          float v[4];
+          int id[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (id[j] == wi) {      // the winner leaves the race
-              v[j] = -INFINITY;
-              id[j] = 0x7fffffff;
-            }
-          if (lane == 0) out[rr] = make_int2(__float_as_int(wv), wi);
+          for (int j = 0; j < 4; ++j) {
+            v[j] = tile[c * TP + lane + 32 * j];
+            id[j] = n0 + lane + 32 * j;
+          }
+          warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk);
         }
       }
     }
@@ -319,10 +406,15 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             }
           }
           if (p.epi == EPI_QKV && part < 2) {
-            const int m = mu[u];
-            const int pos = __ldg(p.ctx_len + m / p.rows_per_req) + m % p.rows_per_req;
-            cs[u][0] = __ldg(p.rope + (size_t)pos * 64 + lane);
-            cs[u][1] = __ldg(p.rope + (size_t)pos * 64 + lane + 32);
+            if (cb == rank + p.S * (warp - 2)) {
+              cs[u][0] = qk_cs[u][0];
+              cs[u][1] = qk_cs[u][1];
+            } else {
+              const int m = mu[u];
+              const int pos = __ldg(p.ctx_len + m / p.rows_per_req) + m % p.rows_per_req;
+              cs[u][0] = __ldg(p.rope + (size_t)pos * 64 + lane);
+              cs[u][1] = __ldg(p.rope + (size_t)pos * 64 + lane + 32);
+            }
           }
         }
 #pragma unroll
@@ -330,6 +422,20 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           const int m = mu[u];
           if (m < 0) continue;
           float *x = a[u];
+          if (p.epi == EPI_TOPK) {
+            // split-K LM head: the reduced column's best topk of this tile
+            float v[4];
+            int id[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = n0 + lane + 32 * j;
+              v[j] = n < p.N ? x[j] : -INFINITY;
+              id[j] = n;
+              if (n < p.N && p.y) p.y[(size_t)m * p.ldy + n] = x[j];
+            }
+            warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk);
+            continue;
+          }
           if (p.epi == EPI_SWIGLU) {
             // rows lane, lane + 32 are gate; lane + 64, lane + 96 the matching up rows
             const size_t o = (size_t)m * p.ldo + (size_t)blockIdx.y * 64 + lane;
@@ -466,7 +572,8 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   const int base = p.t_tiles * p.n_tiles;
   const int s_max = std::max(1, std::min(8, p.kb / 4));    // a portable cluster holds 8 CTAs
   int S = std::max(1, std::min((per_sm * t->num_sms) / base, s_max));
-  if (d.epi == EPI_TOPK) S = 1;          // the top-k epilogue needs whole sums
+  // the top-k epilogue ranks whole sums: split K only through the cluster reduction
+  if (d.epi == EPI_TOPK) S = std::min(S, s_max);
   p.kb_per = (p.kb + S - 1) / S;
   p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
   return p;
