@@ -38,6 +38,12 @@ Readings where the pages leave a step open (each is also listed in the design no
     fp32 (or an exact bf16 hi+lo pair as a tensor-core operand) on the GPU. Argmax and
     top-k are decided on the logits rounded to fp32, ties to the lowest index.
   * top-k: k values sorted descending, indices tie-broken by lowest index.
+  * Sampling mode ([P2] §2.3, §3.3, §4.2): both the draft and the target distribution go
+    through the same truncation — logits / temperature, keep the top_k largest (ties to
+    the lower index), softmax over those, then keep the shortest prefix of them in
+    descending order whose mass reaches top_p, renormalised. Draws are inverse-CDF over
+    the vocabulary in index order with caller-supplied uniforms; the drafted tokens are
+    inputs (drawn from q by the caller).
 
 Parity status: every function here is pinned by the CPU tests (brute force, closed
 forms, library routines or exact rational arithmetic) — see tests/test_oracle_pins.py.
@@ -50,6 +56,7 @@ __all__ = [
     "round_to", "bf16_round", "f32_round", "rmsnorm", "rope", "silu", "softmax",
     "OracleDraft", "topk_desc", "argmax_lowest", "verify_greedy",
     "accept_prob", "residual_dist", "sample_index", "verify_sample", "as_fraction_dist",
+    "sampling_probs", "sample_token", "verify_sample_logits",
 ]
 
 
@@ -360,3 +367,47 @@ def as_fraction_dist(values):
     """Helper for exact tests: normalise a sequence of positive ints to Fractions."""
     total = sum(values)
     return [Fraction(v, total) for v in values]
+
+
+# ----------------------------------------------------------------------------- sampling mode
+def sampling_probs(logits, temperature, top_k, top_p):
+    """Truncated sampling distribution of one row of logits ([P2] §3.3: the same top-k /
+    top-p truncation applied to the draft and the target).
+
+    temperature > 0; top_k in [1, V] (V keeps every token); 0 < top_p <= 1. Returns a
+    length-V float64 vector: zero outside the kept set, summing to one.
+    """
+    z = np.asarray(logits, dtype=np.float64) / float(temperature)
+    V = z.shape[0]
+    k = min(int(top_k), V)
+    # descending by value, ties to the lower index (a stable sort of -z)
+    order = np.argsort(-z, kind="stable")
+    kept = order[:k]
+    e = np.exp(z[kept] - z[kept[0]])
+    p = e / e.sum()
+    if top_p < 1.0:
+        mass = 0.0
+        n = 0
+        for n in range(1, k + 1):
+            mass += p[n - 1]
+            if mass >= top_p:
+                break
+        kept = kept[:n]
+        p = p[:n] / p[:n].sum()
+    out = np.zeros(V, dtype=np.float64)
+    out[kept] = p
+    return out
+
+
+def sample_token(logits, u, temperature, top_k, top_p):
+    """One draw from sampling_probs(...) with the uniform u (inverse CDF, index order)."""
+    return sample_index(list(sampling_probs(logits, temperature, top_k, top_p)), u)
+
+
+def verify_sample_logits(target_logits, draft_logits, draft, u_accept, u_resample,
+                         temperature, top_k, top_p):
+    """verify_sample on the truncated distributions of the target's K+1 rows and the
+    draft's K rows (sampling mode of [P2] §2.3)."""
+    p_rows = [sampling_probs(r, temperature, top_k, top_p) for r in target_logits]
+    q_rows = [sampling_probs(r, temperature, top_k, top_p) for r in draft_logits]
+    return verify_sample(p_rows, q_rows, draft, u_accept, u_resample)

@@ -475,3 +475,91 @@ def test_cache_is_stored_in_the_storage_type_and_activations_are_not(dtype, rnd)
         np.testing.assert_array_equal(rnd(od.cache[0]["V"][l]), od.cache[0]["V"][l])
     g = od.fuse(fe)
     assert np.any(O.bf16_round(g) != g) and np.any(O.f32_round(g) != g)
+
+
+# ----------------------------------------------------------------------------- sampling mode
+def test_sampling_probs_without_truncation_is_the_tempered_softmax():
+    """top_k = V and top_p = 1 leave softmax(logits / T) (torch's routine) untouched."""
+    rng = np.random.default_rng(41)
+    for T in (0.5, 1.0, 1.7):
+        lg = rng.normal(0, 2, 97)
+        ref = torch.softmax(torch.tensor(lg, dtype=torch.float64) / T, 0).numpy()
+        np.testing.assert_allclose(O.sampling_probs(lg, T, 97, 1.0), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_sampling_probs_top_k_is_the_softmax_of_the_k_largest():
+    """top-k keeps torch.topk's set (distinct logits) and renormalises over it."""
+    rng = np.random.default_rng(42)
+    lg = rng.permutation(np.linspace(-3, 3, 64))
+    for k in (1, 5, 20):
+        vals, idx = torch.topk(torch.tensor(lg, dtype=torch.float64), k)
+        ref = np.zeros(64)
+        ref[idx.numpy()] = torch.softmax(vals / 0.8, 0).numpy()
+        np.testing.assert_allclose(O.sampling_probs(lg, 0.8, k, 1.0), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_sampling_probs_top_p_closed_form():
+    """logits (2, 1, 0, -1), T = 1, top_p = 0.8: softmax mass 0.644 < 0.8 <= 0.881 after two
+    tokens, so two survive with probabilities sigmoid(1) and 1 - sigmoid(1)."""
+    p = O.sampling_probs(np.array([2.0, 1.0, 0.0, -1.0]), 1.0, 4, 0.8)
+    s = 1.0 / (1.0 + np.exp(-1.0))
+    np.testing.assert_allclose(p, [s, 1.0 - s, 0.0, 0.0], rtol=1e-14)
+
+
+def test_sampling_probs_top_p_keeps_the_shortest_sufficient_prefix():
+    """The kept set is a prefix of the descending order whose softmax mass reaches top_p,
+    and dropping its last token falls short (minimality), after top-k truncation."""
+    rng = np.random.default_rng(43)
+    for trial in range(50):
+        V = int(rng.integers(5, 60))
+        lg = rng.normal(0, 1.5, V)
+        k = int(rng.integers(1, V + 1))
+        top_p = float(rng.uniform(0.05, 0.99))
+        T = float(rng.uniform(0.3, 2.0))
+        p = O.sampling_probs(lg, T, k, top_p)
+        kept = np.flatnonzero(p)
+        order = np.argsort(-lg, kind="stable")[:k]
+        full = np.exp(lg[order] / T - np.max(lg[order] / T))
+        full /= full.sum()
+        n = len(kept)
+        assert set(kept) == set(order[:n])
+        assert full[:n].sum() >= top_p - 1e-12
+        if n > 1:
+            assert full[:n - 1].sum() < top_p
+        np.testing.assert_allclose(p.sum(), 1.0, rtol=1e-12)
+
+
+def test_sampling_probs_temperature_scaling_and_ties():
+    """Temperature T equals dividing the logits by T first; a tie at the top-k boundary
+    keeps the lower vocabulary index."""
+    lg = np.array([0.5, 2.0, -1.0, 2.0, 1.0])
+    np.testing.assert_allclose(O.sampling_probs(lg, 0.25, 3, 0.9), O.sampling_probs(lg * 4, 1.0, 3, 0.9))
+    p = O.sampling_probs(np.array([1.0, 3.0, 2.0, 2.0]), 1.0, 2, 1.0)
+    assert p[2] > 0 and p[3] == 0
+
+
+def test_sample_token_inverse_cdf_steps():
+    """Draws follow the cumulative distribution in index order."""
+    lg = np.log(np.array([0.1, 0.2, 0.3, 0.4]))
+    assert O.sample_token(lg, 0.05, 1.0, 4, 1.0) == 0
+    assert O.sample_token(lg, 0.15, 1.0, 4, 1.0) == 1
+    assert O.sample_token(lg, 0.59, 1.0, 4, 1.0) == 2
+    assert O.sample_token(lg, 0.61, 1.0, 4, 1.0) == 3
+
+
+def test_verify_sample_logits_first_token_follows_truncated_target():
+    """With drafts drawn from the truncated draft distribution, the first emitted token
+    of the sampling verify follows the truncated target distribution (Monte Carlo)."""
+    rng = np.random.default_rng(44)
+    V, K, T, k, tp = 12, 2, 0.9, 6, 0.9
+    tl = rng.normal(0, 1.2, (K + 1, V))
+    dl = rng.normal(0, 1.2, (K, V))
+    p0 = O.sampling_probs(tl[0], T, k, tp)
+    n = 20000
+    counts = np.zeros(V)
+    for _ in range(n):
+        d = [O.sample_token(dl[j], rng.random(), T, k, tp) for j in range(K)]
+        a, toks = O.verify_sample_logits(tl, dl, d, rng.random(K), rng.random(), T, k, tp)
+        assert 1 <= len(toks) == a + 1 <= K + 1
+        counts[toks[0]] += 1
+    assert np.all(np.abs(counts / n - p0) < 5 * np.sqrt(p0 * (1 - p0) / n) + 1e-3)
