@@ -163,6 +163,34 @@ class Context:
         self._check(st)
         return accept_len, out_tokens, next_anchor
 
+    def sample_tokens(self, logits, u, temperature, top_k, top_p, tokens=None, stream=None):
+        """One draw per row of fp32 logits [rows, V] from the truncated distribution."""
+        rows = logits.shape[0]
+        if tokens is None:
+            tokens = torch.empty((rows,), dtype=torch.int32, device=logits.device)
+        sp = _ffi.Sampling(float(temperature), int(top_k), float(top_p))
+        st = self.lib.dflash_sample_tokens(self.h, _stream_ptr(stream), rows, ctypes.byref(sp),
+                                           _ptr(logits), _ptr(u), _ptr(tokens))
+        self._check(st)
+        return tokens
+
+    def verify_sample(self, target_logits, draft_logits, draft, u_accept, u_resample, temperature,
+                      top_k, top_p, accept_len=None, out_tokens=None, next_anchor=None, stream=None):
+        """Rejection-sampling verification; returns (accept_len, out_tokens, next_anchor)."""
+        B, K = draft.shape
+        dev = draft.device
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+            out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+            next_anchor = torch.empty((B,), dtype=torch.int32, device=dev)
+        sp = _ffi.Sampling(float(temperature), int(top_k), float(top_p))
+        st = self.lib.dflash_verify_sample(self.h, _stream_ptr(stream), B, ctypes.byref(sp),
+                                           _ptr(target_logits), _ptr(draft_logits), _ptr(draft),
+                                           _ptr(u_accept), _ptr(u_resample), _ptr(accept_len),
+                                           _ptr(out_tokens), _ptr(next_anchor))
+        self._check(st)
+        return accept_len, out_tokens, next_anchor
+
     def release(self, req_id):
         self._check(self.lib.dflash_release(self.h, int(req_id)))
 
@@ -229,6 +257,17 @@ def dflash_draft_step(ctx: Context, req_ids, anchors, argmax, topk_idx=None, top
 
 def dflash_verify_greedy(ctx: Context, draft, target, accept_len, out_tokens, next_anchor, stream=None):
     return ctx.verify(draft, target, accept_len, out_tokens, next_anchor, stream=stream)
+
+
+def dflash_sample_tokens(ctx: Context, logits, u, temperature, top_k, top_p, tokens=None, stream=None):
+    return ctx.sample_tokens(logits, u, temperature, top_k, top_p, tokens, stream=stream)
+
+
+def dflash_verify_sample(ctx: Context, target_logits, draft_logits, draft, u_accept, u_resample,
+                         temperature, top_k, top_p, accept_len=None, out_tokens=None,
+                         next_anchor=None, stream=None):
+    return ctx.verify_sample(target_logits, draft_logits, draft, u_accept, u_resample, temperature,
+                             top_k, top_p, accept_len, out_tokens, next_anchor, stream=stream)
 
 
 def dflash_release(ctx: Context, req_id):

@@ -44,6 +44,8 @@ SIGNATURES = {
     "dflash_inject_context": (_I32, [_P, _P, _I32, _I32P, _I32P, _I32, ctypes.POINTER(_P)]),
     "dflash_draft_step": (_I32, [_P, _P, _I32, _I32P, _P, _P, _P, _P, _P]),
     "dflash_verify_greedy": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P]),
+    "dflash_sample_tokens": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
+    "dflash_verify_sample": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_release": (_I32, [_P, _I32]),
     "dflash_truncate": (_I32, [_P, _I32, _I32]),
     "dflash_context_len": (_I32, [_P, _I32, _I32P]),
@@ -59,6 +61,11 @@ SIGNATURES = {
     "dflash_timing_read": (_I32, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                   ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _I32]),
 }
+
+class Sampling(ctypes.Structure):
+    """dflash_sampling: temperature > 0, 1 <= top_k <= 32, 0 < top_p <= 1."""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
 
 _lib = None
 

@@ -41,11 +41,13 @@ int round_up(int a, int b) { return (a + b - 1) / b * b; }
 // Kernel classes of the timing records.
 enum KCls : int {
   K_GEMM_FC, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_LMHEAD,
-  K_ATTN, K_RMSNORM, K_ROPE, K_INJECT_KV, K_SWIGLU, K_EMBED, K_TOPK, K_VERIFY, K_EXPORT, K_NUM
+  K_ATTN, K_RMSNORM, K_ROPE, K_INJECT_KV, K_SWIGLU, K_EMBED, K_TOPK, K_VERIFY, K_EXPORT, K_SAMPLE,
+  K_NUM
 };
 const char *kClsName[K_NUM] = {"gemm_fc", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup",
                                "gemm_down", "gemm_lmhead", "attention", "rmsnorm", "qk_norm_rope",
-                               "inject_kv", "swiglu", "embed", "topk", "verify", "export_kv"};
+                               "inject_kv", "swiglu", "embed", "topk", "verify", "export_kv",
+                               "sample"};
 
 struct DraftGraph {
   long long key;
@@ -90,6 +92,9 @@ struct dflash_ctx {
   // injection scratch
   float *fc_out = nullptr, *kvproj = nullptr;
   void *g = nullptr;
+  // sampling mode: truncated distributions of a batch's target and draft rows
+  int32_t *smp_tok = nullptr, *smp_n = nullptr;
+  float *smp_p = nullptr;
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -357,7 +362,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 // ------------------------------------------------------------------------------ create / destroy
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
-                 c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj};
+                 c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -449,6 +454,9 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->fc_out, (size_t)C * m.H * f4},
       {&c->g, (size_t)C * m.H * f4},
       {(void **)&c->kvproj, (size_t)C * m.L * 2 * m.kv_dim() * f4},
+      {(void **)&c->smp_tok, (size_t)(R + RK) * SMP_K * sizeof(int32_t)},
+      {(void **)&c->smp_p, (size_t)(R + RK) * SMP_K * sizeof(float)},
+      {(void **)&c->smp_n, (size_t)(R + RK) * sizeof(int32_t)},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -1014,6 +1022,73 @@ extern "C" dflash_status dflash_verify_greedy(dflash_ctx *c, void *stream, int32
                 return launch_verify(n_req, c->m.K, draft, target, accept_len, out_tokens,
                                      next_anchor, (cudaStream_t)stream);
               }));
+  return DFLASH_OK;
+}
+
+static dflash_status check_sampling(dflash_ctx *c, const dflash_sampling *sp) {
+  if (!sp) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL sampling parameters");
+  if (sp->top_k == 0)
+    return set_err(c, DFLASH_ERR_UNSUPPORTED, "top_k = 0 (top-p over the whole vocabulary) is not supported");
+  if (!(sp->temperature > 0.f) || sp->top_k < 1 || sp->top_k > SMP_K || !(sp->top_p > 0.f) || sp->top_p > 1.f)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "need temperature > 0, 1 <= top_k <= %d, 0 < top_p <= 1", SMP_K);
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_sample_tokens(dflash_ctx *c, void *stream, int32_t rows,
+                                              const dflash_sampling *sp, const float *logits,
+                                              const float *u, int32_t *tokens) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if ((st = check_sampling(c, sp)) != DFLASH_OK) return st;
+  if (rows < 0) return set_err(c, DFLASH_ERR_INVALID_ARG, "rows < 0");
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !u || !tokens) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  const int V = c->m.V;
+  CK(c, timed(c, K_SAMPLE, (cudaStream_t)stream, 8.0 * rows * V, 4.0 * rows * V, 1, [&] {
+       return launch_trunc_dist(rows, V, sp->temperature, sp->top_k, sp->top_p, logits, u, tokens,
+                                nullptr, nullptr, nullptr, 2 * c->num_sms, (cudaStream_t)stream);
+     }));
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_verify_sample(dflash_ctx *c, void *stream, int32_t n_req,
+                                              const dflash_sampling *sp, const float *target_logits,
+                                              const float *draft_logits, const int32_t *draft,
+                                              const float *u_accept, const float *u_resample,
+                                              int32_t *accept_len, int32_t *out_tokens,
+                                              int32_t *next_anchor) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if ((st = check_sampling(c, sp)) != DFLASH_OK) return st;
+  if (n_req < 0 || n_req > c->cfg.max_batch)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req=%d outside [0, max_batch=%d]", n_req, c->cfg.max_batch);
+  if (n_req == 0) return DFLASH_OK;
+  if (!target_logits || !draft_logits || !draft || !u_accept || !u_resample || !accept_len || !out_tokens ||
+      !next_anchor)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int V = c->m.V, K = c->m.K, Q = c->m.Q();
+  const int tr = n_req * Q, dr = n_req * K;
+  int32_t *ptok = c->smp_tok, *qtok = c->smp_tok + (size_t)tr * SMP_K;
+  float *pp = c->smp_p, *qp = c->smp_p + (size_t)tr * SMP_K;
+  int32_t *pn = c->smp_n, *qn = c->smp_n + tr;
+  CK(c, timed(c, K_SAMPLE, s, 4.0 * (tr + dr) * V, 4.0 * (tr + dr) * V, 2, [&] {
+       cudaError_t e = launch_trunc_dist(tr, V, sp->temperature, sp->top_k, sp->top_p, target_logits,
+                                         nullptr, nullptr, ptok, pp, pn, 2 * c->num_sms, s);
+       if (e != cudaSuccess) return e;
+       return launch_trunc_dist(dr, V, sp->temperature, sp->top_k, sp->top_p, draft_logits, nullptr,
+                                nullptr, qtok, qp, qn, 2 * c->num_sms, s);
+     }));
+  CK(c, timed(c, K_VERIFY, s, 4.0 * n_req * (3 * K + 4), (double)n_req * K, 1, [&] {
+       return launch_verify_sample(n_req, K, ptok, pp, pn, qtok, qp, qn, draft, u_accept, u_resample,
+                                   accept_len, out_tokens, next_anchor, s);
+     }));
   return DFLASH_OK;
 }
 

@@ -131,14 +131,95 @@ __device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int 
   }
 }
 
+constexpr int ROWS_CAP = 2048;   // gathered candidates per row before falling back
+
+// The body of the row selection for one row x[V], run by the whole CTA; the shared scratch
+// (tmax, pool, n_pool, thr) is the caller's. Writes argmax_out[0] (if non-null) and the
+// sorted best k to idx_out / val_out (if non-null); they may point to shared memory.
+__device__ __forceinline__ void row_select(const float *x, int V, int k, float *tmax, int2 *pool,
+                                           int *n_pool, float *thr, int32_t *argmax_out,
+                                           int32_t *idx_out, float *val_out) {
+  const bool vec = (V & 3) == 0 && ((uintptr_t)x & 15u) == 0;
+  const int n4 = V / 4;
+  const float4 *x4 = (const float4 *)x;
+  auto scan = [&](auto &&visit) {
+    if (vec) {
+      for (int b = 0; b < n4; b += TK_THREADS * 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = b + threadIdx.x + j * TK_THREADS;
+          v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
+          if (i < V) {
+            visit(v[j].x, i);
+            visit(v[j].y, i + 1);
+            visit(v[j].z, i + 2);
+            visit(v[j].w, i + 3);
+          }
+        }
+      }
+    } else {
+      for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
+    }
+  };
+  // pass 1: per-thread maximum
+  float mv = -INFINITY;
+  scan([&](float v, int) { mv = fmaxf(mv, v); });
+  tmax[threadIdx.x] = mv;
+  if (threadIdx.x == 0) *n_pool = 0;
+  __syncthreads();
+  {
+    // stable rank of this thread's maximum among all; rank k - 1 is the bound
+    int rank = 0;
+    for (int j = 0; j < TK_THREADS; ++j) {
+      const float u = tmax[j];
+      rank += (u > mv) | ((u == mv) & (j < (int)threadIdx.x));
+    }
+    if (rank == k - 1) *thr = mv;
+  }
+  __syncthreads();
+  const float T = *thr;
+  // pass 2: gather the values >= T
+  scan([&](float v, int i) {
+    if (v >= T) {
+      const int slot = atomicAdd(n_pool, 1);
+      if (slot < ROWS_CAP) pool[slot] = make_int2(__float_as_int(v), i);
+    }
+  });
+  __syncthreads();
+  const int np = *n_pool;
+  if (np <= ROWS_CAP) {
+    for (int i = threadIdx.x; i < np; i += TK_THREADS) {
+      const int2 c = pool[i];
+      const float v = __int_as_float(c.x);
+      int rank = 0;
+      for (int j = 0; j < np; ++j) {
+        const int2 d = pool[j];
+        rank += better(__int_as_float(d.x), d.y, v, c.y);
+      }
+      if (rank < k) {
+        if (rank == 0 && argmax_out) *argmax_out = c.y;
+        if (idx_out) idx_out[rank] = c.y;
+        if (val_out) val_out[rank] = v;
+      }
+    }
+  } else {
+    int32_t dummy;
+    block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; },
+               argmax_out ? argmax_out : &dummy, idx_out, val_out);
+  }
+}
+
 // Two passes over the row: (1) every thread's maximum; the k-th best of those maxima is a
 // lower bound T of the row's k-th best value (k threads each hold a value >= T); (2) the
 // values >= T (a few more than k) are gathered in shared memory and placed by rank: a
 // value's output slot is the number of gathered values that beat it. If more than ROWS_CAP
 // values reach T (ties), the block-wide list selector ranks the row instead. CTA b takes
 // rows b, b + gridDim.x, ...
-constexpr int ROWS_CAP = 2048;
-
 __global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
                                                           float *topk_val) {
@@ -149,82 +230,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, in
   __shared__ int n_pool;
   __shared__ float thr;
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const float *x = logits + (size_t)row * V;
-    const bool vec = (V & 3) == 0;
-    const int n4 = V / 4;
-    const float4 *x4 = (const float4 *)x;
-    int32_t *oi = topk_idx ? topk_idx + (size_t)row * k : nullptr;
-    float *ov = topk_val ? topk_val + (size_t)row * k : nullptr;
-    auto scan = [&](auto &&visit) {
-      if (vec) {
-        for (int b = 0; b < n4; b += TK_THREADS * 8) {
-          float4 v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = b + threadIdx.x + j * TK_THREADS;
-            v[j] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = 4 * (b + threadIdx.x + j * TK_THREADS);
-            if (i < V) {
-              visit(v[j].x, i);
-              visit(v[j].y, i + 1);
-              visit(v[j].z, i + 2);
-              visit(v[j].w, i + 3);
-            }
-          }
-        }
-      } else {
-        for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
-      }
-    };
-    // pass 1: per-thread maximum
-    float mv = -INFINITY;
-    scan([&](float v, int) { mv = fmaxf(mv, v); });
-    tmax[threadIdx.x] = mv;
-    if (threadIdx.x == 0) n_pool = 0;
-    __syncthreads();
-    {
-      // stable rank of this thread's maximum among all; rank k - 1 is the bound
-      int rank = 0;
-      for (int j = 0; j < TK_THREADS; ++j) {
-        const float u = tmax[j];
-        rank += (u > mv) | ((u == mv) & (j < (int)threadIdx.x));
-      }
-      if (rank == k - 1) thr = mv;
-    }
-    __syncthreads();
-    const float T = thr;
-    // pass 2: gather the values >= T
-    scan([&](float v, int i) {
-      if (v >= T) {
-        const int slot = atomicAdd(&n_pool, 1);
-        if (slot < ROWS_CAP) pool[slot] = make_int2(__float_as_int(v), i);
-      }
-    });
-    __syncthreads();
-    const int np = n_pool;
-    if (np <= ROWS_CAP) {
-      for (int i = threadIdx.x; i < np; i += TK_THREADS) {
-        const int2 c = pool[i];
-        const float v = __int_as_float(c.x);
-        int rank = 0;
-        for (int j = 0; j < np; ++j) {
-          const int2 d = pool[j];
-          rank += better(__int_as_float(d.x), d.y, v, c.y);
-        }
-        if (rank < k) {
-          if (rank == 0) argmax[row] = c.y;
-          if (oi) {
-            oi[rank] = c.y;
-            ov[rank] = v;
-          }
-        }
-      }
-    } else {
-      block_topk(V, k, [&](int i, float &v, int &id) { v = x[i]; id = i; }, argmax + row, oi, ov);
-    }
+    row_select(logits + (size_t)row * V, V, k, tmax, pool, &n_pool, &thr, argmax + row,
+               topk_idx ? topk_idx + (size_t)row * k : nullptr, topk_val ? topk_val + (size_t)row * k : nullptr);
     __syncthreads();                   // the shared scratch is reused by the next row
   }
 }
@@ -376,6 +383,176 @@ cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int3
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
   return launch_pdl(k_topk_merge, dim3(rows), dim3(TK_THREADS), 0, s, tiles, rows, k, cand, argmax,
                     topk_idx, topk_val);
+}
+
+// ------------------------------------------------------------------------- sampling mode
+// Truncated sampling distributions and the sampling verification (DFlash 2 块扩散投机解码技术
+// 详解 §2.3 rejection sampling, §3.3 the same top-k / top-p truncation on the draft and the
+// target side, §4.2 the fallback to p when the residual vanishes). A row's distribution:
+// logits / temperature, the top_k largest kept (ties to the lower index), softmax over them,
+// then the shortest prefix in descending order whose mass reaches top_p, renormalised. It
+// is stored as at most SMP_K (token, probability) pairs in descending order. Draws are
+// inverse-CDF over the kept tokens in vocabulary order against a caller-supplied uniform.
+
+// Inverse-CDF draw over n (token, p) pairs: the pairs are visited in token order (insertion
+// sort of at most SMP_K entries, single thread), the first token whose running sum exceeds
+// u times the total is drawn (the last kept token if rounding leaves none).
+__device__ __forceinline__ int32_t draw_in_vocab_order(const int32_t *tok, const float *p, int n, float u) {
+  int32_t t[SMP_K];
+  float q[SMP_K];
+  for (int i = 0; i < n; ++i) {
+    int j = i;
+    while (j > 0 && t[j - 1] > tok[i]) {
+      t[j] = t[j - 1];
+      q[j] = q[j - 1];
+      --j;
+    }
+    t[j] = tok[i];
+    q[j] = p[i];
+  }
+  float total = 0.f;
+  for (int i = 0; i < n; ++i) total += q[i];
+  float acc = 0.f;
+  for (int i = 0; i < n; ++i) {
+    acc += q[i];
+    if (acc > u * total) return t[i];
+  }
+  return n > 0 ? t[n - 1] : 0;
+}
+
+// One CTA per row (rows b, b + gridDim.x, ...): the row's truncated distribution into
+// dist_tok / dist_p / dist_n ([rows][SMP_K], [rows]; skipped when dist_tok is null); with u
+// non-null also a draw per row into draw.
+__global__ void __launch_bounds__(TK_THREADS, 2) k_trunc_dist(int rows, int V, float temperature, int top_k,
+                                                           float top_p, const float *logits, const float *u,
+                                                           int32_t *draw, int32_t *dist_tok, float *dist_p,
+                                                           int32_t *dist_n) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
+  pdl_wait();
+  __shared__ float tmax[TK_THREADS];
+  __shared__ int2 pool[ROWS_CAP];
+  __shared__ int n_pool;
+  __shared__ float thr;
+  __shared__ int32_t sidx[TK];
+  __shared__ float sval[TK];
+  const int k = min(top_k, V);
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    row_select(logits + (size_t)row * V, V, k, tmax, pool, &n_pool, &thr, nullptr, sidx, sval);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // softmax of the kept values at the temperature, in descending order
+      float p[SMP_K];
+      const float z0 = sval[0] / temperature;
+      float sum = 0.f;
+      for (int i = 0; i < k; ++i) {
+        p[i] = expf(sval[i] / temperature - z0);
+        sum += p[i];
+      }
+      for (int i = 0; i < k; ++i) p[i] /= sum;
+      int n = k;
+      if (top_p < 1.f) {
+        float mass = 0.f;
+        for (n = 1; n <= k; ++n) {
+          mass += p[n - 1];
+          if (mass >= top_p) break;
+        }
+        if (n > k) n = k;
+        float kept = 0.f;
+        for (int i = 0; i < n; ++i) kept += p[i];
+        for (int i = 0; i < n; ++i) p[i] /= kept;
+      }
+      if (dist_tok) {
+        for (int i = 0; i < n; ++i) {
+          dist_tok[(size_t)row * SMP_K + i] = sidx[i];
+          dist_p[(size_t)row * SMP_K + i] = p[i];
+        }
+        dist_n[row] = n;
+      }
+      if (u) draw[row] = draw_in_vocab_order(sidx, p, n, u[row]);
+    }
+    __syncthreads();                   // the shared scratch is reused by the next row
+  }
+}
+
+__device__ __forceinline__ float dist_lookup(const int32_t *tok, const float *p, int n, int32_t t) {
+  for (int i = 0; i < n; ++i)
+    if (tok[i] == t) return p[i];
+  return 0.f;
+}
+
+// One thread per request: position j accepts draft[j] when u_accept[j] < min(1, p(d)/q(d))
+// (q(d) = 0 accepts iff p(d) > 0); the first rejection emits a draw from norm(max(p - q, 0))
+// (from p when that is all zero) and ends the round; with all K accepted a bonus is drawn
+// from p at position K. Target rows are [B][K+1], draft rows [B][K] of the distributions.
+__global__ void k_verify_sample(int B, int K, const int32_t *ptok, const float *pp, const int32_t *pn,
+                                const int32_t *qtok, const float *qp, const int32_t *qn,
+                                const int32_t *draft, const float *u_accept, const float *u_resample,
+                                int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int32_t *o = out_tokens + (size_t)b * (K + 1);
+  int a = K;
+  int32_t last = -1;
+  for (int j = 0; j < K; ++j) {
+    const size_t pr = (size_t)b * (K + 1) + j, qr = (size_t)b * K + j;
+    const int32_t *Pt = ptok + pr * SMP_K, *Qt = qtok + qr * SMP_K;
+    const float *Pp = pp + pr * SMP_K, *Qp = qp + qr * SMP_K;
+    const int np_ = pn[pr], nq_ = qn[qr];
+    const int32_t d = draft[qr];
+    const float pd = dist_lookup(Pt, Pp, np_, d), qd = dist_lookup(Qt, Qp, nq_, d);
+    const float ratio = qd > 0.f ? pd / qd : (pd > 0.f ? 1.f : 0.f);
+    if (u_accept[qr] < fminf(1.f, ratio)) {
+      o[j] = d;
+      continue;
+    }
+    // residual max(p - q, 0): only tokens with p > 0 can carry mass
+    float r[SMP_K];
+    float tot = 0.f;
+    for (int i = 0; i < np_; ++i) {
+      r[i] = fmaxf(Pp[i] - dist_lookup(Qt, Qp, nq_, Pt[i]), 0.f);
+      tot += r[i];
+    }
+    if (tot > 0.f) {
+      for (int i = 0; i < np_; ++i) r[i] /= tot;
+      last = draw_in_vocab_order(Pt, r, np_, u_resample[b]);
+    } else {
+      last = draw_in_vocab_order(Pt, Pp, np_, u_resample[b]);
+    }
+    o[j] = last;
+    a = j;
+    break;
+  }
+  if (a == K) {
+    const size_t pr = (size_t)b * (K + 1) + K;
+    last = draw_in_vocab_order(ptok + pr * SMP_K, pp + pr * SMP_K, pn[pr], u_resample[b]);
+    o[K] = last;
+  }
+  for (int j = a + 1; j <= K; ++j) o[j] = -1;
+  accept_len[b] = a;
+  next_anchor[b] = last;
+}
+
+cudaError_t launch_trunc_dist(int rows, int V, float temperature, int top_k, float top_p,
+                              const float *logits, const float *u, int32_t *draw, int32_t *dist_tok,
+                              float *dist_p, int32_t *dist_n, int max_ctas, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (top_k < 1 || top_k > SMP_K || !(temperature > 0.f) || !(top_p > 0.f) || top_p > 1.f)
+    return cudaErrorInvalidValue;
+  const int g = max_ctas > 0 ? std::min(rows, max_ctas) : rows;
+  return launch_pdl(k_trunc_dist, dim3(g), dim3(TK_THREADS), 0, s, rows, V, temperature, top_k, top_p,
+                    logits, u, draw, dist_tok, dist_p, dist_n);
+}
+
+cudaError_t launch_verify_sample(int B, int K, const int32_t *ptok, const float *pp, const int32_t *pn,
+                                 const int32_t *qtok, const float *qp, const int32_t *qn,
+                                 const int32_t *draft, const float *u_accept, const float *u_resample,
+                                 int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
+                                 cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  return launch_pdl(k_verify_sample, dim3((B + 127) / 128), dim3(128), 0, s, B, K, ptok, pp, pn, qtok, qp,
+                    qn, draft, u_accept, u_resample, accept_len, out_tokens, next_anchor);
 }
 
 // ------------------------------------------------------------------------- no-allocation variant

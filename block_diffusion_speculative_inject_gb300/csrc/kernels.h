@@ -46,6 +46,19 @@ cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &b, int la
                                  const float *qkv, const AttnMaps *maps, float scale_log2,
                                  float *part_o, float *part_ml, cudaStream_t s);
 
+// Sampling mode: truncated distributions (at most SMP_K kept tokens per row) of fp32 logits
+// [rows, V], optionally with one draw per row against uniforms u; the verification of a batch
+// from its target rows [B][K+1] and draft rows [B][K] of such distributions.
+constexpr int SMP_K = 32;
+cudaError_t launch_trunc_dist(int rows, int V, float temperature, int top_k, float top_p,
+                              const float *logits, const float *u, int32_t *draw, int32_t *dist_tok,
+                              float *dist_p, int32_t *dist_n, int max_ctas, cudaStream_t s);
+cudaError_t launch_verify_sample(int B, int K, const int32_t *ptok, const float *pp, const int32_t *pn,
+                                 const int32_t *qtok, const float *qp, const int32_t *qn,
+                                 const int32_t *draft, const float *u_accept, const float *u_resample,
+                                 int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
+                                 cudaStream_t s);
+
 // Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V], on at
 // most max_ctas CTAs (<= 0: one per row) that loop over the rows.
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,

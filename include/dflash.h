@@ -171,6 +171,44 @@ dflash_status dflash_verify_greedy(dflash_ctx *ctx, void *stream, int32_t n_req,
                                    int32_t *accept_len, int32_t *out_tokens,
                                    int32_t *next_anchor);
 
+/* Sampling mode ("DFlash 2 块扩散投机解码技术详解" §2.3 rejection sampling, §3.3 the same
+ * top-k / top-p truncation on the draft and the target side, §4.2 the fallback to p).
+ * A row of logits becomes a distribution by: logits / temperature; keep the top_k largest
+ * (ties to the lower vocabulary index); softmax over those; keep the shortest prefix in
+ * descending order whose probability mass reaches top_p; renormalise. Draws are inverse-CDF
+ * over the kept tokens in vocabulary order: the first token whose running mass exceeds
+ * u times the total. Uniforms are inputs (the caller owns the random stream).
+ * Limits: temperature > 0, 1 <= top_k <= 32, 0 < top_p <= 1 (top_k = 0, i.e. top-p over
+ * the whole vocabulary, is not supported: DFLASH_ERR_UNSUPPORTED). Computed in fp32. */
+typedef struct {
+  float temperature;
+  int32_t top_k;
+  float top_p;
+} dflash_sampling;
+
+/* One draw per row from the sampling distribution of fp32 logits [rows, V] (DEVICE,
+ * row-major, V = the config's vocab) with uniforms u [rows] in [0, 1) (DEVICE fp32) into
+ * tokens [rows] int32 (DEVICE). Used to draw the drafts from the draft's logits. */
+dflash_status dflash_sample_tokens(dflash_ctx *ctx, void *stream, int32_t rows,
+                                   const dflash_sampling *sampling, const float *logits,
+                                   const float *u, int32_t *tokens);
+
+/* Sampling verification of n_req rows (n_req <= max_batch), all DEVICE:
+ *   target_logits [n_req, K+1, V] fp32: the target's logits after the anchor and after
+ *                 each draft; draft_logits [n_req, K, V] fp32: the draft's logits;
+ *   draft [n_req, K] int32: tokens drawn from the draft's distributions;
+ *   u_accept [n_req, K] fp32, u_resample [n_req] fp32: uniforms in [0, 1).
+ * Position j accepts draft[j] when u_accept[j] < min(1, p_j(d)/q_j(d)) (q_j(d) = 0 accepts
+ * iff p_j(d) > 0); the first rejection emits a draw from norm(max(p_j - q_j, 0)), or from
+ * p_j when that is zero, and ends the row; with all K accepted a bonus is drawn from p_K.
+ * Outputs as dflash_verify_greedy: accept_len [n_req] (= a), out_tokens [n_req, K+1] (the
+ * a accepted drafts, the emitted token, -1 padding), next_anchor [n_req]. */
+dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                   const dflash_sampling *sampling, const float *target_logits,
+                                   const float *draft_logits, const int32_t *draft,
+                                   const float *u_accept, const float *u_resample,
+                                   int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor);
+
 /* Forgets a request and returns its pages to the pool (host only). Work already
  * enqueued that reads those pages must precede any later call in stream order. */
 dflash_status dflash_release(dflash_ctx *ctx, int32_t req_id);
