@@ -214,6 +214,28 @@ class StepLoop:
         self.anchor = wl.anchors_d[0].clone()
         self.lens = list(wl.ctx)
         self.records = []
+        self.sampling = None
+
+    def enable_sampling(self, temperature, top_k, top_p, steps, seed=7):
+        """Sampling-mode verification: the drafts are drawn from the draft's logits and checked
+        against synthetic target logits by rejection sampling (uniforms drawn up front)."""
+        B, K, V, dev = self.wl.B, self.cfg.block_k, self.cfg.vocab, self.device
+        g = torch.Generator(device=dev).manual_seed(seed)
+        self.sampling = (temperature, top_k, top_p)
+        self.logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+        self.drafts = torch.empty((B, K), dtype=torch.int32, device=dev)
+        self.target_logits = [torch.randn((B, K + 1, V), generator=g, device=dev) * 2.0 for _ in range(2)]
+        self.u_draft = torch.rand((steps, B * K), generator=g, device=dev)
+        self.u_acc = torch.rand((steps, B, K), generator=g, device=dev)
+        self.u_res = torch.rand((steps, B), generator=g, device=dev)
+
+    def _verify_sampling(self, s, target_logits=None):
+        ctx, out, (T, k, tp) = self.ctx, self.out, self.sampling
+        B, K, V = self.wl.B, self.cfg.block_k, self.cfg.vocab
+        ctx.sample_tokens(self.logits.view(B * K, V), self.u_draft[s], T, k, tp, tokens=self.drafts.view(-1))
+        tl = self.target_logits[s % 2] if target_logits is None else target_logits
+        ctx.verify_sample(tl, self.logits, self.drafts, self.u_acc[s], self.u_res[s], T, k, tp,
+                          out["acc"], out["toks"], out["nxt"])
 
     def step(self, s, feats=None, anchors=None, targets=None):
         ctx, wl, out = self.ctx, self.wl, self.out
@@ -223,9 +245,13 @@ class StepLoop:
                 ctx.truncate(r, c - n)
             ctx.inject(wl.reqs, wl.n_new[s], feats)
             ctx.draft(wl.reqs, wl.anchors_d[s] if anchors is None else anchors, argmax=out["argmax"],
-                      topk_idx=out["topk_idx"], topk_val=out["topk_val"])
-            ctx.verify(out["argmax"], wl.targets_d[s] if targets is None else targets,
-                       out["acc"], out["toks"], out["nxt"])
+                      topk_idx=out["topk_idx"], topk_val=out["topk_val"],
+                      logits=self.logits if self.sampling else None)
+            if self.sampling:
+                self._verify_sampling(s, targets)
+            else:
+                ctx.verify(out["argmax"], wl.targets_d[s] if targets is None else targets,
+                           out["acc"], out["toks"], out["nxt"])
             self.records.append((list(wl.ctx), sum(wl.n_new[s])))
             return
         # verify-driven: draft, verify against targets following the argmax, inject a + 1
@@ -273,6 +299,10 @@ def run_ours(args):
     ctx, w_cpu = _make_context(cfg, wl, device, n_steps)
     _prefill(ctx, cfg, wl)
     loop = StepLoop(ctx, cfg, wl, device)
+    if args.verify == "sample":
+        if cfg.verify_driven:
+            raise SystemExit("--verify sample runs on the steady workloads")
+        loop.enable_sampling(args.temperature, args.top_k, args.top_p, n_steps)
     B, K = wl.B, cfg.block_k
     stream = torch.cuda.current_stream()
     for s in range(W):
@@ -322,6 +352,10 @@ def run_ours(args):
                         toks=torch.empty((B, K + 1), dtype=torch.int32).pin_memory())
         anc_d = torch.empty((B,), dtype=torch.int32, device=device)
         tgt_d = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+        if loop.sampling:
+            # sampling mode: the target's logits are the step's host input
+            tl_h = [t.cpu().pin_memory() for t in loop.target_logits]
+            tl_d = torch.empty_like(loop.target_logits[0])
         h2d = d2h = 0
         e2e_steps = timed if not cfg.verify_driven else list(range(W + 2 * K_, W + 3 * K_))
         _barrier(ws)
@@ -336,8 +370,14 @@ def run_ours(args):
                 fs.append(d)
                 h2d += f.numel() * f.element_size()
             anc_d.copy_(wl.anchors_h[s], non_blocking=True)
-            tgt_d.copy_(wl.targets_h[s], non_blocking=True)
-            h2d += wl.anchors_h[s].numel() * 4 + wl.targets_h[s].numel() * 4
+            h2d += wl.anchors_h[s].numel() * 4
+            if loop.sampling:
+                tl_d.copy_(tl_h[s % 2], non_blocking=True)
+                h2d += tl_d.numel() * 4
+                tgt_d = tl_d
+            else:
+                tgt_d.copy_(wl.targets_h[s], non_blocking=True)
+                h2d += wl.targets_h[s].numel() * 4
             loop.step(s, feats=fs, anchors=anc_d, targets=tgt_d)
             host_out["argmax"].copy_(loop.out["argmax"], non_blocking=True)
             host_out["acc"].copy_(loop.out["acc"], non_blocking=True)
@@ -396,6 +436,9 @@ def run_ours(args):
                    else f"U[1,{cfg.n_new_max}] per request",
                    "l2": "inputs larger than L2: every step streams all weights (GBs) from HBM",
                    "parallelism": f"{ws} independent replica(s)",
+                   "verify": ("greedy prefix match" if args.verify == "greedy" else
+                              f"rejection sampling (temperature {args.temperature}, top_k {args.top_k}, "
+                              f"top_p {args.top_p}) against synthetic target logits"),
                    **({"overrides": over} if over else {})},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches,
@@ -510,6 +553,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify", default="greedy", choices=["greedy", "sample"],
+                    help="greedy prefix match, or rejection sampling against synthetic target logits")
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--top-k", type=int, default=20)
+    ap.add_argument("--top-p", type=float, default=0.95)
     ap.add_argument("--set", action="append", metavar="KEY=VALUE",
                     help="override a workload field (profiling cases), e.g. --set n_layers=1")
     args = ap.parse_args()
