@@ -30,6 +30,9 @@ Readings where the pages leave a step open (each is also listed in the design no
   * Block K/V are never written to the cache; after a verify the caller injects the
     anchor plus the accepted drafts (a + 1 positions).
   * RMSNorm: y = x / sqrt(mean(x^2) + eps) * w.
+  * Variants (off by default): a causal mask inside the block (block row j sees block keys
+    0..j), a trained mask embedding replacing E[mask_id] for the mask rows, and the logits
+    scaled by output_multiplier then soft-capped as c * tanh(logits / c).
   * Precision: the stored operands of the method — weights, the target hidden states
     and the context K/V cache — have the storage type (bf16 or fp32); the cache is
     rounded to it (round-to-nearest-even) when written. Every other value (the fused
@@ -222,14 +225,20 @@ class OracleDraft:
             k = rmsnorm(k, lw["k_norm"], c.rms_eps)
         q = rope(q, pos, c.rope_theta)
         k = rope(k, pos, c.rope_theta)
-        # context K/V first, then the block's own K/V; no mask inside the block
+        # context K/V first, then the block's own K/V; no mask inside the block by default
+        # ([P4] §5.3); the causal variant ([P2] 1.x, "块内保持因果掩码") lets block row j see
+        # block keys 0..j only
         keys = np.concatenate([ctx_k, k], axis=0)         # [n_ctx + K + 1, nkv, hd]
         vals = np.concatenate([ctx_v, v], axis=0)
+        n_ctx = ctx_k.shape[0]
         group = nq // nkv
         o = np.empty((q_rows, nq, hd))
         for h in range(nq):
             kvh = h // group
             s = (q[:, h, :] @ keys[:, kvh, :].T) / np.sqrt(hd)   # [K+1, n_keys]
+            if getattr(c, "block_causal", 0):
+                for j in range(q_rows):
+                    s[j, n_ctx + j + 1:] = -np.inf
             o[:, h, :] = softmax(s, axis=-1) @ vals[:, kvh, :]
         o = o.reshape(q_rows, nq * hd)
         x = x + o @ _f64(lw["wo"]).T
@@ -243,7 +252,11 @@ class OracleDraft:
         ent = self.cache[req]
         n_ctx = ent["K"][0].shape[0]
         toks = self.block_tokens(anchor)
-        x = _f64(self.w["embed"][toks]) * c.input_embedding_scale
+        emb = _f64(self.w["embed"][toks])
+        if getattr(c, "mask_embedding", 0):
+            # a trained mask embedding replaces the word embedding of the mask rows ([P4] §5.2)
+            emb[1:] = _f64(self.w["mask_embedding"])
+        x = emb * c.input_embedding_scale
         pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
         for l in range(c.n_layers):
             x = self.layer(x, l, ent["K"][l], ent["V"][l], pos)
@@ -258,6 +271,11 @@ class OracleDraft:
         out = np.empty((h.shape[0], V))
         for v0 in range(0, V, chunk):
             out[:, v0:v0 + chunk] = h @ _f64(lm[v0:v0 + chunk]).T
+        # optional output scale and soft cap ([P2] 1.x compute_logits): c * tanh(x / c)
+        out = out * getattr(self.cfg, "output_multiplier", 1.0)
+        cap = getattr(self.cfg, "logit_softcap", 0.0)
+        if cap > 0:
+            out = cap * np.tanh(out / cap)
         return out
 
     def draft(self, req, anchor):

@@ -45,6 +45,11 @@ class DraftConfig:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     input_embedding_scale: float = 1.0
+    # variants the pages mention besides the default path
+    block_causal: int = 0           # 1: causal mask inside the query block
+    output_multiplier: float = 1.0  # logits scale
+    logit_softcap: float = 0.0      # > 0: logits = c * tanh(logits / c) after the scale
+    mask_embedding: int = 0         # 1: a trained mask embedding replaces E[mask_id]
     # workload
     batch: int = 1
     ctx_min: int = 64

@@ -95,6 +95,8 @@ def make_weights(cfg: DraftConfig, seed: int = 0, threads: int = 8):
         flat = dict(ex.map(one, specs))
     w = {k: flat[k] for k in ("embed", "lm_head", "fc", "fc_norm", "final_norm")}
     w["layers"] = [{k: flat[f"L{i}.{k}"] for k in LAYER_KEYS} for i in range(cfg.n_layers)]
+    if cfg.mask_embedding:
+        w["mask_embedding"] = _normal((cfg.hidden,), 0.02, 0.0, dt, "weights", cfg.name, seed, "mask_embedding")
     return w
 
 

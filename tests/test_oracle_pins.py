@@ -172,8 +172,14 @@ def _torch_layer(c, lw, x, ctx_k, ctx_v, pos):
     k = t(O.rope(k.numpy(), pos, c.rope_theta))
     keys = torch.cat([t(ctx_k), k], 0).transpose(0, 1)    # [nkv, S, hd]
     vals = torch.cat([t(ctx_v), v], 0).transpose(0, 1)
+    mask = None
+    if getattr(c, "block_causal", 0):
+        # context keys visible to all rows; block key i visible to block rows j >= i
+        n_ctx = ctx_k.shape[0]
+        mask = torch.ones((n, n_ctx + n), dtype=torch.bool)
+        mask[:, n_ctx:] = torch.tril(torch.ones((n, n), dtype=torch.bool))
     o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], keys[None], vals[None],
-                                       enable_gqa=True)[0]           # no mask: bidirectional
+                                       attn_mask=mask, enable_gqa=True)[0]   # None: bidirectional
     o = o.transpose(0, 1).reshape(n, -1)
     X = X + F.linear(o, t(lw["wo"]))
     xn2 = F.rms_norm(X, (c.hidden,), t(lw["post_norm"]), eps=c.rms_eps)
@@ -563,3 +569,65 @@ def test_verify_sample_logits_first_token_follows_truncated_target():
         assert 1 <= len(toks) == a + 1 <= K + 1
         counts[toks[0]] += 1
     assert np.all(np.abs(counts / n - p0) < 5 * np.sqrt(p0 * (1 - p0) / n) + 1e-3)
+
+
+# ----------------------------------------------------------------------------- variants
+def test_causal_block_layer_matches_torch_masked_attention():
+    """The causal variant equals torch's scaled_dot_product_attention with a mask that
+    shows every context key and block keys 0..j to block row j; a row does not depend on
+    later block rows."""
+    c = _cfg(n_q_heads=4, n_kv_heads=2, block_causal=1)
+    w = _weights(c, seed=61)
+    od = O.OracleDraft(c, w)
+    rng = np.random.default_rng(62)
+    n_ctx = 21
+    x = rng.normal(0, 1, (c.block_k + 1, c.hidden))
+    ck = rng.normal(0, 1, (n_ctx, 2, c.head_dim))
+    cv = rng.normal(0, 1, (n_ctx, 2, c.head_dim))
+    pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
+    full = od.layer(x, 0, ck, cv, pos)
+    np.testing.assert_allclose(full, _torch_layer(c, w["layers"][0], x, ck, cv, pos), rtol=1e-10, atol=1e-11)
+    for j in (0, 2):
+        part = od.layer(x[:j + 1], 0, ck, cv, pos[:j + 1])
+        np.testing.assert_allclose(part[j], full[j], rtol=1e-12, atol=1e-13)
+    bi = O.OracleDraft(_cfg(n_q_heads=4, n_kv_heads=2), w).layer(x, 0, ck, cv, pos)
+    assert np.abs(bi[0] - full[0]).max() > 1e-6      # the flag changes the anchor row
+
+
+def test_mask_embedding_replaces_the_mask_rows_only():
+    """With the trained mask embedding equal to E[mask_id] the draft is unchanged; another
+    vector changes the mask rows' logits."""
+    c0 = _cfg()
+    c1 = _cfg(mask_embedding=1)
+    w = _weights(c0, seed=63)
+    fe = _feats(c0, 12, 64)
+    base = O.OracleDraft(c0, w)
+    base.inject(0, fe)
+    same = O.OracleDraft(c1, dict(w, mask_embedding=np.array(w["embed"][c0.mask_id])))
+    same.inject(0, fe)
+    np.testing.assert_allclose(same.logits(0, 5), base.logits(0, 5), rtol=1e-13, atol=1e-13)
+    other = O.OracleDraft(c1, dict(w, mask_embedding=np.random.default_rng(65).normal(0, 0.02, c0.hidden)))
+    other.inject(0, fe)
+    assert np.abs(other.logits(0, 5) - base.logits(0, 5)).max() > 1e-6
+
+
+def test_output_multiplier_and_softcap_properties():
+    """The scale alone is linear; the soft cap keeps the order, stays inside (-c, c) and
+    inverts through atanh back to the scaled logits."""
+    c0 = _cfg()
+    w = _weights(c0, seed=66)
+    fe = _feats(c0, 10, 67)
+    raw = O.OracleDraft(c0, w)
+    raw.inject(0, fe)
+    r = raw.logits(0, 9)
+    sc = O.OracleDraft(_cfg(output_multiplier=3.5), w)
+    sc.inject(0, fe)
+    np.testing.assert_allclose(sc.logits(0, 9), 3.5 * r, rtol=1e-13)
+    cap = 1.0
+    cp = O.OracleDraft(_cfg(output_multiplier=3.5, logit_softcap=cap), w)
+    cp.inject(0, fe)
+    y = cp.logits(0, 9)
+    assert np.all(np.abs(y) < cap)
+    for row_r, row_y in zip(r, y):
+        np.testing.assert_array_equal(np.argsort(row_r, kind="stable"), np.argsort(row_y, kind="stable"))
+    np.testing.assert_allclose(cap * np.arctanh(y / cap), 3.5 * r, rtol=1e-9, atol=1e-12)
