@@ -73,7 +73,10 @@ def make_config(cfg, limits: Limits):
         max_pages=limits.max_pages, page_size=64, max_positions=limits.max_positions,
         max_inject_rows=limits.max_inject_rows, rms_eps=cfg.rms_eps, rope_theta=cfg.rope_theta,
         input_embedding_scale=cfg.input_embedding_scale,
-        dtype=_ffi.BF16 if cfg.dtype == "bf16" else _ffi.F32)
+        dtype=_ffi.BF16 if cfg.dtype == "bf16" else _ffi.F32,
+        block_causal=getattr(cfg, "block_causal", 0),
+        output_multiplier=getattr(cfg, "output_multiplier", 1.0),
+        logit_softcap=getattr(cfg, "logit_softcap", 0.0))
 
 
 def dflash_validate_config(cfg, limits: Limits):
@@ -102,7 +105,9 @@ class Context:
         self._w = _ffi.Weights(embed=weights["embed"].data_ptr(), lm_head=weights["lm_head"].data_ptr(),
                                fc=weights["fc"].data_ptr(), fc_norm=weights["fc_norm"].data_ptr(),
                                final_norm=weights["final_norm"].data_ptr(),
-                               layers=ctypes.cast(layers, ctypes.POINTER(_ffi.LayerWeights)))
+                               layers=ctypes.cast(layers, ctypes.POINTER(_ffi.LayerWeights)),
+                               mask_embedding=(weights["mask_embedding"].data_ptr()
+                                               if weights.get("mask_embedding") is not None else None))
         h = ctypes.c_void_p()
         st = self.lib.dflash_create(ctypes.byref(self._c), ctypes.byref(self._w), device, ctypes.byref(h))
         if st != _ffi.OK:

@@ -18,7 +18,9 @@ class Config(ctypes.Structure):
         "n_feat", "target_hidden", "block_k", "topk", "mask_token_id", "qk_norm", "max_batch",
         "max_requests", "max_pages", "page_size", "max_positions", "max_inject_rows")] + [
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
-        ("input_embedding_scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+        ("input_embedding_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
+        ("block_causal", ctypes.c_int32), ("output_multiplier", ctypes.c_float),
+        ("logit_softcap", ctypes.c_float)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -30,7 +32,7 @@ class LayerWeights(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p), ("fc", ctypes.c_void_p),
                 ("fc_norm", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
-                ("layers", ctypes.POINTER(LayerWeights))]
+                ("layers", ctypes.POINTER(LayerWeights)), ("mask_embedding", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p

@@ -164,6 +164,15 @@ struct GemmDesc {
   // EPI_SWIGLU
   OpOut out;                     // [M, ldo] operand planes
   int ldo;
+  // EPI_TOPK: logits *= out_mult, then out_cap * tanh(logits / out_cap) when out_cap > 0,
+  // applied before ranking (out_xf = 0: untouched)
+  int out_xf;
+  float out_mult, out_cap;
 };
+
+__device__ __forceinline__ float logit_xform(float x, float mult, float cap) {
+  x *= mult;
+  return cap > 0.f ? cap * tanhf(x / cap) : x;
+}
 
 }  // namespace dflash

@@ -342,6 +342,9 @@ extern "C" dflash_status dflash_validate_config(const dflash_config *c, char *ms
   if (c->max_positions < c->block_k + 2 || c->max_positions > (1 << 22))
     return bad(DFLASH_ERR_INVALID_ARG, "max_positions must be in [block_k + 2, 2^22]");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad(DFLASH_ERR_INVALID_ARG, "rms_eps / rope_theta");
+  if (c->block_causal != 0 && c->block_causal != 1) return bad(DFLASH_ERR_INVALID_ARG, "block_causal must be 0 or 1");
+  if (!(c->output_multiplier >= 0.f) || !(c->logit_softcap >= 0.f))
+    return bad(DFLASH_ERR_INVALID_ARG, "output_multiplier and logit_softcap must be >= 0");
   if (msg && msg_len > 0) msg[0] = 0;
   return DFLASH_OK;
 }
@@ -417,6 +420,9 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   m.hd = cfg->head_dim; m.I = cfg->intermediate; m.V = cfg->vocab; m.K = cfg->block_k;
   m.n_feat = cfg->n_feat; m.Ht = cfg->target_hidden; m.topk = cfg->topk; m.qk_norm = cfg->qk_norm;
   m.eps = cfg->rms_eps; m.emb_scale = cfg->input_embedding_scale;
+  m.causal = cfg->block_causal;
+  m.out_mult = cfg->output_multiplier == 0.f ? 1.f : cfg->output_multiplier;
+  m.softcap = cfg->logit_softcap;
 
   auto fail = [&](dflash_status s) {
     free_all(c);
@@ -842,6 +848,9 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     add_wseg(lm, c->w.lm_head, m.V);
     lm.topk = m.topk;
     lm.cand = c->cand;
+    lm.out_xf = m.out_mult != 1.f || m.softcap > 0.f;
+    lm.out_mult = m.out_mult;
+    lm.out_cap = m.softcap;
     if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
   } else {
     float *lg = logits ? logits : c->logits;
@@ -849,6 +858,9 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     set_x(c, lm, xf, m.H);
     add_wseg(lm, c->w.lm_head, m.V);
     if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
+    if (m.out_mult != 1.f || m.softcap > 0.f)
+      CK(c, timed(c, K_TOPK, s, 8.0 * RK * m.V, 4.0 * RK * m.V, 1,
+                  [&] { return launch_logit_xform((long)RK * m.V, m.out_mult, m.softcap, lg, s); }));
   }
   return DFLASH_OK;
 }
@@ -981,8 +993,8 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   // block embedding [anchor, mask x K] x scale, fused with the first layer's input norm
   const OpOut xn0 = op_of(c, c->xn, (size_t)c->rows_max * m.H);
   CK(c, timed(c, K_EMBED, s, (double)B * Q * m.H * (c->esz + 8), (double)B * Q * m.H * 4, 1, [&] {
-       return launch_embed_norm(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed, c->x,
-                                xn0, c->layers[0].in_norm, c->err_d, s);
+       return launch_embed_norm(c->dtype, m, B, anchors, c->cfg.mask_token_id, c->w.embed,
+                                c->w.mask_embedding, c->x, xn0, c->layers[0].in_norm, c->err_d, s);
      }));
   if (use_graph) {
     if ((st = run_layers_graph(c, B, bt, s)) != DFLASH_OK) return st;

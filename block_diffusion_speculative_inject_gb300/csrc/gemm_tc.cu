@@ -63,6 +63,8 @@ struct TcParams {
   int rows_per_req, q_dim, kv_dim;
   OpOut out;                          // EPI_SWIGLU
   int ldo;
+  int out_xf;                         // EPI_TOPK: logit scale / soft cap
+  float out_mult, out_cap;
   int *err;
 };
 
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c0 + j;
           const bool valid = ok && n < p.N && m < p.M;
-          const float v = __uint_as_float(r[j]);
+          const float v = p.out_xf ? logit_xform(__uint_as_float(r[j]), p.out_mult, p.out_cap) : __uint_as_float(r[j]);
           tile[(c0 + j) * TP + q * 32 + lane] = valid ? v : -INFINITY;
           if (valid && p.y) p.y[(size_t)m * p.ldy + n] = v;
         }
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int n = n0 + lane + 32 * j;
+              if (p.out_xf) x[j] = logit_xform(x[j], p.out_mult, p.out_cap);
               v[j] = n < p.N ? x[j] : -INFINITY;
               id[j] = n;
               if (n < p.N && p.y) p.y[(size_t)m * p.ldy + n] = x[j];
@@ -673,6 +676,9 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.kv_dim = d.kv_dim;
   p.out = d.out;
   p.ldo = d.ldo;
+  p.out_xf = d.out_xf;
+  p.out_mult = d.out_mult;
+  p.out_cap = d.out_cap;
   p.err = t->err;
   if (d.part) {
     // partials mode: the (already reduced) product goes to the caller's buffer [M][N]

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
                                                                const int32_t *n_split, int max_split,
                                                                const float *part_o,
                                                                const float *part_ml, const float *qkv,
-                                                               float scale_log2, OpOut o) {
+                                                               float scale_log2, int causal, OpOut o) {
   pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
   constexpr int DPL = HD / 32;
@@ -192,15 +192,17 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
   }
   __syncthreads();
   if (r >= R) return;
+  // block key `lane` is seen by this row unless the causal variant hides keys after it
+  const bool see = lane < Q && (!causal || lane <= j);
   float sk = -INFINITY;
-  if (lane < Q) {
+  if (see) {
     float t = 0.f;
 #pragma unroll 16
     for (int d = 0; d < HD; ++d) t = fmaf(qs[warp][d], ks[lane * KP + d], t);
     sk = t * scale_log2;
   }
   const float M = warp_max(fmaxf(sk, ms));
-  const float pk = lane < Q ? exp2f(sk - M) : 0.f;
+  const float pk = see ? exp2f(sk - M) : 0.f;
   const float cs = lane < ns ? exp2f(ms - M) : 0.f;
   const float Lsum = warp_sum(pk + cs * ls);
   float acc[DPL] = {};
@@ -247,7 +249,7 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
   dim3 g2(m.nkv, bt.B, (R + CB_ROWS - 1) / CB_ROWS);
   auto go = [&](auto kern) {
     return launch_pdl(kern, g2, dim3(32 * CB_ROWS), 0, s, m.nq, m.nkv, m.Q(), bt.n_split, bt.max_split,
-                      (const float *)part_o, (const float *)part_ml, qkv, scale_log2, o);
+                      (const float *)part_o, (const float *)part_ml, qkv, scale_log2, m.causal, o);
   };
   // register room for the partial outputs follows the largest split count
   if (bt.max_split <= 2) return go(k_attn_combine<HD, 2>);

@@ -257,8 +257,8 @@ cudaError_t launch_post_kv(int dtype, const ModelDims &m, int T, const float *ws
 template <typename TW>
 __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, const int32_t *anchors,
                                                            int mask_id, float scale, const TW *embed,
-                                                           float *x, OpOut out, const TW *w, float eps,
-                                                           int *err) {
+                                                           const TW *mask_emb, float *x, OpOut out,
+                                                           const TW *w, float eps, int *err) {
   pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
   __shared__ float red[PN_THREADS / 32];
@@ -268,7 +268,8 @@ __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, 
     if (threadIdx.x == 0) raise_err(err, DEV_ERR_TOKEN);
     tok = 0;
   }
-  const TW *__restrict__ src = embed + (size_t)tok * H;
+  // a trained mask embedding, when given, replaces the word embedding of the mask rows
+  const TW *__restrict__ src = (j > 0 && mask_emb) ? mask_emb : embed + (size_t)tok * H;
   float vals[4 * PN_VEC];
   // all loads first (the row is read once), then the stores
 #pragma unroll
@@ -300,15 +301,17 @@ __global__ void __launch_bounds__(PN_THREADS) k_embed_norm(int H, int Q, int V, 
 }
 
 cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_t *anchors, int mask_id,
-                              const void *embed, float *x, OpOut out, const void *w, int *err,
-                              cudaStream_t s) {
+                              const void *embed, const void *mask_emb, float *x, OpOut out, const void *w,
+                              int *err, cudaStream_t s) {
   if (m.H > 4 * PN_VEC * PN_THREADS) return cudaErrorInvalidValue;
   dim3 g(B * m.Q());
   if (dtype)
     return launch_pdl(k_embed_norm<bf16>, g, dim3(PN_THREADS), 0, s, m.H, m.Q(), m.V, anchors, mask_id,
-                      m.emb_scale, (const bf16 *)embed, x, out, (const bf16 *)w, m.eps, err);
+                      m.emb_scale, (const bf16 *)embed, (const bf16 *)mask_emb, x, out, (const bf16 *)w,
+                      m.eps, err);
   return launch_pdl(k_embed_norm<float>, g, dim3(PN_THREADS), 0, s, m.H, m.Q(), m.V, anchors, mask_id,
-                    m.emb_scale, (const float *)embed, x, out, (const float *)w, m.eps, err);
+                    m.emb_scale, (const float *)embed, (const float *)mask_emb, x, out, (const float *)w,
+                    m.eps, err);
 }
 
 }  // namespace dflash

@@ -6,6 +6,21 @@ namespace dflash {
 
 constexpr int PAGE = KV_PAGE;
 
+// ------------------------------------------------------------------------- logit scale / soft cap
+// The optional output scale and logit soft cap of the LM head ("DFlash 2 块扩散投机解码技术
+// 详解" §1.x compute_logits), in place on fp32 logits [n] (the unfused LM-head path).
+__global__ void k_logit_xform(long n, float mult, float cap, float *logits) {
+  pdl_trigger();                       // dependents may launch and prefetch; they still wait
+  pdl_wait();
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) logits[i] = logit_xform(logits[i], mult, cap);
+}
+
+cudaError_t launch_logit_xform(long n, float mult, float cap, float *logits, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(k_logit_xform, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, n, mult, cap, logits);
+}
+
 // ------------------------------------------------------------------------- greedy verify
 // a = number of leading j < K with draft[j] == target[j]; emit draft[0..a-1] then target[a]
 // ("DFlash 2 块扩散投机解码技术详解" §2.3; at most K+1 tokens: "DFlash：把串行 Draft 变成并行“填空”" §2).

@@ -10,6 +10,8 @@ struct ModelDims {
   int H, L, nq, nkv, hd, I, V, K, n_feat, Ht, topk;
   int qk_norm;
   float eps, emb_scale;
+  int causal;                 // causal mask inside the query block
+  float out_mult, softcap;    // logits *= out_mult, then softcap * tanh(logits / softcap) if > 0
   int q_dim() const { return nq * hd; }
   int kv_dim() const { return nkv * hd; }
   int qkv_dim() const { return (nq + 2 * nkv) * hd; }
@@ -59,6 +61,9 @@ cudaError_t launch_verify_sample(int B, int K, const int32_t *ptok, const float 
                                  int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
                                  cudaStream_t s);
 
+// logits[i] = logit_xform(logits[i]) over n fp32 values, in place.
+cudaError_t launch_logit_xform(long n, float mult, float cap, float *logits, cudaStream_t s);
+
 // Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V], on at
 // most max_ctas CTAs (<= 0: one per row) that loop over the rows.
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
@@ -79,8 +84,8 @@ cudaError_t launch_post_kv(int dtype, const ModelDims &m, int T, const float *ws
                            const int32_t *slot, const int32_t *pos, const float2 *rope,
                            const void *const *k_norms, void *pool, cudaStream_t s);
 cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_t *anchors, int mask_id,
-                              const void *embed, float *x, OpOut out, const void *w, int *err,
-                              cudaStream_t s);
+                              const void *embed, const void *mask_emb, float *x, OpOut out, const void *w,
+                              int *err, cudaStream_t s);
 
 cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *target,
                           int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,

@@ -89,6 +89,12 @@ typedef struct {
   float rope_theta;          /* RoPE base                                              */
   float input_embedding_scale; /* multiplies the block's embedding rows                */
   dflash_dtype dtype;        /* storage / GEMM operand type                            */
+  /* Variants ("DFlash 2 块扩散投机解码技术详解" §1.x: the causal in-block mask and the
+   * optional output_multiplier / logit soft cap of compute_logits). Zero-initialised
+   * fields give the default path: bidirectional block, logits unscaled, no cap. */
+  int32_t block_causal;      /* 1: block row j attends to block keys 0..j only          */
+  float output_multiplier;   /* logits *= m (0 is read as 1; must be > 0 otherwise)     */
+  float logit_softcap;       /* c > 0: logits = c * tanh(logits / c) after the scale    */
 } dflash_config;
 
 /* One draft decoder layer (pre-norm, Qwen3-style). All [out, in] row-major. */
@@ -113,6 +119,9 @@ typedef struct {
   const void *fc_norm;     /* [H] RMSNorm after fc                                   */
   const void *final_norm;  /* [H] RMSNorm before the LM head                         */
   const dflash_layer_weights *layers; /* host array of n_layers entries (copied)     */
+  const void *mask_embedding; /* [H] or NULL: a trained mask embedding used instead of
+                               * embed[mask_token_id] for the K mask rows
+                               * ("DFlash：把串行 Draft 变成并行“填空”" §5.2)          */
 } dflash_weights;
 
 typedef struct dflash_ctx dflash_ctx;
