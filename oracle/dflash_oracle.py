@@ -60,6 +60,7 @@ __all__ = [
     "OracleDraft", "topk_desc", "argmax_lowest", "verify_greedy",
     "accept_prob", "residual_dist", "sample_index", "verify_sample", "as_fraction_dist",
     "sampling_probs", "sample_token", "verify_sample_logits",
+    "log_softmax_norm", "ddtree_build", "ddtree_mask", "ddtree_walk",
 ]
 
 
@@ -429,3 +430,71 @@ def verify_sample_logits(target_logits, draft_logits, draft, u_accept, u_resampl
     p_rows = [sampling_probs(r, temperature, top_k, top_p) for r in target_logits]
     q_rows = [sampling_probs(r, temperature, top_k, top_p) for r in draft_logits]
     return verify_sample(p_rows, q_rows, draft, u_accept, u_resample)
+
+
+# ----------------------------------------------------------------------------- DDTree
+def log_softmax_norm(logits):
+    """log sum_v exp(logits[v]) per row (the normaliser of the draft's softmax)."""
+    x = np.asarray(logits, dtype=np.float64)
+    m = np.max(x, axis=-1, keepdims=True)
+    return (m + np.log(np.sum(np.exp(x - m), axis=-1, keepdims=True)))[..., 0]
+
+
+def ddtree_build(cand_logp, cand_tok, budget):
+    """Best-first draft tree ("DDTree" §2.3, Algorithm 1, and Proposition 2).
+
+    cand_logp [L][kc]: log-probabilities of each block position's candidates, best first;
+    cand_tok [L][kc]: their tokens. A prefix is a rank tuple (r_1 .. r_d) (r_i = which
+    candidate position i takes); its log-probability is the sum of its entries. The heap
+    starts with (best of position 1); each pop adds the prefix as a node and pushes its next
+    sibling (last rank + 1) and its first child (a best candidate at the next position).
+    Ties pop by (log-probability desc, depth asc, parent node asc, last rank asc).
+    Returns the popped nodes in order as (token, parent node or -1 for the root, depth,
+    log-probability): at most `budget` of them, prefix-closed.
+    """
+    import heapq
+    L, kc = len(cand_logp), len(cand_logp[0])
+    nodes = []
+    heap = [(-float(cand_logp[0][0]), 1, -1, 0)]     # (-logp, depth, parent, rank)
+    while heap and len(nodes) < budget:
+        nlp, depth, parent, rank = heapq.heappop(heap)
+        lp = -nlp
+        me = len(nodes)
+        nodes.append((int(cand_tok[depth - 1][rank]), parent, depth, lp))
+        base = 0.0 if parent < 0 else nodes[parent][3]
+        if rank + 1 < kc:
+            heapq.heappush(heap, (-(base + float(cand_logp[depth - 1][rank + 1])), depth, parent, rank + 1))
+        if depth < L:
+            heapq.heappush(heap, (-(lp + float(cand_logp[depth][0])), depth + 1, me, 0))
+    return nodes
+
+
+def ddtree_mask(nodes):
+    """Ancestor-only visibility ("DDTree" §3.3): index 0 is the root (the anchor / bonus
+    token), node i is index i + 1; each index sees the root, its ancestors and itself."""
+    n = len(nodes) + 1
+    m = np.zeros((n, n), dtype=bool)
+    m[:, 0] = True
+    for i in range(1, n):
+        j = i
+        while j > 0:
+            m[i, j] = True
+            j = nodes[j - 1][1] + 1
+    return m
+
+
+def ddtree_walk(nodes, target_next):
+    """Greedy verifier walk over the tree ("DDTree" §3.5): target_next[0] is the target's
+    token after the root, target_next[i + 1] after node i. From the root, move to the child
+    whose token equals the target's next token while one exists; emit the matched tokens and
+    then the target's token where the walk stopped. Returns (accepted, emitted tokens)."""
+    cur = -1
+    out = []
+    while True:
+        t = int(target_next[cur + 1])
+        child = [i for i, nd in enumerate(nodes) if nd[1] == cur and nd[0] == t]
+        if not child:
+            out.append(t)
+            return len(out) - 1, out
+        out.append(t)
+        cur = child[0]

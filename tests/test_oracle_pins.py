@@ -631,3 +631,78 @@ def test_output_multiplier_and_softcap_properties():
     for row_r, row_y in zip(r, y):
         np.testing.assert_array_equal(np.argsort(row_r, kind="stable"), np.argsort(row_y, kind="stable"))
     np.testing.assert_allclose(cap * np.arctanh(y / cap), 3.5 * r, rtol=1e-9, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- DDTree
+def _tuples(nodes):
+    """Rank-free identity of each node: the token path from the root."""
+    out = []
+    for tok, parent, depth, lp in nodes:
+        out.append((out[parent] if parent >= 0 else ()) + (tok,))
+    return out
+
+
+def test_log_softmax_norm_matches_scipy():
+    from scipy.special import logsumexp
+    x = np.random.default_rng(70).normal(0, 3, (4, 1000))
+    np.testing.assert_allclose(O.log_softmax_norm(x), logsumexp(x, axis=-1), rtol=1e-14)
+
+
+@pytest.mark.parametrize("L,kc,budget", [(3, 3, 5), (3, 4, 11), (4, 2, 9), (2, 5, 10)])
+def test_ddtree_is_the_top_budget_prefixes(L, kc, budget):
+    """Proposition 2 by brute force: the popped nodes are exactly the `budget` most likely
+    prefixes over every depth, and each node's parent is popped before it."""
+    rng = np.random.default_rng(L * 100 + kc * 10 + budget)
+    for _ in range(20):
+        p = rng.dirichlet(np.ones(kc + 3), size=L)[:, :kc]
+        p = -np.sort(-p, axis=1)
+        lp = np.log(p)
+        tok = rng.permutation(1000)[:L * kc].reshape(L, kc)
+        nodes = O.ddtree_build(lp, tok, budget)
+        allp = []
+        for d in range(1, L + 1):
+            for ranks in itertools.product(range(kc), repeat=d):
+                allp.append((sum(lp[i][r] for i, r in enumerate(ranks)),
+                             tuple(int(tok[i][r]) for i, r in enumerate(ranks))))
+        allp.sort(key=lambda e: -e[0])
+        want = {t for _, t in allp[:budget]}
+        assert set(_tuples(nodes)) == want
+        for i, (t, parent, depth, v) in enumerate(nodes):
+            assert parent < i and (parent < 0) == (depth == 1)
+            if parent >= 0:
+                assert nodes[parent][2] == depth - 1
+
+
+def test_ddtree_mask_is_the_prefix_relation():
+    rng = np.random.default_rng(71)
+    lp = np.log(-np.sort(-rng.dirichlet(np.ones(6), size=4)[:, :4], axis=1))
+    tok = np.arange(16).reshape(4, 4) + 100
+    nodes = O.ddtree_build(lp, tok, 12)
+    paths = [()] + _tuples(nodes)
+    m = O.ddtree_mask(nodes)
+    for i, pi in enumerate(paths):
+        for j, pj in enumerate(paths):
+            assert m[i, j] == (pi[:len(pj)] == pj)
+
+
+def test_ddtree_walk_follows_the_target_down_the_tree():
+    """The walk against a direct search: from the root, extend the accepted path while the
+    target's next token labels a child of the current path."""
+    rng = np.random.default_rng(72)
+    lp = np.log(-np.sort(-rng.dirichlet(np.ones(5), size=3)[:, :3], axis=1))
+    tok = np.array([[1, 2, 3], [1, 2, 3], [1, 2, 3]])
+    nodes = O.ddtree_build(lp, tok, 9)
+    paths = _tuples(nodes)
+    index = {p: i for i, p in enumerate(paths)}
+    for _ in range(200):
+        tn = rng.integers(1, 5, len(nodes) + 1)
+        a, out = O.ddtree_walk(nodes, tn)
+        path, cur = (), -1
+        while True:
+            t = int(tn[cur + 1])
+            if path + (t,) in index:
+                path = path + (t,)
+                cur = index[path]
+            else:
+                break
+        assert a == len(path) and out == list(path) + [t]
