@@ -140,7 +140,7 @@ class Context:
         self._check(st)
 
     def draft(self, req_ids, anchors, argmax=None, topk_idx=None, topk_val=None, logits=None,
-              want_topk=True, want_logits=False, stream=None):
+              want_topk=True, want_logits=False, stream=None, lse=None, want_lse=False):
         B, K, k, V = len(req_ids), self.cfg.block_k, self.cfg.topk, self.cfg.vocab
         dev = anchors.device
         if argmax is None:
@@ -150,11 +150,18 @@ class Context:
             topk_val = torch.empty((B, K, k), dtype=torch.float32, device=dev)
         if want_logits and logits is None:
             logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
-        st = self.lib.dflash_draft_step(self.h, _stream_ptr(stream), B, _i32_array(req_ids),
-                                        _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
-                                        _ptr(topk_val), _ptr(logits))
+        if want_lse and lse is None:
+            lse = torch.empty((B, K), dtype=torch.float32, device=dev)
+        if lse is not None:
+            st = self.lib.dflash_draft_step_lse(self.h, _stream_ptr(stream), B, _i32_array(req_ids),
+                                                _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
+                                                _ptr(topk_val), _ptr(logits), _ptr(lse))
+        else:
+            st = self.lib.dflash_draft_step(self.h, _stream_ptr(stream), B, _i32_array(req_ids),
+                                            _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
+                                            _ptr(topk_val), _ptr(logits))
         self._check(st)
-        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits)
+        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits, lse=lse)
 
     def verify(self, draft, target, accept_len=None, out_tokens=None, next_anchor=None, stream=None):
         B, K = draft.shape
@@ -273,6 +280,42 @@ def dflash_verify_sample(ctx: Context, target_logits, draft_logits, draft, u_acc
                          next_anchor=None, stream=None):
     return ctx.verify_sample(target_logits, draft_logits, draft, u_accept, u_resample, temperature,
                              top_k, top_p, accept_len, out_tokens, next_anchor, stream=stream)
+
+
+def ddtree_build(cand_tok, cand_logp, budget, with_mask=True, stream=None):
+    """Best-first draft trees (dflash_ddtree_build) from candidates [n, L, kc] (int32 tokens,
+    fp32 log-probabilities, best first). Returns a dict of device tensors."""
+    lib = library()
+    n, L, kc = cand_tok.shape
+    dev = cand_tok.device
+    out = dict(tok=torch.empty((n, budget), dtype=torch.int32, device=dev),
+               parent=torch.empty((n, budget), dtype=torch.int32, device=dev),
+               depth=torch.empty((n, budget), dtype=torch.int32, device=dev),
+               logp=torch.empty((n, budget), dtype=torch.float32, device=dev),
+               n_nodes=torch.empty((n,), dtype=torch.int32, device=dev))
+    words = (budget + 1 + 31) // 32
+    out["mask"] = (torch.empty((n, budget + 1, words), dtype=torch.int32, device=dev) if with_mask else None)
+    st = lib.dflash_ddtree_build(_stream_ptr(stream), n, L, kc, budget, _ptr(cand_tok), _ptr(cand_logp),
+                                 _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["logp"]),
+                                 _ptr(out["n_nodes"]), _ptr(out["mask"]))
+    if st != _ffi.OK:
+        raise DFlashError(st, "dflash_ddtree_build failed")
+    return out
+
+
+def ddtree_walk(tree, L, target_next, stream=None):
+    """Greedy verifier walk (dflash_ddtree_walk); returns (accept_len, out_tokens, next_anchor)."""
+    lib = library()
+    n, budget = tree["tok"].shape
+    dev = tree["tok"].device
+    acc = torch.empty((n,), dtype=torch.int32, device=dev)
+    toks = torch.empty((n, L + 1), dtype=torch.int32, device=dev)
+    nxt = torch.empty((n,), dtype=torch.int32, device=dev)
+    st = lib.dflash_ddtree_walk(_stream_ptr(stream), n, L, budget, _ptr(tree["tok"]), _ptr(tree["parent"]),
+                                _ptr(tree["n_nodes"]), _ptr(target_next), _ptr(acc), _ptr(toks), _ptr(nxt))
+    if st != _ffi.OK:
+        raise DFlashError(st, "dflash_ddtree_walk failed")
+    return acc, toks, nxt
 
 
 def dflash_release(ctx: Context, req_id):

@@ -168,6 +168,7 @@ struct GemmDesc {
   // applied before ranking (out_xf = 0: untouched)
   int out_xf;
   float out_mult, out_cap;
+  float2 *lse_part;              // EPI_TOPK: [tiles][M] (max, sum exp) of each tile column, or null
 };
 
 __device__ __forceinline__ float logit_xform(float x, float mult, float cap) {

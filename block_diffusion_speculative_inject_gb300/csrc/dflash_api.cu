@@ -88,6 +88,7 @@ struct dflash_ctx {
   void *xn = nullptr, *ao = nullptr, *hmid = nullptr, *xf = nullptr;
   float *logits = nullptr, *part_o = nullptr, *part_ml = nullptr;
   int2 *cand = nullptr;    // LM-head per-tile top-k candidates [V/128][rows][topk]
+  float2 *lse_part = nullptr;   // LM-head per-tile (max, sum exp) of each row [V/128][rows]
   int rows_max = 0, rows_k_max = 0;
   // injection scratch
   float *fc_out = nullptr, *kvproj = nullptr;
@@ -365,7 +366,8 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 // ------------------------------------------------------------------------------ create / destroy
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
-                 c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p};
+                 c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
+                 c->lse_part};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -455,6 +457,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {&c->xf, (size_t)RK * m.H * f4},
       {(void **)&c->logits, (size_t)RK * m.V * f4},
       {(void **)&c->cand, (size_t)((m.V + 127) / 128) * RK * m.topk * sizeof(int2)},
+      {(void **)&c->lse_part, (size_t)((m.V + 127) / 128) * RK * sizeof(float2)},
       {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * f4},
       {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * f4},
       {(void **)&c->fc_out, (size_t)C * m.H * f4},
@@ -848,6 +851,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     add_wseg(lm, c->w.lm_head, m.V);
     lm.topk = m.topk;
     lm.cand = c->cand;
+    lm.lse_part = c->lse_part;
     lm.out_xf = m.out_mult != 1.f || m.softcap > 0.f;
     lm.out_mult = m.out_mult;
     lm.out_cap = m.softcap;
@@ -922,10 +926,9 @@ static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt
   return draft_layers(c, B, bt, 0, 0, nullptr, s);
 }
 
-extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t n_req,
-                                           const int32_t *req_ids, const int32_t *anchors,
-                                           int32_t *argmax, int32_t *topk_idx, float *topk_val,
-                                           float *logits) {
+static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
+                                     const int32_t *req_ids, const int32_t *anchors, int32_t *argmax,
+                                     int32_t *topk_idx, float *topk_val, float *logits, float *lse) {
   if (!c) return DFLASH_ERR_INVALID_ARG;
   dflash_status st = check_device_flag(c);
   if (st != DFLASH_OK) return st;
@@ -1004,15 +1007,29 @@ extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t 
   if (fused_topk(c, RK)) {
     const int tiles = (m.V + 127) / 128;
     CK(c, timed(c, K_TOPK, s, 8.0 * tiles * RK * m.topk, 1.0 * tiles * RK * m.topk, 1, [&] {
-         return launch_topk_merge(tiles, RK, m.topk, c->cand, argmax, topk_idx, topk_val, s);
+         return launch_topk_merge(tiles, RK, m.topk, c->cand, argmax, topk_idx, topk_val, c->lse_part, lse, s);
        }));
   } else {
     float *lg = logits ? logits : c->logits;
     CK(c, timed(c, K_TOPK, s, 4.0 * RK * m.V, 1.0 * RK * m.V, 1, [&] {
-         return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, 0, s);
+         return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, lse, 0, s);
        }));
   }
   return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_draft_step(dflash_ctx *c, void *stream, int32_t n_req,
+                                           const int32_t *req_ids, const int32_t *anchors,
+                                           int32_t *argmax, int32_t *topk_idx, float *topk_val,
+                                           float *logits) {
+  return draft_step_impl(c, stream, n_req, req_ids, anchors, argmax, topk_idx, topk_val, logits, nullptr);
+}
+
+extern "C" dflash_status dflash_draft_step_lse(dflash_ctx *c, void *stream, int32_t n_req,
+                                               const int32_t *req_ids, const int32_t *anchors,
+                                               int32_t *argmax, int32_t *topk_idx, float *topk_val,
+                                               float *logits, float *lse) {
+  return draft_step_impl(c, stream, n_req, req_ids, anchors, argmax, topk_idx, topk_val, logits, lse);
 }
 
 // ------------------------------------------------------------------------------ verify / export

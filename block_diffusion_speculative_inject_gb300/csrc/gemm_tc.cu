@@ -65,6 +65,7 @@ struct TcParams {
   int ldo;
   int out_xf;                         // EPI_TOPK: logit scale / soft cap
   float out_mult, out_cap;
+  float2 *lse_part;                   // EPI_TOPK: per (tile, token) (max, sum exp) or null
   int *err;
 };
 
@@ -151,6 +152,18 @@ __device__ __forceinline__ void warp_tile_topk_multi(float (&v)[T][4], int (&id)
       if (lane == 0 && out[t]) out[t][rr] = make_int2(__float_as_int(wv[t]), wi[t]);
     }
   }
+}
+
+// Softmax normaliser partial of one tile column held as 4 values per lane (-inf outside the
+// tile): (max, sum exp(v - max)), written by lane 0 to *out when out is non-null.
+__device__ __forceinline__ void warp_tile_lse(const float (&v)[4], int lane, float2 *out) {
+  float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+  mx = warp_max(mx);
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s += v[j] == -INFINITY ? 0.f : expf(v[j] - mx);
+  s = warp_sum(s);
+  if (lane == 0 && out) *out = make_float2(mx, s);
 }
 
 // ------------------------------------------------------------------------- the kernel
@@ -350,6 +363,13 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
               id[t][j] = n0 + lane + 32 * j;
             }
           }
+          if (p.lse_part) {
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+              const int c = warp - 2 + 4 * (t0 + t), m = m0 + c;
+              warp_tile_lse(v[t], lane, out[t] ? p.lse_part + (size_t)blockIdx.y * p.M + m : nullptr);
+            }
+          }
           warp_tile_topk_multi<T>(v, id, p.topk, lane, out);
         }
       } else {
@@ -363,6 +383,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             v[j] = tile[c * TP + lane + 32 * j];
             id[j] = n0 + lane + 32 * j;
           }
+          if (p.lse_part) warp_tile_lse(v, lane, p.lse_part + (size_t)blockIdx.y * p.M + m);
           warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk);
         }
       }
@@ -436,6 +457,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
               id[j] = n;
               if (n < p.N && p.y) p.y[(size_t)m * p.ldy + n] = x[j];
             }
+            if (p.lse_part) warp_tile_lse(v, lane, p.lse_part + (size_t)blockIdx.y * p.M + m);
             warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk);
             continue;
           }
@@ -677,6 +699,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.out = d.out;
   p.ldo = d.ldo;
   p.out_xf = d.out_xf;
+  p.lse_part = d.lse_part;
   p.out_mult = d.out_mult;
   p.out_cap = d.out_cap;
   p.err = t->err;

@@ -133,12 +133,46 @@ __device__ __forceinline__ void block_merge(float (&lv)[TK], int (&li)[TK], int 
 
 constexpr int ROWS_CAP = 2048;   // gathered candidates per row before falling back
 
+// Online softmax normaliser: (m, s) stands for s * exp(m); merging keeps the larger max.
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float M = fmaxf(m, m2);
+  s = s * expf(m - M) + s2 * expf(m2 - M);
+  m = M;
+}
+
+// The block's log(sum exp): every thread holds a partial (m, s); the result (m + log s) is
+// returned to all threads. scratch: 2 * (TK_THREADS / 32) floats of shared memory.
+__device__ __forceinline__ float block_lse(float m, float s, float *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    scratch[2 * warp] = m;
+    scratch[2 * warp + 1] = s;
+  }
+  __syncthreads();
+  float M = -INFINITY, S = 0.f;
+  for (int w = 0; w < TK_THREADS / 32; ++w) lse_merge(M, S, scratch[2 * w], scratch[2 * w + 1]);
+  return M + logf(S);
+}
+
 // The body of the row selection for one row x[V], run by the whole CTA; the shared scratch
 // (tmax, pool, n_pool, thr) is the caller's. Writes argmax_out[0] (if non-null) and the
 // sorted best k to idx_out / val_out (if non-null); they may point to shared memory.
 __device__ __forceinline__ void row_select(const float *x, int V, int k, float *tmax, int2 *pool,
                                            int *n_pool, float *thr, int32_t *argmax_out,
-                                           int32_t *idx_out, float *val_out) {
+                                           int32_t *idx_out, float *val_out, float *lse_out = nullptr,
+                                           float *lse_scratch = nullptr) {
   const bool vec = (V & 3) == 0 && ((uintptr_t)x & 15u) == 0;
   const int n4 = V / 4;
   const float4 *x4 = (const float4 *)x;
@@ -166,9 +200,24 @@ __device__ __forceinline__ void row_select(const float *x, int V, int k, float *
       for (int i = threadIdx.x; i < V; i += TK_THREADS) visit(x[i], i);
     }
   };
-  // pass 1: per-thread maximum
+  // pass 1: per-thread maximum (and, when asked, the running softmax normaliser)
   float mv = -INFINITY;
-  scan([&](float v, int) { mv = fmaxf(mv, v); });
+  if (lse_out) {
+    float s = 0.f;
+    scan([&](float v, int) {
+      if (v == -INFINITY) return;
+      if (v > mv) {
+        s = (mv == -INFINITY ? 0.f : s * expf(mv - v)) + 1.f;
+        mv = v;
+      } else {
+        s += expf(v - mv);
+      }
+    });
+    const float l = block_lse(mv, s, lse_scratch);
+    if (threadIdx.x == 0) *lse_out = l;
+  } else {
+    scan([&](float v, int) { mv = fmaxf(mv, v); });
+  }
   tmax[threadIdx.x] = mv;
   if (threadIdx.x == 0) *n_pool = 0;
   __syncthreads();
@@ -222,16 +271,18 @@ __device__ __forceinline__ void row_select(const float *x, int V, int k, float *
 // rows b, b + gridDim.x, ...
 __global__ void __launch_bounds__(TK_THREADS, 2) k_topk_rows(int rows, int V, int k, const float *logits,
                                                           int32_t *argmax, int32_t *topk_idx,
-                                                          float *topk_val) {
+                                                          float *topk_val, float *lse) {
   pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
   __shared__ float tmax[TK_THREADS];
   __shared__ int2 pool[ROWS_CAP];
   __shared__ int n_pool;
   __shared__ float thr;
+  __shared__ float lse_scratch[2 * (TK_THREADS / 32)];
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     row_select(logits + (size_t)row * V, V, k, tmax, pool, &n_pool, &thr, argmax + row,
-               topk_idx ? topk_idx + (size_t)row * k : nullptr, topk_val ? topk_val + (size_t)row * k : nullptr);
+               topk_idx ? topk_idx + (size_t)row * k : nullptr, topk_val ? topk_val + (size_t)row * k : nullptr,
+               lse ? lse + row : nullptr, lse_scratch);
     __syncthreads();                   // the shared scratch is reused by the next row
   }
 }
@@ -251,13 +302,25 @@ constexpr int MERGE_TILES = MERGE_PER_THREAD * TK_THREADS;
 
 __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, int k,
                                                            const int2 *cand, int32_t *argmax,
-                                                           int32_t *topk_idx, float *topk_val) {
+                                                           int32_t *topk_idx, float *topk_val,
+                                                           const float2 *lse_part, float *lse) {
   pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
   __shared__ int2 pool[MERGE_CAP];
   __shared__ int n_pool;
   __shared__ float warp_best[TK_THREADS / 32][TK];
   __shared__ float thr;
+  __shared__ float lse_scratch[2 * (TK_THREADS / 32)];
+  if (lse) {
+    // the row's softmax normaliser from the tiles' (max, sum exp) partials
+    float m = -INFINITY, sum = 0.f;
+    for (int t = threadIdx.x; t < tiles; t += TK_THREADS) {
+      const float2 pt = lse_part[(size_t)t * rows + blockIdx.x];
+      lse_merge(m, sum, pt.x, pt.y);
+    }
+    const float l = block_lse(m, sum, lse_scratch);
+    if (threadIdx.x == 0) lse[blockIdx.x] = l;
+  }
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto at = [&](int t, int j) { return cand[((size_t)t * rows + row) * k + j]; };
@@ -369,20 +432,21 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_merge(int tiles, int rows, 
 }
 
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
-                        int32_t *topk_idx, float *topk_val, int max_ctas, cudaStream_t s) {
+                        int32_t *topk_idx, float *topk_val, float *lse, int max_ctas, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
   const int g = max_ctas > 0 ? std::min(rows, max_ctas) : rows;
   return launch_pdl(k_topk_rows, dim3(g), dim3(TK_THREADS), 0, s, rows, V, k, logits, argmax, topk_idx,
-                    topk_val);
+                    topk_val, lse);
 }
 
 cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
-                              int32_t *topk_idx, float *topk_val, cudaStream_t s) {
+                              int32_t *topk_idx, float *topk_val, const float2 *lse_part, float *lse,
+                              cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (k < 1 || k > TK) return cudaErrorInvalidValue;
   return launch_pdl(k_topk_merge, dim3(rows), dim3(TK_THREADS), 0, s, tiles, rows, k, cand, argmax,
-                    topk_idx, topk_val);
+                    topk_idx, topk_val, lse_part, lse);
 }
 
 // ------------------------------------------------------------------------- sampling mode
@@ -631,7 +695,8 @@ extern "C" dflash_status dflash_topk_noalloc(void *stream, int32_t rows, int32_t
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_pdl(k_topk_chunks, dim3((unsigned)chunks, (unsigned)rows), dim3(TK_THREADS), 0, s,
                              (int)vocab, (int)k, (int)chunks, (int)rows, logits, scratch);
-  if (e == cudaSuccess) e = launch_topk_merge((int)chunks, rows, k, scratch, argmax, topk_idx, topk_val, s);
+  if (e == cudaSuccess)
+    e = launch_topk_merge((int)chunks, rows, k, scratch, argmax, topk_idx, topk_val, nullptr, nullptr, s);
   if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, cudaGetErrorString(e));
   return DFLASH_OK;
 }

@@ -65,13 +65,16 @@ cudaError_t launch_verify_sample(int B, int K, const int32_t *ptok, const float 
 cudaError_t launch_logit_xform(long n, float mult, float cap, float *logits, cudaStream_t s);
 
 // Row-wise top-k (values descending, ties to the lower index) of fp32 logits [rows, V], on at
-// most max_ctas CTAs (<= 0: one per row) that loop over the rows.
+// most max_ctas CTAs (<= 0: one per row) that loop over the rows; lse [rows] (or null) gets
+// each row's log(sum exp).
 cudaError_t launch_topk(int rows, int V, int k, const float *logits, int32_t *argmax,
-                        int32_t *topk_idx, float *topk_val, int max_ctas, cudaStream_t s);
+                        int32_t *topk_idx, float *topk_val, float *lse, int max_ctas, cudaStream_t s);
 
-// Merge of the per-tile candidates [tiles][rows][k] of the tensor-core LM-head epilogue.
+// Merge of the per-tile candidates [tiles][rows][k] of the tensor-core LM-head epilogue; with
+// lse non-null also each row's log(sum exp) from the tiles' (max, sum exp) partials.
 cudaError_t launch_topk_merge(int tiles, int rows, int k, const int2 *cand, int32_t *argmax,
-                              int32_t *topk_idx, float *topk_val, cudaStream_t s);
+                              int32_t *topk_idx, float *topk_val, const float2 *lse_part, float *lse,
+                              cudaStream_t s);
 
 // GEMM post-ops over split-K partials ws[S][M][N] (see k_post.cu).
 cudaError_t launch_post_qkv(int dtype, const ModelDims &m, int B, const float *ws, int S, float *qkv,

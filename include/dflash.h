@@ -167,6 +167,15 @@ dflash_status dflash_draft_step(dflash_ctx *ctx, void *stream, int32_t n_req,
                                 int32_t *argmax, int32_t *topk_idx, float *topk_val,
                                 float *logits);
 
+/* dflash_draft_step that also writes lse [n_req, K] fp32 DEVICE (NULL: not written): the
+ * log of the softmax normaliser of each mask row's logits, log sum_v exp(logits[v]), so that
+ * topk_val - lse are the draft's full-vocabulary log-probabilities of its candidates (the
+ * input of a draft tree, "DDTree" §2.3). Computed in fp32. */
+dflash_status dflash_draft_step_lse(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                    const int32_t *req_ids, const int32_t *anchors,
+                                    int32_t *argmax, int32_t *topk_idx, float *topk_val,
+                                    float *logits, float *lse);
+
 /* Greedy verification ("DFlash 2 块扩散投机解码技术详解" §2.3): for each of n_req rows,
  *   draft  [n_req, K] int32 DEVICE, target [n_req, K+1] int32 DEVICE (the target's token
  *   after the anchor and after each draft), outputs (DEVICE):
@@ -217,6 +226,36 @@ dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
                                    const float *draft_logits, const int32_t *draft,
                                    const float *u_accept, const float *u_resample,
                                    int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor);
+
+/* Draft trees ("DDTree" §2.3 Algorithm 1 / Proposition 2, §3.3 ancestor-only mask, §3.5
+ * the verifier walk). No context needed; all pointers DEVICE, row-major.
+ * dflash_ddtree_build: per request, L block positions with kc candidates each, best first:
+ *   cand_tok [n_req, L, kc] int32 and cand_logp [n_req, L, kc] fp32 (log-probabilities,
+ *   e.g. topk_val - lse of dflash_draft_step_lse). The `budget` most likely prefixes (a
+ *   prefix takes one candidate at each of positions 1..d; its log-probability is the sum)
+ *   are popped best-first from a max-heap seeded with the best candidate of position 1,
+ *   each pop pushing the next sibling and the first child; ties pop by (log-probability
+ *   desc, depth asc, parent asc, rank asc). With kc >= min(budget, V) the tree is the
+ *   optimal one; with fewer candidates it is the best tree over those candidates.
+ *   Outputs [n_req, budget] in pop order: tree_tok, tree_parent (-1: child of the root, the
+ *   anchor), tree_depth (1..L), tree_logp; n_nodes [n_req] (fewer than budget only when the
+ *   candidates run out; unused slots hold token -1); mask [n_req, budget+1, W] uint32 or
+ *   NULL, W = ceil((budget+1)/32): row i (0 = the root, node j = row j+1) has bit j set when
+ *   index j is the root, an ancestor of i, or i itself.
+ *   Limits: 1 <= L <= 31, 1 <= kc <= 32, 1 <= budget <= 1024; else DFLASH_ERR_INVALID_ARG.
+ * dflash_ddtree_walk: greedy verification of built trees; target_next [n_req, budget+1]
+ *   int32 is the target's token after the root (index 0) and after node j (index j+1).
+ *   From the root, the walk moves to the child whose token equals the target's next token
+ *   while one exists. Outputs accept_len [n_req], out_tokens [n_req, L+1] (the accepted
+ *   tokens, then the target's token where the walk stopped, then -1), next_anchor [n_req]. */
+dflash_status dflash_ddtree_build(void *stream, int32_t n_req, int32_t L, int32_t kc, int32_t budget,
+                                  const int32_t *cand_tok, const float *cand_logp, int32_t *tree_tok,
+                                  int32_t *tree_parent, int32_t *tree_depth, float *tree_logp,
+                                  int32_t *n_nodes, uint32_t *mask);
+dflash_status dflash_ddtree_walk(void *stream, int32_t n_req, int32_t L, int32_t budget,
+                                 const int32_t *tree_tok, const int32_t *tree_parent,
+                                 const int32_t *n_nodes, const int32_t *target_next,
+                                 int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor);
 
 /* Forgets a request and returns its pages to the pool (host only). Work already
  * enqueued that reads those pages must precede any later call in stream order. */
