@@ -215,6 +215,7 @@ class StepLoop:
         self.lens = list(wl.ctx)
         self.records = []
         self.sampling = None
+        self.tree_budget = 0
 
     def enable_sampling(self, temperature, top_k, top_p, steps, seed=7):
         """Sampling-mode verification: the drafts are drawn from the draft's logits and checked
@@ -228,6 +229,30 @@ class StepLoop:
         self.u_draft = torch.rand((steps, B * K), generator=g, device=dev)
         self.u_acc = torch.rand((steps, B, K), generator=g, device=dev)
         self.u_res = torch.rand((steps, B), generator=g, device=dev)
+
+    def enable_tree(self, budget, steps, seed=9):
+        """Tree mode: a best-first draft tree of `budget` nodes per request from its top-k
+        (topk_val with the softmax normaliser lse subtracted in the tree kernel), with the
+        ancestor-only mask, walked greedily against synthetic target tokens (uniform over the
+        vocabulary, like the greedy mode's targets on these workloads)."""
+        B, dev = self.wl.B, self.device
+        g = torch.Generator().manual_seed(seed)
+        self.tree_budget = budget
+        self.lse = torch.empty((B, self.cfg.block_k), dtype=torch.float32, device=dev)
+        self.tree_next_h = [torch.randint(0, self.cfg.vocab, (B, budget + 1), generator=g,
+                                          dtype=torch.int32).pin_memory() for _ in range(steps)]
+        self.tree_next = [t.to(dev) for t in self.tree_next_h]
+
+    def _verify_tree(self, s, target_next=None):
+        from block_diffusion_speculative_inject_gb300 import ddtree_build, ddtree_walk
+        out = self.out
+        tree = ddtree_build(out["topk_idx"], out["topk_val"], self.tree_budget, with_mask=True, lse=self.lse)
+        tn = self.tree_next[s] if target_next is None else target_next
+        self.tree = tree
+        acc, toks, anchor = ddtree_walk(tree, self.cfg.block_k, tn)
+        out["acc"].copy_(acc)
+        out["toks"].copy_(toks)
+        out["nxt"].copy_(anchor)
 
     def _verify_sampling(self, s, target_logits=None):
         ctx, out, (T, k, tp) = self.ctx, self.out, self.sampling
@@ -246,9 +271,12 @@ class StepLoop:
             ctx.inject(wl.reqs, wl.n_new[s], feats)
             ctx.draft(wl.reqs, wl.anchors_d[s] if anchors is None else anchors, argmax=out["argmax"],
                       topk_idx=out["topk_idx"], topk_val=out["topk_val"],
-                      logits=self.logits if self.sampling else None)
+                      logits=self.logits if self.sampling else None,
+                      lse=self.lse if self.tree_budget else None)
             if self.sampling:
                 self._verify_sampling(s, targets)
+            elif self.tree_budget:
+                self._verify_tree(s, targets)
             else:
                 ctx.verify(out["argmax"], wl.targets_d[s] if targets is None else targets,
                            out["acc"], out["toks"], out["nxt"])
@@ -299,10 +327,12 @@ def run_ours(args):
     ctx, w_cpu = _make_context(cfg, wl, device, n_steps)
     _prefill(ctx, cfg, wl)
     loop = StepLoop(ctx, cfg, wl, device)
+    if args.verify != "greedy" and cfg.verify_driven:
+        raise SystemExit(f"--verify {args.verify} runs on the steady workloads")
     if args.verify == "sample":
-        if cfg.verify_driven:
-            raise SystemExit("--verify sample runs on the steady workloads")
         loop.enable_sampling(args.temperature, args.top_k, args.top_p, n_steps)
+    elif args.verify == "tree":
+        loop.enable_tree(args.budget, n_steps)
     B, K = wl.B, cfg.block_k
     stream = torch.cuda.current_stream()
     for s in range(W):
@@ -324,6 +354,8 @@ def run_ours(args):
         torch.cuda.synchronize()
     _barrier(ws)
     launches = ctx.launch_count() - launches0
+    if loop.tree_budget:
+        launches += 2 * K_          # the tree build and walk take no context and are not counted by it
     ms = e0.elapsed_time(e1)
     ms_max = _max_over_ranks(ws, ms, device)
     records = list(loop.records)
@@ -375,6 +407,10 @@ def run_ours(args):
                 tl_d.copy_(tl_h[s % 2], non_blocking=True)
                 h2d += tl_d.numel() * 4
                 tgt_d = tl_d
+            elif loop.tree_budget:
+                tgt_d = torch.empty_like(loop.tree_next[s])
+                tgt_d.copy_(loop.tree_next_h[s], non_blocking=True)
+                h2d += tgt_d.numel() * 4
             else:
                 tgt_d.copy_(wl.targets_h[s], non_blocking=True)
                 h2d += wl.targets_h[s].numel() * 4
@@ -438,7 +474,9 @@ def run_ours(args):
                    "parallelism": f"{ws} independent replica(s)",
                    "verify": ("greedy prefix match" if args.verify == "greedy" else
                               f"rejection sampling (temperature {args.temperature}, top_k {args.top_k}, "
-                              f"top_p {args.top_p}) against synthetic target logits"),
+                              f"top_p {args.top_p}) against synthetic target logits" if args.verify == "sample"
+                              else f"draft tree of {args.budget} nodes from the top-k, greedy walk against "
+                                   "synthetic target tokens"),
                    **({"overrides": over} if over else {})},
         "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches,
@@ -553,8 +591,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--verify", default="greedy", choices=["greedy", "sample"],
-                    help="greedy prefix match, or rejection sampling against synthetic target logits")
+    ap.add_argument("--verify", default="greedy", choices=["greedy", "sample", "tree"],
+                    help="greedy prefix match, rejection sampling against synthetic target logits, "
+                         "or a best-first draft tree walked against synthetic target tokens")
+    ap.add_argument("--budget", type=int, default=64, help="draft-tree nodes per request (--verify tree)")
     ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--top-k", type=int, default=20)
     ap.add_argument("--top-p", type=float, default=0.95)

@@ -282,9 +282,10 @@ def dflash_verify_sample(ctx: Context, target_logits, draft_logits, draft, u_acc
                              top_k, top_p, accept_len, out_tokens, next_anchor, stream=stream)
 
 
-def ddtree_build(cand_tok, cand_logp, budget, with_mask=True, stream=None):
+def ddtree_build(cand_tok, cand_logp, budget, with_mask=True, stream=None, lse=None):
     """Best-first draft trees (dflash_ddtree_build) from candidates [n, L, kc] (int32 tokens,
-    fp32 log-probabilities, best first). Returns a dict of device tensors."""
+    fp32 values, best first): log-probabilities, or logits when lse [n, L] (the rows'
+    normalisers, subtracted in the kernel) is given. Returns a dict of device tensors."""
     lib = library()
     n, L, kc = cand_tok.shape
     dev = cand_tok.device
@@ -296,7 +297,7 @@ def ddtree_build(cand_tok, cand_logp, budget, with_mask=True, stream=None):
     words = (budget + 1 + 31) // 32
     out["mask"] = (torch.empty((n, budget + 1, words), dtype=torch.int32, device=dev) if with_mask else None)
     st = lib.dflash_ddtree_build(_stream_ptr(stream), n, L, kc, budget, _ptr(cand_tok), _ptr(cand_logp),
-                                 _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["logp"]),
+                                 _ptr(lse), _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["logp"]),
                                  _ptr(out["n_nodes"]), _ptr(out["mask"]))
     if st != _ffi.OK:
         raise DFlashError(st, "dflash_ddtree_build failed")

@@ -48,7 +48,7 @@ SIGNATURES = {
     "dflash_verify_greedy": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     "dflash_sample_tokens": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
     "dflash_draft_step_lse": (_I32, [_P, _P, _I32, _I32P, _P, _P, _P, _P, _P, _P]),
-    "dflash_ddtree_build": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dflash_ddtree_build": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_ddtree_walk": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_verify_sample": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_release": (_I32, [_P, _I32]),

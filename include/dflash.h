@@ -230,8 +230,9 @@ dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
 /* Draft trees ("DDTree" §2.3 Algorithm 1 / Proposition 2, §3.3 ancestor-only mask, §3.5
  * the verifier walk). No context needed; all pointers DEVICE, row-major.
  * dflash_ddtree_build: per request, L block positions with kc candidates each, best first:
- *   cand_tok [n_req, L, kc] int32 and cand_logp [n_req, L, kc] fp32 (log-probabilities,
- *   e.g. topk_val - lse of dflash_draft_step_lse). The `budget` most likely prefixes (a
+ *   cand_tok [n_req, L, kc] int32 and cand_logp [n_req, L, kc] fp32; cand_lse is NULL
+ *   (cand_logp are log-probabilities) or [n_req, L] fp32 row normalisers subtracted from
+ *   cand_logp (cand_logp = topk_val and cand_lse = lse of dflash_draft_step_lse). The `budget` most likely prefixes (a
  *   prefix takes one candidate at each of positions 1..d; its log-probability is the sum)
  *   are popped best-first from a max-heap seeded with the best candidate of position 1,
  *   each pop pushing the next sibling and the first child; ties pop by (log-probability
@@ -249,7 +250,8 @@ dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
  *   while one exists. Outputs accept_len [n_req], out_tokens [n_req, L+1] (the accepted
  *   tokens, then the target's token where the walk stopped, then -1), next_anchor [n_req]. */
 dflash_status dflash_ddtree_build(void *stream, int32_t n_req, int32_t L, int32_t kc, int32_t budget,
-                                  const int32_t *cand_tok, const float *cand_logp, int32_t *tree_tok,
+                                  const int32_t *cand_tok, const float *cand_logp, const float *cand_lse,
+                                  int32_t *tree_tok,
                                   int32_t *tree_parent, int32_t *tree_depth, float *tree_logp,
                                   int32_t *n_nodes, uint32_t *mask);
 dflash_status dflash_ddtree_walk(void *stream, int32_t n_req, int32_t L, int32_t budget,

@@ -28,14 +28,21 @@ def _grid_candidates(rng, n, L, kc):
     return lp.astype(np.float32), tok.astype(np.int32)
 
 
-@pytest.mark.parametrize("L,kc,budget", [(1, 4, 10), (7, 1, 5), (7, 4, 1), (7, 16, 64), (15, 32, 300),
-                                         (15, 8, 1024), (31, 3, 200)])
-def test_ddtree_build_matches_oracle(L, kc, budget):
+@pytest.mark.parametrize("L,kc,budget,with_lse", [(1, 4, 10, 0), (7, 1, 5, 0), (7, 4, 1, 1), (7, 16, 64, 0),
+                                                  (15, 32, 300, 1), (15, 8, 1024, 0), (31, 3, 200, 1)])
+def test_ddtree_build_matches_oracle(L, kc, budget, with_lse):
+    """with_lse: the kernel gets logits (log-probabilities plus a per-row offset on the same
+    grid) and the offsets as the rows' normalisers, so it must recover the same values."""
     from block_diffusion_speculative_inject_gb300 import ddtree_build
     rng = np.random.default_rng(L * 1000 + kc * 10 + budget)
     n = 5
     lp, tok = _grid_candidates(rng, n, L, kc)
-    out = ddtree_build(torch.from_numpy(tok).cuda(), torch.from_numpy(lp).cuda(), budget)
+    if with_lse:
+        off = (rng.integers(-64 * 8, 64 * 8, (n, L)) / 64.0).astype(np.float32)
+        out = ddtree_build(torch.from_numpy(tok).cuda(), torch.from_numpy(lp + off[..., None]).cuda(), budget,
+                           lse=torch.from_numpy(off).cuda())
+    else:
+        out = ddtree_build(torch.from_numpy(tok).cuda(), torch.from_numpy(lp).cuda(), budget)
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in out.items()}
     words = (budget + 1 + 31) // 32
@@ -100,6 +107,10 @@ def test_draft_lse_and_tree_from_draft(name, lens):
     budget = 48
     tree = ddtree_build(out["topk_idx"], lp, budget, with_mask=False)
     g_tok, g_lp = tree["tok"].cpu().numpy(), tree["logp"].cpu().numpy()
+    # the normaliser subtracted in the kernel: the same fp32 subtraction, the same tree
+    tree2 = ddtree_build(out["topk_idx"], out["topk_val"], budget, with_mask=False, lse=out["lse"])
+    for key in ("tok", "parent", "depth", "logp", "n_nodes"):
+        assert torch.equal(tree[key], tree2[key]), key
     lp_np = lp.cpu().numpy().astype(np.float64)
     ti = out["topk_idx"].cpu().numpy()
     for i in range(B):
