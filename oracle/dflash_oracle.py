@@ -41,6 +41,18 @@ Readings where the pages leave a step open (each is also listed in the design no
     fp32 (or an exact bf16 hi+lo pair as a tensor-core operand) on the GPU. Argmax and
     top-k are decided on the logits rounded to fp32, ties to the lowest index.
   * top-k: k values sorted descending, indices tie-broken by lowest index.
+  * DFlash 2 local convolution ([P2] §3.2.3), off by default: four two-tap dynamic depthwise
+    convolutions per layer — on the attention input (after the input norm), on the attention
+    output (after the output projection, before the residual add), on the MLP input (after
+    the post-attention norm) and on the MLP output (before the residual add). Over the K+1
+    block rows of one request, y_t = k_t0 * x_t + k_t1 * x_{t-1} with x_{-1} = 0; the taps
+    are k_ti[c] = base[i][c] + (P x_t)[i*G + c // 16], P [2G, H], G = H / 16 (the correction
+    is computed from the convolution's own input row and shared by 16 channels).
+  * DFlash 2 path selector ([P2] §3.1), off by default: over each mask position's top-k
+    candidates, S_t(a, b) = U_t(b) + <A(a) * g_t, B(b)>, U_t = the draft's logits, A / B the
+    predecessor / successor codebooks [V, r], g_t = W_h h_t with h_t the final-normed hidden
+    row of mask position t; a greedy walk from the anchor takes the best-scoring candidate
+    at each position (the first in candidate order among equal scores).
   * Sampling mode ([P2] §2.3, §3.3, §4.2): both the draft and the target distribution go
     through the same truncation — logits / temperature, keep the top_k largest (ties to
     the lower index), softmax over those, then keep the shortest prefix of them in
@@ -61,6 +73,7 @@ __all__ = [
     "accept_prob", "residual_dist", "sample_index", "verify_sample", "as_fraction_dist",
     "sampling_probs", "sample_token", "verify_sample_logits",
     "log_softmax_norm", "ddtree_build", "ddtree_mask", "ddtree_walk",
+    "dyn_conv", "select_path",
 ]
 
 
@@ -217,7 +230,10 @@ class OracleDraft:
         c, lw = self.cfg, self.w["layers"][l]
         nq, nkv, hd = c.n_q_heads, c.n_kv_heads, c.head_dim
         q_rows = x.shape[0]
+        conv = getattr(c, "dyn_conv", 0)
         xn = rmsnorm(x, lw["in_norm"], c.rms_eps)
+        if conv:
+            xn = dyn_conv(xn, lw["conv_base"][0], lw["conv_proj"][0])
         q = (xn @ _f64(lw["wq"]).T).reshape(q_rows, nq, hd)
         k = (xn @ _f64(lw["wk"]).T).reshape(q_rows, nkv, hd)
         v = (xn @ _f64(lw["wv"]).T).reshape(q_rows, nkv, hd)
@@ -242,10 +258,18 @@ class OracleDraft:
                     s[j, n_ctx + j + 1:] = -np.inf
             o[:, h, :] = softmax(s, axis=-1) @ vals[:, kvh, :]
         o = o.reshape(q_rows, nq * hd)
-        x = x + o @ _f64(lw["wo"]).T
+        attn_out = o @ _f64(lw["wo"]).T
+        if conv:
+            attn_out = dyn_conv(attn_out, lw["conv_base"][1], lw["conv_proj"][1])
+        x = x + attn_out
         xn2 = rmsnorm(x, lw["post_norm"], c.rms_eps)
+        if conv:
+            xn2 = dyn_conv(xn2, lw["conv_base"][2], lw["conv_proj"][2])
         hmid = silu(xn2 @ _f64(lw["w_gate"]).T) * (xn2 @ _f64(lw["w_up"]).T)
-        return x + hmid @ _f64(lw["w_down"]).T
+        mlp_out = hmid @ _f64(lw["w_down"]).T
+        if conv:
+            mlp_out = dyn_conv(mlp_out, lw["conv_base"][3], lw["conv_proj"][3])
+        return x + mlp_out
 
     def hidden(self, req, anchor):
         """Final-normed hidden rows of the K mask positions, [K, H]."""
@@ -285,6 +309,16 @@ class OracleDraft:
         lg32 = f32_round(lg)
         idx, val = topk_desc(lg32, self.cfg.topk)
         return argmax_lowest(lg32), idx, val, lg
+
+    def select(self, req, anchor, cand_tok=None, unary=None):
+        """The path selector's walk ([P2] §3.1) for one request: (tokens [K], scores [K, k]).
+        Candidates and their unary scores default to this oracle's own top-k of the logits;
+        g_t comes from this oracle's final-normed hidden rows."""
+        if cand_tok is None:
+            _, cand_tok, unary, _ = self.draft(req, anchor)
+        gate = self.hidden(req, anchor) @ _f64(self.w["sel_hidden_proj"]).T      # [K, r]
+        return select_path(anchor, cand_tok, unary, gate, self.w["sel_pred_codebook"],
+                           self.w["sel_succ_codebook"])
 
 
 # ----------------------------------------------------------------------------- selection
@@ -498,3 +532,45 @@ def ddtree_walk(nodes, target_next):
             return len(out) - 1, out
         out.append(t)
         cur = child[0]
+
+
+# ----------------------------------------------------------------------------- DFlash 2 modules
+def dyn_conv(x, base, proj, group=16):
+    """Two-tap dynamic depthwise convolution over the rows of one block ([P2] §3.2.3):
+    y_t = k_t0 * x_t + k_t1 * x_{t-1}, the row before the first being zero. The taps are a
+    learned base per channel plus a correction computed from the input row by the linear
+    map `proj` [2G, H] (rows 0..G-1 tap 0, rows G..2G-1 tap 1), one value per group of
+    `group` channels: k_ti[c] = base[i][c] + (proj @ x_t)[i*G + c // group]."""
+    x = _f64(x)
+    base, proj = _f64(base), _f64(proj)
+    T, H = x.shape
+    G = H // group
+    corr = x @ proj.T                                      # [T, 2G]
+    y = np.empty_like(x)
+    for t in range(T):
+        k0 = base[0] + np.repeat(corr[t, :G], group)
+        k1 = base[1] + np.repeat(corr[t, G:], group)
+        prev = x[t - 1] if t > 0 else np.zeros(H)
+        y[t] = k0 * x[t] + k1 * prev
+    return y
+
+
+def select_path(anchor, cand_tok, unary, gate, pred_cb, succ_cb):
+    """Greedy walk of the path selector ([P2] §3.1) over K positions with k candidates each:
+    starting from the anchor as predecessor a, position t scores its candidates b by
+    S_t(a, b) = unary[t, b] + sum_r pred_cb[a, r] * gate[t, r] * succ_cb[b, r] and takes the
+    best (the first in candidate order among equal scores), which becomes the next
+    predecessor. Returns (tokens [K], scores [K, k])."""
+    cand_tok = np.asarray(cand_tok)
+    unary, gate = _f64(unary), _f64(gate)
+    K, k = cand_tok.shape
+    prev = int(anchor)
+    toks, scores = [], np.empty((K, k))
+    for t in range(K):
+        a = _f64(pred_cb[prev]) * gate[t]                             # [r]
+        for j in range(k):
+            scores[t, j] = unary[t, j] + float(a @ _f64(succ_cb[int(cand_tok[t, j])]))
+        best = int(np.argmax(scores[t]))                                # first maximum
+        prev = int(cand_tok[t, best])
+        toks.append(prev)
+    return np.array(toks, dtype=np.int64), scores

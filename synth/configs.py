@@ -50,6 +50,8 @@ class DraftConfig:
     output_multiplier: float = 1.0  # logits scale
     logit_softcap: float = 0.0      # > 0: logits = c * tanh(logits / c) after the scale
     mask_embedding: int = 0         # 1: a trained mask embedding replaces E[mask_id]
+    dyn_conv: int = 0               # 1: DFlash 2 two-tap dynamic convolutions in every layer
+    selector_rank: int = 0          # r > 0: DFlash 2 path selector with rank-r codebooks
     # workload
     batch: int = 1
     ctx_min: int = 64

@@ -18,6 +18,9 @@ mis-indexed norm weight changes the result):
   synthetic target ids:                         the given draft argmax with probability
                                                 accept_p, else uniform over [0, V);
                                                 the bonus position is uniform
+  dynamic convolutions (when configured):       base taps 0.5 + N(0, 0.1), correction
+                                                maps N(0, 0.005)
+  path selector (when configured):              codebooks N(0, 0.25), hidden map N(0, 0.02)
 """
 import hashlib
 from concurrent.futures import ThreadPoolExecutor
@@ -75,11 +78,26 @@ def weight_specs(cfg: DraftConfig):
             (f"L{i}.w_up", (I, H), _WEIGHT_STD, 0.0),
             (f"L{i}.w_down", (H, I), _WEIGHT_STD, 0.0),
         ]
+        if cfg.dyn_conv:
+            # four convolutions per layer: attention input / output, MLP input / output
+            specs += [
+                (f"L{i}.conv_base", (4, 2, H), _NORM_STD, 0.5),
+                (f"L{i}.conv_proj", (4, 2 * (H // 16), H), 0.005, 0.0),
+            ]
+    if cfg.selector_rank:
+        r = cfg.selector_rank
+        specs += [
+            ("sel_pred_codebook", (V, r), 0.25, 0.0),
+            ("sel_succ_codebook", (V, r), 0.25, 0.0),
+            ("sel_hidden_proj", (r, H), _WEIGHT_STD, 0.0),
+        ]
     return specs
 
 
 LAYER_KEYS = ("in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "post_norm",
               "w_gate", "w_up", "w_down")
+CONV_KEYS = ("conv_base", "conv_proj")
+SELECTOR_KEYS = ("sel_pred_codebook", "sel_succ_codebook", "sel_hidden_proj")
 
 
 def make_weights(cfg: DraftConfig, seed: int = 0, threads: int = 8):
@@ -94,7 +112,11 @@ def make_weights(cfg: DraftConfig, seed: int = 0, threads: int = 8):
     with ThreadPoolExecutor(max_workers=threads) as ex:
         flat = dict(ex.map(one, specs))
     w = {k: flat[k] for k in ("embed", "lm_head", "fc", "fc_norm", "final_norm")}
-    w["layers"] = [{k: flat[f"L{i}.{k}"] for k in LAYER_KEYS} for i in range(cfg.n_layers)]
+    keys = LAYER_KEYS + (CONV_KEYS if cfg.dyn_conv else ())
+    w["layers"] = [{k: flat[f"L{i}.{k}"] for k in keys} for i in range(cfg.n_layers)]
+    for k in SELECTOR_KEYS:
+        if k in flat:
+            w[k] = flat[k]
     if cfg.mask_embedding:
         w["mask_embedding"] = _normal((cfg.hidden,), 0.02, 0.0, dt, "weights", cfg.name, seed, "mask_embedding")
     return w

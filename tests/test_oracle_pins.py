@@ -706,3 +706,190 @@ def test_ddtree_walk_follows_the_target_down_the_tree():
             else:
                 break
         assert a == len(path) and out == list(path) + [t]
+
+
+# ----------------------------------------------------------------------------- DFlash 2 modules
+def _conv_weights(rng, H, n=4, tap0=1.0, tap1=0.4, std=0.05):
+    base = np.stack([np.stack([tap0 + rng.normal(0, 0.1, H), tap1 + rng.normal(0, 0.1, H)]) for _ in range(n)])
+    proj = rng.normal(0, std, (n, 2 * (H // 16), H))
+    return base, proj
+
+
+def test_dyn_conv_static_taps_match_torch_depthwise_conv1d():
+    """With no correction the convolution is a depthwise two-tap conv1d over the block rows
+    with zero padding in front (torch's conv1d is a cross-correlation: weight[c] = (tap 1,
+    tap 0))."""
+    rng = np.random.default_rng(70)
+    H, T = 64, 9
+    x = rng.normal(0, 1, (T, H))
+    base = rng.normal(0, 1, (2, H))
+    y = O.dyn_conv(x, base, np.zeros((2 * H // 16, H)))
+    inp = F.pad(torch.from_numpy(x.T[None]), (1, 0))                       # [1, H, T + 1]
+    wt = torch.from_numpy(np.stack([base[1], base[0]], axis=1)[:, None, :])  # [H, 1, 2]
+    want = F.conv1d(inp, wt, groups=H)[0].numpy().T
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("tap", [0, 1])
+def test_dyn_conv_correction_is_one_value_per_16_channels(tap):
+    """A single nonzero row g of the correction map (tap 0 or tap 1) changes exactly the 16
+    channels of group g, by (v . x_t) times x_t (tap 0) or x_{t-1} (tap 1)."""
+    rng = np.random.default_rng(71 + tap)
+    H, T, G, g = 64, 6, 4, 2
+    x = rng.normal(0, 1, (T, H))
+    v = rng.normal(0, 1, H)
+    proj = np.zeros((2 * G, H))
+    proj[tap * G + g] = v
+    y = O.dyn_conv(x, np.zeros((2, H)), proj)
+    src = x if tap == 0 else np.vstack([np.zeros((1, H)), x[:-1]])
+    want = np.zeros((T, H))
+    want[:, 16 * g:16 * g + 16] = (x @ v)[:, None] * src[:, 16 * g:16 * g + 16]
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_dyn_conv_row_depends_on_itself_and_the_row_before_only():
+    rng = np.random.default_rng(73)
+    H, T = 32, 7
+    x = rng.normal(0, 1, (T, H))
+    base, proj = rng.normal(0, 1, (2, H)), rng.normal(0, 0.1, (2 * H // 16, H))
+    y = O.dyn_conv(x, base, proj)
+    for j in range(T):
+        xp = x.copy()
+        xp[j] += rng.normal(0, 1, H)
+        d = np.abs(O.dyn_conv(xp, base, proj) - y).max(axis=1)
+        changed = {t for t in range(T) if d[t] > 0}
+        assert changed == ({j, j + 1} & set(range(T)))
+
+
+def _torch_conv(x, base, proj):
+    """The convolution from torch pieces: the static part through conv1d, the correction
+    expanded to channels through a 0/1 group matrix."""
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    X, H = t(x), x.shape[1]
+    G = H // 16
+    E = torch.kron(torch.eye(G, dtype=torch.float64), torch.ones((1, 16), dtype=torch.float64))  # [G, H]
+    corr = F.linear(X, t(proj))
+    k0 = t(base[0]) + corr[:, :G] @ E
+    k1 = t(base[1]) + corr[:, G:] @ E
+    prev = F.pad(X, (0, 0, 1, 0))[:-1]
+    return k0 * X + k1 * prev
+
+
+def test_conv_layer_places_four_convolutions():
+    """The conv layer equals a torch composition with a convolution on the attention input
+    (after the input norm), on the output projection's result, on the MLP input (after the
+    post-attention norm) and on the down projection's result; identity convolutions give
+    back the plain layer."""
+    c = _cfg(dyn_conv=1)
+    w = _weights(c, seed=74)
+    rng = np.random.default_rng(75)
+    for lw in w["layers"]:
+        lw["conv_base"], lw["conv_proj"] = _conv_weights(rng, c.hidden)
+    od = O.OracleDraft(c, w)
+    n_ctx = 19
+    x = rng.normal(0, 1, (c.block_k + 1, c.hidden))
+    ck = rng.normal(0, 1, (n_ctx, c.n_kv_heads, c.head_dim))
+    cv = rng.normal(0, 1, (n_ctx, c.n_kv_heads, c.head_dim))
+    pos = np.arange(n_ctx, n_ctx + c.block_k + 1)
+    lw = w["layers"][0]
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    n = x.shape[0]
+    X = t(x)
+    xn = _torch_conv(F.rms_norm(X, (c.hidden,), t(lw["in_norm"]), eps=c.rms_eps).numpy(),
+                     lw["conv_base"][0], lw["conv_proj"][0])
+    q = F.rms_norm(F.linear(xn, t(lw["wq"])).view(n, c.n_q_heads, c.head_dim), (c.head_dim,), t(lw["q_norm"]),
+                   eps=c.rms_eps)
+    k = F.rms_norm(F.linear(xn, t(lw["wk"])).view(n, c.n_kv_heads, c.head_dim), (c.head_dim,), t(lw["k_norm"]),
+                   eps=c.rms_eps)
+    v = F.linear(xn, t(lw["wv"])).view(n, c.n_kv_heads, c.head_dim)
+    q, k = t(O.rope(q.numpy(), pos, c.rope_theta)), t(O.rope(k.numpy(), pos, c.rope_theta))
+    keys = torch.cat([t(ck), k], 0).transpose(0, 1)
+    vals = torch.cat([t(cv), v], 0).transpose(0, 1)
+    o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], keys[None], vals[None], enable_gqa=True)[0]
+    o = F.linear(o.transpose(0, 1).reshape(n, -1), t(lw["wo"]))
+    X = X + _torch_conv(o.numpy(), lw["conv_base"][1], lw["conv_proj"][1])
+    xn2 = _torch_conv(F.rms_norm(X, (c.hidden,), t(lw["post_norm"]), eps=c.rms_eps).numpy(),
+                      lw["conv_base"][2], lw["conv_proj"][2])
+    h = F.silu(F.linear(xn2, t(lw["w_gate"]))) * F.linear(xn2, t(lw["w_up"]))
+    want = X + _torch_conv(F.linear(h, t(lw["w_down"])).numpy(), lw["conv_base"][3], lw["conv_proj"][3])
+    np.testing.assert_allclose(od.layer(x, 0, ck, cv, pos), want.numpy(), rtol=1e-10, atol=1e-11)
+    # identity convolutions: the plain layer
+    for lw in w["layers"]:
+        lw["conv_base"] = np.stack([np.stack([np.ones(c.hidden), np.zeros(c.hidden)])] * 4)
+        lw["conv_proj"] = np.zeros_like(lw["conv_proj"])
+    np.testing.assert_allclose(O.OracleDraft(c, w).layer(x, 0, ck, cv, pos),
+                               _torch_layer(c, w["layers"][0], x, ck, cv, pos), rtol=1e-10, atol=1e-11)
+
+
+def _sel_case(rng, K=5, k=4, V=40, r=8):
+    cand = np.stack([rng.permutation(V)[:k] for _ in range(K)])
+    unary = -np.sort(-rng.normal(0, 1, (K, k)), axis=1)
+    return cand, unary, rng.normal(0, 1, (K, r)), rng.normal(0, 1, (V, r)), rng.normal(0, 1, (V, r))
+
+
+def test_select_path_without_pair_scores_is_the_argmax_path():
+    rng = np.random.default_rng(80)
+    cand, unary, gate, A, B = _sel_case(rng)
+    for args in ((gate, np.zeros_like(A), B), (gate, A, np.zeros_like(B)), (np.zeros_like(gate), A, B)):
+        toks, _ = O.select_path(7, cand, unary, *args)
+        np.testing.assert_array_equal(toks, cand[:, 0])
+
+
+def test_select_path_follows_a_planted_chain():
+    """Codebooks that give the pair (d_{t-1}, d_t) a score of 100 and every other pair 0
+    make the walk take the planted tokens, whatever their unary rank."""
+    rng = np.random.default_rng(81)
+    K, k, V = 5, 4, 40
+    cand, unary, _, _, _ = _sel_case(rng, K, k, V)
+    unary = unary / 10.0
+    pick = rng.integers(0, k, K)
+    d = cand[np.arange(K), pick]
+    anchor = int(np.setdiff1d(np.arange(V), cand.ravel())[0])
+    r = K + 1
+    A, B = np.zeros((V, r)), np.zeros((V, r))
+    A[anchor, 0] = 10.0
+    for t in range(K):
+        B[d[t], t] = 10.0
+        A[d[t], t + 1] = 10.0
+    toks, scores = O.select_path(anchor, cand, unary, np.ones((K, r)), A, B)
+    np.testing.assert_array_equal(toks, d)
+    np.testing.assert_allclose(scores[np.arange(K), pick], unary[np.arange(K), pick] + 100.0)
+
+
+def test_select_path_ignores_candidate_order_and_breaks_ties_by_it():
+    rng = np.random.default_rng(82)
+    cand, unary, gate, A, B = _sel_case(rng)
+    toks, _ = O.select_path(3, cand, unary, gate, A, B)
+    perm = np.stack([rng.permutation(cand.shape[1]) for _ in range(cand.shape[0])])
+    toks_p, _ = O.select_path(3, np.take_along_axis(cand, perm, 1), np.take_along_axis(unary, perm, 1), gate, A, B)
+    np.testing.assert_array_equal(toks, toks_p)
+    # two candidates with equal scores: the first in candidate order is taken
+    cand2 = np.array([[5, 6]])
+    B2 = np.zeros((10, 2))
+    toks2, sc = O.select_path(1, cand2, np.array([[0.5, 0.5]]), np.ones((1, 2)), np.ones((10, 2)), B2)
+    assert sc[0, 0] == sc[0, 1] and toks2[0] == 5
+    toks3, _ = O.select_path(1, cand2[:, ::-1], np.array([[0.5, 0.5]]), np.ones((1, 2)), np.ones((10, 2)), B2)
+    assert toks3[0] == 6
+
+
+def test_draft_selector_uses_the_final_hidden_rows():
+    """OracleDraft.select: zero codebooks give the draft's argmax; otherwise every pick is one
+    of its position's candidates and the gate is W_h applied to the final-normed rows."""
+    c = _cfg()
+    w = _weights(c, seed=83)
+    rng = np.random.default_rng(84)
+    w["sel_hidden_proj"] = rng.normal(0, 0.3, (8, c.hidden))
+    w["sel_pred_codebook"] = np.zeros((c.vocab, 8))
+    w["sel_succ_codebook"] = rng.normal(0, 1, (c.vocab, 8))
+    od = O.OracleDraft(c, w)
+    od.inject(0, _feats(c, 14, 85))
+    am, idx, val, _ = od.draft(0, 11)
+    toks, _ = od.select(0, 11)
+    np.testing.assert_array_equal(toks, am)
+    w["sel_pred_codebook"] = rng.normal(0, 1, (c.vocab, 8))
+    toks, scores = od.select(0, 11)
+    gate = od.hidden(0, 11) @ w["sel_hidden_proj"].T
+    want, _ = O.select_path(11, idx, val, gate, w["sel_pred_codebook"], w["sel_succ_codebook"])
+    np.testing.assert_array_equal(toks, want)
+    assert all(toks[t] in idx[t] for t in range(c.block_k))
+    assert np.any(toks != am)
