@@ -211,6 +211,10 @@ class StepLoop:
                         acc=torch.empty((B,), dtype=torch.int32, device=device),
                         toks=torch.empty((B, K + 1), dtype=torch.int32, device=device),
                         nxt=torch.empty((B,), dtype=torch.int32, device=device))
+        # with the path selector the drafted tokens are its walk, else the argmax
+        self.sel = (torch.empty((B, K), dtype=torch.int32, device=device)
+                    if getattr(cfg, "selector_rank", 0) else None)
+        self.draft_tok = self.sel if self.sel is not None else self.out["argmax"]
         self.anchor = wl.anchors_d[0].clone()
         self.lens = list(wl.ctx)
         self.records = []
@@ -272,22 +276,22 @@ class StepLoop:
             ctx.draft(wl.reqs, wl.anchors_d[s] if anchors is None else anchors, argmax=out["argmax"],
                       topk_idx=out["topk_idx"], topk_val=out["topk_val"],
                       logits=self.logits if self.sampling else None,
-                      lse=self.lse if self.tree_budget else None)
+                      lse=self.lse if self.tree_budget else None, selected=self.sel)
             if self.sampling:
                 self._verify_sampling(s, targets)
             elif self.tree_budget:
                 self._verify_tree(s, targets)
             else:
-                ctx.verify(out["argmax"], wl.targets_d[s] if targets is None else targets,
+                ctx.verify(self.draft_tok, wl.targets_d[s] if targets is None else targets,
                            out["acc"], out["toks"], out["nxt"])
             self.records.append((list(wl.ctx), sum(wl.n_new[s])))
             return
         # verify-driven: draft, verify against targets following the argmax, inject a + 1
         ctx.draft(wl.reqs, self.anchor, argmax=out["argmax"], topk_idx=out["topk_idx"],
-                  topk_val=out["topk_val"])
+                  topk_val=out["topk_val"], selected=self.sel)
         rnd = wl.targets_d[s] if targets is None else targets
-        tgt = torch.cat([torch.where(wl.coin_d[s], out["argmax"], rnd[:, :-1]), rnd[:, -1:]], 1)
-        ctx.verify(out["argmax"], tgt, out["acc"], out["toks"], out["nxt"])
+        tgt = torch.cat([torch.where(wl.coin_d[s], self.draft_tok, rnd[:, :-1]), rnd[:, -1:]], 1)
+        ctx.verify(self.draft_tok, tgt, out["acc"], out["toks"], out["nxt"])
         n_new = (out["acc"] + 1).tolist()                     # the scheduler reads a + 1
         rows = torch.tensor([r * self.cfg.n_new_max + i for r, n in enumerate(n_new) for i in range(n)],
                             device=self.device)

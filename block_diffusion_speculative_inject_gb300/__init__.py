@@ -76,7 +76,9 @@ def make_config(cfg, limits: Limits):
         dtype=_ffi.BF16 if cfg.dtype == "bf16" else _ffi.F32,
         block_causal=getattr(cfg, "block_causal", 0),
         output_multiplier=getattr(cfg, "output_multiplier", 1.0),
-        logit_softcap=getattr(cfg, "logit_softcap", 0.0))
+        logit_softcap=getattr(cfg, "logit_softcap", 0.0),
+        dyn_conv=getattr(cfg, "dyn_conv", 0),
+        selector_rank=getattr(cfg, "selector_rank", 0))
 
 
 def dflash_validate_config(cfg, limits: Limits):
@@ -107,7 +109,9 @@ class Context:
                                final_norm=weights["final_norm"].data_ptr(),
                                layers=ctypes.cast(layers, ctypes.POINTER(_ffi.LayerWeights)),
                                mask_embedding=(weights["mask_embedding"].data_ptr()
-                                               if weights.get("mask_embedding") is not None else None))
+                                               if weights.get("mask_embedding") is not None else None),
+                               **{k: (weights[k].data_ptr() if weights.get(k) is not None else None)
+                                  for k in ("sel_pred_codebook", "sel_succ_codebook", "sel_hidden_proj")})
         h = ctypes.c_void_p()
         st = self.lib.dflash_create(ctypes.byref(self._c), ctypes.byref(self._w), device, ctypes.byref(h))
         if st != _ffi.OK:
@@ -140,7 +144,8 @@ class Context:
         self._check(st)
 
     def draft(self, req_ids, anchors, argmax=None, topk_idx=None, topk_val=None, logits=None,
-              want_topk=True, want_logits=False, stream=None, lse=None, want_lse=False):
+              want_topk=True, want_logits=False, stream=None, lse=None, want_lse=False, selected=None,
+              want_selected=False):
         B, K, k, V = len(req_ids), self.cfg.block_k, self.cfg.topk, self.cfg.vocab
         dev = anchors.device
         if argmax is None:
@@ -152,7 +157,14 @@ class Context:
             logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
         if want_lse and lse is None:
             lse = torch.empty((B, K), dtype=torch.float32, device=dev)
-        if lse is not None:
+        if want_selected and selected is None:
+            selected = torch.empty((B, K), dtype=torch.int32, device=dev)
+        if selected is not None:
+            out = _ffi.DraftOut(argmax=argmax.data_ptr(), topk_idx=_ptr(topk_idx), topk_val=_ptr(topk_val),
+                                logits=_ptr(logits), lse=_ptr(lse), selected=selected.data_ptr())
+            st = self.lib.dflash_draft_step_ex(self.h, _stream_ptr(stream), B, _i32_array(req_ids), _ptr(anchors),
+                                               ctypes.byref(out))
+        elif lse is not None:
             st = self.lib.dflash_draft_step_lse(self.h, _stream_ptr(stream), B, _i32_array(req_ids),
                                                 _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
                                                 _ptr(topk_val), _ptr(logits), _ptr(lse))
@@ -161,7 +173,7 @@ class Context:
                                             _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
                                             _ptr(topk_val), _ptr(logits))
         self._check(st)
-        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits, lse=lse)
+        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits, lse=lse, selected=selected)
 
     def verify(self, draft, target, accept_len=None, out_tokens=None, next_anchor=None, stream=None):
         B, K = draft.shape
@@ -302,6 +314,24 @@ def ddtree_build(cand_tok, cand_logp, budget, with_mask=True, stream=None, lse=N
     if st != _ffi.OK:
         raise DFlashError(st, "dflash_ddtree_build failed")
     return out
+
+
+def select_path(anchors, cand_tok, unary, gate, pred_codebook, succ_codebook, want_scores=False, stream=None):
+    """The DFlash 2 path selector's walk on its own (dflash_select_path): anchors [n],
+    cand_tok / unary [n, K, kc], gate [n, K, r] fp32, codebooks [V, r] (bf16 or fp32).
+    Returns (selected [n, K], scores [n, K, kc] or None)."""
+    lib = library()
+    n, K, kc = cand_tok.shape
+    V, r = pred_codebook.shape
+    dev = cand_tok.device
+    dt = _ffi.BF16 if pred_codebook.dtype == torch.bfloat16 else _ffi.F32
+    sel = torch.empty((n, K), dtype=torch.int32, device=dev)
+    sc = torch.empty((n, K, kc), dtype=torch.float32, device=dev) if want_scores else None
+    st = lib.dflash_select_path(_stream_ptr(stream), n, K, kc, r, V, dt, _ptr(anchors), _ptr(cand_tok), _ptr(unary),
+                                _ptr(gate), _ptr(pred_codebook), _ptr(succ_codebook), _ptr(sel), _ptr(sc))
+    if st != _ffi.OK:
+        raise DFlashError(st, "dflash_select_path failed")
+    return sel, sc
 
 
 def ddtree_walk(tree, L, target_next, stream=None):

@@ -20,19 +20,25 @@ class Config(ctypes.Structure):
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
         ("input_embedding_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
         ("block_causal", ctypes.c_int32), ("output_multiplier", ctypes.c_float),
-        ("logit_softcap", ctypes.c_float)]
+        ("logit_softcap", ctypes.c_float), ("dyn_conv", ctypes.c_int32), ("selector_rank", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "in_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "post_norm", "w_gate", "w_up",
-        "w_down")]
+        "w_down", "conv_base", "conv_proj")]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p), ("fc", ctypes.c_void_p),
                 ("fc_norm", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
-                ("layers", ctypes.POINTER(LayerWeights)), ("mask_embedding", ctypes.c_void_p)]
+                ("layers", ctypes.POINTER(LayerWeights)), ("mask_embedding", ctypes.c_void_p),
+                ("sel_pred_codebook", ctypes.c_void_p), ("sel_succ_codebook", ctypes.c_void_p),
+                ("sel_hidden_proj", ctypes.c_void_p)]
+
+
+class DraftOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "topk_idx", "topk_val", "logits", "lse", "selected")]
 
 
 _P = ctypes.c_void_p
@@ -48,6 +54,8 @@ SIGNATURES = {
     "dflash_verify_greedy": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     "dflash_sample_tokens": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
     "dflash_draft_step_lse": (_I32, [_P, _P, _I32, _I32P, _P, _P, _P, _P, _P, _P]),
+    "dflash_draft_step_ex": (_I32, [_P, _P, _I32, _I32P, _P, ctypes.POINTER(DraftOut)]),
+    "dflash_select_path": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_ddtree_build": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_ddtree_walk": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_verify_sample": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),

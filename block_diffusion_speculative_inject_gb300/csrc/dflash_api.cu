@@ -42,12 +42,13 @@ int round_up(int a, int b) { return (a + b - 1) / b * b; }
 enum KCls : int {
   K_GEMM_FC, K_GEMM_KV, K_GEMM_QKV, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_LMHEAD,
   K_ATTN, K_RMSNORM, K_ROPE, K_INJECT_KV, K_SWIGLU, K_EMBED, K_TOPK, K_VERIFY, K_EXPORT, K_SAMPLE,
+  K_GEMM_CONV, K_CONV, K_SELECT,
   K_NUM
 };
 const char *kClsName[K_NUM] = {"gemm_fc", "gemm_kv", "gemm_qkv", "gemm_o", "gemm_gateup",
                                "gemm_down", "gemm_lmhead", "attention", "rmsnorm", "qk_norm_rope",
                                "inject_kv", "swiglu", "embed", "topk", "verify", "export_kv",
-                               "sample"};
+                               "sample", "gemm_conv", "conv", "select"};
 
 struct DraftGraph {
   long long key;
@@ -96,6 +97,10 @@ struct dflash_ctx {
   // sampling mode: truncated distributions of a batch's target and draft rows
   int32_t *smp_tok = nullptr, *smp_n = nullptr;
   float *smp_p = nullptr;
+  // DFlash 2 modules: the convolved operand, the tap corrections [rows][2G], the
+  // selector's gate rows [rows_k][r] and score tables [batch][K][topk][topk]
+  void *xc = nullptr;
+  float *corr = nullptr, *sel_gate = nullptr, *sel_tab = nullptr;
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -346,6 +351,9 @@ extern "C" dflash_status dflash_validate_config(const dflash_config *c, char *ms
   if (c->block_causal != 0 && c->block_causal != 1) return bad(DFLASH_ERR_INVALID_ARG, "block_causal must be 0 or 1");
   if (!(c->output_multiplier >= 0.f) || !(c->logit_softcap >= 0.f))
     return bad(DFLASH_ERR_INVALID_ARG, "output_multiplier and logit_softcap must be >= 0");
+  if (c->dyn_conv != 0 && c->dyn_conv != 1) return bad(DFLASH_ERR_INVALID_ARG, "dyn_conv must be 0 or 1");
+  if (c->selector_rank != 0 && (c->selector_rank < 32 || c->selector_rank > 512 || c->selector_rank % 32))
+    return bad(DFLASH_ERR_UNSUPPORTED, "selector_rank must be 0 or a multiple of 32 in [32, 512]");
   if (msg && msg_len > 0) msg[0] = 0;
   return DFLASH_OK;
 }
@@ -367,7 +375,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -407,6 +415,13 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
     for (const void *p : ps)
       if (!p || !aligned16(p)) return DFLASH_ERR_INVALID_ARG;
     if (cfg->qk_norm && (!lw.q_norm || !lw.k_norm)) return DFLASH_ERR_INVALID_ARG;
+    if (cfg->dyn_conv && (!lw.conv_base || !lw.conv_proj || !aligned16(lw.conv_base) || !aligned16(lw.conv_proj)))
+      return DFLASH_ERR_INVALID_ARG;
+  }
+  if (cfg->selector_rank) {
+    const void *sel[] = {w->sel_pred_codebook, w->sel_succ_codebook, w->sel_hidden_proj};
+    for (const void *p : sel)
+      if (!p || !aligned16(p)) return DFLASH_ERR_INVALID_ARG;
   }
 
   dflash_ctx *c = new dflash_ctx();
@@ -425,6 +440,8 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   m.causal = cfg->block_causal;
   m.out_mult = cfg->output_multiplier == 0.f ? 1.f : cfg->output_multiplier;
   m.softcap = cfg->logit_softcap;
+  m.conv = cfg->dyn_conv;
+  m.sel_r = cfg->selector_rank;
 
   auto fail = [&](dflash_status s) {
     free_all(c);
@@ -466,6 +483,10 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->smp_tok, (size_t)(R + RK) * SMP_K * sizeof(int32_t)},
       {(void **)&c->smp_p, (size_t)(R + RK) * SMP_K * sizeof(float)},
       {(void **)&c->smp_n, (size_t)(R + RK) * sizeof(int32_t)},
+      {&c->xc, m.conv ? (size_t)R * m.H * f4 : 0},
+      {(void **)&c->corr, m.conv ? (size_t)R * 2 * (m.H / 16) * f4 : 0},
+      {(void **)&c->sel_gate, (size_t)RK * m.sel_r * f4},
+      {(void **)&c->sel_tab, m.sel_r ? (size_t)RK * m.topk * m.topk * f4 : 0},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -773,13 +794,51 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
   const OpOut ao = op_of(c, c->ao, (size_t)c->rows_max * m.q_dim());
   const OpOut hm = op_of(c, c->hmid, (size_t)c->rows_max * m.I);
   const OpOut xf = op_of(c, c->xf, (size_t)c->rows_k_max * m.H);
+  // DFlash 2 convolutions: the tap corrections come from a GEMM over the convolution's
+  // input rows; xc holds the convolved operand (input side) or the sublayer output as an
+  // operand (output side)
+  const OpOut xc = op_of(c, c->xc, (size_t)c->rows_max * m.H);
+  const int G2 = 2 * (m.H / 16);
+  auto conv_taps = [&](const dflash_layer_weights &lw, int j, const void **base) -> dflash_status {
+    *base = (const char *)lw.conv_base + (size_t)j * 2 * m.H * c->esz;
+    const void *proj = (const char *)lw.conv_proj + (size_t)j * G2 * m.H * c->esz;
+    GemmDesc d = gemm_desc(R, G2, m.H, EPI_STORE, c->corr, G2);
+    set_x(c, d, j % 2 ? xc : xn, m.H);
+    add_wseg(d, proj, G2);
+    return run_gemm(c, K_GEMM_CONV, d, s);
+  };
+  auto conv_in = [&](const dflash_layer_weights &lw, int j) -> dflash_status {
+    const void *base;
+    dflash_status e = conv_taps(lw, j, &base);
+    if (e != DFLASH_OK) return e;
+    CK(c, timed(c, K_CONV, s, (double)R * m.H * 12 + (double)R * G2 * 4, 4.0 * R * m.H, 1, [&] {
+         return launch_conv_in(c->dtype, R, m.Q(), m.H, xn, c->corr, base, xc, s);
+       }));
+    return DFLASH_OK;
+  };
+  // output side: the GEMM product in ws -> operand -> taps -> x += conv, next norm
+  auto conv_out = [&](const dflash_layer_weights &lw, int j, int S_, OpOut out, const void *nw,
+                      int skip) -> dflash_status {
+    if (S_ != 1) return set_err(c, DFLASH_ERR_CUDA, "convolution after a split GEMM product");
+    CK(c, timed(c, K_CONV, s, (double)R * m.H * 8, 0.0, 1,
+                [&] { return launch_to_op((long)R * m.H, c->ws, xc, s); }));
+    const void *base;
+    dflash_status e = conv_taps(lw, j, &base);
+    if (e != DFLASH_OK) return e;
+    CK(c, timed(c, K_CONV, s, (double)R * m.H * 20 + (double)R * G2 * 4, 8.0 * R * m.H, 1, [&] {
+         return launch_conv_out_norm(c->dtype, R, m.Q(), m.H, c->ws, c->corr, base, c->x, out, nw, m.eps,
+                                     skip, s);
+       }));
+    return DFLASH_OK;
+  };
   int S = 1;
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
+    if (m.conv && (st = conv_in(lw, 0)) != DFLASH_OK) return st;
     // q/k/v projection with per-head q/k norm + RoPE: in the tensor-core GEMM's epilogue
     // (one 128-wide head per tile), else as a post-op
     GemmDesc d = gemm_desc(R, m.qkv_dim(), m.H, EPI_STORE, nullptr, m.qkv_dim());
-    set_x(c, d, xn, m.H);
+    set_x(c, d, m.conv ? xc : xn, m.H);
     add_wseg(d, lw.wq, m.q_dim());
     add_wseg(d, lw.wk, m.kv_dim());
     add_wseg(d, lw.wv, m.kv_dim());
@@ -811,13 +870,18 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     set_x(c, o, ao, m.q_dim());
     add_wseg(o, lw.wo, m.H);
     if ((st = gemm_ws(c, K_GEMM_O, o, s, &S)) != DFLASH_OK) return st;
-    CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
-         return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, xn, lw.post_norm, m.eps, 0, s);
-       }));
+    if (m.conv) {
+      if ((st = conv_out(lw, 1, S, xn, lw.post_norm, 0)) != DFLASH_OK) return st;
+      if ((st = conv_in(lw, 2)) != DFLASH_OK) return st;
+    } else {
+      CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
+           return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, xn, lw.post_norm, m.eps, 0, s);
+         }));
+    }
     // gate/up projection with SwiGLU: in the tensor-core GEMM's epilogue (a tile takes 64
     // gate and the same 64 up rows), else as a post-op
     GemmDesc gu = gemm_desc(R, 2 * m.I, m.H, EPI_STORE, nullptr, 2 * m.I);
-    set_x(c, gu, xn, m.H);
+    set_x(c, gu, m.conv ? xc : xn, m.H);
     add_wseg(gu, lw.w_gate, m.I);
     add_wseg(gu, lw.w_up, m.I);
     if (fused_epilogues(c) && m.I % 64 == 0) {
@@ -838,10 +902,14 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     if ((st = gemm_ws(c, K_GEMM_DOWN, dn, s, &S)) != DFLASH_OK) return st;
     const bool last = l + 1 == m.L;
     const void *nw = last ? c->w.final_norm : c->layers[l + 1].in_norm;
-    CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
-         return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, last ? xf : xn, nw, m.eps,
-                                 last ? m.K : 0, s);
-       }));
+    if (m.conv) {
+      if ((st = conv_out(lw, 3, S, last ? xf : xn, nw, last ? m.K : 0)) != DFLASH_OK) return st;
+    } else {
+      CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
+           return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, last ? xf : xn, nw, m.eps,
+                                   last ? m.K : 0, s);
+         }));
+    }
   }
   if (fused_topk(c, RK)) {
     // tensor-core LM head: per-tile top-k in the GEMM epilogue (merged afterwards); full
@@ -928,7 +996,8 @@ static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt
 
 static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
                                      const int32_t *req_ids, const int32_t *anchors, int32_t *argmax,
-                                     int32_t *topk_idx, float *topk_val, float *logits, float *lse) {
+                                     int32_t *topk_idx, float *topk_val, float *logits, float *lse,
+                                     int32_t *selected = nullptr) {
   if (!c) return DFLASH_ERR_INVALID_ARG;
   dflash_status st = check_device_flag(c);
   if (st != DFLASH_OK) return st;
@@ -937,6 +1006,8 @@ static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
   if (!req_ids || !anchors || !argmax) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
   if ((topk_idx == nullptr) != (topk_val == nullptr))
     return set_err(c, DFLASH_ERR_INVALID_ARG, "topk_idx and topk_val must both be given or both NULL");
+  if (selected && (!c->m.sel_r || !topk_idx))
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "selected needs selector_rank > 0 and the top-k outputs");
   const ModelDims &m = c->m;
   const int B = n_req, Q = m.Q();
   std::vector<int32_t> desc(4 * B + 1);
@@ -1015,6 +1086,21 @@ static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
          return launch_topk(RK, m.V, m.topk, lg, argmax, topk_idx, topk_val, lse, 0, s);
        }));
   }
+  if (selected) {
+    // path selector: gate rows g_t = W_h h_t from the final-normed rows, then the score
+    // tables and the walk
+    const int r = m.sel_r;
+    GemmDesc gd = gemm_desc(RK, r, m.H, EPI_STORE, c->sel_gate, r);
+    set_x(c, gd, op_of(c, c->xf, (size_t)c->rows_k_max * m.H), m.H);
+    add_wseg(gd, c->w.sel_hidden_proj, r);
+    if ((st = run_gemm(c, K_SELECT, gd, s)) != DFLASH_OK) return st;
+    const double rows = (double)RK * m.topk * 2 + B;
+    CK(c, timed(c, K_SELECT, s, rows * r * c->esz + (double)RK * r * 4, 2.0 * RK * m.topk * m.topk * r, 2, [&] {
+         return launch_select_path(c->dtype, B, m.K, m.topk, r, m.V, anchors, topk_idx, topk_val, c->sel_gate,
+                                   c->w.sel_pred_codebook, c->w.sel_succ_codebook, c->sel_tab, selected,
+                                   nullptr, s);
+       }));
+  }
   return DFLASH_OK;
 }
 
@@ -1030,6 +1116,15 @@ extern "C" dflash_status dflash_draft_step_lse(dflash_ctx *c, void *stream, int3
                                                int32_t *argmax, int32_t *topk_idx, float *topk_val,
                                                float *logits, float *lse) {
   return draft_step_impl(c, stream, n_req, req_ids, anchors, argmax, topk_idx, topk_val, logits, lse);
+}
+
+extern "C" dflash_status dflash_draft_step_ex(dflash_ctx *c, void *stream, int32_t n_req,
+                                              const int32_t *req_ids, const int32_t *anchors,
+                                              const dflash_draft_out *out) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  if (!out) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL outputs");
+  return draft_step_impl(c, stream, n_req, req_ids, anchors, out->argmax, out->topk_idx, out->topk_val,
+                         out->logits, out->lse, out->selected);
 }
 
 // ------------------------------------------------------------------------------ verify / export

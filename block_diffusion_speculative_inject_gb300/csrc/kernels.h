@@ -12,6 +12,8 @@ struct ModelDims {
   float eps, emb_scale;
   int causal;                 // causal mask inside the query block
   float out_mult, softcap;    // logits *= out_mult, then softcap * tanh(logits / softcap) if > 0
+  int conv;                   // DFlash 2 dynamic convolutions in every layer
+  int sel_r;                  // DFlash 2 path selector rank (0: off)
   int q_dim() const { return nq * hd; }
   int kv_dim() const { return nkv * hd; }
   int qkv_dim() const { return (nq + 2 * nkv) * hd; }
@@ -93,6 +95,17 @@ cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_
 cudaError_t launch_verify(int n, int K, const int32_t *draft, const int32_t *target,
                           int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor,
                           cudaStream_t s);
+
+// DFlash 2 modules (k_dflash2.cu). corr [M][2G] holds each row's tap corrections (G = H/16).
+cudaError_t launch_conv_in(int dtype, int M, int Q, int H, OpOut in, const float *corr, const void *base,
+                           OpOut out, cudaStream_t s);
+cudaError_t launch_conv_out_norm(int dtype, int M, int Q, int H, const float *y, const float *corr,
+                                 const void *base, float *x, OpOut out, const void *w, float eps,
+                                 int out_skip_k, cudaStream_t s);
+cudaError_t launch_to_op(long n, const float *src, OpOut out, cudaStream_t s);
+cudaError_t launch_select_path(int dtype, int n, int K, int kc, int r, int V, const int32_t *anchors,
+                               const int32_t *cand_tok, const float *unary, const float *gate, const void *pred,
+                               const void *succ, float *tab, int32_t *selected, float *scores, cudaStream_t s);
 
 cudaError_t launch_export_kv(int dtype, const ModelDims &m, int layer, int pos0, int n,
                              const int32_t *pages, const void *pool, void *k_out, void *v_out,

@@ -95,6 +95,10 @@ typedef struct {
   int32_t block_causal;      /* 1: block row j attends to block keys 0..j only          */
   float output_multiplier;   /* logits *= m (0 is read as 1; must be > 0 otherwise)     */
   float logit_softcap;       /* c > 0: logits = c * tanh(logits / c) after the scale    */
+  /* DFlash 2 modules ("DFlash 2 块扩散投机解码技术详解" §3.1, §3.2.3); zero: off. */
+  int32_t dyn_conv;          /* 1: four two-tap dynamic convolutions in every layer      */
+  int32_t selector_rank;     /* r > 0: the path selector with rank-r codebooks; r a
+                              * multiple of 32, <= 512; needs topk outputs              */
 } dflash_config;
 
 /* One draft decoder layer (pre-norm, Qwen3-style). All [out, in] row-major. */
@@ -110,6 +114,14 @@ typedef struct {
   const void *w_gate;    /* [I, H]              */
   const void *w_up;      /* [I, H]              */
   const void *w_down;    /* [H, I]              */
+  /* dyn_conv only (else may be NULL): four two-tap dynamic depthwise convolutions, index
+   * 0 on the attention input (after in_norm), 1 on the attention output (after wo, before
+   * the residual add), 2 on the MLP input (after post_norm), 3 on the MLP output (after
+   * w_down, before the residual add). Over the K+1 block rows of a request,
+   * y_t = k_t0 * x_t + k_t1 * x_{t-1} (x_{-1} = 0), with taps
+   * k_ti[c] = conv_base[j][i][c] + (conv_proj[j] x_t)[i*G + c/16], G = H/16. */
+  const void *conv_base; /* [4, 2, H]           */
+  const void *conv_proj; /* [4, 2*G, H]         */
 } dflash_layer_weights;
 
 typedef struct {
@@ -122,6 +134,10 @@ typedef struct {
   const void *mask_embedding; /* [H] or NULL: a trained mask embedding used instead of
                                * embed[mask_token_id] for the K mask rows
                                * ("DFlash：把串行 Draft 变成并行“填空”" §5.2)          */
+  /* selector_rank > 0 only (else may be NULL): the path selector's codebooks and gate. */
+  const void *sel_pred_codebook; /* [V, r] predecessor embedding A                   */
+  const void *sel_succ_codebook; /* [V, r] successor embedding B                     */
+  const void *sel_hidden_proj;   /* [r, H] gate g_t = W_h h_t of the final hidden row  */
 } dflash_weights;
 
 typedef struct dflash_ctx dflash_ctx;
@@ -175,6 +191,39 @@ dflash_status dflash_draft_step_lse(dflash_ctx *ctx, void *stream, int32_t n_req
                                     const int32_t *req_ids, const int32_t *anchors,
                                     int32_t *argmax, int32_t *topk_idx, float *topk_val,
                                     float *logits, float *lse);
+
+/* Outputs of dflash_draft_step_ex (all DEVICE; NULL: not written). argmax is required;
+ * topk_idx / topk_val both or neither; lse as in dflash_draft_step_lse. selected [n_req, K]
+ * int32 (needs selector_rank > 0 and the top-k outputs): the path selector's walk
+ * ("DFlash 2 块扩散投机解码技术详解" §3.1) — from the anchor, position t takes the candidate b
+ * of its top-k with the largest S_t(a, b) = topk_val[t, b] + <A(a) * g_t, B(b)>, a being the
+ * token taken at t-1 (the anchor at t = 0), g_t = sel_hidden_proj h_t with h_t the
+ * final-normed hidden row of mask position t; equal scores go to the earlier candidate.
+ * Scores are computed in fp32. */
+typedef struct {
+  int32_t *argmax;
+  int32_t *topk_idx;
+  float *topk_val;
+  float *logits;
+  float *lse;
+  int32_t *selected;
+} dflash_draft_out;
+
+dflash_status dflash_draft_step_ex(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                   const int32_t *req_ids, const int32_t *anchors,
+                                   const dflash_draft_out *out);
+
+/* The selector's walk on its own (no context): n_req requests, K positions with kc <= 32
+ * candidates each. anchors [n_req] int32, cand_tok [n_req, K, kc] int32, unary
+ * [n_req, K, kc] fp32, gate [n_req, K, r] fp32, pred / succ codebooks [V, r] of `dtype`,
+ * outputs selected [n_req, K] int32 and scores [n_req, K, kc] fp32 or NULL (each position's
+ * scores given the predecessor taken). All DEVICE. Tokens outside [0, vocab) read as zero
+ * codebook rows. Limits: 1 <= K <= 31, 1 <= kc <= 32, r a multiple of 32 in [32, 512];
+ * else DFLASH_ERR_INVALID_ARG. Scratch comes from the stream-ordered allocator. */
+dflash_status dflash_select_path(void *stream, int32_t n_req, int32_t K, int32_t kc, int32_t r,
+                                 int32_t vocab, dflash_dtype dtype, const int32_t *anchors, const int32_t *cand_tok,
+                                 const float *unary, const float *gate, const void *pred_codebook,
+                                 const void *succ_codebook, int32_t *selected, float *scores);
 
 /* Greedy verification ("DFlash 2 块扩散投机解码技术详解" §2.3): for each of n_req rows,
  *   draft  [n_req, K] int32 DEVICE, target [n_req, K+1] int32 DEVICE (the target's token
@@ -232,8 +281,9 @@ dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
  * dflash_ddtree_build: per request, L block positions with kc candidates each, best first:
  *   cand_tok [n_req, L, kc] int32 and cand_logp [n_req, L, kc] fp32; cand_lse is NULL
  *   (cand_logp are log-probabilities) or [n_req, L] fp32 row normalisers subtracted from
- *   cand_logp (cand_logp = topk_val and cand_lse = lse of dflash_draft_step_lse). The `budget` most likely prefixes (a
- *   prefix takes one candidate at each of positions 1..d; its log-probability is the sum)
+ *   cand_logp (cand_logp = topk_val and cand_lse = lse of dflash_draft_step_lse). The
+ *   `budget` most likely prefixes (a prefix takes one candidate at each of positions 1..d;
+ *   its log-probability is the sum)
  *   are popped best-first from a max-heap seeded with the best candidate of position 1,
  *   each pop pushing the next sibling and the first child; ties pop by (log-probability
  *   desc, depth asc, parent asc, rank asc). With kc >= min(budget, V) the tree is the
