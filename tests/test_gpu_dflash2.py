@@ -29,8 +29,10 @@ def _built():
 
 # ----------------------------------------------------------------------------- convolution
 @pytest.mark.parametrize("lens", [[120, 37], [50, 173, 300]])
-def test_dyn_conv_steps_bf16(lens):
-    cfg = get_config("mini_bf16", dyn_conv=1)
+@pytest.mark.parametrize("hidden", [512, 1024])
+def test_dyn_conv_steps_bf16(lens, hidden):
+    """Two widths: 32 and 64 channel groups per correction row."""
+    cfg = get_config("mini_bf16", dyn_conv=1, hidden=hidden)
     _run_steps(cfg, _limits(max_batch=4, max_pages=32, max_positions=512, max_inject_rows=100), lens, steps=2)
 
 
@@ -44,10 +46,11 @@ def test_dyn_conv_with_variants():
     _run_steps(cfg, _limits(max_batch=4, max_pages=16, max_positions=512, max_inject_rows=64), [90, 64], steps=1)
 
 
-def test_dyn_conv_graph_replay_matches_eager():
+@pytest.mark.parametrize("hidden", [512, 1024])
+def test_dyn_conv_graph_replay_matches_eager(hidden):
     """Without full logits the layer stack is captured into a CUDA graph on the second call
     and replayed after; every call must give the eager result."""
-    cfg = get_config("mini_bf16", dyn_conv=1)
+    cfg = get_config("mini_bf16", dyn_conv=1, hidden=hidden)
     pair = Pair(cfg, _limits(max_batch=4, max_pages=32, max_positions=512, max_inject_rows=100))
     reqs = [3, 4]
     pair.inject(reqs, [77, 140], "prefill", reset=True)
