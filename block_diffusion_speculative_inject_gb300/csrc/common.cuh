@@ -130,6 +130,10 @@ enum GemmEpi : int {
                    // heads get their RMSNorm (if q_norm/k_norm) and RoPE at ctx_len[b] + j
   EPI_SWIGLU = 4,  // W = [gate; up] ([2I, K] as two segments of I rows): a tile holds 64 gate
                    // and the same 64 up rows; out = silu(gate) * up as an operand [M, I]
+  EPI_RESNORM = 5, // residual add with the next RMSNorm left to the consumer: Y = Y + acc (in
+                   // place), out = Y * norm_w as an operand, ss_part[tile][m] = the tile's sum
+                   // of Y^2 for row m; the consuming GEMM scales its rows by
+                   // rsqrt(sum_tiles ss_part / dim + eps) (rs_part below)
 };
 
 constexpr int GEMM_MAX_XSEG = 8;
@@ -169,6 +173,13 @@ struct GemmDesc {
   int out_xf;
   float out_mult, out_cap;
   float2 *lse_part;              // EPI_TOPK: [tiles][M] (max, sum exp) of each tile column, or null
+  // EPI_RESNORM
+  const void *norm_w;            // bf16 [N] RMSNorm weight
+  float *ss_part;                // [N / 128][M]
+  // any epilogue: X holds unnormalised rows x * w; row m of the product is first scaled by
+  // rsqrt(sum_{t < rs_tiles} rs_part[t][m] / rs_dim + eps) (null: no scaling)
+  const float *rs_part;
+  int rs_tiles, rs_dim;
 };
 
 __device__ __forceinline__ float logit_xform(float x, float mult, float cap) {

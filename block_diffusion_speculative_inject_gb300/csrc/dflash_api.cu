@@ -101,6 +101,10 @@ struct dflash_ctx {
   // selector's gate rows [rows_k][r] and score tables [batch][K][topk][topk]
   void *xc = nullptr;
   float *corr = nullptr, *sel_gate = nullptr, *sel_tab = nullptr;
+  // RMSNorm row statistics left by a GEMM epilogue for the next GEMM: per 128-column tile
+  // and row, the sum of squares of the residual stream ([H/128][rows]; after the output
+  // projection, after the down projection)
+  float *ss_o = nullptr, *ss_d = nullptr;
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -375,7 +379,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -487,6 +491,8 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->corr, m.conv ? (size_t)R * 2 * (m.H / 16) * f4 : 0},
       {(void **)&c->sel_gate, (size_t)RK * m.sel_r * f4},
       {(void **)&c->sel_tab, m.sel_r ? (size_t)RK * m.topk * m.topk * f4 : 0},
+      {(void **)&c->ss_o, (size_t)(m.H / 128) * R * f4},
+      {(void **)&c->ss_d, (size_t)(m.H / 128) * R * f4},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -831,6 +837,20 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
        }));
     return DFLASH_OK;
   };
+  // tensor-core path with few rows: the residual add runs in the output / down projection's
+  // epilogue, which also writes x * w (w the next RMSNorm's weight) as the next GEMM's
+  // operand and each 128-column tile's sum of squares per row; the next GEMM scales its
+  // rows by the RMSNorm factor. This saves two dependent launches per layer, which is what
+  // a batch-1 step is made of; with more rows the epilogue's per-token residual loads cost
+  // more than the launches (measured), and the row kernel stays. The last layer's final
+  // norm is always the row kernel (it feeds the LM head the K mask rows only).
+  const bool fnorm = fused_epilogues(c) && !m.conv && m.I % 64 == 0 && R <= 32;
+  auto rs_from = [&](GemmDesc &d, const float *ss) {
+    d.rs_part = ss;
+    d.rs_tiles = m.H / 128;
+    d.rs_dim = m.H;
+    d.eps = m.eps;
+  };
   int S = 1;
   for (int l = 0; l < m.L; ++l) {
     const dflash_layer_weights &lw = c->layers[l];
@@ -853,6 +873,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
       d.rows_per_req = m.Q();
       d.q_dim = m.q_dim();
       d.kv_dim = m.kv_dim();
+      if (fnorm && l > 0) rs_from(d, c->ss_d);     // layer 0's input comes normalised
       if ((st = run_gemm(c, K_GEMM_QKV, d, s)) != DFLASH_OK) return st;
     } else {
       if ((st = gemm_ws(c, K_GEMM_QKV, d, s, &S)) != DFLASH_OK) return st;
@@ -869,11 +890,21 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     GemmDesc o = gemm_desc(R, m.H, m.q_dim(), EPI_STORE, nullptr, m.H);
     set_x(c, o, ao, m.q_dim());
     add_wseg(o, lw.wo, m.H);
-    if ((st = gemm_ws(c, K_GEMM_O, o, s, &S)) != DFLASH_OK) return st;
+    if (fnorm) {
+      o.epi = EPI_RESNORM;
+      o.y = c->x;
+      o.out = xn;
+      o.ldo = m.H;
+      o.norm_w = lw.post_norm;
+      o.ss_part = c->ss_o;
+      if ((st = run_gemm(c, K_GEMM_O, o, s)) != DFLASH_OK) return st;
+    } else if ((st = gemm_ws(c, K_GEMM_O, o, s, &S)) != DFLASH_OK) {
+      return st;
+    }
     if (m.conv) {
       if ((st = conv_out(lw, 1, S, xn, lw.post_norm, 0)) != DFLASH_OK) return st;
       if ((st = conv_in(lw, 2)) != DFLASH_OK) return st;
-    } else {
+    } else if (!fnorm) {
       CK(c, timed(c, K_RMSNORM, s, 4.0 * R * m.H * (S + 3), 4.0 * R * m.H, 1, [&] {
            return launch_post_norm(c->dtype, R, m.H, c->ws, S, c->x, xn, lw.post_norm, m.eps, 0, s);
          }));
@@ -888,6 +919,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
       gu.epi = EPI_SWIGLU;
       gu.out = hm;
       gu.ldo = m.I;
+      if (fnorm) rs_from(gu, c->ss_o);
       if ((st = run_gemm(c, K_GEMM_GATEUP, gu, s)) != DFLASH_OK) return st;
     } else {
       if ((st = gemm_ws(c, K_GEMM_GATEUP, gu, s, &S)) != DFLASH_OK) return st;
@@ -899,9 +931,19 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     GemmDesc dn = gemm_desc(R, m.H, m.I, EPI_STORE, nullptr, m.H);
     set_x(c, dn, hm, m.I);
     add_wseg(dn, lw.w_down, m.H);
-    if ((st = gemm_ws(c, K_GEMM_DOWN, dn, s, &S)) != DFLASH_OK) return st;
     const bool last = l + 1 == m.L;
     const void *nw = last ? c->w.final_norm : c->layers[l + 1].in_norm;
+    if (fnorm && !last) {
+      dn.epi = EPI_RESNORM;
+      dn.y = c->x;
+      dn.out = xn;
+      dn.ldo = m.H;
+      dn.norm_w = nw;
+      dn.ss_part = c->ss_d;
+      if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
+      continue;
+    }
+    if ((st = gemm_ws(c, K_GEMM_DOWN, dn, s, &S)) != DFLASH_OK) return st;
     if (m.conv) {
       if ((st = conv_out(lw, 3, S, last ? xf : xn, nw, last ? m.K : 0)) != DFLASH_OK) return st;
     } else {

@@ -66,6 +66,10 @@ struct TcParams {
   int out_xf;                         // EPI_TOPK: logit scale / soft cap
   float out_mult, out_cap;
   float2 *lse_part;                   // EPI_TOPK: per (tile, token) (max, sum exp) or null
+  const bf16 *norm_w;                 // EPI_RESNORM
+  float *ss_part;
+  const float *rs_part;               // row scales of an unnormalised X (or null)
+  int rs_tiles, rs_dim;
   int *err;
 };
 
@@ -167,7 +171,9 @@ __device__ __forceinline__ void warp_tile_lse(const float (&v)[4], int lane, flo
 }
 
 // ------------------------------------------------------------------------- the kernel
-template <int BN>
+// FN: the fused-norm epilogue pieces (EPI_RESNORM, rs_part), compiled into the few-token
+// instances only so that the others keep their code
+template <int BN, bool FN = false>
 __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
-  const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU;
+  const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU || (FN && (p.epi == EPI_RESNORM || p.rs_part));
   const int kb0 = split * p.kb_per;
   const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
 
@@ -445,6 +451,29 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           const int m = mu[u];
           if (m < 0) continue;
           float *x = a[u];
+          if (FN && p.rs_part) {
+            // the producer left the RMSNorm's row scale: lane t holds tile t's sum of squares
+            float ss = 0.f;
+            for (int t = lane; t < p.rs_tiles; t += 32) ss += __ldg(p.rs_part + (size_t)t * p.M + m);
+            const float rs = rsqrtf(warp_sum(ss) / (float)p.rs_dim + p.eps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] *= rs;
+          }
+          if (FN && p.epi == EPI_RESNORM) {
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = n0 + lane + 32 * j;
+              const size_t o = (size_t)m * p.ldy + n;
+              const float y = p.y[o] + x[j];
+              p.y[o] = y;
+              write_op(p.out, (size_t)m * p.ldo + n, y * __bfloat162float(p.norm_w[n]));
+              ss += y * y;
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) p.ss_part[(size_t)blockIdx.y * p.M + m] = ss;
+            continue;
+          }
           if (p.epi == EPI_TOPK) {
             // split-K LM head: the reduced column's best topk of this tile
             float v[4];
@@ -511,7 +540,7 @@ struct TcGemm {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
   int generation = 0;
-  bool attr_set[4] = {false, false, false, false};
+  bool attr_set[6] = {false, false, false, false, false, false};
 };
 
 cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag) {
@@ -610,10 +639,10 @@ int tc_gemm_splits(const TcGemm *, const GemmDesc &) { return 1; }   // reduced 
 
 int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 1; }
 
-template <int BN>
+template <int BN, bool FN = false>
 static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan &pl, cudaStream_t s) {
   if (!t->attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, FN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
     t->attr_set[slot] = true;
@@ -632,7 +661,7 @@ static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, p);
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, FN>, p);
 }
 
 cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
@@ -649,6 +678,10 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     return cudaErrorInvalidValue;
   if (d.epi == EPI_QKV && (d.q_dim % TC_BM || d.kv_dim % TC_BM || !d.ctx_len || !d.rope || d.part ||
                            d.rows_per_req < 1))
+    return cudaErrorInvalidValue;
+  if (d.epi == EPI_RESNORM && (d.N % TC_BM || !d.y || !d.out.lo || !d.norm_w || !d.ss_part || d.part))
+    return cudaErrorInvalidValue;
+  if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1 || d.part || d.epi == EPI_TOPK))
     return cudaErrorInvalidValue;
   p.n_wseg = d.n_wseg;
   for (int i = 0; i < d.n_wseg; ++i) {
@@ -700,6 +733,11 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.ldo = d.ldo;
   p.out_xf = d.out_xf;
   p.lse_part = d.lse_part;
+  p.norm_w = (const bf16 *)d.norm_w;
+  p.ss_part = d.ss_part;
+  p.rs_part = d.rs_part;
+  p.rs_tiles = d.rs_tiles;
+  p.rs_dim = d.rs_dim;
   p.out_mult = d.out_mult;
   p.out_cap = d.out_cap;
   p.err = t->err;
@@ -710,6 +748,10 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     p.epi = EPI_STORE;
   }
   cudaError_t e;
+  if (d.rs_part || d.epi == EPI_RESNORM) {
+    if (pl.bn > 32) return cudaErrorInvalidValue;      // few-token instances only
+    return pl.bn == 16 ? launch_bn<16, true>(t, 4, p, pl, s) : launch_bn<32, true>(t, 5, p, pl, s);
+  }
   switch (pl.bn) {
     case 16: e = launch_bn<16>(t, 0, p, pl, s); break;
     case 32: e = launch_bn<32>(t, 1, p, pl, s); break;
