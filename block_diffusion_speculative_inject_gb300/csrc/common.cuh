@@ -131,7 +131,7 @@ enum GemmEpi : int {
   EPI_SWIGLU = 4,  // W = [gate; up] ([2I, K] as two segments of I rows): a tile holds 64 gate
                    // and the same 64 up rows; out = silu(gate) * up as an operand [M, I]
   EPI_RESNORM = 5, // residual add with the next RMSNorm left to the consumer: Y = Y + acc (in
-                   // place), out = Y * norm_w as an operand, ss_part[tile][m] = the tile's sum
+                   // place; Y null: no residual, Y stands for acc), out = Y * norm_w as an operand, ss_part[tile][m] = the tile's sum
                    // of Y^2 for row m; the consuming GEMM scales its rows by
                    // rsqrt(sum_tiles ss_part / dim + eps) (rs_part below)
 };

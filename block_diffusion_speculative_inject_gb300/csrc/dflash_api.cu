@@ -105,6 +105,7 @@ struct dflash_ctx {
   // and row, the sum of squares of the residual stream ([H/128][rows]; after the output
   // projection, after the down projection)
   float *ss_o = nullptr, *ss_d = nullptr;
+  float *ss_inj = nullptr;   // the same after the injection's fc ([H/128][32])
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -379,7 +380,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -493,6 +494,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->sel_tab, m.sel_r ? (size_t)RK * m.topk * m.topk * f4 : 0},
       {(void **)&c->ss_o, (size_t)(m.H / 128) * R * f4},
       {(void **)&c->ss_d, (size_t)(m.H / 128) * R * f4},
+      {(void **)&c->ss_inj, (size_t)(m.H / 128) * 32 * f4},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -706,14 +708,32 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     d.x_k0[m.n_feat] = F;
     add_wseg(d, c->w.fc, m.H);
     int S = 1;
-    if ((st = gemm_ws(c, K_GEMM_FC, d, s, &S)) != DFLASH_OK) return st;
     OpOut g = op_of(c, c->g, (size_t)C * m.H);
-    CK(c, timed(c, K_RMSNORM, s, 4.0 * n * m.H * (S + 1), 4.0 * n * m.H, 1, [&] {
-         return launch_post_norm(c->dtype, n, m.H, c->ws, S, nullptr, g, c->w.fc_norm, m.eps, 0, s);
-       }));
+    // few rows on the tensor cores: the fc epilogue writes fc_out * fc_norm and its per-tile
+    // sums of squares, and the K/V GEMM applies the RMSNorm row scale (one launch fewer)
+    const bool fnorm = c->tc && c->dtype == DFLASH_BF16 && n <= 32;
+    if (fnorm) {
+      d.epi = EPI_RESNORM;
+      d.out = g;
+      d.ldo = m.H;
+      d.norm_w = c->w.fc_norm;
+      d.ss_part = c->ss_inj;
+      if ((st = run_gemm(c, K_GEMM_FC, d, s)) != DFLASH_OK) return st;
+    } else {
+      if ((st = gemm_ws(c, K_GEMM_FC, d, s, &S)) != DFLASH_OK) return st;
+      CK(c, timed(c, K_RMSNORM, s, 4.0 * n * m.H * (S + 1), 4.0 * n * m.H, 1, [&] {
+           return launch_post_norm(c->dtype, n, m.H, c->ws, S, nullptr, g, c->w.fc_norm, m.eps, 0, s);
+         }));
+    }
     // every layer's [Wk; Wv] in one GEMM, then k-norm + RoPE + paged write
     GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, nullptr, kvw);
     set_x(c, e, g, m.H);
+    if (fnorm) {
+      e.rs_part = c->ss_inj;
+      e.rs_tiles = m.H / 128;
+      e.rs_dim = m.H;
+      e.eps = m.eps;
+    }
     for (int l = 0; l < m.L; ++l) {
       add_wseg(e, c->layers[l].wk, m.kv_dim());
       add_wseg(e, c->layers[l].wv, m.kv_dim());

@@ -465,8 +465,8 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             for (int j = 0; j < 4; ++j) {
               const int n = n0 + lane + 32 * j;
               const size_t o = (size_t)m * p.ldy + n;
-              const float y = p.y[o] + x[j];
-              p.y[o] = y;
+              const float y = p.y ? p.y[o] + x[j] : x[j];       // no residual: the norm alone
+              if (p.y) p.y[o] = y;
               write_op(p.out, (size_t)m * p.ldo + n, y * __bfloat162float(p.norm_w[n]));
               ss += y * y;
             }
@@ -679,10 +679,9 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   if (d.epi == EPI_QKV && (d.q_dim % TC_BM || d.kv_dim % TC_BM || !d.ctx_len || !d.rope || d.part ||
                            d.rows_per_req < 1))
     return cudaErrorInvalidValue;
-  if (d.epi == EPI_RESNORM && (d.N % TC_BM || !d.y || !d.out.lo || !d.norm_w || !d.ss_part || d.part))
+  if (d.epi == EPI_RESNORM && (d.N % TC_BM || !d.out.lo || !d.norm_w || !d.ss_part || d.part))
     return cudaErrorInvalidValue;
-  if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1 || d.part || d.epi == EPI_TOPK))
-    return cudaErrorInvalidValue;
+  if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1 || d.epi == EPI_TOPK)) return cudaErrorInvalidValue;
   p.n_wseg = d.n_wseg;
   for (int i = 0; i < d.n_wseg; ++i) {
     const long rows = d.w_n0[i + 1] - d.w_n0[i];

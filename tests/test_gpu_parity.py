@@ -130,14 +130,18 @@ def test_incremental_injection_equals_one_shot():
         b.ctx.inject([1], [m], [f[s:s + m].contiguous() for f in fg])
         s += m
     # The GEMM's split-K factor follows the row count of each call, so the fp32 sums differ in
-    # order between chunkings; the stored bf16 K/V then agree except for rare rounding flips
-    # of one unit in the last place.
+    # order between chunkings, and chunks of at most 32 rows apply the fc RMSNorm as a row
+    # scale after the K/V GEMM instead of before it. Both orders carry the activations to
+    # about 2^-17 relative, so a bf16 rounding of the stored K/V flips by one unit in the last
+    # place with probability about 2 * 2^-17 / 2^-8 (0.4%).
     for l in range(cfg.n_layers):
         for x, y in zip(a.ctx.export_kv(1, l, 0, n), b.ctx.export_kv(1, l, 0, n)):
             x, y = x.float(), y.float()
-            assert torch.mean((x == y).float()).item() > 0.999
+            assert torch.mean((x == y).float()).item() > 0.99
+            # one unit in the last place of the value, plus an absolute floor for values that
+            # RoPE's rotation made small relative to their operands (2^-15 of the largest |K|)
             ulp = torch.abs(x) * 2.0 ** -7 + 1e-30
-            assert torch.all(torch.abs(x - y) <= ulp + 1e-6)
+            assert torch.all(torch.abs(x - y) <= ulp + 2.0 ** -15 * torch.abs(x).max())
 
 
 def test_results_independent_of_batch_composition():
