@@ -525,7 +525,9 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         }
       }
     }
-    if (p.S > 1) cluster_sync_all();   // peers keep their shared memory until all are done
+    // peers keep their shared memory until all have read it; this barrier orders nothing
+    // else, so its arrive is relaxed (the epilogue's global stores need not drain first)
+    if (p.S > 1) cluster_sync_relaxed();
   }
   if (warp == 1) {
     tc_fence_after();
