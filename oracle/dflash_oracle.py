@@ -52,7 +52,11 @@ Readings where the pages leave a step open (each is also listed in the design no
     candidates, S_t(a, b) = U_t(b) + <A(a) * g_t, B(b)>, U_t = the draft's logits, A / B the
     predecessor / successor codebooks [V, r], g_t = W_h h_t with h_t the final-normed hidden
     row of mask position t; a greedy walk from the anchor takes the best-scoring candidate
-    at each position (the first in candidate order among equal scores).
+    at each position (the first in candidate order among equal scores). In sampling mode the
+    walk draws position t's token from softmax(S_t(a, .) / temperature) over the k
+    candidates (inverse CDF in vocabulary order, a caller-supplied uniform); that subset
+    distribution, as a distribution over the vocabulary (zero outside the candidates), is
+    the draft's q in rejection sampling.
   * Sampling mode ([P2] §2.3, §3.3, §4.2): both the draft and the target distribution go
     through the same truncation — logits / temperature, keep the top_k largest (ties to
     the lower index), softmax over those, then keep the shortest prefix of them in
@@ -73,7 +77,7 @@ __all__ = [
     "accept_prob", "residual_dist", "sample_index", "verify_sample", "as_fraction_dist",
     "sampling_probs", "sample_token", "verify_sample_logits",
     "log_softmax_norm", "ddtree_build", "ddtree_mask", "ddtree_walk",
-    "dyn_conv", "select_path",
+    "dyn_conv", "select_path", "select_sample", "subset_to_vocab",
 ]
 
 
@@ -574,3 +578,32 @@ def select_path(anchor, cand_tok, unary, gate, pred_cb, succ_cb):
         prev = int(cand_tok[t, best])
         toks.append(prev)
     return np.array(toks, dtype=np.int64), scores
+
+
+def subset_to_vocab(tokens, probs, V):
+    """A distribution over k distinct candidate tokens as a length-V vector (zero elsewhere)."""
+    full = np.zeros(V)
+    for t, q in zip(tokens, probs):
+        full[int(t)] += float(q)
+    return full
+
+
+def select_sample(anchor, cand_tok, unary, gate, pred_cb, succ_cb, temperature, u, V):
+    """The path selector's walk in sampling mode ([P2] §3.1.3): at position t the scores
+    S_t(a, b) of select_path (a = the token drawn at t-1, the anchor at t = 0) become the
+    distribution softmax(S_t / temperature) over the k candidates, and the token is drawn
+    from it by inverse CDF in vocabulary order with u[t]. Returns (tokens [K], q [K][V]): the
+    drawn tokens and each position's subset distribution over the vocabulary."""
+    cand_tok = np.asarray(cand_tok)
+    K, k = cand_tok.shape
+    prev = int(anchor)
+    toks, q_rows = [], []
+    for t in range(K):
+        _, sc = select_path(prev, cand_tok[t:t + 1], np.asarray(unary)[t:t + 1], np.asarray(gate)[t:t + 1],
+                            pred_cb, succ_cb)
+        q = softmax(sc[0] / temperature)
+        full = subset_to_vocab(cand_tok[t], q, V)
+        prev = sample_index(full, float(u[t]))
+        toks.append(prev)
+        q_rows.append(full)
+    return np.array(toks, dtype=np.int64), q_rows

@@ -893,3 +893,54 @@ def test_draft_selector_uses_the_final_hidden_rows():
     np.testing.assert_array_equal(toks, want)
     assert all(toks[t] in idx[t] for t in range(c.block_k))
     assert np.any(toks != am)
+
+
+def test_select_sample_distribution_and_draws():
+    """Sampling-mode selector: each position's q is the softmax of the greedy walk's scores
+    over the candidates (zero elsewhere, summing to one); with zero codebooks it is the
+    softmax of the unary scores; a uniform in the middle of a candidate's CDF step (in
+    vocabulary order) draws that candidate; the walk continues from the drawn token."""
+    rng = np.random.default_rng(90)
+    K, k, V, r = 4, 5, 30, 6
+    cand, unary, gate, A, B = _sel_case(rng, K, k, V, r)
+    T = 0.7
+    u = rng.uniform(0, 1, K)
+    toks, q = O.select_sample(3, cand, unary, gate, A, B, T, u, V)
+    prev = 3
+    for t in range(K):
+        _, sc = O.select_path(prev, cand[t:t + 1], unary[t:t + 1], gate[t:t + 1], A, B)
+        want = np.exp((sc[0] - sc[0].max()) / T)
+        want /= want.sum()
+        np.testing.assert_allclose(q[t][cand[t]], want, rtol=1e-12)
+        assert abs(q[t].sum() - 1) < 1e-12 and np.all(q[t][np.setdiff1d(np.arange(V), cand[t])] == 0)
+        # the draw: the first candidate in vocabulary order whose running mass exceeds u
+        order = np.argsort(cand[t])
+        cum = np.cumsum(want[order])
+        assert toks[t] == cand[t][order][np.searchsorted(cum, u[t], side="right")]
+        prev = toks[t]
+    _, q0 = O.select_sample(3, cand, unary, gate, np.zeros_like(A), B, T, u, V)
+    for t in range(K):
+        w = np.exp((unary[t] - unary[t].max()) / T)
+        np.testing.assert_allclose(q0[t][cand[t]], w / w.sum(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_rejection_sampling_with_selector_q_is_exact(seed):
+    """Rejection sampling against the selector's subset distribution reproduces the target's
+    distribution exactly (enumerated over all draws, exact rationals), K = 1: the subset q
+    over the vocabulary is a valid draft distribution."""
+    rng = np.random.default_rng(200 + seed)
+    V, k = 4, 3
+    cand = np.array([rng.permutation(V)[:k]])
+    unary = rng.normal(0, 1, (1, k))
+    gate = rng.normal(0, 1, (1, 2))
+    A, B = rng.normal(0, 1, (V, 2)), rng.normal(0, 1, (V, 2))
+    _, sc = O.select_path(1, cand, unary, gate, A, B)
+    q = O.subset_to_vocab(cand[0], O.softmax(sc[0] / 0.9), V)
+    qf = [Fraction(float(x)) for x in q]
+    qf = [x / sum(qf) for x in qf]
+    assert sum(1 for x in qf if x == 0) == V - k        # zero outside the candidates
+    p0, p1 = _rand_dist(rng, V), _rand_dist(rng, V, zeros=True)
+    law = _exact_output_distribution(lambda prefix: p0 if len(prefix) == 0 else p1, [qf], V, 1)
+    for seq in itertools.product(range(V), repeat=2):
+        assert law.get(seq, 0) == p0[seq[0]] * p1[seq[1]], seq
