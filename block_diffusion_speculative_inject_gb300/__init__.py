@@ -145,7 +145,9 @@ class Context:
 
     def draft(self, req_ids, anchors, argmax=None, topk_idx=None, topk_val=None, logits=None,
               want_topk=True, want_logits=False, stream=None, lse=None, want_lse=False, selected=None,
-              want_selected=False):
+              want_selected=False, sel_uniform=None, sel_temperature=1.0):
+        """One draft step. With sel_uniform [B, K] the path selector samples (its draft
+        distributions come back as sel_q_tok / sel_q_p [B, K, 32] and sel_q_n [B, K])."""
         B, K, k, V = len(req_ids), self.cfg.block_k, self.cfg.topk, self.cfg.vocab
         dev = anchors.device
         if argmax is None:
@@ -157,11 +159,18 @@ class Context:
             logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
         if want_lse and lse is None:
             lse = torch.empty((B, K), dtype=torch.float32, device=dev)
-        if want_selected and selected is None:
+        if (want_selected or sel_uniform is not None) and selected is None:
             selected = torch.empty((B, K), dtype=torch.int32, device=dev)
+        q = {}
+        if sel_uniform is not None:
+            q = dict(sel_q_tok=torch.empty((B, K, 32), dtype=torch.int32, device=dev),
+                     sel_q_p=torch.empty((B, K, 32), dtype=torch.float32, device=dev),
+                     sel_q_n=torch.empty((B, K), dtype=torch.int32, device=dev))
         if selected is not None:
             out = _ffi.DraftOut(argmax=argmax.data_ptr(), topk_idx=_ptr(topk_idx), topk_val=_ptr(topk_val),
-                                logits=_ptr(logits), lse=_ptr(lse), selected=selected.data_ptr())
+                                logits=_ptr(logits), lse=_ptr(lse), selected=selected.data_ptr(),
+                                sel_temperature=float(sel_temperature), sel_uniform=_ptr(sel_uniform),
+                                **{k: v.data_ptr() for k, v in q.items()})
             st = self.lib.dflash_draft_step_ex(self.h, _stream_ptr(stream), B, _i32_array(req_ids), _ptr(anchors),
                                                ctypes.byref(out))
         elif lse is not None:
@@ -173,7 +182,8 @@ class Context:
                                             _ptr(anchors), _ptr(argmax), _ptr(topk_idx),
                                             _ptr(topk_val), _ptr(logits))
         self._check(st)
-        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits, lse=lse, selected=selected)
+        return dict(argmax=argmax, topk_idx=topk_idx, topk_val=topk_val, logits=logits, lse=lse, selected=selected,
+                    **q)
 
     def verify(self, draft, target, accept_len=None, out_tokens=None, next_anchor=None, stream=None):
         B, K = draft.shape
@@ -212,6 +222,23 @@ class Context:
                                            _ptr(target_logits), _ptr(draft_logits), _ptr(draft),
                                            _ptr(u_accept), _ptr(u_resample), _ptr(accept_len),
                                            _ptr(out_tokens), _ptr(next_anchor))
+        self._check(st)
+        return accept_len, out_tokens, next_anchor
+
+    def verify_sample_q(self, target_logits, q_tok, q_p, q_n, draft, u_accept, u_resample, temperature, top_k,
+                        top_p, stream=None):
+        """Rejection sampling against draft distributions given as candidate lists
+        (dflash_verify_sample_q); returns (accept_len, out_tokens, next_anchor)."""
+        B, K = draft.shape
+        dev = draft.device
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        next_anchor = torch.empty((B,), dtype=torch.int32, device=dev)
+        sp = _ffi.Sampling(float(temperature), int(top_k), float(top_p))
+        st = self.lib.dflash_verify_sample_q(self.h, _stream_ptr(stream), B, ctypes.byref(sp), _ptr(target_logits),
+                                             _ptr(q_tok), _ptr(q_p), _ptr(q_n), _ptr(draft), _ptr(u_accept),
+                                             _ptr(u_resample), _ptr(accept_len), _ptr(out_tokens),
+                                             _ptr(next_anchor))
         self._check(st)
         return accept_len, out_tokens, next_anchor
 
@@ -332,6 +359,26 @@ def select_path(anchors, cand_tok, unary, gate, pred_codebook, succ_codebook, wa
     if st != _ffi.OK:
         raise DFlashError(st, "dflash_select_path failed")
     return sel, sc
+
+
+def select_sample(anchors, cand_tok, unary, gate, pred_codebook, succ_codebook, temperature, u, stream=None):
+    """The path selector's sampling walk on its own (dflash_select_sample). Returns
+    (selected [n, K], q_tok [n, K, 32], q_p [n, K, 32], q_n [n, K])."""
+    lib = library()
+    n, K, kc = cand_tok.shape
+    V, r = pred_codebook.shape
+    dev = cand_tok.device
+    dt = _ffi.BF16 if pred_codebook.dtype == torch.bfloat16 else _ffi.F32
+    sel = torch.empty((n, K), dtype=torch.int32, device=dev)
+    q_tok = torch.empty((n, K, 32), dtype=torch.int32, device=dev)
+    q_p = torch.empty((n, K, 32), dtype=torch.float32, device=dev)
+    q_n = torch.empty((n, K), dtype=torch.int32, device=dev)
+    st = lib.dflash_select_sample(_stream_ptr(stream), n, K, kc, r, V, dt, float(temperature), _ptr(anchors),
+                                  _ptr(cand_tok), _ptr(unary), _ptr(gate), _ptr(pred_codebook), _ptr(succ_codebook),
+                                  _ptr(u), _ptr(sel), _ptr(q_tok), _ptr(q_p), _ptr(q_n))
+    if st != _ffi.OK:
+        raise DFlashError(st, "dflash_select_sample failed")
+    return sel, q_tok, q_p, q_n
 
 
 def ddtree_walk(tree, L, target_next, stream=None):

@@ -38,7 +38,9 @@ class Weights(ctypes.Structure):
 
 
 class DraftOut(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "topk_idx", "topk_val", "logits", "lse", "selected")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "topk_idx", "topk_val", "logits", "lse", "selected")] + [
+        ("sel_temperature", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("sel_uniform", "sel_q_tok", "sel_q_p", "sel_q_n")]
 
 
 _P = ctypes.c_void_p
@@ -59,6 +61,9 @@ SIGNATURES = {
     "dflash_ddtree_build": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_ddtree_walk": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_verify_sample": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dflash_verify_sample_q": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dflash_select_sample": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _P]),
     "dflash_release": (_I32, [_P, _I32]),
     "dflash_truncate": (_I32, [_P, _I32, _I32]),
     "dflash_context_len": (_I32, [_P, _I32, _I32P]),

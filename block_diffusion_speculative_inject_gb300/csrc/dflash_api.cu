@@ -1059,7 +1059,7 @@ static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt
 static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
                                      const int32_t *req_ids, const int32_t *anchors, int32_t *argmax,
                                      int32_t *topk_idx, float *topk_val, float *logits, float *lse,
-                                     int32_t *selected = nullptr) {
+                                     int32_t *selected = nullptr, const SelSample *sel_smp = nullptr) {
   if (!c) return DFLASH_ERR_INVALID_ARG;
   dflash_status st = check_device_flag(c);
   if (st != DFLASH_OK) return st;
@@ -1160,7 +1160,7 @@ static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
     CK(c, timed(c, K_SELECT, s, rows * r * c->esz + (double)RK * r * 4, 2.0 * RK * m.topk * m.topk * r, 2, [&] {
          return launch_select_path(c->dtype, B, m.K, m.topk, r, m.V, anchors, topk_idx, topk_val, c->sel_gate,
                                    c->w.sel_pred_codebook, c->w.sel_succ_codebook, c->sel_tab, selected,
-                                   nullptr, s);
+                                   nullptr, s, sel_smp);
        }));
   }
   return DFLASH_OK;
@@ -1185,9 +1185,16 @@ extern "C" dflash_status dflash_draft_step_ex(dflash_ctx *c, void *stream, int32
                                               const dflash_draft_out *out) {
   if (!c) return DFLASH_ERR_INVALID_ARG;
   if (!out) return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL outputs");
+  SelSample smp{out->sel_temperature, out->sel_uniform, out->sel_q_tok, out->sel_q_p, out->sel_q_n};
+  if (out->sel_uniform) {
+    if (!out->selected || !out->sel_q_tok || !out->sel_q_p || !out->sel_q_n || !(out->sel_temperature > 0.f))
+      return set_err(c, DFLASH_ERR_INVALID_ARG,
+                     "the sampling walk needs selected, sel_q_tok/p/n and sel_temperature > 0");
+  }
   return draft_step_impl(c, stream, n_req, req_ids, anchors, out->argmax, out->topk_idx, out->topk_val,
-                         out->logits, out->lse, out->selected);
+                         out->logits, out->lse, out->selected, out->sel_uniform ? &smp : nullptr);
 }
+
 
 // ------------------------------------------------------------------------------ verify / export
 extern "C" dflash_status dflash_verify_greedy(dflash_ctx *c, void *stream, int32_t n_req,
@@ -1274,6 +1281,38 @@ extern "C" dflash_status dflash_verify_sample(dflash_ctx *c, void *stream, int32
   CK(c, timed(c, K_VERIFY, s, 4.0 * n_req * (3 * K + 4), (double)n_req * K, 1, [&] {
        return launch_verify_sample(n_req, K, ptok, pp, pn, qtok, qp, qn, draft, u_accept, u_resample,
                                    accept_len, out_tokens, next_anchor, s);
+     }));
+  return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_verify_sample_q(dflash_ctx *c, void *stream, int32_t n_req,
+                                                const dflash_sampling *sp, const float *target_logits,
+                                                const int32_t *q_tok, const float *q_p, const int32_t *q_n,
+                                                const int32_t *draft, const float *u_accept,
+                                                const float *u_resample, int32_t *accept_len,
+                                                int32_t *out_tokens, int32_t *next_anchor) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_device_flag(c);
+  if (st != DFLASH_OK) return st;
+  if ((st = check_sampling(c, sp)) != DFLASH_OK) return st;
+  if (n_req < 0 || n_req > c->cfg.max_batch)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req=%d outside [0, max_batch=%d]", n_req, c->cfg.max_batch);
+  if (n_req == 0) return DFLASH_OK;
+  if (!target_logits || !q_tok || !q_p || !q_n || !draft || !u_accept || !u_resample || !accept_len ||
+      !out_tokens || !next_anchor)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(c->device);
+  if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int V = c->m.V, K = c->m.K, Q = c->m.Q();
+  const int tr = n_req * Q;
+  CK(c, timed(c, K_SAMPLE, s, 4.0 * tr * V, 4.0 * tr * V, 1, [&] {
+       return launch_trunc_dist(tr, V, sp->temperature, sp->top_k, sp->top_p, target_logits, nullptr, nullptr,
+                                c->smp_tok, c->smp_p, c->smp_n, 2 * c->num_sms, s);
+     }));
+  CK(c, timed(c, K_VERIFY, s, 4.0 * n_req * (3 * K + 4), (double)n_req * K, 1, [&] {
+       return launch_verify_sample(n_req, K, c->smp_tok, c->smp_p, c->smp_n, q_tok, q_p, q_n, draft, u_accept,
+                                   u_resample, accept_len, out_tokens, next_anchor, s);
      }));
   return DFLASH_OK;
 }

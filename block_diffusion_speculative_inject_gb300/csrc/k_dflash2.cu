@@ -16,6 +16,8 @@
 //   T_t[a][b] = unary[t][b] + sum_r A(a)[r] g_t[r] B(b)[r],
 // with predecessors the anchor (t = 0) or the candidates of t-1; a warp per request then
 // walks the tables from the anchor.
+#include <climits>
+
 #include "../../include/dflash.h"
 #include "kernels.h"
 
@@ -221,10 +223,53 @@ __global__ void k_sel_walk(int n, int K, int kc, const int32_t *__restrict__ can
   }
 }
 
+// Sampling mode: position t's candidates get q = softmax(T_t[prev] / temperature); the token
+// is drawn by inverse CDF in vocabulary order against u[b][t] (the first candidate, by token
+// id, whose running mass exceeds u times the total; if rounding leaves none, the largest
+// token with q > 0); q goes out as lists of stride SMP_K (q_tok, q_p, q_n), the form the
+// sampling verification reads.
+__global__ void k_sel_walk_sample(int n, int K, int kc, const int32_t *__restrict__ cand_tok,
+                                  const float *__restrict__ tab, float temperature, const float *__restrict__ u,
+                                  int32_t *__restrict__ selected, int32_t *__restrict__ q_tok,
+                                  float *__restrict__ q_p, int32_t *__restrict__ q_n) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  if (b >= n) return;
+  int prev = 0;
+  for (int t = 0; t < K; ++t) {
+    const size_t bt = (size_t)b * K + t;
+    const float *row = tab + (bt * kc + prev) * kc;
+    const bool in = lane < kc;
+    const float v = in ? row[lane] : -INFINITY;
+    const int32_t tok = in ? cand_tok[bt * kc + lane] : INT_MAX;
+    const float mx = warp_max(v);
+    const float e = in ? expf((v - mx) / temperature) : 0.f;
+    const float q = e / warp_sum(e);
+    q_tok[bt * SMP_K + lane] = in ? tok : -1;
+    q_p[bt * SMP_K + lane] = q;
+    if (lane == 0) q_n[bt] = kc;
+    float before = 0.f;                      // mass of the candidates with a smaller token id
+    for (int i = 0; i < 32; ++i) {
+      const float qi = __shfl_sync(0xffffffffu, q, i);
+      const int32_t ti = __shfl_sync(0xffffffffu, tok, i);
+      if (ti < tok) before += qi;
+    }
+    const float thr = u[bt] * warp_sum(q);
+    const bool hit = in && q > 0.f && before + q > thr;
+    int32_t pick = __reduce_min_sync(0xffffffffu, hit ? tok : INT_MAX);
+    if (pick == INT_MAX) pick = __reduce_max_sync(0xffffffffu, in && q > 0.f ? tok : INT_MIN);
+    prev = max(0, __ffs(__ballot_sync(0xffffffffu, tok == pick)) - 1);   // 0 if scores were NaN
+    if (lane == 0) selected[bt] = pick;
+  }
+}
+
 cudaError_t launch_select_path(int dtype, int n, int K, int kc, int r, int V, const int32_t *anchors,
                                const int32_t *cand_tok, const float *unary, const float *gate, const void *pred,
-                               const void *succ, float *tab, int32_t *selected, float *scores, cudaStream_t s) {
+                               const void *succ, float *tab, int32_t *selected, float *scores, cudaStream_t s,
+                               const SelSample *smp) {
   if (n == 0) return cudaSuccess;
+  if (smp && !(smp->temperature > 0.f)) return cudaErrorInvalidValue;
   if (K < 1 || kc < 1 || kc > SEL_MAX_KC || r < 32 || r > SEL_MAX_R || r % 32) return cudaErrorInvalidValue;
   static bool smem_opt_in[2] = {false, false};
   const size_t smem = sel_smem(kc, r);
@@ -243,6 +288,9 @@ cudaError_t launch_select_path(int dtype, int n, int K, int kc, int r, int V, co
             : launch_pdl(k_sel_table<float>, g, dim3(SEL_THREADS), smem, s, K, kc, r, V, anchors, cand_tok,
                          unary, gate, (const float *)pred, (const float *)succ, tab);
   if (e != cudaSuccess) return e;
+  if (smp)
+    return launch_pdl(k_sel_walk_sample, dim3(n), dim3(32), 0, s, n, K, kc, cand_tok, tab, smp->temperature, smp->u,
+                      selected, smp->q_tok, smp->q_p, smp->q_n);
   return launch_pdl(k_sel_walk, dim3(n), dim3(32), 0, s, n, K, kc, cand_tok, tab, selected, scores);
 }
 
@@ -266,6 +314,31 @@ extern "C" dflash_status dflash_select_path(void *stream, int32_t n_req, int32_t
     return DFLASH_ERR_CUDA;
   cudaError_t e = launch_select_path(dtype == DFLASH_BF16, n_req, K, kc, r, vocab, anchors, cand_tok, unary, gate,
                                      pred_codebook, succ_codebook, tab, selected, scores, (cudaStream_t)stream);
+  cudaFreeAsync(tab, (cudaStream_t)stream);
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+extern "C" dflash_status dflash_select_sample(void *stream, int32_t n_req, int32_t K, int32_t kc, int32_t r,
+                                              int32_t vocab, dflash_dtype dtype, float temperature,
+                                              const int32_t *anchors, const int32_t *cand_tok, const float *unary,
+                                              const float *gate, const void *pred_codebook,
+                                              const void *succ_codebook, const float *u, int32_t *selected,
+                                              int32_t *q_tok, float *q_p, int32_t *q_n) {
+  if (n_req < 0 || K < 1 || K > 31 || kc < 1 || kc > SEL_MAX_KC || r < 32 || r > SEL_MAX_R || r % 32 ||
+      vocab < 1 || (dtype != DFLASH_F32 && dtype != DFLASH_BF16) || !(temperature > 0.f))
+    return DFLASH_ERR_INVALID_ARG;
+  if (n_req == 0) return DFLASH_OK;
+  if (!anchors || !cand_tok || !unary || !gate || !pred_codebook || !succ_codebook || !u || !selected || !q_tok ||
+      !q_p || !q_n)
+    return DFLASH_ERR_INVALID_ARG;
+  float *tab = nullptr;
+  if (cudaMallocAsync((void **)&tab, (size_t)n_req * K * kc * kc * sizeof(float), (cudaStream_t)stream) !=
+      cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  const SelSample smp{temperature, u, q_tok, q_p, q_n};
+  cudaError_t e = launch_select_path(dtype == DFLASH_BF16, n_req, K, kc, r, vocab, anchors, cand_tok, unary, gate,
+                                     pred_codebook, succ_codebook, tab, selected, nullptr, (cudaStream_t)stream,
+                                     &smp);
   cudaFreeAsync(tab, (cudaStream_t)stream);
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }

@@ -103,9 +103,19 @@ cudaError_t launch_conv_out_norm(int dtype, int M, int Q, int H, const float *y,
                                  const void *base, float *x, OpOut out, const void *w, float eps,
                                  int out_skip_k, cudaStream_t s);
 cudaError_t launch_to_op(long n, const float *src, OpOut out, cudaStream_t s);
+// Sampling mode of the selector's walk (null: the greedy walk): temperature, uniforms
+// [n][K], and the drawn positions' candidate distributions as lists of stride SMP_K.
+struct SelSample {
+  float temperature;
+  const float *u;
+  int32_t *q_tok;
+  float *q_p;
+  int32_t *q_n;
+};
 cudaError_t launch_select_path(int dtype, int n, int K, int kc, int r, int V, const int32_t *anchors,
                                const int32_t *cand_tok, const float *unary, const float *gate, const void *pred,
-                               const void *succ, float *tab, int32_t *selected, float *scores, cudaStream_t s);
+                               const void *succ, float *tab, int32_t *selected, float *scores, cudaStream_t s,
+                               const SelSample *smp = nullptr);
 
 cudaError_t launch_export_kv(int dtype, const ModelDims &m, int layer, int pos0, int n,
                              const int32_t *pages, const void *pool, void *k_out, void *v_out,

@@ -199,7 +199,12 @@ dflash_status dflash_draft_step_lse(dflash_ctx *ctx, void *stream, int32_t n_req
  * of its top-k with the largest S_t(a, b) = topk_val[t, b] + <A(a) * g_t, B(b)>, a being the
  * token taken at t-1 (the anchor at t = 0), g_t = sel_hidden_proj h_t with h_t the
  * final-normed hidden row of mask position t; equal scores go to the earlier candidate.
- * Scores are computed in fp32. */
+ * Scores are computed in fp32. With sel_uniform [n_req, K] fp32 given, the walk samples
+ * instead (the selector's sampling mode, §3.1.3): position t draws from
+ * q = softmax(S_t(a, .) / sel_temperature) over its candidates, by inverse CDF in vocabulary
+ * order against sel_uniform[b][t]; the drawn token is the next predecessor, and q goes to
+ * sel_q_tok / sel_q_p [n_req, K, 32] (entries 0..topk-1) and sel_q_n [n_req, K] (= topk),
+ * the draft distribution that dflash_verify_sample_q takes. */
 typedef struct {
   int32_t *argmax;
   int32_t *topk_idx;
@@ -207,6 +212,11 @@ typedef struct {
   float *logits;
   float *lse;
   int32_t *selected;
+  float sel_temperature;
+  const float *sel_uniform;
+  int32_t *sel_q_tok;
+  float *sel_q_p;
+  int32_t *sel_q_n;
 } dflash_draft_out;
 
 dflash_status dflash_draft_step_ex(dflash_ctx *ctx, void *stream, int32_t n_req,
@@ -224,6 +234,16 @@ dflash_status dflash_select_path(void *stream, int32_t n_req, int32_t K, int32_t
                                  int32_t vocab, dflash_dtype dtype, const int32_t *anchors, const int32_t *cand_tok,
                                  const float *unary, const float *gate, const void *pred_codebook,
                                  const void *succ_codebook, int32_t *selected, float *scores);
+
+/* The selector's sampling walk on its own (no context): as dflash_select_path, with
+ * temperature > 0 and uniforms u [n_req, K]; outputs selected [n_req, K] and the draft
+ * distributions q_tok / q_p [n_req, K, 32] (entries 0..kc-1), q_n [n_req, K] (= kc). */
+dflash_status dflash_select_sample(void *stream, int32_t n_req, int32_t K, int32_t kc, int32_t r,
+                                   int32_t vocab, dflash_dtype dtype, float temperature,
+                                   const int32_t *anchors, const int32_t *cand_tok, const float *unary,
+                                   const float *gate, const void *pred_codebook, const void *succ_codebook,
+                                   const float *u, int32_t *selected, int32_t *q_tok, float *q_p,
+                                   int32_t *q_n);
 
 /* Greedy verification ("DFlash 2 块扩散投机解码技术详解" §2.3): for each of n_req rows,
  *   draft  [n_req, K] int32 DEVICE, target [n_req, K+1] int32 DEVICE (the target's token
@@ -275,6 +295,18 @@ dflash_status dflash_verify_sample(dflash_ctx *ctx, void *stream, int32_t n_req,
                                    const float *draft_logits, const int32_t *draft,
                                    const float *u_accept, const float *u_resample,
                                    int32_t *accept_len, int32_t *out_tokens, int32_t *next_anchor);
+
+/* dflash_verify_sample with the draft distributions given as candidate lists instead of
+ * draft logits (the path selector's sampling mode, "DFlash 2 块扩散投机解码技术详解" §3.1.3:
+ * its draft distribution lives on the k candidates): q_tok / q_p [n_req, K, 32] DEVICE
+ * (entries 0..q_n-1, distinct tokens, probabilities summing to 1), q_n [n_req, K] DEVICE in
+ * 1..32. The target side is truncated from target_logits as in dflash_verify_sample; the
+ * acceptance test, residual and bonus are the same. */
+dflash_status dflash_verify_sample_q(dflash_ctx *ctx, void *stream, int32_t n_req, const dflash_sampling *sp,
+                                     const float *target_logits, const int32_t *q_tok, const float *q_p,
+                                     const int32_t *q_n, const int32_t *draft, const float *u_accept,
+                                     const float *u_resample, int32_t *accept_len, int32_t *out_tokens,
+                                     int32_t *next_anchor);
 
 /* Draft trees ("DDTree" §2.3 Algorithm 1 / Proposition 2, §3.3 ancestor-only mask, §3.5
  * the verifier walk). No context needed; all pointers DEVICE, row-major.
