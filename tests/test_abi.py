@@ -59,6 +59,9 @@ def _cfg_struct(**over):
     ("mask_token_id", 2048, -1), ("mask_token_id", -1, -1), ("max_batch", 0, -1),
     ("max_positions", 5, -1), ("dtype", 7, -1), ("n_layers", 9, -6), ("target_hidden", 96, -6),
     ("intermediate", 700, -6), ("rms_eps", -1.0, -1),
+    ("block_causal", 2, -1), ("output_multiplier", -1.0, -1), ("logit_softcap", -0.5, -1),
+    ("dyn_conv", 2, -1), ("selector_rank", 48, -6), ("selector_rank", 544, -6), ("selector_rank", 16, -6),
+    ("selector_rank", 64, 0), ("dyn_conv", 1, 0), ("block_causal", 1, 0), ("logit_softcap", 30.0, 0),
 ])
 def test_validate_config(lib, field, value, status):
     c = _cfg_struct(**({field: value} if field else {}))
@@ -88,3 +91,26 @@ def test_package_fails_loudly_without_the_library(tmp_path):
     from block_diffusion_speculative_inject_gb300 import _ffi
     with pytest.raises(ImportError):
         _ffi.load(str(tmp_path / "missing.so"))
+
+
+def test_context_free_calls_check_their_arguments_first(lib):
+    """The tree, selector and top-k calls reject bad sizes on the host, before any CUDA call
+    (so this runs without a GPU), and accept zero requests as a no-op."""
+    P = None
+    # dflash_ddtree_build(stream, n, L, kc, budget, ...): L in 1..31, kc in 1..32, budget in 1..1024
+    for n, L, kc, budget in [(1, 0, 4, 8), (1, 32, 4, 8), (1, 7, 0, 8), (1, 7, 33, 8), (1, 7, 4, 0), (1, 7, 4, 1025),
+                             (-1, 7, 4, 8)]:
+        assert lib.dflash_ddtree_build(P, n, L, kc, budget, P, P, P, P, P, P, P, P, P) == -1
+    assert lib.dflash_ddtree_build(P, 0, 7, 4, 8, P, P, P, P, P, P, P, P, P) == 0
+    assert lib.dflash_ddtree_build(P, 2, 7, 4, 8, P, P, P, P, P, P, P, P, P) == -1      # NULL buffers
+    assert lib.dflash_ddtree_walk(P, 1, 0, 8, P, P, P, P, P, P, P) == -1
+    assert lib.dflash_ddtree_walk(P, 0, 7, 8, P, P, P, P, P, P, P) == 0
+    # dflash_select_path(stream, n, K, kc, r, vocab, dtype, ...): r a multiple of 32 in [32, 512]
+    for n, K, kc, r, V, dt in [(1, 7, 16, 48, 100, 1), (1, 7, 16, 544, 100, 1), (1, 0, 16, 64, 100, 1),
+                               (1, 32, 16, 64, 100, 1), (1, 7, 33, 64, 100, 1), (1, 7, 16, 64, 0, 1),
+                               (1, 7, 16, 64, 100, 5)]:
+        assert lib.dflash_select_path(P, n, K, kc, r, V, dt, P, P, P, P, P, P, P, P) == -1
+    assert lib.dflash_select_path(P, 0, 7, 16, 64, 100, 1, P, P, P, P, P, P, P, P) == 0
+    assert lib.dflash_select_sample(P, 1, 7, 16, 64, 100, 1, ctypes.c_float(0.0), P, P, P, P, P, P, P, P, P, P, P) == -1
+    assert lib.dflash_select_sample(P, 1, 7, 16, 64, 100, 1, ctypes.c_float(1.0), P, P, P, P, P, P, P, P, P, P, P) == -1
+    assert lib.dflash_select_sample(P, 0, 7, 16, 64, 100, 1, ctypes.c_float(1.0), P, P, P, P, P, P, P, P, P, P, P) == 0
