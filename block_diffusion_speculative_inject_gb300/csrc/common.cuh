@@ -180,6 +180,8 @@ struct GemmDesc {
   // rsqrt(sum_{t < rs_tiles} rs_part[t][m] / rs_dim + eps) (null: no scaling)
   const float *rs_part;
   int rs_tiles, rs_dim;
+  int out_skip_k;                // EPI_RESNORM: K > 0 keeps only the K mask rows of each
+                                 // (K+1)-row block (operand and sums at row b*K + j - 1)
 };
 
 __device__ __forceinline__ float logit_xform(float x, float mult, float cap) {

@@ -106,6 +106,7 @@ struct dflash_ctx {
   // projection, after the down projection)
   float *ss_o = nullptr, *ss_d = nullptr;
   float *ss_inj = nullptr;   // the same after the injection's fc ([H/128][32])
+  float *ss_f = nullptr;     // and for the final norm of the K mask rows ([H/128][rows_k])
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -380,7 +381,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj, c->ss_f};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -495,6 +496,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->ss_o, (size_t)(m.H / 128) * R * f4},
       {(void **)&c->ss_d, (size_t)(m.H / 128) * R * f4},
       {(void **)&c->ss_inj, (size_t)(m.H / 128) * 32 * f4},
+      {(void **)&c->ss_f, (size_t)(m.H / 128) * RK * f4},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -804,6 +806,16 @@ static bool fused_topk(const dflash_ctx *c, int rows) { return c->tc && rows <= 
 
 // q/k norm + RoPE and SwiGLU run in the tensor-core GEMM epilogues when a head is one
 // 128-row weight tile; otherwise (FFMA GEMM, head_dim 64) they are separate post-ops.
+static bool fused_epilogues(const dflash_ctx *c);
+
+// Whether a step of R block rows defers its RMSNorms to the next GEMM (the residual add in
+// the output / down projection epilogues, the row scale applied by the consumer). The final
+// norm's operand xf then holds x * w_final, and every GEMM that reads it (the LM head, the
+// selector's gate) takes the row scale from ss_f.
+static bool fused_norms(const dflash_ctx *c, int R) {
+  return fused_epilogues(c) && !c->m.conv && c->m.I % 64 == 0 && R <= 32;
+}
+
 static bool fused_epilogues(const dflash_ctx *c) {
   return c->tc && c->m.hd == 128 && c->m.q_dim() % 128 == 0 && c->m.kv_dim() % 128 == 0;
 }
@@ -864,7 +876,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
   // a batch-1 step is made of; with more rows the epilogue's per-token residual loads cost
   // more than the launches (measured), and the row kernel stays. The last layer's final
   // norm is always the row kernel (it feeds the LM head the K mask rows only).
-  const bool fnorm = fused_epilogues(c) && !m.conv && m.I % 64 == 0 && R <= 32;
+  const bool fnorm = fused_norms(c, R);
   auto rs_from = [&](GemmDesc &d, const float *ss) {
     d.rs_part = ss;
     d.rs_tiles = m.H / 128;
@@ -953,13 +965,16 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     add_wseg(dn, lw.w_down, m.H);
     const bool last = l + 1 == m.L;
     const void *nw = last ? c->w.final_norm : c->layers[l + 1].in_norm;
-    if (fnorm && !last) {
+    if (fnorm) {
+      // the last layer leaves the final norm's operand (K mask rows only) and sums for the
+      // LM head
       dn.epi = EPI_RESNORM;
       dn.y = c->x;
-      dn.out = xn;
+      dn.out = last ? xf : xn;
       dn.ldo = m.H;
       dn.norm_w = nw;
-      dn.ss_part = c->ss_d;
+      dn.ss_part = last ? c->ss_f : c->ss_d;
+      dn.out_skip_k = last ? m.K : 0;
       if ((st = run_gemm(c, K_GEMM_DOWN, dn, s)) != DFLASH_OK) return st;
       continue;
     }
@@ -985,6 +1000,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
     lm.out_xf = m.out_mult != 1.f || m.softcap > 0.f;
     lm.out_mult = m.out_mult;
     lm.out_cap = m.softcap;
+    if (fnorm) rs_from(lm, c->ss_f);
     if ((st = run_gemm(c, K_GEMM_LMHEAD, lm, s)) != DFLASH_OK) return st;
   } else {
     float *lg = logits ? logits : c->logits;
@@ -1155,6 +1171,12 @@ static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
     GemmDesc gd = gemm_desc(RK, r, m.H, EPI_STORE, c->sel_gate, r);
     set_x(c, gd, op_of(c, c->xf, (size_t)c->rows_k_max * m.H), m.H);
     add_wseg(gd, c->w.sel_hidden_proj, r);
+    if (fused_norms(c, B * Q)) {          // xf holds x * w_final: apply the norm's row scale
+      gd.rs_part = c->ss_f;
+      gd.rs_tiles = m.H / 128;
+      gd.rs_dim = m.H;
+      gd.eps = m.eps;
+    }
     if ((st = run_gemm(c, K_SELECT, gd, s)) != DFLASH_OK) return st;
     const double rows = (double)RK * m.topk * 2 + B;
     CK(c, timed(c, K_SELECT, s, rows * r * c->esz + (double)RK * r * 4, 2.0 * RK * m.topk * m.topk * r, 2, [&] {

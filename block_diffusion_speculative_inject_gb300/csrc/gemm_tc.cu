@@ -70,6 +70,7 @@ struct TcParams {
   float *ss_part;
   const float *rs_part;               // row scales of an unnormalised X (or null)
   int rs_tiles, rs_dim;
+  int out_skip_k;                     // EPI_RESNORM: operand rows for the K mask rows only
   int *err;
 };
 
@@ -194,7 +195,9 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
-  const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU || (FN && (p.epi == EPI_RESNORM || p.rs_part));
+  // (the one-split top-k epilogue stages its own layout and scales by rs_lane)
+  const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU ||
+                      (FN && (p.epi == EPI_RESNORM || (p.rs_part && p.epi != EPI_TOPK)));
   const int kb0 = split * p.kb_per;
   const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
 
@@ -308,6 +311,13 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         }
       }
     }
+    // the unstaged top-k epilogue scales token column c by the row scale held by lane c
+    float rs_lane = 1.f;
+    if (FN && p.rs_part && p.epi == EPI_TOPK && m0 + lane < p.M) {
+      float ss = 0.f;
+      for (int t = 0; t < p.rs_tiles; ++t) ss += __ldg(p.rs_part + (size_t)t * p.M + m0 + lane);
+      rs_lane = rsqrtf(ss / (float)p.rs_dim + p.eps);
+    }
     const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
     tc_fence_after();
     const int n = n0 + q * 32 + lane;
@@ -324,7 +334,9 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c0 + j;
           const bool valid = ok && n < p.N && m < p.M;
-          const float v = p.out_xf ? logit_xform(__uint_as_float(r[j]), p.out_mult, p.out_cap) : __uint_as_float(r[j]);
+          float acc = __uint_as_float(r[j]);
+          if (FN && p.rs_part) acc *= __shfl_sync(0xffffffffu, rs_lane, (c0 + j) & 31);
+          const float v = p.out_xf ? logit_xform(acc, p.out_mult, p.out_cap) : acc;
           tile[(c0 + j) * TP + q * 32 + lane] = valid ? v : -INFINITY;
           if (valid && p.y) p.y[(size_t)m * p.ldy + n] = v;
         }
@@ -460,6 +472,15 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             for (int j = 0; j < 4; ++j) x[j] *= rs;
           }
           if (FN && p.epi == EPI_RESNORM) {
+            // out_skip_k = K: only the K mask rows of each (K+1)-row block go on, to row
+            // b*K + j - 1 of the operand and of the sums (the final norm before the LM head)
+            int orow = m, ldss = p.M;
+            if (p.out_skip_k > 0) {
+              const int Q = p.out_skip_k + 1, jj = m % Q;
+              if (jj == 0) continue;
+              orow = (m / Q) * p.out_skip_k + jj - 1;
+              ldss = p.M / Q * p.out_skip_k;
+            }
             float ss = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -467,11 +488,11 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
               const size_t o = (size_t)m * p.ldy + n;
               const float y = p.y ? p.y[o] + x[j] : x[j];       // no residual: the norm alone
               if (p.y) p.y[o] = y;
-              write_op(p.out, (size_t)m * p.ldo + n, y * __bfloat162float(p.norm_w[n]));
+              write_op(p.out, (size_t)orow * p.ldo + n, y * __bfloat162float(p.norm_w[n]));
               ss += y * y;
             }
             ss = warp_sum(ss);
-            if (lane == 0) p.ss_part[(size_t)blockIdx.y * p.M + m] = ss;
+            if (lane == 0) p.ss_part[(size_t)blockIdx.y * ldss + orow] = ss;
             continue;
           }
           if (p.epi == EPI_TOPK) {
@@ -683,7 +704,8 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     return cudaErrorInvalidValue;
   if (d.epi == EPI_RESNORM && (d.N % TC_BM || !d.out.lo || !d.norm_w || !d.ss_part || d.part))
     return cudaErrorInvalidValue;
-  if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1 || d.epi == EPI_TOPK)) return cudaErrorInvalidValue;
+  if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1)) return cudaErrorInvalidValue;
+  if (d.epi == EPI_RESNORM && d.out_skip_k > 0 && d.M % (d.out_skip_k + 1)) return cudaErrorInvalidValue;
   p.n_wseg = d.n_wseg;
   for (int i = 0; i < d.n_wseg; ++i) {
     const long rows = d.w_n0[i + 1] - d.w_n0[i];
@@ -739,6 +761,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.rs_part = d.rs_part;
   p.rs_tiles = d.rs_tiles;
   p.rs_dim = d.rs_dim;
+  p.out_skip_k = d.out_skip_k;
   p.out_mult = d.out_mult;
   p.out_cap = d.out_cap;
   p.err = t->err;
