@@ -134,6 +134,10 @@ enum GemmEpi : int {
                    // place; Y null: no residual, Y stands for acc), out = Y * norm_w as an operand, ss_part[tile][m] = the tile's sum
                    // of Y^2 for row m; the consuming GEMM scales its rows by
                    // rsqrt(sum_tiles ss_part / dim + eps) (rs_part below)
+  EPI_KVCACHE = 6, // injection: W = [Wk_0; Wv_0; Wk_1; ...] (kv_dim rows each, head_dim 128: one
+                   // head per tile); K heads get the layer's k-norm (if any) and RoPE at
+                   // kv_pos[m], and K and V go to the paged cache at slot kv_slot[m] in the
+                   // storage type
 };
 
 constexpr int GEMM_MAX_XSEG = 8;
@@ -182,6 +186,11 @@ struct GemmDesc {
   int rs_tiles, rs_dim;
   int out_skip_k;                // EPI_RESNORM: K > 0 keeps only the K mask rows of each
                                  // (K+1)-row block (operand and sums at row b*K + j - 1)
+  // EPI_KVCACHE (also uses rope, eps, kv_dim)
+  const int32_t *kv_slot, *kv_pos;   // [M] cache slot (page * 64 + offset) and position
+  void *kv_pool;                     // bf16 paged cache [pages][L][2][nkv][64][hd] (V as [hd][64])
+  const void *kv_knorm[8];           // bf16 [hd] per layer, or null (no k-norm)
+  int kv_L, kv_nkv;
 };
 
 __device__ __forceinline__ float logit_xform(float x, float mult, float cap) {

@@ -315,6 +315,8 @@ static void set_x(const dflash_ctx *c, GemmDesc &d, const OpOut &o, int ld) {
   d.ldx[0] = ld;
 }
 
+static bool fused_epilogues(const dflash_ctx *c);
+
 static void add_wseg(GemmDesc &d, const void *w, int rows) {
   int i = d.n_wseg++;
   d.w[i] = w;
@@ -740,6 +742,20 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
       add_wseg(e, c->layers[l].wk, m.kv_dim());
       add_wseg(e, c->layers[l].wv, m.kv_dim());
     }
+    if (fnorm && fused_epilogues(c) && m.L <= 8) {
+      // ... and its epilogue does the k-norm, RoPE and paged-cache write (one head per tile)
+      e.epi = EPI_KVCACHE;
+      e.kv_slot = dslot;
+      e.kv_pos = dslot + n;
+      e.kv_pool = c->pool;
+      for (int l = 0; l < m.L; ++l) e.kv_knorm[l] = m.qk_norm ? c->layers[l].k_norm : nullptr;
+      e.kv_L = m.L;
+      e.kv_nkv = m.nkv;
+      e.kv_dim = m.kv_dim();
+      e.rope = c->rope;
+      if ((st = run_gemm(c, K_GEMM_KV, e, s)) != DFLASH_OK) return st;
+      continue;
+    }
     if ((st = gemm_ws(c, K_GEMM_KV, e, s, &S)) != DFLASH_OK) return st;
     CK(c, timed(c, K_INJECT_KV, s, (double)n * kvw * (4.0 * S + c->esz), 8.0 * n * kvw, 1, [&] {
          return launch_post_kv(c->dtype, m, n, c->ws, S, dslot, dslot + n, c->rope, knorm.data(),
@@ -806,8 +822,6 @@ static bool fused_topk(const dflash_ctx *c, int rows) { return c->tc && rows <= 
 
 // q/k norm + RoPE and SwiGLU run in the tensor-core GEMM epilogues when a head is one
 // 128-row weight tile; otherwise (FFMA GEMM, head_dim 64) they are separate post-ops.
-static bool fused_epilogues(const dflash_ctx *c);
-
 // Whether a step of R block rows defers its RMSNorms to the next GEMM (the residual add in
 // the output / down projection epilogues, the row scale applied by the consumer). The final
 // norm's operand xf then holds x * w_final, and every GEMM that reads it (the LM head, the

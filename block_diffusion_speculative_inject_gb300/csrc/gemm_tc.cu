@@ -71,8 +71,13 @@ struct TcParams {
   const float *rs_part;               // row scales of an unnormalised X (or null)
   int rs_tiles, rs_dim;
   int out_skip_k;                     // EPI_RESNORM: operand rows for the K mask rows only
+  const int32_t *kv_slot, *kv_pos;    // EPI_KVCACHE
+  bf16 *kv_pool;
+  const bf16 *kv_knorm[8];
+  int kv_L, kv_nkv;
   int *err;
 };
+static_assert(sizeof(TcParams) <= 4096, "kernel parameters above 4 KB");
 
 
 
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
   // (the one-split top-k epilogue stages its own layout and scales by rs_lane)
   const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU ||
-                      (FN && (p.epi == EPI_RESNORM || (p.rs_part && p.epi != EPI_TOPK)));
+                      (FN && (p.epi == EPI_RESNORM || p.epi == EPI_KVCACHE || (p.rs_part && p.epi != EPI_TOPK)));
   const int kb0 = split * p.kb_per;
   const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
 
@@ -471,6 +476,34 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] *= rs;
           }
+          if (FN && p.epi == EPI_KVCACHE) {
+            // this tile is one head: K (norm + RoPE) or V of layer l, into the paged cache
+            const int seg = n0 / p.kv_dim, l = seg >> 1, h = (n0 % p.kv_dim) >> 7;
+            const int slot = __ldg(p.kv_slot + m), page = slot / KV_PAGE, off = slot % KV_PAGE;
+            if ((seg & 1) == 0) {
+              const bf16 *kn = p.kv_knorm[l];
+              if (kn) {
+                const float rk =
+                    rsqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]) / 128.f + p.eps);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = x[j] * rk * __bfloat162float(kn[lane + 32 * j]);
+              }
+              const int pos = __ldg(p.kv_pos + m);
+              const float2 c0 = __ldg(p.rope + (size_t)pos * 64 + lane), c1 = __ldg(p.rope + (size_t)pos * 64 + lane + 32);
+              const float o0 = x[0] * c0.x - x[2] * c0.y, o2 = x[2] * c0.x + x[0] * c0.y;
+              const float o1 = x[1] * c1.x - x[3] * c1.y, o3 = x[3] * c1.x + x[1] * c1.y;
+              bf16 *dk = p.kv_pool + kv_block(page, l, 0, h, p.kv_L, p.kv_nkv, 128) + (size_t)off * 128;
+              dk[lane] = __float2bfloat16_rn(o0);
+              dk[lane + 32] = __float2bfloat16_rn(o1);
+              dk[lane + 64] = __float2bfloat16_rn(o2);
+              dk[lane + 96] = __float2bfloat16_rn(o3);
+            } else {
+              bf16 *dv = p.kv_pool + kv_block(page, l, 1, h, p.kv_L, p.kv_nkv, 128) + off;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dv[(size_t)(lane + 32 * j) * KV_PAGE] = __float2bfloat16_rn(x[j]);
+            }
+            continue;
+          }
           if (FN && p.epi == EPI_RESNORM) {
             // out_skip_k = K: only the K mask rows of each (K+1)-row block go on, to row
             // b*K + j - 1 of the operand and of the sums (the final norm before the LM head)
@@ -706,6 +739,10 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     return cudaErrorInvalidValue;
   if (d.rs_part && (d.rs_tiles < 1 || d.rs_dim < 1)) return cudaErrorInvalidValue;
   if (d.epi == EPI_RESNORM && d.out_skip_k > 0 && d.M % (d.out_skip_k + 1)) return cudaErrorInvalidValue;
+  if (d.epi == EPI_KVCACHE && (d.kv_dim % TC_BM || d.kv_L < 1 || d.kv_L > 8 || d.kv_nkv * TC_BM != d.kv_dim ||
+                               d.N != d.kv_L * 2 * d.kv_dim || !d.kv_slot || !d.kv_pos || !d.kv_pool || !d.rope ||
+                               d.part))
+    return cudaErrorInvalidValue;
   p.n_wseg = d.n_wseg;
   for (int i = 0; i < d.n_wseg; ++i) {
     const long rows = d.w_n0[i + 1] - d.w_n0[i];
@@ -762,6 +799,12 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.rs_tiles = d.rs_tiles;
   p.rs_dim = d.rs_dim;
   p.out_skip_k = d.out_skip_k;
+  p.kv_slot = d.kv_slot;
+  p.kv_pos = d.kv_pos;
+  p.kv_pool = (bf16 *)d.kv_pool;
+  for (int l = 0; l < 8; ++l) p.kv_knorm[l] = (const bf16 *)d.kv_knorm[l];
+  p.kv_L = d.kv_L;
+  p.kv_nkv = d.kv_nkv;
   p.out_mult = d.out_mult;
   p.out_cap = d.out_cap;
   p.err = t->err;
@@ -772,7 +815,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     p.epi = EPI_STORE;
   }
   cudaError_t e;
-  if (d.rs_part || d.epi == EPI_RESNORM) {
+  if (d.rs_part || d.epi == EPI_RESNORM || d.epi == EPI_KVCACHE) {
     if (pl.bn > 32) return cudaErrorInvalidValue;      // few-token instances only
     return pl.bn == 16 ? launch_bn<16, true>(t, 4, p, pl, s) : launch_bn<32, true>(t, 5, p, pl, s);
   }
