@@ -81,7 +81,7 @@ __device__ __forceinline__ void raise_wait_err(int *flag, int site, const volati
 enum : int {
   SITE_GEMM_EMPTY = 0x101, SITE_GEMM_FULL = 0x102, SITE_GEMM_ACC = 0x103,
   SITE_ATT_EMPTY = 0x201, SITE_ATT_FULL = 0x202, SITE_ATT_PFULL = 0x203, SITE_ATT_SFULL = 0x204,
-  SITE_ATT_PVDONE = 0x205, SITE_ATT_OFULL = 0x206,
+  SITE_ATT_PVDONE = 0x205, SITE_ATT_OFULL = 0x206, SITE_ATT_COMBINE = 0x207,
 };
 
 // ---------------------------------------------------------------- paged KV pool

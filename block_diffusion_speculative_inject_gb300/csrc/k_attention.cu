@@ -10,6 +10,7 @@
 // (q.k * log2(e) / sqrt(hd)). The combine kernel adds the block's own K+1 keys (fp32, from
 // the q/k/v rows) and merges the splits in a fixed order. Splits run on the tensor cores
 // (k_attention_tc.cu) for bf16 caches with head_dim 128, on the FFMA cores otherwise.
+#include "attn_combine.cuh"
 #include "kernels.h"
 
 namespace dflash {
@@ -134,93 +135,22 @@ __global__ void __launch_bounds__(32 * CB_ROWS) k_attn_combine(int nq, int nkv, 
                                                                float scale_log2, int causal, OpOut o) {
   pdl_trigger();                       // dependents may launch and prefetch; they still wait
   pdl_wait();
-  constexpr int DPL = HD / 32;
-  constexpr int KP = HD + 1;                       // padded row: lane-per-key reads are conflict free
-  __shared__ float ks[32 * KP];
+  __shared__ float ks[32 * CombineSmem<HD>::KP];
   __shared__ float vs[32 * HD];
   __shared__ float qs[CB_ROWS][HD];
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int G = nq / nkv, R = G * Q;
-  const int qkv_dim = (nq + 2 * nkv) * HD;
+  const int R = (nq / nkv) * Q;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  {
-    // block keys and values: float4 loads, all issued before any store
-    constexpr int V4 = HD / 4;
-    float4 kv4[4], vv4[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = tid + u * 32 * CB_ROWS;   // float4 index over [Q][HD/4]
-      const int kk = i / V4, d4 = i % V4;
-      const bool in = kk < Q;
-      const float4 *row = (const float4 *)(qkv + ((size_t)b * Q + (in ? kk : 0)) * qkv_dim + (size_t)nq * HD);
-      kv4[u] = in ? row[(size_t)kvh * V4 + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
-      vv4[u] = in ? row[(size_t)(nkv + kvh) * V4 + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = tid + u * 32 * CB_ROWS;
-      const int kk = i / V4, d4 = i % V4;
-      if (kk < Q) {
-        const float4 a = kv4[u], v = vv4[u];
-        ks[kk * KP + 4 * d4 + 0] = a.x; ks[kk * KP + 4 * d4 + 1] = a.y;
-        ks[kk * KP + 4 * d4 + 2] = a.z; ks[kk * KP + 4 * d4 + 3] = a.w;
-        *(float4 *)&vs[kk * HD + 4 * d4] = v;
-      }
-    }
-  }
+  const CombineSmem<HD> sm{ks, vs};
   const int r = blockIdx.z * CB_ROWS + warp;
-  const int g = r / Q, j = r % Q, h = kvh * G + g;
-  const size_t row = (size_t)b * Q + j;
   const int ns = n_split[b];
-  const size_t base = (row * nq + h) * max_split;
-  // every load of this row (its q, the splits' (m, l) and partial outputs) is issued before
-  // any of them is used: one round trip instead of one per split
-  float ms = -INFINITY, ls = 0.f;
-  float po[MS][DPL];
-  if (r < R) {
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) qs[warp][lane + 32 * d] = qkv[row * qkv_dim + (size_t)h * HD + lane + 32 * d];
-    if (lane < ns) {
-      ms = part_ml[(base + lane) * 2];
-      ls = part_ml[(base + lane) * 2 + 1];
-    }
-#pragma unroll
-    for (int sp = 0; sp < MS; ++sp)
-#pragma unroll
-      for (int d = 0; d < DPL; ++d)
-        po[sp][d] = sp < ns ? part_o[(base + sp) * HD + lane + 32 * d] : 0.f;
-  }
+  // the block K/V first (its registers are free again before the row's loads go out)
+  stage_block_kv<HD>(b, kvh, nq, nkv, Q, qkv, sm, tid, 32 * CB_ROWS);
+  CombineRow<HD, MS> cr;
+  if (r < R) combine_load<HD, MS, false>(cr, r, b, kvh, nq, nkv, Q, ns, max_split, part_o, part_ml, qkv, qs[warp], lane);
   __syncthreads();
   if (r >= R) return;
-  // block key `lane` is seen by this row unless the causal variant hides keys after it
-  const bool see = lane < Q && (!causal || lane <= j);
-  float sk = -INFINITY;
-  if (see) {
-    float t = 0.f;
-#pragma unroll 16
-    for (int d = 0; d < HD; ++d) t = fmaf(qs[warp][d], ks[lane * KP + d], t);
-    sk = t * scale_log2;
-  }
-  const float M = warp_max(fmaxf(sk, ms));
-  const float pk = see ? exp2f(sk - M) : 0.f;
-  const float cs = lane < ns ? exp2f(ms - M) : 0.f;
-  const float Lsum = warp_sum(pk + cs * ls);
-  float acc[DPL] = {};
-#pragma unroll
-  for (int sp = 0; sp < MS; ++sp) {
-    const float c = __shfl_sync(0xffffffffu, cs, sp);     // 0 for sp >= ns
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(c, po[sp][d], acc[d]);
-  }
-  for (int kk = 0; kk < Q; ++kk) {
-    const float p = __shfl_sync(0xffffffffu, pk, kk);
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[d] = fmaf(p, vs[kk * HD + lane + 32 * d], acc[d]);
-  }
-  const float inv = 1.f / Lsum;
-  const size_t dst = row * (nq * HD) + (size_t)h * HD;
-#pragma unroll
-  for (int d = 0; d < DPL; ++d) write_op(o, dst + lane + 32 * d, acc[d] * inv);
+  combine_finish<HD, MS>(cr, r, b, kvh, nq, nkv, Q, ns, scale_log2, causal, o, sm, qs[warp], lane);
 }
 
 template <typename T, int HD>
@@ -232,7 +162,9 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
   cudaError_t e = cudaSuccess;
   if (bt.max_split > 0) {
     if (maps && maps->valid && HD == 128 && sizeof(T) == 2) {
-      e = launch_attn_split_tc(m, bt, layer, qkv, maps, scale_log2, part_o, part_ml, s);
+      const bool fuse = attn_fused_combine(m, bt, maps);
+      e = launch_attn_split_tc(m, bt, layer, qkv, maps, scale_log2, part_o, part_ml, s, fuse, o);
+      if (e != cudaSuccess || fuse) return e;        // fused: the splits merged themselves
     } else {
       size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
       e = cudaFuncSetAttribute(k_attn_split<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
