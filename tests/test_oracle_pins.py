@@ -944,3 +944,29 @@ def test_rejection_sampling_with_selector_q_is_exact(seed):
     law = _exact_output_distribution(lambda prefix: p0 if len(prefix) == 0 else p1, [qf], V, 1)
     for seq in itertools.product(range(V), repeat=2):
         assert law.get(seq, 0) == p0[seq[0]] * p1[seq[1]], seq
+
+
+def test_ddtree_takes_every_prefix_when_the_budget_allows():
+    """With a budget above the number of prefixes (sum of kc^d for d = 1..L) the tree is the
+    whole prefix tree, in an order that pops every parent first, and stops there."""
+    rng = np.random.default_rng(91)
+    L, kc = 3, 2
+    lp = np.log(-np.sort(-rng.dirichlet(np.ones(kc), size=L), axis=1))
+    tok = np.arange(L * kc).reshape(L, kc)
+    nodes = O.ddtree_build(lp, tok, 100)
+    assert len(nodes) == sum(kc ** d for d in range(1, L + 1))
+    assert len(set(_tuples(nodes))) == len(nodes)
+    assert all(parent < i for i, (_, parent, _, _) in enumerate(nodes))
+
+
+def test_bench_prefill_flops_match_the_scope_table():
+    """The bench's prefill FLOP count (fc and every layer's K/V projection, once per
+    position) for the 27B-shaped draft's whole contexts: 96.2 TF for 262,144 positions."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(os.path.dirname(GOLDEN), "..", "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from synth import get_config
+    rep = bench._prefill_report(get_config("q27b_b8"), 1000.0, 8 * 32768)
+    assert abs(rep["tflops"] * 1.0 - 96.2) < 0.1       # over 1 s
+    assert rep["positions"] == 262144
