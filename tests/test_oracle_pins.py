@@ -970,3 +970,37 @@ def test_bench_prefill_flops_match_the_scope_table():
     rep = bench._prefill_report(get_config("q27b_b8"), 1000.0, 8 * 32768)
     assert abs(rep["tflops"] * 1.0 - 96.2) < 0.1       # over 1 s
     assert rep["positions"] == 262144
+
+
+def test_select_path_worked_example_golden():
+    """The pages' walk: with the printed scores (as unary scores, no pair term) the path is
+    cat, sat."""
+    g = json.load(open(os.path.join(GOLDEN, "selector_walk_example.json")))
+    v = g["vocab"]
+    cand = np.array([[v[t] for t in pos["candidates"]] for pos in g["positions"]])
+    unary = np.array([pos["scores"] for pos in g["positions"]])
+    A = np.zeros((len(v), 4))
+    toks, _ = O.select_path(v[g["anchor"]], cand, unary, np.ones((len(cand), 4)), A, A)
+    inv = {i: t for t, i in v.items()}
+    assert [inv[int(t)] for t in toks] == g["expected_path"]
+
+
+@pytest.mark.parametrize("L,V,budget", [(3, 3, 5), (2, 4, 6), (3, 2, 7)])
+def test_ddtree_value_is_the_expected_acceptance_under_q(L, V, budget):
+    """Proposition 1: under the drafter's factorized distribution Q, the expected number of
+    tokens a tree accepts (the longest prefix of Y that is a path of the tree) equals the sum
+    of its nodes' prefix probabilities. Brute force over every Y in V^L."""
+    rng = np.random.default_rng(L * 10 + V + budget)
+    q = rng.dirichlet(np.ones(V), size=L)                       # [L][V], full distributions
+    order = np.argsort(-q, axis=1, kind="stable")
+    lp = np.log(np.take_along_axis(q, order, 1))
+    nodes = O.ddtree_build(lp, order, budget)
+    paths = set(_tuples(nodes))
+    expect = 0.0
+    for y in itertools.product(range(V), repeat=L):
+        prob = np.prod([q[i][y[i]] for i in range(L)])
+        a = 0
+        while a < L and tuple(y[:a + 1]) in paths:
+            a += 1
+        expect += prob * a
+    np.testing.assert_allclose(expect, sum(np.exp(n[3]) for n in nodes), rtol=1e-12)
