@@ -99,17 +99,24 @@ __host__ __device__ __forceinline__ size_t kv_block(int page, int l, int kv, int
 // Activations are fp32. Where an activation is the X operand of a GEMM it is written as
 // an "operand": fp32 for fp32 weights, or for bf16 weights an exact pair of bf16 planes
 // hi = bf16(v), lo = bf16(v - hi), so a bf16 tensor-core product W.hi + W.lo carries the
-// activation to ~2^-17 relative precision.
+// activation to ~2^-17 relative precision. The fused context feature g, whose K/V
+// projection is rounded to the storage type when cached, takes a third plane
+// lo2 = bf16(v - hi - lo) (~2^-25 relative): with two planes the cached values land on
+// the other neighbour of their rounding often enough to move the logits by ~2e-3.
 struct OpOut {
-  void *hi;   // fp32 [rows, ld] when lo == nullptr, else bf16 [rows, ld]
-  void *lo;   // bf16 [rows, ld] or nullptr
+  void *hi;              // fp32 [rows, ld] when lo == nullptr, else bf16 [rows, ld]
+  void *lo;              // bf16 [rows, ld] or nullptr
+  void *lo2 = nullptr;   // bf16 [rows, ld] third plane, or nullptr
 };
 
 __device__ __forceinline__ void write_op(const OpOut &o, size_t idx, float v) {
   if (o.lo) {
-    bf16 h = __float2bfloat16_rn(v);
+    const bf16 h = __float2bfloat16_rn(v);
+    const float r = v - __bfloat162float(h);           // exact in fp32
+    const bf16 l = __float2bfloat16_rn(r);
     ((bf16 *)o.hi)[idx] = h;
-    ((bf16 *)o.lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+    ((bf16 *)o.lo)[idx] = l;
+    if (o.lo2) ((bf16 *)o.lo2)[idx] = __float2bfloat16_rn(r - __bfloat162float(l));
   } else {
     ((float *)o.hi)[idx] = v;
   }
@@ -149,6 +156,7 @@ struct GemmDesc {
   int n_xseg;
   const void *x[GEMM_MAX_XSEG];
   const void *x_lo[GEMM_MAX_XSEG];   // lo plane (bf16 pair) or nullptr
+  const void *x_lo2;             // third plane of segment 0 (with x_lo[0]) or nullptr
   int x_k0[GEMM_MAX_XSEG + 1];   // K offset where segment s starts; x_k0[n_xseg] = K
   int ldx[GEMM_MAX_XSEG];        // row stride (elements) of each X segment
   int n_wseg;

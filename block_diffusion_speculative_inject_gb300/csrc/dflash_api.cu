@@ -254,7 +254,7 @@ static dflash_status stage_upload_to(dflash_ctx *c, cudaStream_t s, const void *
 }
 
 static dflash_status run_gemm(dflash_ctx *c, int cls, const GemmDesc &d, cudaStream_t s) {
-  const double xsz = (d.x_bf16 && !d.x_lo[0]) ? 2.0 : 4.0;
+  const double xsz = !d.x_bf16 ? 4.0 : d.x_lo2 ? 6.0 : d.x_lo[0] ? 4.0 : 2.0;
   const double out_bytes = d.epi == EPI_SWIGLU ? (double)d.M * (d.N / 2) * 4.0
                                                : (double)d.M * d.N * 4.0 * (d.epi == EPI_RESID ? 2 : 1);
   const double bytes = (double)d.N * d.K * c->esz + (double)d.M * d.K * xsz + out_bytes;
@@ -311,6 +311,7 @@ static void set_x(const dflash_ctx *c, GemmDesc &d, const OpOut &o, int ld) {
   d.n_xseg = 1;
   d.x[0] = o.hi;
   d.x_lo[0] = o.lo;
+  d.x_lo2 = o.lo2;
   d.x_k0[0] = 0;
   d.x_k0[1] = d.K;
   d.ldx[0] = ld;
@@ -487,7 +488,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->part_o, (size_t)R * m.nq * kMaxSplit * m.hd * f4},
       {(void **)&c->part_ml, (size_t)R * m.nq * kMaxSplit * 2 * f4},
       {(void **)&c->fc_out, (size_t)C * m.H * f4},
-      {&c->g, (size_t)C * m.H * f4},
+      {&c->g, (size_t)C * m.H * (c->dtype == DFLASH_BF16 ? 6 : 4)},
       {(void **)&c->kvproj, (size_t)C * m.L * 2 * m.kv_dim() * f4},
       {(void **)&c->smp_tok, (size_t)(R + RK) * SMP_K * sizeof(int32_t)},
       {(void **)&c->smp_p, (size_t)(R + RK) * SMP_K * sizeof(float)},
@@ -719,6 +720,7 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     add_wseg(d, c->w.fc, m.H);
     int S = 1;
     OpOut g = op_of(c, c->g, (size_t)C * m.H);
+    if (g.lo) g.lo2 = (bf16 *)g.lo + (size_t)C * m.H;   // g carries three planes
     // few rows on the tensor cores: the fc epilogue writes fc_out * fc_norm and its per-tile
     // sums of squares, and the K/V GEMM applies the RMSNorm row scale (one launch fewer)
     const bool fnorm = c->tc && c->dtype == DFLASH_BF16 && n <= 32;

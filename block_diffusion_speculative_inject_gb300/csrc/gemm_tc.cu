@@ -6,9 +6,10 @@
 // The draft step multiplies few token rows (16 at batch 1) by large weight matrices, so
 // the product is computed transposed ("swap AB"): a CTA owns 128 weight rows (the UMMA M
 // dimension) and BN token rows (the UMMA N dimension, 16..128), and streams its weight
-// slab through the pipeline once. When X is an exact bf16 hi/lo pair (an fp32 activation),
-// both planes are multiplied by the same staged weight tile and accumulate into the same
-// TMEM columns, so the weights are read from HBM once. Small grids are split along K
+// slab through the pipeline once. When X is an exact bf16 hi/lo pair (an fp32 activation;
+// hi/lo/lo2 for the injected context feature), every plane is multiplied by the same staged
+// weight tile and accumulates into the same TMEM columns, so the weights are read from HBM
+// once. Small grids are split along K
 // (split-K, S <= 8) so every SM streams weights; the S CTAs of one output tile form a
 // thread-block cluster, stage their fp32 partial tiles in their own shared memory, and each
 // rank sums a share of the tile's columns over all ranks through distributed shared memory,
@@ -41,12 +42,12 @@ constexpr int TC_THREADS = 192;
 
 struct TcParams {
   CUtensorMap wmap[TC_MAX_WSEG];      // one per weight segment, box {64, 128}
-  CUtensorMap xmap[TC_MAX_XMAP];      // X segments (box {64, BN}); split: [0] hi, [1] lo
+  CUtensorMap xmap[TC_MAX_XMAP];      // X segments (box {64, BN}); planes > 1: [0] hi, [1] lo, [2] lo2
   int n_wseg;
   int w_n0[TC_MAX_WSEG + 1];
   int n_xseg;
   int x_k0[TC_MAX_XMAP + 1];
-  int split;                          // X is a hi/lo pair
+  int planes;                         // X planes: 1, or 2 / 3 for a split fp32 activation
   int M, N, K;
   int kb_total, kb_per, S;
   int stages;
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   pdl_trigger();
   constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
   constexpr uint32_t B_BYTES = BN * TC_BK * 2;
-  const uint32_t stage_bytes = A_BYTES + B_BYTES * (p.split ? 2 : 1);
+  const uint32_t stage_bytes = A_BYTES + B_BYTES * p.planes;
   const int stages = p.stages;
 
   const uint32_t raw = smem_u32(smem_raw);
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     // the activation maps are first used after the dependency wait: fetch them now
     tma_prefetch_map(wm);
     if (glu) tma_prefetch_map(&p.wmap[1]);
-    for (int i = 0; i < (p.split ? 2 : p.n_xseg); ++i) tma_prefetch_map(&p.xmap[i]);
+    for (int i = 0; i < (p.planes > 1 ? p.planes : p.n_xseg); ++i) tma_prefetch_map(&p.xmap[i]);
     // the first stages' weight tiles do not depend on the previous kernel: start streaming
     // them before waiting for it
     const int pre = min(stages, nkb);
@@ -261,9 +262,8 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         mbar_expect_tx(fb, stage_bytes);
         load_w(st, k, fb);
       }
-      if (p.split) {
-        tma_load_2d(st + A_BYTES, &p.xmap[0], k, m0, fb);
-        tma_load_2d(st + A_BYTES + B_BYTES, &p.xmap[1], k, m0, fb);
+      if (p.planes > 1) {
+        for (int pl = 0; pl < p.planes; ++pl) tma_load_2d(st + A_BYTES + pl * B_BYTES, &p.xmap[pl], k, m0, fb);
       } else {
         int xs = 0;
         while (xs + 1 < p.n_xseg && k >= p.x_k0[xs + 1]) ++xs;
@@ -292,10 +292,10 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       for (int kk = 0; kk < TC_BK / 16; ++kk)
         umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                   (i > 0 || kk > 0) ? 1u : 0u);
-      if (p.split) {
+      for (int pl = 1; pl < p.planes; ++pl) {
 #pragma unroll
         for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + B_BYTES + kk * 32), idesc, 1u);
+          umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc, 1u);
       }
       umma_commit(empty0 + 8u * s);       // frees the stage once these MMAs have read it
     }
@@ -670,8 +670,8 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   p.t_tiles = (d.M + p.bn - 1) / p.bn;
   p.n_tiles = (d.N + TC_BM - 1) / TC_BM;
   p.kb = d.K / TC_BK;
-  const bool split = d.x_lo[0] != nullptr;
-  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * (split ? 2 : 1);
+  const int planes = 1 + (d.x_lo[0] ? 1 : 0) + (d.x_lo2 ? 1 : 0);
+  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * planes;
   // Few token rows: a short pipeline and many resident CTAs per SM stream weights fastest
   // (measured); more token rows: a longer pipeline in a CTA of its own.
   p.stages = p.bn <= 32 ? 3 : (int)std::max<size_t>(2, std::min<size_t>(8, (200 * 1024) / stage));
@@ -724,7 +724,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
   if (d.epi == EPI_TOPK && (d.topk < 1 || d.topk > 32 || !d.cand)) return cudaErrorInvalidValue;
   if (!d.x_bf16 || d.K % TC_BK || d.n_wseg > TC_MAX_WSEG || d.n_xseg > TC_MAX_XMAP ||
-      (d.x_lo[0] && d.n_xseg != 1))
+      (d.x_lo[0] && d.n_xseg != 1) || (d.x_lo2 && !d.x_lo[0]))
     return cudaErrorInvalidValue;
   const Plan pl = plan_for(t, d);
   TcParams p;   // kernel parameters (copied at launch)
@@ -751,11 +751,12 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     p.w_n0[i] = d.w_n0[i];
   }
   p.w_n0[d.n_wseg] = d.w_n0[d.n_wseg];
-  p.split = d.x_lo[0] != nullptr;
+  p.planes = 1 + (d.x_lo[0] ? 1 : 0) + (d.x_lo2 ? 1 : 0);
   p.n_xseg = d.n_xseg;
-  if (p.split) {
+  if (p.planes > 1) {
     if (!get_map(t, d.x[0], d.M, d.K, d.ldx[0], pl.bn, &p.xmap[0]) ||
-        !get_map(t, d.x_lo[0], d.M, d.K, d.ldx[0], pl.bn, &p.xmap[1]))
+        !get_map(t, d.x_lo[0], d.M, d.K, d.ldx[0], pl.bn, &p.xmap[1]) ||
+        (d.x_lo2 && !get_map(t, d.x_lo2, d.M, d.K, d.ldx[0], pl.bn, &p.xmap[2])))
       return cudaErrorInvalidValue;
     p.x_k0[0] = 0;
     p.x_k0[1] = d.K;

@@ -16,6 +16,7 @@ __device__ __forceinline__ float load_x(const GemmDesc &d, int s, size_t idx) {
   if (!d.x_bf16) return ((const float *)d.x[s])[idx];
   float v = to_f(((const bf16 *)d.x[s])[idx]);
   if (d.x_lo[s]) v += to_f(((const bf16 *)d.x_lo[s])[idx]);
+  if (s == 0 && d.x_lo2) v += to_f(((const bf16 *)d.x_lo2)[idx]);
   return v;
 }
 

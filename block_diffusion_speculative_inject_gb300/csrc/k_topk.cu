@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_chunks(int V, int k, int ch
   __shared__ int32_t idx[32];
   __shared__ float val[32];
   __shared__ int32_t first;
-  const int chunk = blockIdx.x, row = blockIdx.y;
+  const int row = blockIdx.x, chunk = blockIdx.y;      // rows on x: up to 2^31 - 1 of them
   const int v0 = chunk * NA_CHUNK, n = min(NA_CHUNK, V - v0);
   const float *x = logits + (size_t)row * V + v0;
   block_topk(n, k, [&](int i, float &v, int &id) { v = x[i]; id = v0 + i; }, &first, idx, val);
@@ -670,6 +670,7 @@ extern "C" dflash_status dflash_topk_noalloc(void *stream, int32_t rows, int32_t
   if (!logits || !argmax || ((topk_idx == nullptr) != (topk_val == nullptr)))
     return fail(DFLASH_ERR_INVALID_ARG, "logits and argmax are required; topk_idx/topk_val both or neither");
   const long chunks = (vocab + NA_CHUNK - 1) / NA_CHUNK;
+  if (chunks > 65535) return fail(DFLASH_ERR_INVALID_ARG, "vocab above 65535 * 4096 entries");
   if ((long)rows * chunks * k > NA_MAX_CAND) {
     char why[200];
     snprintf(why, sizeof why, "rows * ceil(vocab/%d) * k = %ld exceeds the fixed scratch of %ld candidates",
@@ -693,7 +694,7 @@ extern "C" dflash_status dflash_topk_noalloc(void *stream, int32_t rows, int32_t
     scratch = g_na_ptr[dev];
   }
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_pdl(k_topk_chunks, dim3((unsigned)chunks, (unsigned)rows), dim3(TK_THREADS), 0, s,
+  cudaError_t e = launch_pdl(k_topk_chunks, dim3((unsigned)rows, (unsigned)chunks), dim3(TK_THREADS), 0, s,
                              (int)vocab, (int)k, (int)chunks, (int)rows, logits, scratch);
   if (e == cudaSuccess)
     e = launch_topk_merge((int)chunks, rows, k, scratch, argmax, topk_idx, topk_val, nullptr, nullptr, s);

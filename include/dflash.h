@@ -389,7 +389,8 @@ dflash_status dflash_timing_read(dflash_ctx *ctx, double *ms, int64_t *launches,
  * recorded into a CUDA graph, or runtimes that own a fixed device-memory budget.
  *   logits [rows, vocab] fp32 DEVICE; argmax [rows] int32 DEVICE; topk_idx [rows, k] int32
  *   and topk_val [rows, k] fp32 DEVICE or both NULL; 1 <= k <= min(32, vocab);
- *   rows * ceil(vocab / 4096) * k must not exceed 524288 (else DFLASH_ERR_INVALID_ARG).
+ *   rows * ceil(vocab / 4096) * k must not exceed 524288, and vocab not 65535 * 4096
+ *   (else DFLASH_ERR_INVALID_ARG, before any launch).
  *   msg (optional, msg_len bytes) receives the reason of an error.
  * The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress); make it before any stream capture. Every call, from any thread

@@ -12,7 +12,7 @@ import oracle as O
 from synth import get_config
 from synth import inputs as S
 
-from harness import TOPK_GAP, LOGIT_TOL, check_argmax, check_logits, check_topk, to_np, weights_cuda, weights_np
+from harness import LOGIT_TOL, check_argmax, check_logits, check_topk, to_np, weights_cuda, weights_np
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -68,7 +68,7 @@ def _run(cfg_name, sample, steps, ctx_override=None):
             lg = to_np(out["logits"][r])
             check_logits(cfg, lg, w_lg, f"{cfg_name} step {step} req {r}")
             check_argmax(am[r], w_lg, f"{cfg_name} step {step} req {r}")
-            check_topk(ti[r], tv[r], w_lg, cfg.topk, tol, f"{cfg_name} step {step} req {r}", TOPK_GAP[cfg.dtype])
+            check_topk(ti[r], tv[r], w_lg, cfg.topk, tol, f"{cfg_name} step {step} req {r}")
             oam[r] = w_am
         target = S.make_targets(cfg, torch.from_numpy(oam), 0, step)
         acc, toks, nxt = ctx.verify(out["argmax"], target.cuda())
@@ -94,5 +94,6 @@ def test_q4b_b128_large_batch():
 
 
 def test_q27b_b8_long_context():
-    """27B-target-shaped draft, 8 requests of context 32768, K=15; request 5."""
-    _run("q27b_b8", sample=(5,), steps=2)
+    """27B-target-shaped draft, 8 requests of context 32768, K=15; request 5, over 8
+    consecutive verify-driven steps (each injects the a + 1 positions its verify accepted)."""
+    _run("q27b_b8", sample=(5,), steps=8)

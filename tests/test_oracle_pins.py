@@ -1004,3 +1004,99 @@ def test_ddtree_value_is_the_expected_acceptance_under_q(L, V, budget):
             a += 1
         expect += prob * a
     np.testing.assert_allclose(expect, sum(np.exp(n[3]) for n in nodes), rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- block forward tail
+class _Recorder(O.OracleDraft):
+    """The oracle with each layer's input rows and positions recorded."""
+
+    def layer(self, x, l, ctx_k, ctx_v, pos):
+        self.seen.append((l, np.array(x), np.array(pos)))
+        return super().layer(x, l, ctx_k, ctx_v, pos)
+
+
+def _torch_block_logits(c, w, feats, anchor):
+    """The K mask rows' logits from torch fp64 library routines alone: the context K/V from
+    g = rms_norm(linear(concat(h_f), W_fc)) through each layer's k/v projection (k-norm,
+    RoPE at positions 0..n-1), the block as F.embedding([anchor, mask x K]) scaled by
+    input_embedding_scale on every row, the decoder layers at positions n..n+K, the final
+    rms_norm of rows 1..K and F.linear with the LM-head matrix."""
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    n = feats[0].shape[0]
+    cat = torch.cat([t(f) for f in feats], 1)
+    g = F.rms_norm(F.linear(cat, t(w["fc"])), (c.hidden,), t(w["fc_norm"]), eps=c.rms_eps)
+    toks = torch.tensor([anchor] + [c.mask_id] * c.block_k)
+    x = F.embedding(toks, t(w["embed"])) * c.input_embedding_scale
+    pos = np.arange(n, n + c.block_k + 1)
+    X = x.numpy()
+    for l, lw in enumerate(w["layers"]):
+        k = F.linear(g, t(lw["wk"])).view(n, c.n_kv_heads, c.head_dim)
+        v = F.linear(g, t(lw["wv"])).view(n, c.n_kv_heads, c.head_dim)
+        k = F.rms_norm(k, (c.head_dim,), t(lw["k_norm"]), eps=c.rms_eps)
+        k = O.rope(k.numpy(), np.arange(n), c.rope_theta)
+        X = _torch_layer(c, lw, X, k, v.numpy(), pos)
+    h = F.rms_norm(t(X)[1:], (c.hidden,), t(w["final_norm"]), eps=c.rms_eps)
+    return F.linear(h, t(w["lm_head"])).numpy()
+
+
+@pytest.mark.parametrize("scale", [0.5, 1.0, 3.0])
+def test_block_logits_match_torch_composition(scale):
+    """hidden() and logits(): the embedding gather x input_embedding_scale on all K+1 block
+    rows ("DFlash 2 块扩散投机解码技术详解" §2.2), block positions ctx_len + j, the anchor
+    row dropped ("DFlash：把串行 Draft 变成并行“填空”" §4.3), the final norm and the LM-head
+    product, against an independent torch composition. The LM head differs from the
+    embedding, so using one for the other fails."""
+    c = _cfg(input_embedding_scale=scale)
+    w = _weights(c, seed=40)
+    assert np.max(np.abs(w["lm_head"] - w["embed"])) > 0.1
+    od = O.OracleDraft(c, w)
+    fe = _feats(c, 23, 41)
+    od.inject(0, fe)
+    for anchor in (3, 250):
+        want = _torch_block_logits(c, w, fe, anchor)
+        np.testing.assert_allclose(od.logits(0, anchor), want, rtol=1e-9, atol=1e-10)
+        # hidden() is the final-normed K mask rows that the LM head multiplies
+        np.testing.assert_allclose(od.hidden(0, anchor) @ w["lm_head"].T, want, rtol=1e-9, atol=1e-10)
+
+
+def test_input_embedding_scale_multiplies_every_block_row_of_the_first_layer_input():
+    c = _cfg(input_embedding_scale=2.5)
+    w = _weights(c, seed=42)
+    od = _Recorder(c, w)
+    od.seen = []
+    od.inject(0, _feats(c, 9, 43))
+    od.hidden(0, 17)
+    l0, x0, pos0 = od.seen[0]
+    assert l0 == 0 and x0.shape == (c.block_k + 1, c.hidden)
+    want = w["embed"][[17] + [c.mask_id] * c.block_k] * 2.5
+    np.testing.assert_array_equal(x0, want)
+    np.testing.assert_array_equal(pos0, np.arange(9, 9 + c.block_k + 1))
+    # every layer sees the same block positions
+    assert all(np.array_equal(p, pos0) for _, _, p in od.seen)
+    # the scale acts through the residual stream: the logits move with it
+    c1 = _cfg(input_embedding_scale=1.0)
+    od1 = O.OracleDraft(c1, w)
+    od1.inject(0, _feats(c1, 9, 43))
+    assert np.max(np.abs(od1.logits(0, 17) - O.OracleDraft.logits(od, 0, 17))) > 1e-3
+
+
+def test_hidden_equals_inline_prepended_context_rows():
+    """One layer, unit input norm, eps 0, unit fc norm: the context enters as leading rows of
+    one sequence [g rows ; scaled block embeddings] at positions 0..n+K with no cache, and
+    the final-normed rows n+1..n+K of that sequence equal hidden() ("LLM的推理加速-DFlash"
+    关键创新 Step 3: g goes through the same K/V projection, prepended to the block)."""
+    for scale in (0.5, 4.0):
+        c = _cfg(n_layers=1, rms_eps=0.0, input_embedding_scale=scale)
+        w = _weights(c, seed=44)
+        w["fc_norm"] = np.ones(c.hidden)
+        w["layers"][0]["in_norm"] = np.ones(c.hidden)
+        od = O.OracleDraft(c, w)
+        n = 13
+        fe = _feats(c, n, 45)
+        od.inject(0, fe)
+        g = od.fuse(fe)
+        xb = w["embed"][[7] + [c.mask_id] * c.block_k] * scale
+        empty = np.zeros((0, c.n_kv_heads, c.head_dim))
+        seq = od.layer(np.concatenate([g, xb]), 0, empty, empty, np.arange(n + c.block_k + 1))
+        want = O.rmsnorm(seq[n + 1:], w["final_norm"], c.rms_eps)
+        np.testing.assert_allclose(od.hidden(0, 7), want, rtol=1e-10, atol=1e-11)

@@ -73,3 +73,43 @@ def test_noalloc_topk_rejects_sizes_beyond_its_scratch():
     st = lib.dflash_topk_noalloc(null, 1, 8, 33, ctypes.c_void_p(logits.data_ptr()),
                                  ctypes.c_void_p(logits.data_ptr()), None, None, msg, 256)
     assert st == -1
+
+
+def test_noalloc_topk_full_vocabulary_with_ties_across_chunks():
+    """vocab 151936 (38 chunks of 4096, more chunks than k = 16, so the merge takes its
+    candidate-pool path) against the definition: values descending, ties to the lower index.
+    Row 1 plants equal values on both sides of chunk boundaries; row 2 is constant."""
+    import oracle as O
+    from block_diffusion_speculative_inject_gb300 import build, library
+    build.build()
+    lib = library()
+    g = torch.Generator().manual_seed(3)
+    V, k = 151936, 16
+    x = torch.randn((4, V), generator=g)
+    for c in (1, 5, 17, 36):                 # 8 equal maxima straddling chunk edges
+        x[1, c * 4096 - 1] = 9.0
+        x[1, c * 4096] = 9.0
+    x[1, 100] = 9.0
+    x[2] = 0.25
+    x[3, -1] = 50.0                          # the last entry of the ragged last chunk
+    for call in range(2):
+        st, msg, am, ti, tv = _noalloc(lib, x.cuda(), k)
+        torch.cuda.synchronize()
+        assert st == 0, msg
+        want_idx, want_val = O.topk_desc(x.double().numpy(), k)
+        np.testing.assert_array_equal(ti.cpu().numpy(), want_idx)
+        np.testing.assert_array_equal(tv.cpu().numpy(), want_val.astype(np.float32))
+        np.testing.assert_array_equal(am.cpu().numpy(), want_idx[:, 0])
+    assert ti[1, :9].tolist() == [100, 4095, 4096, 20479, 20480, 69631, 69632, 147455, 147456]
+    assert ti[2].tolist() == list(range(k))
+
+
+def test_noalloc_topk_more_rows_than_a_grid_dimension_of_65535():
+    from block_diffusion_speculative_inject_gb300 import library
+    lib = library()
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn((70000, 8), generator=g)
+    st, msg, am, ti, tv = _noalloc(lib, x.cuda(), 1)
+    torch.cuda.synchronize()
+    assert st == 0, msg
+    np.testing.assert_array_equal(am.cpu().numpy(), x.argmax(1).numpy())
