@@ -72,6 +72,24 @@ def _dist():
     return ws, rank, local
 
 
+def _spawn_replicas(n):
+    """--gpus N > 1 without a launcher: start N ranks on this node (one per GPU, rendezvous on
+    127.0.0.1) the way the multi-GPU driver does, and return their exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
+def _throughput(ws, batch, block_k, steps, ms_max):
+    """Whole-job draft tokens per second: every replica drafts batch x K tokens per step, and
+    the job takes as long as its slowest replica."""
+    return ws * batch * block_k * steps / (ms_max / 1e3)
+
+
 def _barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -349,11 +367,42 @@ def _algorithmic(cfg, records):
     return flops, byts
 
 
+# The workloads one default run measures, the headline first: the largest single-GPU
+# workload (the most bytes per step: 10.5 GB of weights and context K/V), then the others.
+ALL_WORKLOADS = ["q27b_b8", "q4b_b128", "q8b_b32", "q8b_b1"]
+
+
 def run_ours(args):
     ws, rank, local = _dist()
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    cfg, over = _cfg(args)
+    names = ALL_WORKLOADS if args.config == "all" else [args.config]
+    results = []
+    for i, name in enumerate(names):
+        cfg, over = _cfg(args, name)
+        results.append(measure(args, cfg, over, ws, rank, local, device, headline=i == 0))
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return
+    line = results[0]
+    if "_cpu" in line:
+        line["cpu_baseline"] = cpu_baseline(*line.pop("_cpu"))
+    if len(results) > 1:
+        keep = ("value", "unit", "ms_per_step", "us_per_step", "steps_per_s", "step_roofline", "roofline",
+                "prefill", "e2e", "gpu_launches", "clocks")
+        line["configs"] = {}
+        for r in results[1:]:
+            sub = {k: r[k] for k in keep if k in r}
+            sub["config"] = r["config"]
+            sub["kernels"] = dict(list(r["kernels"].items())[:6])
+            line["configs"][r["config"]["workload"].split(":")[0]] = sub
+    print(json.dumps(line), flush=True)
+
+
+def measure(args, cfg, over, ws, rank, local, device, headline=True):
+    """One workload: prefill, warm-up steps, the timed steps, a per-kernel pass and the
+    end-to-end pass. Returns the result record on rank 0 (None elsewhere)."""
     W, K_ = args.warmup, args.steps
     n_steps = W + (3 * K_ if cfg.verify_driven else K_)      # driven runs never revisit a step
     wl = Workload(cfg, n_steps, seed=0, device=device)
@@ -462,7 +511,8 @@ def run_ours(args):
                "ms_per_step": round(e2e_ms / K_, 4), "host_wall_ms_per_step": round(wall * 1e3 / K_, 4)}
 
     if rank != 0:
-        return
+        ctx.close()
+        return None
     hbm, tf, tf_sus, src = _peaks()
     gemm_cls = [c for c in kern if c.startswith("gemm_")]
     g_ms = sum(kern[c]["ms"] for c in gemm_cls)
@@ -488,7 +538,7 @@ def run_ours(args):
     kernels = {c: {"ms_per_step": round(v["ms"] / len(again), 4), "share": round(v["ms"] / total_k_ms, 4),
                    "launches_per_step": v["launches"] / len(again)}
                for c, v in sorted(kern.items(), key=lambda kv: -kv[1]["ms"])}
-    tok = ws * B * K * K_ / (ms_max / 1e3)
+    tok = _throughput(ws, B, K, K_, ms_max)
     lens = records[0][0] if records else wl.ctx
     res = {
         "metric": "draft_tokens_per_s", "value": round(tok, 1), "unit": "draft tok/s",
@@ -506,7 +556,9 @@ def run_ours(args):
                    else f"U[1,{cfg.n_new_max}] per request",
                    "l2": "inputs larger than L2: every step streams all weights (GBs) from HBM",
                    "parallelism": f"{ws} independent replica(s)",
-                   "verify": ("greedy prefix match" if args.verify == "greedy" else
+                   "verify": (("greedy prefix match" + ("" if cfg.verify_driven else
+                                ", against uniform target ids (the step's injected count is drawn, "
+                                "not taken from the accept length)")) if args.verify == "greedy" else
                               f"rejection sampling (temperature {args.temperature}, top_k {args.top_k}, "
                               f"top_p {args.top_p}) against synthetic target logits" if args.verify == "sample"
                               else f"draft tree of {args.budget} nodes from the top-k, greedy walk against "
@@ -519,9 +571,10 @@ def run_ours(args):
         "ms_per_step_with_kernel_events": round(ms_events / len(again), 4),
     }
     res["clocks"] = clk.summary()
-    if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, wl, w_cpu)
-    print(json.dumps(res), flush=True)
+    ctx.close()
+    if headline and not args.no_cpu_baseline:
+        res["_cpu"] = (cfg, wl, w_cpu)      # timed after every GPU measurement of the run
+    return res
 
 
 # ----------------------------------------------------------------------------- the oracle arm
@@ -570,7 +623,7 @@ def cpu_baseline(cfg, wl, w_cpu):
                       f"+ verify) on the fp64 numpy oracle; one request of a batch of {wl.B}"}
 
 
-def _cfg(args):
+def _cfg(args, name=None):
     """The named workload, with --set KEY=VALUE overrides of its fields (profiling cases:
     fewer layers, a smaller vocabulary or context; such a line is not the named workload)."""
     over = {}
@@ -583,7 +636,8 @@ def _cfg(args):
             except ValueError:
                 pass
         over[k] = v
-    return get_config(args.config, **over), over
+    name = name or (ALL_WORKLOADS[0] if args.config == "all" else args.config)
+    return get_config(name, **over), over
 
 
 def run_reference(args):
@@ -622,7 +676,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="q8b_b1")
+    ap.add_argument("--config", default="all",
+                    help="one workload, or 'all': the largest (q27b_b8) as the headline and the "
+                         "other bf16 workloads under 'configs'")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -638,6 +694,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(_spawn_replicas(args.gpus))
     if args.impl == "reference":
         run_reference(args)
     else:

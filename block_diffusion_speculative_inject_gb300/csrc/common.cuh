@@ -80,6 +80,7 @@ __device__ __forceinline__ void raise_wait_err(int *flag, int site, const volati
 // wait sites reported in flag[1]
 enum : int {
   SITE_GEMM_EMPTY = 0x101, SITE_GEMM_FULL = 0x102, SITE_GEMM_ACC = 0x103,
+  SITE_GEMM_CFULL = 0x104, SITE_GEMM_CEMPTY = 0x105,
   SITE_ATT_EMPTY = 0x201, SITE_ATT_FULL = 0x202, SITE_ATT_PFULL = 0x203, SITE_ATT_SFULL = 0x204,
   SITE_ATT_PVDONE = 0x205, SITE_ATT_OFULL = 0x206, SITE_ATT_COMBINE = 0x207,
 };
@@ -157,6 +158,9 @@ struct GemmDesc {
   const void *x[GEMM_MAX_XSEG];
   const void *x_lo[GEMM_MAX_XSEG];   // lo plane (bf16 pair) or nullptr
   const void *x_lo2;             // third plane of segment 0 (with x_lo[0]) or nullptr
+  int exact_acc;                 // 1: accumulate in short chunks summed in fp32 (round to nearest)
+                                 // on the CUDA cores, for products that are rounded to the storage
+                                 // type afterwards (the tensor core's own accumulation truncates)
   int x_k0[GEMM_MAX_XSEG + 1];   // K offset where segment s starts; x_k0[n_xseg] = K
   int ldx[GEMM_MAX_XSEG];        // row stride (elements) of each X segment
   int n_wseg;

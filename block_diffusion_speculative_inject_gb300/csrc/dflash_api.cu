@@ -718,6 +718,7 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     }
     d.x_k0[m.n_feat] = F;
     add_wseg(d, c->w.fc, m.H);
+    d.exact_acc = 1;                      // g decides how the cached K/V round
     int S = 1;
     OpOut g = op_of(c, c->g, (size_t)C * m.H);
     if (g.lo) g.lo2 = (bf16 *)g.lo + (size_t)C * m.H;   // g carries three planes
@@ -740,6 +741,7 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     // every layer's [Wk; Wv] in one GEMM, then k-norm + RoPE + paged write
     GemmDesc e = gemm_desc(n, kvw, m.H, EPI_STORE, nullptr, kvw);
     set_x(c, e, g, m.H);
+    e.exact_acc = 1;                      // rounded to the storage type in the cache
     if (fnorm) {
       e.rs_part = c->ss_inj;
       e.rs_tiles = m.H / 128;

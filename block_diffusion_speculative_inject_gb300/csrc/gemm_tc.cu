@@ -24,8 +24,11 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
+#include <cstdio>
 #include <map>
+#include <set>
 #include <tuple>
 #include <vector>
 
@@ -48,8 +51,11 @@ struct TcParams {
   int n_xseg;
   int x_k0[TC_MAX_XMAP + 1];
   int planes;                         // X planes: 1, or 2 / 3 for a split fp32 activation
+  int chunk;                          // > 0: k-blocks per partial accumulator (folded in fp32)
+  int pf;                             // > 0: L2 prefetch of the weight boxes pf k-blocks ahead
   int M, N, K;
   int kb_total, kb_per, S;
+  int n_tiles;                        // 128-row weight tiles of N
   int stages;
   int epi;
   float *y;
@@ -180,13 +186,15 @@ __device__ __forceinline__ void warp_tile_lse(const float (&v)[4], int lane, flo
 // ------------------------------------------------------------------------- the kernel
 // FN: the fused-norm epilogue pieces (EPI_RESNORM, rs_part), compiled into the few-token
 // instances only so that the others keep their code
-template <int BN, bool FN = false>
+// WM: 128-row weight tiles per CTA (1 or 2); with 2 the tiles share every staged activation
+// tile, which halves the activation bytes read from L2 per weight byte (the big-M instance)
+template <int BN, bool FN = false, int WM = 1>
 __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
-  constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+  constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;          // one 128-row weight tile
   constexpr uint32_t B_BYTES = BN * TC_BK * 2;
-  const uint32_t stage_bytes = A_BYTES + B_BYTES * p.planes;
+  const uint32_t stage_bytes = WM * A_BYTES + B_BYTES * p.planes;
   const int stages = p.stages;
 
   const uint32_t raw = smem_u32(smem_raw);
@@ -196,16 +204,29 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   const uint32_t full0 = smem_u32(bars);                   // full[s]  = full0 + 8 s
   const uint32_t empty0 = full0 + 8u * stages;             // empty[s] = empty0 + 8 s
   const uint32_t accf = empty0 + 8u * stages;
-  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * stages + 1);
+  const uint32_t cfull0 = accf + 8u;                       // chunk buffer b written: cfull0 + 8 b
+  const uint32_t cempty0 = accf + 24u;                     // chunk buffer b folded: cempty0 + 8 b
+  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * stages + 5);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BN, n0 = blockIdx.y * TC_BM, split = blockIdx.z;
+  const int m0 = blockIdx.x * BN, split = blockIdx.z;
+  const int n0 = (int)blockIdx.y * WM * TC_BM;             // first weight row of weight tile 0
+  const int wm_live = min(WM, p.n_tiles - (int)blockIdx.y * WM);   // weight tiles inside N
   // (the one-split top-k epilogue stages its own layout and scales by rs_lane)
   const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU ||
                       (FN && (p.epi == EPI_RESNORM || p.epi == EPI_KVCACHE || (p.rs_part && p.epi != EPI_TOPK)));
   const int kb0 = split * p.kb_per;
   const int nkb = min(p.kb_total, kb0 + p.kb_per) - kb0;
+  // Chunked accumulation: chunk c of `chunk` k-blocks accumulates from zero into TMEM buffer
+  // c % 2 (columns [(c % 2) BNW, ...)), the epilogue warps add it into the sum region at 2 BNW
+  // in fp32 and hand the buffer back; the epilogue then reads the sum instead of one long
+  // tensor-core accumulation (whose additions truncate: ~2e-5 relative at K = 20480).
+  constexpr int BNW = BN * WM;
+  const int CH = p.chunk;
+  const int n_chunks = CH > 0 ? (nkb + CH - 1) / CH : 0;
+  uint32_t ncols = tmem_cols<BNW>();
+  if (CH > 0) ncols = 3 * BNW <= 64 ? 64 : 3 * BNW <= 128 ? 128 : 3 * BNW <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -213,11 +234,15 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       mbar_init(empty0 + 8u * s, 1);
     }
     mbar_init(accf, 1);
+    mbar_init(cfull0, 1);
+    mbar_init(cfull0 + 8u, 1);
+    mbar_init(cempty0, 128);
+    mbar_init(cempty0 + 8u, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), tmem_cols<BN>());
+    tmem_alloc(smem_u32(tmem_slot), ncols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -229,17 +254,25 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
 
   if (warp == 0 && lane == 0 && nkb > 0) {
     // ---------------- TMA producer
-    int ws = 0;
-    while (ws + 1 < p.n_wseg && n0 >= p.w_n0[ws + 1]) ++ws;
     const bool glu = p.epi == EPI_SWIGLU;                  // rows 0-63 gate, 64-127 up
-    const CUtensorMap *wm = &p.wmap[glu ? 0 : ws];
-    const int wrow = glu ? (int)blockIdx.y * 64 : n0 - p.w_n0[ws];
+    const CUtensorMap *wm[WM];
+    int wrow[WM];
+    for (int w = 0; w < WM; ++w) {
+      const int ty = (int)blockIdx.y * WM + w, n0w = ty * TC_BM;
+      int ws = 0;
+      while (ws + 1 < p.n_wseg && n0w >= p.w_n0[ws + 1]) ++ws;
+      wm[w] = &p.wmap[glu ? 0 : ws];
+      wrow[w] = glu ? ty * 64 : n0w - p.w_n0[ws];
+    }
+    const uint32_t tx = wm_live * A_BYTES + B_BYTES * p.planes;   // bytes landing per stage
     auto load_w = [&](uint32_t st, int k, uint32_t fb) {
-      tma_load_2d(st, wm, k, wrow, fb);
-      if (glu) tma_load_2d(st + 64 * 128, &p.wmap[1], k, wrow, fb);
+      for (int w = 0; w < wm_live; ++w) {
+        tma_load_2d(st + w * A_BYTES, wm[w], k, wrow[w], fb);
+        if (glu) tma_load_2d(st + w * A_BYTES + 64 * 128, &p.wmap[1], k, wrow[w], fb);
+      }
     };
     // the activation maps are first used after the dependency wait: fetch them now
-    tma_prefetch_map(wm);
+    for (int w = 0; w < wm_live; ++w) tma_prefetch_map(wm[w]);
     if (glu) tma_prefetch_map(&p.wmap[1]);
     for (int i = 0; i < (p.planes > 1 ? p.planes : p.n_xseg); ++i) tma_prefetch_map(&p.xmap[i]);
     // the first stages' weight tiles do not depend on the previous kernel: start streaming
@@ -247,7 +280,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     const int pre = min(stages, nkb);
     for (int i = 0; i < pre; ++i) {
       const uint32_t fb = full0 + 8u * i;
-      mbar_expect_tx(fb, stage_bytes);
+      mbar_expect_tx(fb, tx);
       load_w(tiles + (uint32_t)i * stage_bytes, (kb0 + i) * TC_BK, fb);
     }
     pdl_wait();
@@ -259,15 +292,23 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       const int k = (kb0 + i) * TC_BK;
       if (i >= pre) {
         if (u > 0 && !mbar_wait(empty0 + 8u * s, (u - 1) & 1, abort_flag, p.err, SITE_GEMM_EMPTY)) break;
-        mbar_expect_tx(fb, stage_bytes);
+        mbar_expect_tx(fb, tx);
         load_w(st, k, fb);
       }
+      if (p.pf > 0 && i + p.pf < nkb) {
+        // the weight boxes of k-block i + pf into L2, so that their TMA loads find them there
+        for (int w = 0; w < wm_live; ++w) {
+          tma_prefetch_l2_2d(wm[w], k + p.pf * TC_BK, wrow[w]);
+          if (glu) tma_prefetch_l2_2d(&p.wmap[1], k + p.pf * TC_BK, wrow[w]);
+        }
+      }
+      const uint32_t xb = st + WM * A_BYTES;
       if (p.planes > 1) {
-        for (int pl = 0; pl < p.planes; ++pl) tma_load_2d(st + A_BYTES + pl * B_BYTES, &p.xmap[pl], k, m0, fb);
+        for (int pl = 0; pl < p.planes; ++pl) tma_load_2d(xb + pl * B_BYTES, &p.xmap[pl], k, m0, fb);
       } else {
         int xs = 0;
         while (xs + 1 < p.n_xseg && k >= p.x_k0[xs + 1]) ++xs;
-        tma_load_2d(st + A_BYTES, &p.xmap[xs], k - p.x_k0[xs], m0, fb);
+        tma_load_2d(xb, &p.xmap[xs], k - p.x_k0[xs], m0, fb);
       }
       issued = i + 1;
     }
@@ -284,20 +325,31 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     constexpr uint32_t idesc = idesc_bf16(TC_BM, BN);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % stages, u = i / stages;
+      // chunked: k-block i goes to buffer (i / CH) % 2, which the epilogue must have folded
+      // (chunk i / CH - 2) before the chunk's first MMA overwrites it
+      const int ci = CH > 0 ? i / CH : 0;
+      const bool first = CH > 0 ? i % CH == 0 : i == 0;
+      if (CH > 0 && first && ci >= 2 &&
+          !mbar_wait(cempty0 + 8u * (ci & 1), ((ci >> 1) - 1) & 1, abort_flag, p.err, SITE_GEMM_CEMPTY))
+        break;
       if (!mbar_wait(full0 + 8u * s, u & 1, abort_flag, p.err, SITE_GEMM_FULL)) break;
       tc_fence_after();
-      const uint32_t a = tiles + (uint32_t)s * stage_bytes;
-      const uint32_t b = a + A_BYTES;
+      const uint32_t b = tiles + (uint32_t)s * stage_bytes + WM * A_BYTES;
+      const uint32_t dbuf = tmem + (uint32_t)(CH > 0 ? (ci & 1) * BNW : 0);
+      for (int w = 0; w < wm_live; ++w) {
+        // weight tile w accumulates into TMEM columns [w BN, (w + 1) BN) of the buffer; the
+        // small planes first, so that in a fresh (chunked) accumulator only the hi plane's
+        // additions truncate at the full magnitude of the sum
+        const uint32_t a = tiles + (uint32_t)s * stage_bytes + w * A_BYTES, d = dbuf + (uint32_t)(w * BN);
+        for (int pl = p.planes - 1; pl >= 0; --pl) {
 #pragma unroll
-      for (int kk = 0; kk < TC_BK / 16; ++kk)
-        umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-      for (int pl = 1; pl < p.planes; ++pl) {
-#pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc, 1u);
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc,
+                      (!first || kk > 0 || pl != p.planes - 1) ? 1u : 0u);
+        }
       }
       umma_commit(empty0 + 8u * s);       // frees the stage once these MMAs have read it
+      if (CH > 0 && (i % CH == CH - 1 || i == nkb - 1)) umma_commit(cfull0 + 8u * (ci & 1));
     }
     umma_commit(accf);                    // accumulator complete (all MMAs issued above)
   } else if (warp >= 2) {
@@ -323,16 +375,52 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       for (int t = 0; t < p.rs_tiles; ++t) ss += __ldg(p.rs_part + (size_t)t * p.M + m0 + lane);
       rs_lane = rsqrtf(ss / (float)p.rs_dim + p.eps);
     }
-    const bool ok = nkb > 0 && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
-    tc_fence_after();
-    const int n = n0 + q * 32 + lane;
-    // the top-k epilogue stages the tile [BN tokens][128 rows] in the (now idle) stage memory
+    bool ok = nkb > 0;
+    if (CH == 0) {
+      ok = ok && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
+      tc_fence_after();
+    } else {
+      // fold chunk c (buffer c % 2) into the sum region in fp32, then hand the buffer back
+      const uint32_t lanes = (uint32_t)(q * 32) << 16;
+      for (int c = 0; ok && c < n_chunks; ++c) {
+        // warp-uniform, so that the aligned TMEM loads below run on every lane or none
+        ok = __all_sync(0xffffffffu, mbar_wait(cfull0 + 8u * (c & 1), (c >> 1) & 1, abort_flag, p.err,
+                                               SITE_GEMM_CFULL));
+        tc_fence_after();
+        if (ok) {
+          const uint32_t part = tmem + lanes + (uint32_t)((c & 1) * BNW), sum = tmem + lanes + (uint32_t)(2 * BNW);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BNW; c0 += 16) {
+            uint32_t r[16], t[16];
+            tmem_ld16(part + c0, r);
+            if (c > 0) tmem_ld16(sum + c0, t);
+            tmem_ld_wait();
+            if (c > 0) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
+            }
+            tmem_st16(sum + c0, r);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(cempty0 + 8u * (c & 1));
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    // the accumulator the epilogue reads: the sum region when chunked
+    const uint32_t tacc = tmem + (uint32_t)(CH > 0 ? 2 * BNW : 0);
+    // the top-k epilogue stages the tile [BN tokens][128 rows] in the (now idle) stage memory;
+    // the staged epilogues [WM][BN][128]
     float *tile = (float *)gen_tiles;
     constexpr int TP = TC_BM + 1;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
+    for (int cw = 0; cw < BN * wm_live; cw += 16) {
+      const int w = cw / BN, c0 = cw % BN;
+      const int n = n0 + w * TC_BM + q * 32 + lane;
       uint32_t r[16];
-      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+      tmem_ld16(tacc + ((uint32_t)(q * 32) << 16) + (uint32_t)cw, r);
       tmem_ld_wait();
       if (p.epi == EPI_TOPK && p.S == 1) {
 #pragma unroll
@@ -351,7 +439,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         // stage this CTA's (partial) tile [BN][128] for the split-K reduction and the
         // per-token epilogues
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tile[(c0 + j) * TC_BM + q * 32 + lane] = ok ? __uint_as_float(r[j]) : 0.f;
+        for (int j = 0; j < 16; ++j) tile[(cw + j) * TC_BM + q * 32 + lane] = ok ? __uint_as_float(r[j]) : 0.f;
         continue;
       }
       if (!ok || n >= p.N) continue;
@@ -420,10 +508,13 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     // order (lane l: rows l, l + 32, l + 64, l + 96) and applies the epilogue
     if (p.S > 1) cluster_sync_all();
     if (warp >= 2) {
-      const uint32_t base = smem_u32(gen_tiles);
-      const float *own = (const float *)gen_tiles;
-      const int part = n0 < p.q_dim ? 0 : (n0 < p.q_dim + p.kv_dim ? 1 : 2);   // EPI_QKV
-      const int rank = (int)cluster_ctarank();
+     const int rank = (int)cluster_ctarank();
+     for (int w = 0; w < wm_live; ++w) {
+      // weight tile w: rows n0w.. of the output, staged at [w][BN][128]
+      const int ty = (int)blockIdx.y * WM + w, n0w = ty * TC_BM;
+      const uint32_t base = smem_u32(gen_tiles) + (uint32_t)(w * BN * TC_BM * 4);
+      const float *own = (const float *)gen_tiles + (size_t)w * BN * TC_BM;
+      const int part = n0w < p.q_dim ? 0 : (n0w < p.q_dim + p.kv_dim ? 1 : 2);   // EPI_QKV
       constexpr int U = 4;                     // tokens per warp per round: loads in flight
       for (int cb = rank + p.S * (warp - 2); cb < BN; cb += 4 * U * p.S) {
         float a[U][4];
@@ -452,7 +543,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             }
           }
           if (p.epi == EPI_QKV && part < 2) {
-            if (cb == rank + p.S * (warp - 2)) {
+            if (w == 0 && cb == rank + p.S * (warp - 2)) {
               cs[u][0] = qk_cs[u][0];
               cs[u][1] = qk_cs[u][1];
             } else {
@@ -478,7 +569,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           }
           if (FN && p.epi == EPI_KVCACHE) {
             // this tile is one head: K (norm + RoPE) or V of layer l, into the paged cache
-            const int seg = n0 / p.kv_dim, l = seg >> 1, h = (n0 % p.kv_dim) >> 7;
+            const int seg = n0w / p.kv_dim, l = seg >> 1, h = (n0w % p.kv_dim) >> 7;
             const int slot = __ldg(p.kv_slot + m), page = slot / KV_PAGE, off = slot % KV_PAGE;
             if ((seg & 1) == 0) {
               const bf16 *kn = p.kv_knorm[l];
@@ -517,7 +608,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             float ss = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int n = n0 + lane + 32 * j;
+              const int n = n0w + lane + 32 * j;
               const size_t o = (size_t)m * p.ldy + n;
               const float y = p.y ? p.y[o] + x[j] : x[j];       // no residual: the norm alone
               if (p.y) p.y[o] = y;
@@ -525,7 +616,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
               ss += y * y;
             }
             ss = warp_sum(ss);
-            if (lane == 0) p.ss_part[(size_t)blockIdx.y * ldss + orow] = ss;
+            if (lane == 0) p.ss_part[(size_t)ty * ldss + orow] = ss;
             continue;
           }
           if (p.epi == EPI_TOPK) {
@@ -534,19 +625,19 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
             int id[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int n = n0 + lane + 32 * j;
+              const int n = n0w + lane + 32 * j;
               if (p.out_xf) x[j] = logit_xform(x[j], p.out_mult, p.out_cap);
               v[j] = n < p.N ? x[j] : -INFINITY;
               id[j] = n;
               if (n < p.N && p.y) p.y[(size_t)m * p.ldy + n] = x[j];
             }
-            if (p.lse_part) warp_tile_lse(v, lane, p.lse_part + (size_t)blockIdx.y * p.M + m);
-            warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk);
+            if (p.lse_part) warp_tile_lse(v, lane, p.lse_part + (size_t)ty * p.M + m);
+            warp_tile_topk(v, id, p.topk, lane, p.cand + ((size_t)ty * p.M + m) * p.topk);
             continue;
           }
           if (p.epi == EPI_SWIGLU) {
             // rows lane, lane + 32 are gate; lane + 64, lane + 96 the matching up rows
-            const size_t o = (size_t)m * p.ldo + (size_t)blockIdx.y * 64 + lane;
+            const size_t o = (size_t)m * p.ldo + (size_t)ty * 64 + lane;
             write_op(p.out, o, x[0] / (1.f + expf(-x[0])) * x[2]);
             write_op(p.out, o + 32, x[1] / (1.f + expf(-x[1])) * x[3]);
             continue;
@@ -570,7 +661,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int n = n0 + lane + 32 * j;
+            const int n = n0w + lane + 32 * j;
             if (n < p.N) {
               const size_t o = (size_t)m * p.ldy + n;
               p.y[o] = p.epi == EPI_RESID ? p.resid[o] + x[j] : x[j];
@@ -578,6 +669,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           }
         }
       }
+     }
     }
     // peers keep their shared memory until all have read it; this barrier orders nothing
     // else, so its arrive is relaxed (the epilogue's global stores need not drain first)
@@ -585,7 +677,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols<BN>());
+    tmem_dealloc(tmem, ncols);
   }
 }
 
@@ -596,7 +688,12 @@ struct TcGemm {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
   int generation = 0;
-  bool attr_set[6] = {false, false, false, false, false, false};
+  bool attr_set[8] = {};
+  bool wide = true;                   // two weight tiles per CTA for big M (DFLASH_GEMM_WM1=1: one)
+  std::map<std::tuple<const void *, int, long>, int> occ;   // cluster occupancy per instance
+  bool debug_plan = false;            // DFLASH_DEBUG_PLAN=1: print each new GEMM plan to stderr
+  int pf_few = 0, pf_wide = 0;        // L2 prefetch distance (k-blocks) of the few-token / big-M instances
+  std::set<std::tuple<const void *, int, long>> printed;
 };
 
 cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag) {
@@ -611,6 +708,12 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
   t->num_sms = num_sms;
   t->encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
   t->err = err_flag;
+  const char *wm1 = getenv("DFLASH_GEMM_WM1");
+  t->wide = !(wm1 && wm1[0] == '1');
+  if (const char *v = getenv("DFLASH_GEMM_PF_FEW")) t->pf_few = atoi(v);
+  if (const char *v = getenv("DFLASH_GEMM_PF_WIDE")) t->pf_wide = atoi(v);
+  const char *dbg = getenv("DFLASH_DEBUG_PLAN");
+  t->debug_plan = dbg && dbg[0] == '1';
   *out = t;
   return cudaSuccess;
 }
@@ -660,9 +763,13 @@ bool tc_encode_2d(TcGemm *t, const void *ptr, unsigned long long rows, unsigned 
 }
 
 struct Plan {
-  int bn, t_tiles, n_tiles, kb, kb_per, S, stages;
+  int bn, wm, t_tiles, n_tiles, grid_y, kb, kb_per, S, stages;
   size_t smem;
 };
+
+// Few-token instances (FN: the fused-norm / cache-write epilogues) or the wide big-M
+// instance (two weight tiles per CTA) — the kernel instance a GEMM launches with.
+static bool fn_instance(const GemmDesc &d) { return d.rs_part || d.epi == EPI_RESNORM || d.epi == EPI_KVCACHE; }
 
 static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   Plan p{};
@@ -670,23 +777,83 @@ static Plan plan_for(const TcGemm *t, const GemmDesc &d) {
   p.t_tiles = (d.M + p.bn - 1) / p.bn;
   p.n_tiles = (d.N + TC_BM - 1) / TC_BM;
   p.kb = d.K / TC_BK;
+  // more token rows than one tile: two weight tiles per CTA share the staged activations
+  // (the activation planes are the larger part of a stage at 128 tokens)
+  const bool wide = t->wide && p.bn == 128 && !fn_instance(d) && p.n_tiles >= 2 && !d.exact_acc &&
+                    (d.epi == EPI_STORE || d.epi == EPI_RESID || d.epi == EPI_QKV || d.epi == EPI_SWIGLU);
+  p.wm = wide ? 2 : 1;
+  p.grid_y = (p.n_tiles + p.wm - 1) / p.wm;
   const int planes = 1 + (d.x_lo[0] ? 1 : 0) + (d.x_lo2 ? 1 : 0);
-  const size_t stage = (size_t)TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * planes;
+  const size_t stage = (size_t)p.wm * TC_BM * TC_BK * 2 + (size_t)p.bn * TC_BK * 2 * planes;
   // Few token rows: a short pipeline and many resident CTAs per SM stream weights fastest
   // (measured); more token rows: a longer pipeline in a CTA of its own.
-  p.stages = p.bn <= 32 ? 3 : (int)std::max<size_t>(2, std::min<size_t>(8, (200 * 1024) / stage));
-  p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 1) + 16;
-  const int per_sm = std::max(1, std::min(4, (int)((228 * 1024) / (p.smem + 1024))));
-  // split K into as many parts as keep the grid within one wave of resident CTAs (more
-  // CTAs in flight streamed faster than balancing the bytes per SM, measured)
-  const int base = p.t_tiles * p.n_tiles;
-  const int s_max = std::max(1, std::min(8, p.kb / 4));    // a portable cluster holds 8 CTAs
-  int S = std::max(1, std::min((per_sm * t->num_sms) / base, s_max));
-  // the top-k epilogue ranks whole sums: split K only through the cluster reduction
-  if (d.epi == EPI_TOPK) S = std::min(S, s_max);
-  p.kb_per = (p.kb + S - 1) / S;
-  p.S = (p.kb + p.kb_per - 1) / p.kb_per;    // every split non-empty
+  if (p.bn <= 32)
+    p.stages = 3;
+  else if (p.wm == 1)
+    p.stages = (int)std::max<size_t>(2, std::min<size_t>(8, (200 * 1024) / stage));
+  else
+    p.stages = (int)std::max<size_t>(2, std::min<size_t>(4, (220 * 1024) / stage));
+  p.smem = p.stages * stage + 1024 + 8 * (2 * p.stages + 5) + 16;
+  p.S = 1;
+  p.kb_per = p.kb;
   return p;
+}
+
+// Split-K factor of the few-token instances: as many parts as keep the grid within one wave
+// of resident CTAs (more CTAs in flight streamed faster than balancing the bytes per SM,
+// measured).
+static int splits_few(const TcGemm *t, const Plan &p) {
+  const int per_sm = std::max(1, std::min(4, (int)((228 * 1024) / (p.smem + 1024))));
+  const int base = p.t_tiles * p.grid_y;
+  const int s_max = std::max(1, std::min(8, p.kb / 4));    // a portable cluster holds 8 CTAs
+  return std::max(1, std::min((per_sm * t->num_sms) / base, s_max));
+}
+
+// Split-K factor of the big-M instances: the CTAs of a launch run in waves of as many
+// clusters as fit on the GPU at once (the driver's cluster occupancy for this instance and
+// shared-memory size), so the launch takes about waves x (k-blocks per split + a fixed
+// per-CTA cost); splitting K evens out a last wave that would run nearly empty (e.g. 160
+// tiles on 152 SMs).
+static int splits_wide(TcGemm *t, const void *fn, const Plan &p) {
+  const int tiles = p.t_tiles * p.grid_y;
+  const int s_max = std::max(1, std::min(8, p.kb / 8));
+  const double ovh = p.wm == 2 ? 5.0 : 8.0;     // fixed cost of a CTA, in k-blocks of its pipeline
+  int best_S = 1;
+  double best = 0;
+  for (int S = 1; S <= s_max; ++S) {
+    auto key = std::make_tuple(fn, S, (long)p.smem);
+    auto it = t->occ.find(key);
+    int occ;
+    if (it != t->occ.end()) {
+      occ = it->second;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, 1, S);
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = p.smem;
+      cudaLaunchAttribute a;
+      a.id = cudaLaunchAttributeClusterDimension;
+      a.val.clusterDim.x = 1;
+      a.val.clusterDim.y = 1;
+      a.val.clusterDim.z = S;
+      cfg.attrs = &a;
+      cfg.numAttrs = 1;
+      occ = 0;
+      if (cudaOccupancyMaxActiveClusters(&occ, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        occ = 0;
+      }
+      t->occ.emplace(key, occ);
+    }
+    if (occ <= 0) continue;
+    const int kb_per = (p.kb + S - 1) / S;
+    const double cost = (double)((tiles + occ - 1) / occ) * (kb_per + ovh);
+    if (S == 1 || cost < 0.97 * best) {
+      best = cost;
+      best_S = S;
+    }
+  }
+  return best_S;
 }
 
 int tc_gemm_generation(const TcGemm *t) { return t ? t->generation : 0; }
@@ -695,16 +862,28 @@ int tc_gemm_splits(const TcGemm *, const GemmDesc &) { return 1; }   // reduced 
 
 int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 1; }
 
-template <int BN, bool FN = false>
-static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan &pl, cudaStream_t s) {
+template <int BN, bool FN = false, int WM = 1>
+static cudaError_t launch_bn(TcGemm *t, int slot, TcParams &p, Plan pl, cudaStream_t s) {
+  const void *fn = (const void *)k_gemm_tc<BN, FN, WM>;
   if (!t->attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, FN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, FN, WM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
     t->attr_set[slot] = true;
   }
+  const int S = BN <= 32 ? splits_few(t, pl) : splits_wide(t, fn, pl);
+  pl.kb_per = (pl.kb + S - 1) / S;
+  pl.S = (pl.kb + pl.kb_per - 1) / pl.kb_per;    // every split non-empty
+  p.kb_per = pl.kb_per;
+  p.S = pl.S;
+  if (t->debug_plan) {
+    auto key = std::make_tuple((const void *)nullptr, p.M * 131071 + p.N, (long)p.K * 16 + p.epi);
+    if (t->printed.insert(key).second)
+      fprintf(stderr, "[dflash gemm] M %d N %d K %d epi %d planes %d chunk %d pf %d: BN %d WM %d grid %d x %d x %d stages %d smem %zu\n",
+              p.M, p.N, p.K, p.epi, p.planes, p.chunk, p.pf, BN, WM, pl.t_tiles, pl.grid_y, pl.S, pl.stages, pl.smem);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.t_tiles, pl.n_tiles, pl.S);
+  cfg.gridDim = dim3(pl.t_tiles, pl.grid_y, pl.S);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
@@ -717,7 +896,7 @@ static cudaError_t launch_bn(TcGemm *t, int slot, const TcParams &p, const Plan 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, FN>, p);
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, FN, WM>, p);
 }
 
 cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
@@ -773,8 +952,9 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.N = d.N;
   p.K = d.K;
   p.kb_total = pl.kb;
-  p.kb_per = pl.kb_per;
-  p.S = pl.S;
+  p.n_tiles = pl.n_tiles;
+  p.chunk = d.exact_acc ? 1 : 0;       // one k-block (64 products) per partial accumulator
+  p.pf = pl.bn <= 32 ? t->pf_few : t->pf_wide;
   p.stages = pl.stages;
   p.epi = d.epi;
   p.topk = d.topk;
@@ -816,7 +996,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     p.epi = EPI_STORE;
   }
   cudaError_t e;
-  if (d.rs_part || d.epi == EPI_RESNORM || d.epi == EPI_KVCACHE) {
+  if (fn_instance(d)) {
     if (pl.bn > 32) return cudaErrorInvalidValue;      // few-token instances only
     return pl.bn == 16 ? launch_bn<16, true>(t, 4, p, pl, s) : launch_bn<32, true>(t, 5, p, pl, s);
   }
@@ -824,7 +1004,7 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
     case 16: e = launch_bn<16>(t, 0, p, pl, s); break;
     case 32: e = launch_bn<32>(t, 1, p, pl, s); break;
     case 64: e = launch_bn<64>(t, 2, p, pl, s); break;
-    default: e = launch_bn<128>(t, 3, p, pl, s); break;
+    default: e = pl.wm == 2 ? launch_bn<128, false, 2>(t, 6, p, pl, s) : launch_bn<128>(t, 3, p, pl, s); break;
   }
   return e;
 }

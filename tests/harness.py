@@ -88,4 +88,6 @@ def check_topk(got_idx, got_val, logits_oracle, k, tol, what="", gap=TIE_GAP):
                 continue
             # a swap is allowed only among candidates the oracle ranks within `gap`
             assert abs(l32[j, got_idx[j, r]] - want_val[j, r]) < gap, \
-                f"{what} row {j} rank {r}: {got_idx[j, r]} vs {want_idx[j, r]}"
+                (f"{what} row {j} rank {r}: {got_idx[j, r]} vs {want_idx[j, r]}: oracle gap "
+                 f"{want_val[j, r] - l32[j, got_idx[j, r]]:.3g}, gpu values {got_val[j, r]:.7g} "
+                 f"(oracle {l32[j, got_idx[j, r]]:.7g} / {want_val[j, r]:.7g})")
