@@ -107,7 +107,6 @@ struct dflash_ctx {
   float *ss_o = nullptr, *ss_d = nullptr;
   float *ss_inj = nullptr;   // the same after the injection's fc ([H/128][32])
   float *ss_f = nullptr;     // and for the final norm of the K mask rows ([H/128][rows_k])
-  int *attn_sync = nullptr;  // arrive / depart counters of the fused attention combine
 
   std::vector<Stage> ring;
   size_t stage_cap = 0;
@@ -385,7 +384,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj, c->ss_f, c->attn_sync};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj, c->ss_f};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -501,7 +500,6 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       {(void **)&c->ss_d, (size_t)(m.H / 128) * R * f4},
       {(void **)&c->ss_inj, (size_t)(m.H / 128) * 32 * f4},
       {(void **)&c->ss_f, (size_t)(m.H / 128) * RK * f4},
-      {(void **)&c->attn_sync, (size_t)2 * cfg->max_batch * m.nkv * sizeof(int)},
   };
   for (auto &a : allocs)
     if (cudaMalloc(a.p, std::max<size_t>(a.bytes, 256)) != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -564,10 +562,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
       c->amaps.valid = tc_encode_2d(c->tc, c->pool, blocks * kPage, m.hd, m.hd, 64, 64, &c->amaps.k) &&
                        tc_encode_2d(c->tc, c->pool, blocks * m.hd, kPage, kPage, 64, 128, &c->amaps.v);
       c->amaps.err = c->err_d;
-      c->amaps.sync = c->attn_sync;
       c->amaps.num_sms = c->num_sms;
-      if (cudaMemset(c->attn_sync, 0, (size_t)2 * cfg->max_batch * m.nkv * sizeof(int)) != cudaSuccess)
-        return fail(DFLASH_ERR_CUDA);
     }
   }
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(DFLASH_ERR_CUDA);
@@ -938,7 +933,7 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
                                   lw.k_norm, s);
          }));
     }
-    const int attn_launches = bt.max_split == 0 ? 1 : attn_fused_combine(m, bt, c->amaps.valid ? &c->amaps : nullptr) ? 1 : 2;
+    const int attn_launches = bt.max_split == 0 ? 1 : 2;     // the split kernel, then the combine
     CK(c, timed(c, K_ATTN, s, attn_bytes, attn_flops, attn_launches, [&] {
          return launch_attention(c->dtype, m, bt, l, c->qkv, c->pool, c->part_o, c->part_ml, ao,
                                  c->amaps.valid ? &c->amaps : nullptr, s);
@@ -1044,9 +1039,8 @@ static dflash_status draft_layers(dflash_ctx *c, int B, const DraftBatch &bt, do
 // layer stack as a CUDA graph. Capture runs on the library's own stream (captures never
 // execute); the graph is launched on the caller's stream.
 static dflash_status run_layers_graph(dflash_ctx *c, int B, const DraftBatch &bt, cudaStream_t s) {
-  // the split plan, and whether its attention merges the splits in place, select the graph
-  const bool fused = attn_fused_combine(c->m, bt, c->amaps.valid ? &c->amaps : nullptr);
-  const long long key = ((((long long)B << 8) | bt.max_split) << 1) | (fused ? 1 : 0);
+  // the batch size and the split plan select the graph
+  const long long key = ((long long)B << 8) | bt.max_split;
   const int gen = tc_gemm_generation(c->tc) * 4096 + c->ws_gen;
   for (auto &g : c->graphs) {
     if (g.key != key) continue;

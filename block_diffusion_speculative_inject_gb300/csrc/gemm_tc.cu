@@ -41,7 +41,11 @@ constexpr int TC_BM = 128;            // weight rows per tile (UMMA M)
 constexpr int TC_BK = 64;             // K per pipeline stage: 64 bf16 = one 128-byte row
 constexpr int TC_MAX_WSEG = 16;
 constexpr int TC_MAX_XMAP = 8;
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 192;          // few-token instances: TMA warp, MMA warp, 4 epilogue warps
+// Threads of an instance: the big-tile instances run one CTA per SM, so their epilogue gets
+// 8 warps (two per TMEM lane quarter, splitting the columns) to hide its memory latencies.
+template <int BN>
+constexpr int tc_threads() { return BN <= 32 ? TC_THREADS : 64 + 32 * 8; }
 
 struct TcParams {
   CUtensorMap wmap[TC_MAX_WSEG];      // one per weight segment, box {64, 128}
@@ -52,7 +56,6 @@ struct TcParams {
   int x_k0[TC_MAX_XMAP + 1];
   int planes;                         // X planes: 1, or 2 / 3 for a split fp32 activation
   int chunk;                          // > 0: k-blocks per partial accumulator (folded in fp32)
-  int pf;                             // > 0: L2 prefetch of the weight boxes pf k-blocks ahead
   int M, N, K;
   int kb_total, kb_per, S;
   int n_tiles;                        // 128-row weight tiles of N
@@ -183,13 +186,28 @@ __device__ __forceinline__ void warp_tile_lse(const float (&v)[4], int lane, flo
   if (lane == 0 && out) *out = make_float2(mx, s);
 }
 
+// Staged partial tiles [tokens][128 weight rows] (fp32): the four rows a lane reduces and
+// finishes (l, l + 32, l + 64, l + 96) are one 16-byte word, so the split-K reduction reads
+// each rank's values with one 16-byte load per lane; within the word the rows are rotated by
+// a lane-dependent XOR, which keeps the warp's staging stores free of bank conflicts.
+__device__ __forceinline__ int stage_idx(int c, int n) {
+  const int l = n & 31, q = n >> 5;
+  return c * TC_BM + 4 * l + (q ^ ((l >> 3) & 3));
+}
+// element of the staged word of lane `lane` that holds row lane + 32 j
+__device__ __forceinline__ float stage_pick(const float4 &v, int j, int lane) {
+  const int e = j ^ ((lane >> 3) & 3);
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
 // ------------------------------------------------------------------------- the kernel
 // FN: the fused-norm epilogue pieces (EPI_RESNORM, rs_part), compiled into the few-token
 // instances only so that the others keep their code
 // WM: 128-row weight tiles per CTA (1 or 2); with 2 the tiles share every staged activation
-// tile, which halves the activation bytes read from L2 per weight byte (the big-M instance)
-template <int BN, bool FN = false, int WM = 1>
-__global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant__ TcParams p) {
+// tile, which halves the activation bytes read from L2 per weight byte (the big-M instance).
+// CH: chunked (exact) accumulation, see below.
+template <int BN, bool FN = false, int WM = 1, bool CH = false>
+__global__ void __launch_bounds__(tc_threads<BN>(), BN <= 32 ? 3 : 1) k_gemm_tc(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   pdl_trigger();
   constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;          // one 128-row weight tile
@@ -212,7 +230,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BN, split = blockIdx.z;
   const int n0 = (int)blockIdx.y * WM * TC_BM;             // first weight row of weight tile 0
-  const int wm_live = min(WM, p.n_tiles - (int)blockIdx.y * WM);   // weight tiles inside N
+  const int wm_live = WM == 1 ? 1 : min(WM, p.n_tiles - (int)blockIdx.y * WM);   // weight tiles inside N
   // (the one-split top-k epilogue stages its own layout and scales by rs_lane)
   const bool staged = p.S > 1 || p.epi == EPI_QKV || p.epi == EPI_SWIGLU ||
                       (FN && (p.epi == EPI_RESNORM || p.epi == EPI_KVCACHE || (p.rs_part && p.epi != EPI_TOPK)));
@@ -223,10 +241,12 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
   // in fp32 and hand the buffer back; the epilogue then reads the sum instead of one long
   // tensor-core accumulation (whose additions truncate: ~2e-5 relative at K = 20480).
   constexpr int BNW = BN * WM;
-  const int CH = p.chunk;
-  const int n_chunks = CH > 0 ? (nkb + CH - 1) / CH : 0;
-  uint32_t ncols = tmem_cols<BNW>();
-  if (CH > 0) ncols = 3 * BNW <= 64 ? 64 : 3 * BNW <= 128 ? 128 : 3 * BNW <= 256 ? 256 : 512;
+  constexpr int NW = BN <= 32 ? 4 : 8;                      // epilogue warps
+  const int CK = CH ? p.chunk : 1;                         // k-blocks per chunk
+  const int n_chunks = CH ? (nkb + CK - 1) / CK : 0;
+  constexpr uint32_t ncols = !CH ? (uint32_t)tmem_cols<BNW>()
+                                 : 3 * BNW <= 64 ? 64 : 3 * BNW <= 128 ? 128 : 3 * BNW <= 256 ? 256 : 512;
+  static_assert(!CH || 3 * BNW <= 512, "chunked accumulation needs three accumulator regions");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -234,10 +254,12 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       mbar_init(empty0 + 8u * s, 1);
     }
     mbar_init(accf, 1);
-    mbar_init(cfull0, 1);
-    mbar_init(cfull0 + 8u, 1);
-    mbar_init(cempty0, 128);
-    mbar_init(cempty0 + 8u, 128);
+    if (CH) {
+      mbar_init(cfull0, 1);
+      mbar_init(cfull0 + 8u, 1);
+      mbar_init(cempty0, 32 * NW);
+      mbar_init(cempty0 + 8u, 32 * NW);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -295,13 +317,6 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         mbar_expect_tx(fb, tx);
         load_w(st, k, fb);
       }
-      if (p.pf > 0 && i + p.pf < nkb) {
-        // the weight boxes of k-block i + pf into L2, so that their TMA loads find them there
-        for (int w = 0; w < wm_live; ++w) {
-          tma_prefetch_l2_2d(wm[w], k + p.pf * TC_BK, wrow[w]);
-          if (glu) tma_prefetch_l2_2d(&p.wmap[1], k + p.pf * TC_BK, wrow[w]);
-        }
-      }
       const uint32_t xb = st + WM * A_BYTES;
       if (p.planes > 1) {
         for (int pl = 0; pl < p.planes; ++pl) tma_load_2d(xb + pl * B_BYTES, &p.xmap[pl], k, m0, fb);
@@ -327,40 +342,53 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       const int s = i % stages, u = i / stages;
       // chunked: k-block i goes to buffer (i / CH) % 2, which the epilogue must have folded
       // (chunk i / CH - 2) before the chunk's first MMA overwrites it
-      const int ci = CH > 0 ? i / CH : 0;
-      const bool first = CH > 0 ? i % CH == 0 : i == 0;
-      if (CH > 0 && first && ci >= 2 &&
+      const int ci = CH ? i / CK : 0;
+      const bool first = CH ? i % CK == 0 : i == 0;
+      if (CH && first && ci >= 2 &&
           !mbar_wait(cempty0 + 8u * (ci & 1), ((ci >> 1) - 1) & 1, abort_flag, p.err, SITE_GEMM_CEMPTY))
         break;
       if (!mbar_wait(full0 + 8u * s, u & 1, abort_flag, p.err, SITE_GEMM_FULL)) break;
       tc_fence_after();
       const uint32_t b = tiles + (uint32_t)s * stage_bytes + WM * A_BYTES;
-      const uint32_t dbuf = tmem + (uint32_t)(CH > 0 ? (ci & 1) * BNW : 0);
+      const uint32_t dbuf = tmem + (uint32_t)(CH ? (ci & 1) * BNW : 0);
       for (int w = 0; w < wm_live; ++w) {
-        // weight tile w accumulates into TMEM columns [w BN, (w + 1) BN) of the buffer; the
-        // small planes first, so that in a fresh (chunked) accumulator only the hi plane's
-        // additions truncate at the full magnitude of the sum
+        // weight tile w accumulates into TMEM columns [w BN, (w + 1) BN) of the buffer
         const uint32_t a = tiles + (uint32_t)s * stage_bytes + w * A_BYTES, d = dbuf + (uint32_t)(w * BN);
-        for (int pl = p.planes - 1; pl >= 0; --pl) {
+        if constexpr (CH) {
+          // the small planes first: in the chunk's fresh accumulator only the hi plane's
+          // additions truncate at the full magnitude of the sum
+          for (int pl = p.planes - 1; pl >= 0; --pl) {
+#pragma unroll
+            for (int kk = 0; kk < TC_BK / 16; ++kk)
+              umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc,
+                        (!first || kk > 0 || pl != p.planes - 1) ? 1u : 0u);
+          }
+        } else {
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk)
-            umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc,
-                      (!first || kk > 0 || pl != p.planes - 1) ? 1u : 0u);
+            umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc, (!first || kk > 0) ? 1u : 0u);
+          for (int pl = 1; pl < p.planes; ++pl) {
+#pragma unroll
+            for (int kk = 0; kk < TC_BK / 16; ++kk)
+              umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + pl * B_BYTES + kk * 32), idesc, 1u);
+          }
         }
       }
       umma_commit(empty0 + 8u * s);       // frees the stage once these MMAs have read it
-      if (CH > 0 && (i % CH == CH - 1 || i == nkb - 1)) umma_commit(cfull0 + 8u * (ci & 1));
+      if (CH && (i % CK == CK - 1 || i == nkb - 1)) umma_commit(cfull0 + 8u * (ci & 1));
     }
     umma_commit(accf);                    // accumulator complete (all MMAs issued above)
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int ew = warp - 2;              // epilogue warp 0..NW-1
+    const int eh = ew >> 2;               // which of the quarter's NW / 4 warps (column share)
     if (p.epi == EPI_QKV && n0 < p.q_dim + p.kv_dim) {
       // RoPE (cos, sin) of the first tokens this warp finishes, fetched while the MMAs run
       const int rank = (int)cluster_ctarank();
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int c = rank + p.S * (warp - 2) + 4 * p.S * u, m = m0 + c;
+        const int c = rank + p.S * ew + NW * p.S * u, m = m0 + c;
         if (c < BN && m < p.M) {
           const int pos = __ldg(p.ctx_len + m / p.rows_per_req) + m % p.rows_per_req;
           qk_cs[u][0] = __ldg(p.rope + (size_t)pos * 64 + lane);
@@ -376,7 +404,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       rs_lane = rsqrtf(ss / (float)p.rs_dim + p.eps);
     }
     bool ok = nkb > 0;
-    if (CH == 0) {
+    if constexpr (!CH) {
       ok = ok && mbar_wait(accf, 0, abort_flag, p.err, SITE_GEMM_ACC);
       tc_fence_after();
     } else {
@@ -390,7 +418,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         if (ok) {
           const uint32_t part = tmem + lanes + (uint32_t)((c & 1) * BNW), sum = tmem + lanes + (uint32_t)(2 * BNW);
 #pragma unroll 1
-          for (int c0 = 0; c0 < BNW; c0 += 16) {
+          for (int c0 = 16 * eh; c0 < BNW; c0 += 16 * (NW / 4)) {
             uint32_t r[16], t[16];
             tmem_ld16(part + c0, r);
             if (c > 0) tmem_ld16(sum + c0, t);
@@ -410,13 +438,13 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
       tc_fence_after();
     }
     // the accumulator the epilogue reads: the sum region when chunked
-    const uint32_t tacc = tmem + (uint32_t)(CH > 0 ? 2 * BNW : 0);
+    const uint32_t tacc = tmem + (uint32_t)(CH ? 2 * BNW : 0);
     // the top-k epilogue stages the tile [BN tokens][128 rows] in the (now idle) stage memory;
     // the staged epilogues [WM][BN][128]
     float *tile = (float *)gen_tiles;
     constexpr int TP = TC_BM + 1;
 #pragma unroll 1
-    for (int cw = 0; cw < BN * wm_live; cw += 16) {
+    for (int cw = 16 * eh; cw < BN * wm_live; cw += 16 * (NW / 4)) {
       const int w = cw / BN, c0 = cw % BN;
       const int n = n0 + w * TC_BM + q * 32 + lane;
       uint32_t r[16];
@@ -439,7 +467,7 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
         // stage this CTA's (partial) tile [BN][128] for the split-K reduction and the
         // per-token epilogues
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tile[(cw + j) * TC_BM + q * 32 + lane] = ok ? __uint_as_float(r[j]) : 0.f;
+        for (int j = 0; j < 16; ++j) tile[stage_idx(cw + j, q * 32 + lane)] = ok ? __uint_as_float(r[j]) : 0.f;
         continue;
       }
       if (!ok || n >= p.N) continue;
@@ -454,18 +482,18 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     }
     if (p.epi == EPI_TOPK && p.S == 1) {
       // per token: the tile's best topk (value desc, lower index first) by warp arg-max rounds
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * NW) : "memory");
       if constexpr (BN <= 32) {
-        // this warp's token columns (c = warp - 2 + 4 t), four at a time in interleaved passes
+        // this warp's token columns (c = ew + NW t), four at a time in interleaved passes
         constexpr int T = 4;
 #pragma unroll 1
-        for (int t0 = 0; 4 * t0 < BN; t0 += T) {
+        for (int t0 = 0; NW * t0 < BN; t0 += T) {
           float v[T][4];
           int id[T][4];
           int2 *out[T];
 #pragma unroll
           for (int t = 0; t < T; ++t) {
-            const int c = warp - 2 + 4 * (t0 + t), m = m0 + c;
+            const int c = ew + NW * (t0 + t), m = m0 + c;
             const bool live = ok && c < BN && m < p.M;
             out[t] = live ? p.cand + ((size_t)blockIdx.y * p.M + m) * p.topk : nullptr;
 #pragma unroll
@@ -477,14 +505,14 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
           if (p.lse_part) {
 #pragma unroll
             for (int t = 0; t < T; ++t) {
-              const int c = warp - 2 + 4 * (t0 + t), m = m0 + c;
+              const int c = ew + NW * (t0 + t), m = m0 + c;
               warp_tile_lse(v[t], lane, out[t] ? p.lse_part + (size_t)blockIdx.y * p.M + m : nullptr);
             }
           }
           warp_tile_topk_multi<T>(v, id, p.topk, lane, out);
         }
       } else {
-        for (int c = warp - 2; c < BN; c += 4) {
+        for (int c = ew; c < BN; c += NW) {
           const int m = m0 + c;
           if (m >= p.M || !ok) continue;
           float v[4];
@@ -509,41 +537,46 @@ __global__ void __launch_bounds__(TC_THREADS, 3) k_gemm_tc(const __grid_constant
     if (p.S > 1) cluster_sync_all();
     if (warp >= 2) {
      const int rank = (int)cluster_ctarank();
+     const int ew = warp - 2;
      for (int w = 0; w < wm_live; ++w) {
       // weight tile w: rows n0w.. of the output, staged at [w][BN][128]
       const int ty = (int)blockIdx.y * WM + w, n0w = ty * TC_BM;
       const uint32_t base = smem_u32(gen_tiles) + (uint32_t)(w * BN * TC_BM * 4);
       const float *own = (const float *)gen_tiles + (size_t)w * BN * TC_BM;
       const int part = n0w < p.q_dim ? 0 : (n0w < p.q_dim + p.kv_dim ? 1 : 2);   // EPI_QKV
-      constexpr int U = 4;                     // tokens per warp per round: loads in flight
-      for (int cb = rank + p.S * (warp - 2); cb < BN; cb += 4 * U * p.S) {
+      constexpr int U = BN <= 32 ? 2 : 4;      // tokens per warp per round: loads in flight
+      for (int cb = rank + p.S * ew; cb < BN; cb += NW * U * p.S) {
         float a[U][4];
         float2 cs[U][2];
         int mu[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int c = cb + 4 * p.S * u;
+          const int c = cb + NW * p.S * u;
           mu[u] = (c < BN && m0 + c < p.M) ? m0 + c : -1;
           if (mu[u] < 0) continue;
           if (p.S == 1) {
+            const float4 t = *(const float4 *)(own + c * TC_BM + 4 * lane);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) a[u][j] = own[c * TC_BM + lane + 32 * j];
+            for (int j = 0; j < 4; ++j) a[u][j] = stage_pick(t, j, lane);
           } else {
+            // every rank's partial of these four rows, summed in rank order
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint32_t src = base + (uint32_t)((c * TC_BM + 4 * lane) * 4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float v[8];
-#pragma unroll
-              for (int rk = 0; rk < 8; ++rk)
-                v[rk] = rk < p.S ? dsmem_ld(dsmem_addr(base + (uint32_t)((c * TC_BM + lane + 32 * j) * 4),
-                                                       (uint32_t)rk))
-                                 : 0.f;
-              a[u][j] = 0.f;
-#pragma unroll
-              for (int rk = 0; rk < 8; ++rk) a[u][j] += v[rk];
+            for (int rk = 0; rk < 8; ++rk) {
+              if (rk < p.S) {
+                const float4 t = dsmem_ld4(dsmem_addr(src, (uint32_t)rk));
+                acc.x += t.x;
+                acc.y += t.y;
+                acc.z += t.z;
+                acc.w += t.w;
+              }
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[u][j] = stage_pick(acc, j, lane);
           }
           if (p.epi == EPI_QKV && part < 2) {
-            if (w == 0 && cb == rank + p.S * (warp - 2)) {
+            if (w == 0 && cb == rank + p.S * ew) {
               cs[u][0] = qk_cs[u][0];
               cs[u][1] = qk_cs[u][1];
             } else {
@@ -688,11 +721,10 @@ struct TcGemm {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::map<std::tuple<const void *, long, long, long, int>, CUtensorMap> maps;
   int generation = 0;
-  bool attr_set[8] = {};
+  bool attr_set[16] = {};
   bool wide = true;                   // two weight tiles per CTA for big M (DFLASH_GEMM_WM1=1: one)
   std::map<std::tuple<const void *, int, long>, int> occ;   // cluster occupancy per instance
   bool debug_plan = false;            // DFLASH_DEBUG_PLAN=1: print each new GEMM plan to stderr
-  int pf_few = 0, pf_wide = 0;        // L2 prefetch distance (k-blocks) of the few-token / big-M instances
   std::set<std::tuple<const void *, int, long>> printed;
 };
 
@@ -710,8 +742,6 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
   t->err = err_flag;
   const char *wm1 = getenv("DFLASH_GEMM_WM1");
   t->wide = !(wm1 && wm1[0] == '1');
-  if (const char *v = getenv("DFLASH_GEMM_PF_FEW")) t->pf_few = atoi(v);
-  if (const char *v = getenv("DFLASH_GEMM_PF_WIDE")) t->pf_wide = atoi(v);
   const char *dbg = getenv("DFLASH_DEBUG_PLAN");
   t->debug_plan = dbg && dbg[0] == '1';
   *out = t;
@@ -814,7 +844,7 @@ static int splits_few(const TcGemm *t, const Plan &p) {
 // shared-memory size), so the launch takes about waves x (k-blocks per split + a fixed
 // per-CTA cost); splitting K evens out a last wave that would run nearly empty (e.g. 160
 // tiles on 152 SMs).
-static int splits_wide(TcGemm *t, const void *fn, const Plan &p) {
+static int splits_wide(TcGemm *t, const void *fn, int threads, const Plan &p) {
   const int tiles = p.t_tiles * p.grid_y;
   const int s_max = std::max(1, std::min(8, p.kb / 8));
   const double ovh = p.wm == 2 ? 5.0 : 8.0;     // fixed cost of a CTA, in k-blocks of its pipeline
@@ -829,7 +859,7 @@ static int splits_wide(TcGemm *t, const void *fn, const Plan &p) {
     } else {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, 1, S);
-      cfg.blockDim = dim3(TC_THREADS);
+      cfg.blockDim = dim3(threads);
       cfg.dynamicSmemBytes = p.smem;
       cudaLaunchAttribute a;
       a.id = cudaLaunchAttributeClusterDimension;
@@ -862,16 +892,16 @@ int tc_gemm_splits(const TcGemm *, const GemmDesc &) { return 1; }   // reduced 
 
 int tc_gemm_launches(const TcGemm *, const GemmDesc &) { return 1; }
 
-template <int BN, bool FN = false, int WM = 1>
+template <int BN, bool FN = false, int WM = 1, bool CH = false>
 static cudaError_t launch_bn(TcGemm *t, int slot, TcParams &p, Plan pl, cudaStream_t s) {
-  const void *fn = (const void *)k_gemm_tc<BN, FN, WM>;
+  const void *fn = (const void *)k_gemm_tc<BN, FN, WM, CH>;
   if (!t->attr_set[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, FN, WM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, FN, WM, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
     t->attr_set[slot] = true;
   }
-  const int S = BN <= 32 ? splits_few(t, pl) : splits_wide(t, fn, pl);
+  const int S = BN <= 32 ? splits_few(t, pl) : splits_wide(t, fn, tc_threads<BN>(), pl);
   pl.kb_per = (pl.kb + S - 1) / S;
   pl.S = (pl.kb + pl.kb_per - 1) / pl.kb_per;    // every split non-empty
   p.kb_per = pl.kb_per;
@@ -879,12 +909,12 @@ static cudaError_t launch_bn(TcGemm *t, int slot, TcParams &p, Plan pl, cudaStre
   if (t->debug_plan) {
     auto key = std::make_tuple((const void *)nullptr, p.M * 131071 + p.N, (long)p.K * 16 + p.epi);
     if (t->printed.insert(key).second)
-      fprintf(stderr, "[dflash gemm] M %d N %d K %d epi %d planes %d chunk %d pf %d: BN %d WM %d grid %d x %d x %d stages %d smem %zu\n",
-              p.M, p.N, p.K, p.epi, p.planes, p.chunk, p.pf, BN, WM, pl.t_tiles, pl.grid_y, pl.S, pl.stages, pl.smem);
+      fprintf(stderr, "[dflash gemm] M %d N %d K %d epi %d planes %d chunk %d: BN %d WM %d grid %d x %d x %d stages %d smem %zu\n",
+              p.M, p.N, p.K, p.epi, p.planes, p.chunk, BN, WM, pl.t_tiles, pl.grid_y, pl.S, pl.stages, pl.smem);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.t_tiles, pl.grid_y, pl.S);
-  cfg.blockDim = dim3(TC_THREADS);
+  cfg.blockDim = dim3(tc_threads<BN>());
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -896,7 +926,7 @@ static cudaError_t launch_bn(TcGemm *t, int slot, TcParams &p, Plan pl, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, FN, WM>, p);
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, FN, WM, CH>, p);
 }
 
 cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
@@ -954,7 +984,6 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   p.kb_total = pl.kb;
   p.n_tiles = pl.n_tiles;
   p.chunk = d.exact_acc ? 1 : 0;       // one k-block (64 products) per partial accumulator
-  p.pf = pl.bn <= 32 ? t->pf_few : t->pf_wide;
   p.stages = pl.stages;
   p.epi = d.epi;
   p.topk = d.topk;
@@ -998,7 +1027,18 @@ cudaError_t tc_gemm_run(TcGemm *t, const GemmDesc &d, cudaStream_t s) {
   cudaError_t e;
   if (fn_instance(d)) {
     if (pl.bn > 32) return cudaErrorInvalidValue;      // few-token instances only
+    if (p.chunk)
+      return pl.bn == 16 ? launch_bn<16, true, 1, true>(t, 7, p, pl, s) : launch_bn<32, true, 1, true>(t, 8, p, pl, s);
     return pl.bn == 16 ? launch_bn<16, true>(t, 4, p, pl, s) : launch_bn<32, true>(t, 5, p, pl, s);
+  }
+  if (p.chunk) {
+    // exact accumulation of the injection GEMMs (one weight tile per CTA)
+    switch (pl.bn) {
+      case 16: return launch_bn<16, false, 1, true>(t, 9, p, pl, s);
+      case 32: return launch_bn<32, false, 1, true>(t, 10, p, pl, s);
+      case 64: return launch_bn<64, false, 1, true>(t, 11, p, pl, s);
+      default: return launch_bn<128, false, 1, true>(t, 12, p, pl, s);
+    }
   }
   switch (pl.bn) {
     case 16: e = launch_bn<16>(t, 0, p, pl, s); break;

@@ -162,9 +162,7 @@ static cudaError_t attn_impl(const ModelDims &m, const DraftBatch &bt, int layer
   cudaError_t e = cudaSuccess;
   if (bt.max_split > 0) {
     if (maps && maps->valid && HD == 128 && sizeof(T) == 2) {
-      const bool fuse = attn_fused_combine(m, bt, maps);
-      e = launch_attn_split_tc(m, bt, layer, qkv, maps, scale_log2, part_o, part_ml, s, fuse, o);
-      if (e != cudaSuccess || fuse) return e;        // fused: the splits merged themselves
+      e = launch_attn_split_tc(m, bt, layer, qkv, maps, scale_log2, part_o, part_ml, s);
     } else {
       size_t smem = (size_t)(AT_MAXR * HD + AT_KT * (HD + 1) + AT_KT * HD) * sizeof(float);
       e = cudaFuncSetAttribute(k_attn_split<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -26,7 +26,6 @@
 // pair exchanges its row maxima through shared memory once per tile. The S of the next
 // tile is computed while the softmax of the current one runs; the softmax waits for the
 // previous tile's P.V only when it rescales O. All waits are bounded in time.
-#include "attn_combine.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -43,7 +42,6 @@ constexpr size_t AT_TC_SMEM = 1024 + AT_TC_STAGES * A_STAGE + 256 + AX_BYTES;
 constexpr uint32_t AT_TMEM_COLS = 512;
 constexpr uint32_t AT_TMEM_O = 128;               // O accumulator
 constexpr uint32_t AT_TMEM_Q = 256;               // Q hi (64 columns), then Q lo
-constexpr int CB_FUSED_MS = 16;                   // the host plans at most this many splits
 
 struct AttnTcParams {
   CUtensorMap kmap, vmap;
@@ -53,11 +51,6 @@ struct AttnTcParams {
   float scale_log2;
   float *part_o, *part_ml;
   int *err;
-  // fused combine: the CTAs of one (request, kv head) wait for each other, then each merges
-  // the rows r = s, s + ns, ... into o
-  int fuse, causal;
-  int *sync;
-  OpOut o;
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -368,55 +361,11 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     tc_fence_after();
     tmem_dealloc(tmem, AT_TMEM_COLS);
   }
-  if (!p.fuse) return;
-  // ---------------- fused combine. Every active CTA of (b, kvh) publishes its partials and
-  // arrives; once all ns have, each merges its share of the rows (the whole grid is resident,
-  // see attn_fused_combine). The last to leave resets the counters for the next launch.
-  int *arrive = p.sync + 2 * ((size_t)b * p.nkv + kvh), *depart = arrive + 1;
-  const bool aborted = *abort_flag != 0;
-  __threadfence();                                       // this thread's partials, GPU-wide
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    atomicAdd(arrive, 1);
-    const unsigned long long t0 = global_ns();
-    while (atomicAdd(arrive, 0) < ns) {
-      if (global_ns() - t0 > TC_WAIT_NS) {
-        *abort_flag = 1;
-        raise_wait_err(p.err, SITE_ATT_COMBINE);
-        break;
-      }
-    }
-  }
-  __syncthreads();
-  __threadfence();
-  if (!aborted && *abort_flag == 0) {
-    // the K/V ring is idle now: its first bytes hold the block's K/V and the warps' q rows
-    float *fs = reinterpret_cast<float *>(gbase);
-    const CombineSmem<128> sm{fs, fs + 32 * CombineSmem<128>::KP};
-    float *qsw = fs + 32 * CombineSmem<128>::KP + 32 * 128 + warp * 128;
-    stage_block_kv<128>(b, kvh, p.nq, p.nkv, p.Q, p.qkv, sm, threadIdx.x, AT_TC_THREADS);
-    __syncthreads();
-    const int R = (p.nq / p.nkv) * p.Q;
-    for (int r = s + ns * warp; r < R; r += ns * (AT_TC_THREADS / 32)) {
-      CombineRow<128, CB_FUSED_MS> cr;
-      combine_load<128, CB_FUSED_MS, true>(cr, r, b, kvh, p.nq, p.nkv, p.Q, ns, p.max_split, p.part_o, p.part_ml,
-                                           p.qkv, qsw, lane);
-      __syncwarp();
-      combine_finish<128, CB_FUSED_MS>(cr, r, b, kvh, p.nq, p.nkv, p.Q, ns, p.scale_log2, p.causal, p.o, sm, qsw,
-                                       lane);
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(depart, 1) == ns - 1) {
-    atomicExch(arrive, 0);
-    atomicExch(depart, 0);
-  }
 }
 
 cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &bt, int layer,
                                  const float *qkv, const AttnMaps *maps, float scale_log2,
-                                 float *part_o, float *part_ml, cudaStream_t s, bool fuse, OpOut o) {
+                                 float *part_o, float *part_ml, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_attn_split_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -444,11 +393,6 @@ cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &bt, int l
   p.part_o = part_o;
   p.part_ml = part_ml;
   p.err = maps->err;
-  p.fuse = fuse ? 1 : 0;
-  p.causal = m.causal;
-  p.sync = maps->sync;
-  p.o = o;
-  if (fuse && bt.max_split > CB_FUSED_MS) return cudaErrorInvalidValue;
   dim3 g(bt.max_split, m.nkv, bt.B);
   return launch_pdl(k_attn_split_tc, g, dim3(AT_TC_THREADS), AT_TC_SMEM, s, p);
 }

@@ -38,17 +38,8 @@ struct AttnMaps {
   CUtensorMap k, v;
   bool valid;
   int *err;      // device error flag raised by expired waits
-  int *sync;     // [max_batch][nkv][2] arrive / depart counters of the fused combine (zero between launches)
   int num_sms;
 };
-
-// Whether the tensor-core split kernel merges its splits itself (no combine launch): every
-// request has context splits and the whole grid is resident at once (one CTA per SM), so
-// its CTAs can wait for the other splits of their (request, kv head).
-inline bool attn_fused_combine(const ModelDims &m, const DraftBatch &b, const AttnMaps *maps) {
-  return maps && maps->valid && maps->sync && m.hd == 128 && b.min_split >= 1 &&
-         (long)b.max_split * m.nkv * b.B <= maps->num_sms;
-}
 
 // Split-KV attention of the query block of each request over its paged context plus the
 // block's own K/V, then the split combine into the operand o [B*(K+1), q_dim].
@@ -59,8 +50,7 @@ cudaError_t launch_attention(int dtype, const ModelDims &m, const DraftBatch &b,
 // The tensor-core split kernel (bf16 cache, head_dim 128).
 cudaError_t launch_attn_split_tc(const ModelDims &m, const DraftBatch &b, int layer,
                                  const float *qkv, const AttnMaps *maps, float scale_log2,
-                                 float *part_o, float *part_ml, cudaStream_t s, bool fuse = false,
-                                 OpOut o = OpOut{nullptr, nullptr});
+                                 float *part_o, float *part_ml, cudaStream_t s);
 
 // Sampling mode: truncated distributions (at most SMP_K kept tokens per row) of fp32 logits
 // [rows, V], optionally with one draw per row against uniforms u; the verification of a batch

@@ -62,12 +62,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(mbar)
       : "memory");
 }
-// Asks the memory system to bring a tensor box into L2 (no shared memory, no completion):
-// deepens the stream of outstanding HBM reads beyond what the shared-memory ring holds.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(c0), "r"(c1)
-               : "memory");
-}
 // Fetch a tensor map (kernel parameter) into the TMA unit's cache ahead of its first use.
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
@@ -187,6 +181,16 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_saddr, uint32_t ra
 __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// 16 bytes from a peer CTA's shared memory (16-byte aligned address)
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
 

@@ -62,8 +62,10 @@ def _run_steps(cfg, limits, ctx_lens, steps, seed=0, check_kv=True):
                 kv_tol = 1e-4 if cfg.dtype == "f32" else 3e-2
                 np.testing.assert_allclose(to_np(k), wk, atol=kv_tol, rtol=0)
                 np.testing.assert_allclose(to_np(v), wv, atol=kv_tol, rtol=0)
-                if cfg.dtype == "bf16":   # rounding flips are rare
-                    assert np.mean(to_np(k) == wk) > 0.99 and np.mean(to_np(v) == wv) > 0.99
+                if cfg.dtype == "bf16":
+                    # the injection GEMMs accumulate exactly enough that fewer than one stored
+                    # value in a thousand lands on the other bf16 neighbour of the oracle's
+                    assert np.mean(to_np(k) == wk) > 0.999 and np.mean(to_np(v) == wv) > 0.999
     anchors = S.make_anchors(cfg, B, seed, 0)
     for step in range(steps):
         out = pair.ctx.draft(reqs, anchors.cuda(), want_logits=True)
@@ -146,9 +148,9 @@ def test_incremental_injection_equals_one_shot():
         s += m
     # The GEMM's split-K factor follows the row count of each call, so the fp32 sums differ in
     # order between chunkings, and chunks of at most 32 rows apply the fc RMSNorm as a row
-    # scale after the K/V GEMM instead of before it. Both orders carry the activations to
-    # about 2^-17 relative, so a bf16 rounding of the stored K/V flips by one unit in the last
-    # place with probability about 2 * 2^-17 / 2^-8 (0.4%).
+    # scale after the K/V GEMM instead of before it. Both orders carry the pre-rounding K/V to
+    # about 1e-7 relative (fp32 sums of exactly accumulated k-blocks), so a bf16 rounding of
+    # the stored K/V lands on the other neighbour for a small fraction of values.
     for l in range(cfg.n_layers):
         for x, y in zip(a.ctx.export_kv(1, l, 0, n), b.ctx.export_kv(1, l, 0, n)):
             x, y = x.float(), y.float()
