@@ -62,13 +62,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // barrier of the two softmax warps that share a TMEM lane quarter (ids 1..4, 64 threads)
 __device__ __forceinline__ void bar_pair(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
-// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi); two values per 32-bit word
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi); two values per 32-bit word (a in the
+// low half), each pair rounded by one paired conversion
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
-  const bf16 h0 = __float2bfloat16_rn(a), h1 = __float2bfloat16_rn(b);
-  const bf16 l0 = __float2bfloat16_rn(a - __bfloat162float(h0));
-  const bf16 l1 = __float2bfloat16_rn(b - __bfloat162float(h1));
-  hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-  lo = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid_constant__ AttnTcParams p) {
