@@ -780,7 +780,7 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
 // slowest): the layer's attention time is the makespan of that list schedule on `slots`
 // resident CTAs. P is the candidate, from the longest context cut into 1..kMaxSplit
 // chunks, with the smallest simulated makespan; a finer cut must win by 2% to be taken.
-static int choose_split_pages(const std::vector<int> &pages, int nkv, int slots, double ovh) {
+static int choose_split_pages(const std::vector<int> &pages, int nkv, int slots, double ovh, int tile) {
   const int B = (int)pages.size();
   int maxp = 0;
   for (int b = 0; b < B; ++b) maxp = std::max(maxp, pages[b]);
@@ -788,7 +788,8 @@ static int choose_split_pages(const std::vector<int> &pages, int nkv, int slots,
   double best = 0;
   std::vector<double> heap;
   for (int k = 1; k <= kMaxSplit; ++k) {
-    const int P = (maxp + k - 1) / k;
+    // whole tiles of `tile` pages per split (the tensor-core kernel takes two pages a tile)
+    const int P = ((maxp + k - 1) / k + tile - 1) / tile * tile;
     if (P == prev_P) continue;
     prev_P = P;
     long n_cta = 0;
@@ -801,7 +802,8 @@ static int choose_split_pages(const std::vector<int> &pages, int nkv, int slots,
       for (int h = 0; h < nkv; ++h)
         for (int sp = 0; sp < ns; ++sp) {
           std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
-          const double t = heap.back() + std::min(P, pages[b] - sp * P) + ovh;
+          const int len = std::min(P, pages[b] - sp * P);
+          const double t = heap.back() + (len + tile - 1) / tile * tile + ovh;
           heap.back() = t;
           std::push_heap(heap.begin(), heap.end(), std::greater<double>());
           span = std::max(span, t);
@@ -820,13 +822,13 @@ static int choose_split_pages(const std::vector<int> &pages, int nkv, int slots,
 // per rounded batch, so a batch whose contexts grow by a few positions per step (or come
 // back to the same lengths) reuses it. Any split length is a valid plan (the last split of a
 // request is shorter); the rounding only shifts which one the heuristic picks.
-static void plan_splits(dflash_ctx *c, const std::vector<int> &pages, int nkv, int slots, double ovh,
+static void plan_splits(dflash_ctx *c, const std::vector<int> &pages, int nkv, int slots, double ovh, int tile,
                         std::vector<int> &n_split, std::vector<int> &split_len) {
   const int B = (int)pages.size();
   n_split.assign(B, 0);
   split_len.assign(B, kPage);
   int maxp = 0;
-  std::vector<int> key(B + 2);
+  std::vector<int> key(B + 3);
   for (int b = 0; b < B; ++b) {
     maxp = std::max(maxp, pages[b]);
     key[b] = (pages[b] + 7) / 8 * 8;
@@ -834,13 +836,14 @@ static void plan_splits(dflash_ctx *c, const std::vector<int> &pages, int nkv, i
   if (maxp == 0) return;
   key[B] = nkv;
   key[B + 1] = slots;
+  key[B + 2] = tile;
   int P;
   auto it = c->split_cache.find(key);
   if (it != c->split_cache.end()) {
     P = it->second;
   } else {
     std::vector<int> rounded(key.begin(), key.begin() + B);
-    P = choose_split_pages(rounded, nkv, slots, ovh);
+    P = choose_split_pages(rounded, nkv, slots, ovh, tile);
     if (c->split_cache.size() >= 1024) c->split_cache.clear();
     c->split_cache.emplace(std::move(key), P);
   }
@@ -1154,7 +1157,7 @@ static dflash_status draft_step_impl(dflash_ctx *c, void *stream, int32_t n_req,
   }
   // the tensor-core split kernel runs one CTA per SM, the FFMA one two
   const bool attn_tc = c->amaps.valid;
-  plan_splits(c, pages, m.nkv, (attn_tc ? 1 : 2) * c->num_sms, c->split_overhead, ns, sl);
+  plan_splits(c, pages, m.nkv, (attn_tc ? 1 : 2) * c->num_sms, c->split_overhead, attn_tc ? 2 : 1, ns, sl);
   for (int b = 0; b < B; ++b) {
     desc[b] = rq[b]->len;
     desc[B + b] = ns[b];

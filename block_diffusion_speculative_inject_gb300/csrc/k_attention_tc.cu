@@ -2,27 +2,29 @@
 //
 // One CTA = (split s, kv head, request b). Its rows are the G query heads of the kv head
 // times the K+1 block rows (R = G (K+1) <= 128, padded to the UMMA M of 128); its keys are
-// the context positions of split s, one 64-position page per tile. Per tile:
-//   S[128 rows, 64 keys]  = Q . K_tile^T          (tcgen05, A = Q in TMEM, B = K page in smem)
+// the context positions of split s, two 64-position pages per tile (a split's last tile may
+// hold one; its second page is then the first again, masked). Per tile:
+//   S[128 rows, 128 keys] = Q . K_tile^T          (tcgen05, A = Q in TMEM, B = K pages in smem)
 //   P = 2^(S - m)         (two threads per row: max, exp2, row sum; P written over S in TMEM)
-//   O[128 rows, 128 hd]  += P . V_tile            (tcgen05, A = P in TMEM, B = V page [hd][64])
+//   O[128 rows, 128 hd]  += P . V_tile            (tcgen05, A = P in TMEM, B = V pages [hd][64])
+// (128-key tiles: N = 128 MMAs run at the full tensor rate, N = 64 ones at ~70%, measured.)
 // Q (fp32) and P (fp32) enter the tensor core as exact bf16 hi/lo pairs, so each product
 // is two MMAs against the same staged K or V tile; the cache K/V are exact bf16 already.
 // With both A operands in tensor memory the MMAs read only the K/V pages from shared
-// memory, and shared memory holds nothing but a 6-stage K/V ring.
+// memory, and shared memory holds nothing but a 3-stage K/V ring (64 KB per stage).
 // Scores are in log2 units (log2(e)/sqrt(hd) folded into Q). The running max is updated
 // lazily: O in TMEM is rescaled only when a row's max grows by more than 8 (2^8 headroom).
 // The result per row is the unnormalised O, the max and the row sum, merged by the combine
 // kernel with the other splits and the block's own keys.
 //
-// TMEM (512 columns): S/P buffers at 0 and 64 (tile parity), O at 128, Q hi at 256, Q lo
-// at 320. A P buffer holds, for the 32 keys owned by each half of a row, 16 columns of hi
-// words then 16 of lo words, inside the S columns of those same keys.
+// TMEM (512 columns): S/P buffers at 0 and 128 (tile parity), O at 256, Q hi at 384, Q lo
+// at 448. A P buffer holds, for the 64 keys owned by each half of a row, 32 columns of hi
+// words then 32 of lo words, inside the S columns of those same keys.
 //
-// Roles (320 threads): warp 0 lane 0 issues TMA (K page: two boxes of 64 x 64, V page: one
+// Roles (320 threads): warp 0 lane 0 issues TMA (per page, K: two boxes of 64 x 64, V: one
 // box of 64 x 128); warp 1 owns TMEM and its lane 0 issues the MMAs; warps 2-9 fill Q, run
 // the softmax and write the partials. A row is shared by warps w and w + 4 (TMEM lane
-// quarter w % 4): each owns 32 of the tile's 64 keys and 64 of O's 128 columns, and the
+// quarter w % 4): each owns 64 of the tile's 128 keys and 64 of O's 128 columns, and the
 // pair exchanges its row maxima through shared memory once per tile. The S of the next
 // tile is computed while the softmax of the current one runs; the softmax waits for the
 // previous tile's P.V only when it rescales O. All waits are bounded in time.
@@ -32,16 +34,19 @@
 namespace dflash {
 
 constexpr int AT_TC_THREADS = 320;
-constexpr int AT_TC_STAGES = 6;
-constexpr uint32_t AK_SUB = 64 * 128;             // [64 keys x 64 hd] bf16
-constexpr uint32_t AK_BYTES = 2 * AK_SUB;
-constexpr uint32_t AV_BYTES = 128 * 128;          // [128 hd x 64 keys] bf16
+constexpr int AT_TC_STAGES = 3;
+constexpr int AT_KT = 128;                        // keys per tile (two pages)
+constexpr uint32_t AK_SUB = 64 * 128;             // [64 keys x 64 hd] bf16: one page, one hd half
+constexpr uint32_t AK_HALF = 2 * AK_SUB;          // [128 keys x 64 hd]: both pages, one hd half
+constexpr uint32_t AK_BYTES = 2 * AK_HALF;
+constexpr uint32_t AV_PAGE = 128 * 128;           // [128 hd x 64 keys] bf16: one page
+constexpr uint32_t AV_BYTES = 2 * AV_PAGE;
 constexpr uint32_t A_STAGE = AK_BYTES + AV_BYTES;
 constexpr uint32_t AX_BYTES = (4 * 128 + 2 * 128 + 16 + 2) * 4;   // row-max, row-sum, status, progress
 constexpr size_t AT_TC_SMEM = 1024 + AT_TC_STAGES * A_STAGE + 256 + AX_BYTES;
 constexpr uint32_t AT_TMEM_COLS = 512;
-constexpr uint32_t AT_TMEM_O = 128;               // O accumulator
-constexpr uint32_t AT_TMEM_Q = 256;               // Q hi (64 columns), then Q lo
+constexpr uint32_t AT_TMEM_O = 256;               // O accumulator
+constexpr uint32_t AT_TMEM_Q = 384;               // Q hi (64 columns), then Q lo
 
 struct AttnTcParams {
   CUtensorMap kmap, vmap;
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
   const int n_ctx = p.ctx_len[b];
   const int k_begin = s * p.split_len[b];
   const int k_end = min(k_begin + p.split_len[b], n_ctx);
-  const int n_tiles = (k_end - k_begin + 63) / 64;
+  const int n_tiles = (k_end - k_begin + AT_KT - 1) / AT_KT;
   const int G = p.nq / p.nkv, R = G * p.Q;
   const int32_t *pg = p.pages + p.page_off[b];
 
@@ -145,16 +150,21 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
     for (int i = 0; i < n_tiles; ++i) {
       const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
       if (u > 0 && !mbar_wait(empty0 + 8u * stg, (u - 1) & 1, abort_flag, p.err, SITE_ATT_EMPTY, prog)) break;
-      const int page = pg[(k_begin + 64 * i) / 64];
-      const int blk = (page * p.L + p.layer) * 2 * p.nkv;
-      const int krow = (blk + kvh) * 64;               // K view: rows of 128 values
-      const int vrow = (blk + p.nkv + kvh) * 128;      // V view: rows of 64 values
+      const int pos = k_begin + AT_KT * i;
       const uint32_t st = st0 + (uint32_t)stg * A_STAGE;
       const uint32_t fb = full0 + 8u * stg;
       mbar_expect_tx(fb, A_STAGE);
-      tma_load_2d(st, &p.kmap, 0, krow, fb);
-      tma_load_2d(st + AK_SUB, &p.kmap, 64, krow, fb);
-      tma_load_2d(st + AK_BYTES, &p.vmap, 0, vrow, fb);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        // page x of the tile; a missing second page repeats the first (finite data, masked)
+        const int page = pg[(pos + (pos + 64 * x < k_end ? 64 * x : 0)) / 64];
+        const int blk = (page * p.L + p.layer) * 2 * p.nkv;
+        const int krow = (blk + kvh) * 64;             // K view: rows of 128 values
+        const int vrow = (blk + p.nkv + kvh) * 128;    // V view: rows of 64 values
+        tma_load_2d(st + x * AK_SUB, &p.kmap, 0, krow, fb);
+        tma_load_2d(st + AK_HALF + x * AK_SUB, &p.kmap, 64, krow, fb);
+        tma_load_2d(st + AK_BYTES + x * AV_PAGE, &p.vmap, 0, vrow, fb);
+      }
       issued = i + 1;
     }
     for (int i = 0; i < AT_TC_STAGES && i < issued; ++i) {
@@ -174,20 +184,20 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       prog[0] = 1;
       // ---------------- MMA issuer: S of tile i+1 is computed while the softmax of tile i
       // runs, then P.V of tile i
-      constexpr uint32_t idS = idesc_bf16(128, 64);
+      constexpr uint32_t idS = idesc_bf16(128, AT_KT);
       constexpr uint32_t idO = idesc_bf16(128, 128);
       auto issue_s = [&](int i) {
         const int stg = i % AT_TC_STAGES, u = i / AT_TC_STAGES;
         if (!mbar_wait(full0 + 8u * stg, u & 1, abort_flag, p.err, SITE_ATT_FULL)) return false;
         tc_fence_after();
         const uint32_t kst = st0 + (uint32_t)stg * A_STAGE;
-        const uint32_t dS = tmem + (uint32_t)((i & 1) * 64);
+        const uint32_t dS = tmem + (uint32_t)((i & 1) * AT_KT);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)           // hd in steps of 16: 8 TMEM columns of Q
             umma_bf16_ts(dS, tmem + AT_TMEM_Q + 64 * pl + 8 * kk,
-                         sw128_desc(kst + (kk >> 2) * AK_SUB + (kk & 3) * 32), idS, (pl | kk) ? 1u : 0u);
+                         sw128_desc(kst + (kk >> 2) * AK_HALF + (kk & 3) * 32), idS, (pl | kk) ? 1u : 0u);
         umma_commit(s_full0 + 8u * (i & 1));
         return true;
       };
@@ -201,13 +211,13 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
         tc_fence_after();
         const int stg = i % AT_TC_STAGES;
         const uint32_t vst = st0 + (uint32_t)stg * A_STAGE + AK_BYTES;
-        const uint32_t pbuf = tmem + (uint32_t)((i & 1) * 64);
+        const uint32_t pbuf = tmem + (uint32_t)((i & 1) * AT_KT);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)           // keys in steps of 16
-            umma_bf16_ts(tmem + AT_TMEM_O, pbuf + 32 * (kk >> 1) + 16 * pl + 8 * (kk & 1),
-                         sw128_desc(vst + kk * 32), idO, (i | kk | pl) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)           // keys in steps of 16 (kk >> 2: the page)
+            umma_bf16_ts(tmem + AT_TMEM_O, pbuf + 64 * (kk >> 2) + 32 * pl + 8 * (kk & 3),
+                         sw128_desc(vst + (kk >> 2) * AV_PAGE + (kk & 3) * 32), idO, (i | kk | pl) ? 1u : 0u);
         umma_commit(empty0 + 8u * stg);      // K and V of this tile are no longer read
         umma_commit(pv_done);
       }
@@ -258,27 +268,30 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
       // the pair runs the same number of exchanges: a failed wait is passed to the partner
       // through the status word and both leave the loop together
       const bool got = __all_sync(0xffffffffu, ok && mbar_wait(s_full0 + 8u * par, (i >> 1) & 1, abort_flag, p.err, SITE_ATT_SFULL));
-      const uint32_t sa = lane_base + (uint32_t)(par * 64 + half * 32);   // my 32 keys
-      float sc[32];
+      const uint32_t sa = lane_base + (uint32_t)(par * AT_KT + half * 64);   // my 64 keys
+      float sc[64];
       float mt = -INFINITY;
       if (got) {
         tc_fence_after();
-        uint32_t t0[16], t1[16];
-        tmem_ld16(sa, t0);
-        tmem_ld16(sa + 16, t1);
-        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          sc[j] = __uint_as_float(t0[j]);
-          sc[16 + j] = __uint_as_float(t1[j]);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t t0[16], t1[16];
+          tmem_ld16(sa + c0, t0);
+          tmem_ld16(sa + c0 + 16, t1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            sc[c0 + j] = __uint_as_float(t0[j]);
+            sc[c0 + 16 + j] = __uint_as_float(t1[j]);
+          }
         }
-        const int nvalid = min(64, k_end - (k_begin + 64 * i)) - 32 * half;
-        if (nvalid < 32) {
+        const int nvalid = min(AT_KT, k_end - (k_begin + AT_KT * i)) - 64 * half;
+        if (nvalid < 64) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sc[c] = c < nvalid ? sc[c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) sc[c] = c < nvalid ? sc[c] : -INFINITY;
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mt = fmaxf(mt, sc[c]);
+        for (int c = 0; c < 64; ++c) mt = fmaxf(mt, sc[c]);
       }
       xmax[(par * 2 + half) * 128 + r] = mt;
       if (lane == 0) xok[(par * 2 + half) * 4 + q] = got ? 1 : 0;
@@ -313,15 +326,19 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) k_attn_split_tc(const __grid
         }
         l *= corr;
       }
-      uint32_t ph[16], pw[16];
+      // P over this thread's own S columns: 32 words of hi pairs, then 32 of lo pairs
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float e0 = ex2_approx(sc[2 * c] - m_used), e1 = ex2_approx(sc[2 * c + 1] - m_used);
-        l += e0 + e1;
-        split2(e0, e1, ph[c], pw[c]);
+      for (int c0 = 0; c0 < 32; c0 += 16) {
+        uint32_t ph[16], pw[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float e0 = ex2_approx(sc[2 * (c0 + c)] - m_used), e1 = ex2_approx(sc[2 * (c0 + c) + 1] - m_used);
+          l += e0 + e1;
+          split2(e0, e1, ph[c], pw[c]);
+        }
+        tmem_st16(sa + c0, ph);
+        tmem_st16(sa + 32 + c0, pw);
       }
-      tmem_st16(sa, ph);                   // over this thread's own S columns
-      tmem_st16(sa + 16, pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
