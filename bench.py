@@ -397,7 +397,7 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(*line.pop("_cpu"))
     if len(results) > 1:
         keep = ("value", "unit", "ms_per_step", "us_per_step", "steps_per_s", "step_roofline", "roofline",
-                "prefill", "e2e", "gpu_launches", "clocks")
+                "attention_roofline", "prefill", "e2e", "gpu_launches", "clocks")
         line["configs"] = {}
         for r in results[1:]:
             sub = {k: r[k] for k in keep if k in r}
@@ -536,6 +536,15 @@ def measure(args, cfg, over, ws, rank, local, device, headline=True):
                 "algorithmic_bytes_per_launch": round(g_bytes / max(1, g_launch)),
                 "tensor_tflops": round(g_flops / (g_ms / 1e3) / 1e12, 2),
                 "timing": "CUDA events around each launch in a separate pass over the same steps"}
+    # the attention kernels (split + combine) against HBM for the context K/V they read
+    att = kern.get("attention")
+    attention_roofline = None
+    if att and att["ms"] > 0:
+        a_gbs = att["bytes"] / (att["ms"] / 1e3) / 1e9
+        attention_roofline = {"kernel": "k_attn_split_tc + k_attn_combine", "bound": "hbm",
+                              "achieved": round(a_gbs, 1), "peak": hbm, "unit": "GB/s",
+                              "frac": round(a_gbs / hbm, 4),
+                              "ms_per_step": round(att["ms"] / len(again), 4)}
     flops, byts = _algorithmic(cfg, records)
     t_roof = max(flops / (tf * 1e12), byts / (hbm * 1e9))
     step_roof = {"flops_per_step": flops / K_, "bytes_per_step": byts / K_,
@@ -571,7 +580,8 @@ def measure(args, cfg, over, ws, rank, local, device, headline=True):
                               else f"draft tree of {args.budget} nodes from the top-k, greedy walk against "
                                    "synthetic target tokens"),
                    **({"overrides": over} if over else {})},
-        "roofline": roofline, "step_roofline": step_roof, "kernels": kernels,
+        "roofline": roofline, "step_roofline": step_roof, "attention_roofline": attention_roofline,
+        "kernels": kernels,
         "prefill": _prefill_report(cfg, prefill_ms, prefill_pos),
         "e2e": e2e, "gpu_launches": launches,
         "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / K_, 4),
