@@ -123,6 +123,31 @@ __device__ __forceinline__ void write_op(const OpOut &o, size_t idx, float v) {
   }
 }
 
+// Four consecutive operand values (idx a multiple of 4): one 8-byte store per bf16 plane.
+__device__ __forceinline__ void write_op4(const OpOut &o, size_t idx, float4 v) {
+  if (!o.lo) {
+    *(float4 *)((float *)o.hi + idx) = v;
+    return;
+  }
+  const float a[4] = {v.x, v.y, v.z, v.w};
+  uint16_t h[4], l[4], l2[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bf16 hb = __float2bfloat16_rn(a[j]);
+    const float r = a[j] - __bfloat162float(hb);
+    const bf16 lb = __float2bfloat16_rn(r);
+    h[j] = __bfloat16_as_ushort(hb);
+    l[j] = __bfloat16_as_ushort(lb);
+    l2[j] = __bfloat16_as_ushort(__float2bfloat16_rn(r - __bfloat162float(lb)));
+  }
+  auto pack = [](const uint16_t (&q)[4]) {
+    return make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+  };
+  *(uint2 *)((bf16 *)o.hi + idx) = pack(h);
+  *(uint2 *)((bf16 *)o.lo + idx) = pack(l);
+  if (o.lo2) *(uint2 *)((bf16 *)o.lo2 + idx) = pack(l2);
+}
+
 // ---------------------------------------------------------------- GEMM description
 // Y[M, N] = epilogue( X[M, K] . W[N, K]^T ) with fp32 output. W has the storage type.
 // X is fp32, bf16, or a bf16 hi/lo pair (x_lo non-null). X may be split along K into

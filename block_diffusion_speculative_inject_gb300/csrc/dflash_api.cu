@@ -128,7 +128,7 @@ struct dflash_ctx {
 
   // CUDA graphs of the layer stack, keyed by batch size and split plan
   bool graphs_enabled = true;
-  double split_overhead = 2.0;             // attention split planner: CTA overhead in pages
+  double split_overhead = 4.0;             // attention split planner: CTA overhead in pages (measured)
   std::map<std::vector<int>, int> split_cache;   // rounded page counts -> pages per split
   cudaStream_t cap_stream = nullptr;
   int32_t *desc_fixed = nullptr;   // device descriptor read by captured kernels

@@ -726,6 +726,7 @@ struct TcGemm {
   bool wide = true;                   // two weight tiles per CTA for big M (DFLASH_GEMM_WM1=1: one)
   std::map<std::tuple<const void *, int, long>, int> occ;   // cluster occupancy per instance
   bool debug_plan = false;            // DFLASH_DEBUG_PLAN=1: print each new GEMM plan to stderr
+  double ovh = -1;                    // big-tile split-K model: per-CTA cost override (k-blocks)
   std::set<std::tuple<const void *, int, long>> printed;
 };
 
@@ -743,6 +744,7 @@ cudaError_t tc_gemm_create(TcGemm **out, int device, int num_sms, int *err_flag)
   t->err = err_flag;
   const char *wm1 = getenv("DFLASH_GEMM_WM1");
   t->wide = !(wm1 && wm1[0] == '1');
+  if (const char *o = getenv("DFLASH_GEMM_OVH")) t->ovh = atof(o);
   const char *dbg = getenv("DFLASH_DEBUG_PLAN");
   t->debug_plan = dbg && dbg[0] == '1';
   *out = t;
@@ -848,7 +850,8 @@ static int splits_few(const TcGemm *t, const Plan &p) {
 static int splits_wide(TcGemm *t, const void *fn, int threads, const Plan &p) {
   const int tiles = p.t_tiles * p.grid_y;
   const int s_max = std::max(1, std::min(8, p.kb / 8));
-  const double ovh = p.wm == 2 ? 5.0 : 8.0;     // fixed cost of a CTA, in k-blocks of its pipeline
+  // fixed cost of a CTA, in k-blocks of its pipeline (DFLASH_GEMM_OVH: tuning override)
+  const double ovh = t->ovh >= 0 ? t->ovh : p.wm == 2 ? 5.0 : 8.0;
   int best_S = 1;
   double best = 0;
   for (int S = 1; S <= s_max; ++S) {

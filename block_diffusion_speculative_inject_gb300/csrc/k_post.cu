@@ -104,6 +104,20 @@ cudaError_t launch_post_qkv(int dtype, const ModelDims &m, int B, const float *w
 // x != nullptr: x[m] += sum (written back), then the norm of x; else the norm of the sum.
 // out_skip_k = K > 0 writes the norm only for the K mask rows of each (K+1)-row block, to
 // output row b*K + j - 1 (the final norm before the LM head).
+// four consecutive weights as floats (one vector load when the address allows it)
+__device__ __forceinline__ float4 load4(const bf16 *w) {
+  if (((uintptr_t)w & 7u) == 0) {
+    const uint2 u = __ldg((const uint2 *)w);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+  }
+  return make_float4(to_f(w[0]), to_f(w[1]), to_f(w[2]), to_f(w[3]));
+}
+__device__ __forceinline__ float4 load4(const float *w) {
+  if (((uintptr_t)w & 15u) == 0) return __ldg((const float4 *)w);
+  return make_float4(w[0], w[1], w[2], w[3]);
+}
+
 constexpr int PN_THREADS = 128;
 constexpr int PN_VEC = 16;
 
@@ -164,10 +178,8 @@ __global__ void __launch_bounds__(PN_THREADS) k_post_norm(int M, int S, const fl
     const int i = threadIdx.x + t * PN_THREADS;
     if (i < n4) {
       const int e = 4 * i;
-      write_op(out, o + e + 0, v[t].x * rs * to_f(w[e + 0]));
-      write_op(out, o + e + 1, v[t].y * rs * to_f(w[e + 1]));
-      write_op(out, o + e + 2, v[t].z * rs * to_f(w[e + 2]));
-      write_op(out, o + e + 3, v[t].w * rs * to_f(w[e + 3]));
+      const float4 wv = load4(w + e);
+      write_op4(out, o + e, make_float4(v[t].x * rs * wv.x, v[t].y * rs * wv.y, v[t].z * rs * wv.z, v[t].w * rs * wv.w));
     }
   }
 }
