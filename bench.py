@@ -341,16 +341,8 @@ class StepLoop:
         tgt = torch.cat([torch.where(wl.coin_d[s], self.draft_tok, rnd[:, :-1]), rnd[:, -1:]], 1)
         ctx.verify(self.draft_tok, tgt, out["acc"], out["toks"], out["nxt"])
         n_new = (out["acc"] + 1).tolist()                     # the scheduler reads a + 1
-        # the accepted rows of each request's feature block, gathered on the device (the
-        # index goes through pinned memory, asynchronously)
-        idx = [r * self.cfg.n_new_max + i for r, n in enumerate(n_new) for i in range(n)]
-        if not hasattr(self, "rows_h"):
-            self.rows_h = torch.empty(self.wl.B * self.cfg.n_new_max, dtype=torch.int64).pin_memory()
-            self.rows_d = torch.empty(self.wl.B * self.cfg.n_new_max, dtype=torch.int64, device=self.device)
-        self.rows_h[:len(idx)] = torch.tensor(idx, dtype=torch.int64)
-        rows = self.rows_d[:len(idx)]
-        rows.copy_(self.rows_h[:len(idx)], non_blocking=True)
-        ctx.inject(wl.reqs, n_new, [f.index_select(0, rows) for f in feats])
+        # the first a + 1 rows of each request's block of target features go in, read in place
+        ctx.inject_blocks(wl.reqs, n_new, self.cfg.n_new_max, feats)
         self.records.append((list(self.lens), sum(n_new)))
         self.lens = [c + n for c, n in zip(self.lens, n_new)]
         self.anchor.copy_(out["nxt"])

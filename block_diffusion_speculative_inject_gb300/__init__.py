@@ -8,6 +8,7 @@ Functions with the C names take torch tensors (device buffers) and Python ints:
 
     ctx = dflash_create(cfg, weights, limits)                 # -> Context
     dflash_inject_context(ctx, req_ids, n_new, feats, reset=False)
+    dflash_inject_blocks(ctx, req_ids, n_new, block_rows, feats)
     dflash_draft_step(ctx, req_ids, anchors, argmax, topk_idx=None, topk_val=None, logits=None)
     dflash_verify_greedy(ctx, draft, target, accept_len, out_tokens, next_anchor)
     dflash_release / dflash_truncate / dflash_context_len / dflash_export_kv / dflash_destroy
@@ -21,7 +22,7 @@ import torch
 from . import _ffi
 
 __all__ = ["DFlashError", "Context", "Limits", "dflash_create", "dflash_destroy",
-           "dflash_inject_context", "dflash_draft_step", "dflash_verify_greedy",
+           "dflash_inject_context", "dflash_inject_blocks", "dflash_draft_step", "dflash_verify_greedy",
            "dflash_release", "dflash_truncate", "dflash_context_len", "dflash_export_kv",
            "dflash_validate_config", "make_config", "library"]
 
@@ -141,6 +142,14 @@ class Context:
         arr = (ctypes.c_void_p * len(feats))(*[f.data_ptr() for f in feats]) if feats else None
         st = self.lib.dflash_inject_context(self.h, _stream_ptr(stream), n, _i32_array(req_ids),
                                             _i32_array(n_new), 1 if reset else 0, arr)
+        self._check(st)
+
+    def inject_blocks(self, req_ids, n_new, block_rows, feats, stream=None):
+        """Appends the first n_new[b] rows of request b's block of block_rows feature rows
+        (feats[f] is [len(req_ids) * block_rows, H_t]) without gathering them first."""
+        arr = (ctypes.c_void_p * len(feats))(*[f.data_ptr() for f in feats])
+        st = self.lib.dflash_inject_blocks(self.h, _stream_ptr(stream), len(req_ids), _i32_array(req_ids),
+                                           _i32_array(n_new), int(block_rows), arr)
         self._check(st)
 
     def draft(self, req_ids, anchors, argmax=None, topk_idx=None, topk_val=None, logits=None,
@@ -298,6 +307,10 @@ def dflash_destroy(ctx: Context):
 
 def dflash_inject_context(ctx: Context, req_ids, n_new, feats, reset=False, stream=None):
     ctx.inject(req_ids, n_new, feats, reset=reset, stream=stream)
+
+
+def dflash_inject_blocks(ctx: Context, req_ids, n_new, block_rows, feats, stream=None):
+    ctx.inject_blocks(req_ids, n_new, block_rows, feats, stream=stream)
 
 
 def dflash_draft_step(ctx: Context, req_ids, anchors, argmax, topk_idx=None, topk_val=None,

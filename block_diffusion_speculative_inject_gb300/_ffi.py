@@ -52,6 +52,7 @@ SIGNATURES = {
     "dflash_create": (_I32, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _I32, ctypes.POINTER(_P)]),
     "dflash_destroy": (None, [_P]),
     "dflash_inject_context": (_I32, [_P, _P, _I32, _I32P, _I32P, _I32, ctypes.POINTER(_P)]),
+    "dflash_inject_blocks": (_I32, [_P, _P, _I32, _I32P, _I32P, _I32, ctypes.POINTER(_P)]),
     "dflash_draft_step": (_I32, [_P, _P, _I32, _I32P, _P, _P, _P, _P, _P]),
     "dflash_verify_greedy": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     "dflash_sample_tokens": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),

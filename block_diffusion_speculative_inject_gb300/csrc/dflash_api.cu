@@ -107,6 +107,8 @@ struct dflash_ctx {
   // projection, after the down projection)
   float *ss_o = nullptr, *ss_d = nullptr;
   float *ss_inj = nullptr;   // the same after the injection's fc ([H/128][32])
+  void *gath = nullptr;      // packed feature rows of dflash_inject_blocks (grown on demand)
+  size_t gath_bytes = 0;
   float *ss_f = nullptr;     // and for the final norm of the K mask rows ([H/128][rows_k])
 
   std::vector<Stage> ring;
@@ -386,7 +388,7 @@ extern "C" const char *dflash_status_string(dflash_status s) {
 static void free_all(dflash_ctx *c) {
   void *dev[] = {c->pool, c->rope, c->x, c->xn, c->qkv, c->ao, c->gu, c->hmid, c->xf, c->logits, c->cand,
                  c->part_o, c->part_ml, c->fc_out, c->g, c->kvproj, c->smp_tok, c->smp_n, c->smp_p,
-                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj, c->ss_f};
+                 c->lse_part, c->xc, c->corr, c->sel_gate, c->sel_tab, c->ss_o, c->ss_d, c->ss_inj, c->ss_f, c->gath};
   for (void *p : dev)
     if (p) cudaFree(p);
   for (auto &st : c->ring) {
@@ -618,9 +620,13 @@ extern "C" dflash_status dflash_truncate(dflash_ctx *c, int32_t req_id, int32_t 
 }
 
 // ------------------------------------------------------------------------------ injection
-extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int32_t n_req,
-                                               const int32_t *req_ids, const int32_t *n_new,
-                                               int32_t reset, const void *const *feats) {
+// block_rows == 0: the feature rows are packed (sum(n_new) of them, request after request);
+// block_rows > 0: request b owns rows [b * block_rows, (b + 1) * block_rows) and its first
+// n_new[b] are appended: a gather kernel packs them into library memory first, so the GEMMs
+// see exactly the rows of the packed form (and take the same few-row kernels).
+static dflash_status inject_impl(dflash_ctx *c, void *stream, int32_t n_req, const int32_t *req_ids,
+                                 const int32_t *n_new, int32_t reset, const void *const *feats,
+                                 int32_t block_rows) {
   if (!c) return DFLASH_ERR_INVALID_ARG;
   dflash_status st = check_device_flag(c);
   if (st != DFLASH_OK) return st;
@@ -640,6 +646,8 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     if (!seen.insert(req_ids[b]).second)
       return set_err(c, DFLASH_ERR_INVALID_ARG, "request %d appears twice", req_ids[b]);
     if (n_new[b] < 0) return set_err(c, DFLASH_ERR_INVALID_ARG, "n_new[%d] < 0", b);
+    if (block_rows > 0 && n_new[b] > block_rows)
+      return set_err(c, DFLASH_ERR_INVALID_ARG, "n_new[%d] = %d exceeds block_rows = %d", b, n_new[b], block_rows);
     auto it = c->reqs.find(req_ids[b]);
     bool exists = it != c->reqs.end();
     if (!exists) ++new_reqs;
@@ -668,8 +676,24 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
   DeviceGuard guard(c->device);
   if (guard.err != cudaSuccess) return set_err(c, DFLASH_ERR_CUDA, "cudaSetDevice failed");
 
+  const int C = c->cfg.max_inject_rows;
+  const size_t row_bytes = (size_t)m.Ht * c->esz;
+  if (block_rows > 0 && total > 0) {
+    const size_t need = (size_t)m.n_feat * (size_t)std::min<long>(C, total) * row_bytes;
+    if (need > c->gath_bytes) {
+      if (c->gath) cudaFree(c->gath);
+      c->gath = nullptr;
+      c->gath_bytes = 0;
+      if (cudaMalloc(&c->gath, need) != cudaSuccess) {
+        cudaGetLastError();
+        return set_err(c, DFLASH_ERR_CUDA, "cudaMalloc of %zu bytes for the packed feature rows failed", need);
+      }
+      c->gath_bytes = need;
+    }
+  }
+
   // ---- commit: pages and lengths
-  std::vector<int32_t> slot(total), pos(total);
+  std::vector<int32_t> slot(total), pos(total), src(block_rows > 0 ? total : 0);
   long r = 0;
   for (int b = 0; b < n_req; ++b) {
     Req &q = c->reqs[req_ids[b]];
@@ -687,12 +711,12 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
       int p = start[b] + i;
       slot[r] = q.pages[p / kPage] * kPage + p % kPage;
       pos[r] = p;
+      if (block_rows > 0) src[r] = b * block_rows + i;
     }
     q.len = new_len;
   }
 
   // ---- launches, in chunks of max_inject_rows rows
-  const int C = c->cfg.max_inject_rows;
   const int F = m.n_feat * m.Ht;
   const int kvw = m.L * 2 * m.kv_dim();
   std::vector<int32_t> buf;
@@ -702,14 +726,25 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
     int n = (int)std::min<long>(C, total - r0);
     buf.assign(slot.begin() + r0, slot.begin() + r0 + n);
     buf.insert(buf.end(), pos.begin() + r0, pos.begin() + r0 + n);
+    if (block_rows > 0) buf.insert(buf.end(), src.begin() + r0, src.begin() + r0 + n);
     const int32_t *dslot = nullptr;
     if ((st = stage_upload(c, s, buf.data(), buf.size() * 4, &dslot)) != DFLASH_OK) return st;
+    // the feature rows of this chunk: read in place, or the counted rows of the blocks packed
+    const void *fx[8];
+    for (int f = 0; f < m.n_feat; ++f)
+      fx[f] = block_rows > 0 ? (const void *)((const char *)c->gath + (size_t)f * n * row_bytes)
+                             : (const void *)((const char *)feats[f] + (size_t)r0 * row_bytes);
+    if (block_rows > 0)
+      CK(c, timed(c, K_INJECT_KV, s, 2.0 * n * m.n_feat * row_bytes, 0, 1, [&] {
+           return launch_gather_rows(m.n_feat, n, (long)row_bytes, dslot + 2 * n, feats, c->gath,
+                                     (long)n * (long)row_bytes, s);
+         }));
     // fc over the n_feat feature tensors read in place (K segments), then RMSNorm -> g
     GemmDesc d = gemm_desc(n, m.H, F, EPI_STORE, nullptr, m.H);
     d.x_bf16 = c->dtype == DFLASH_BF16;   // the features are exact storage-type values
     d.n_xseg = m.n_feat;
     for (int f = 0; f < m.n_feat; ++f) {
-      d.x[f] = (const char *)feats[f] + (size_t)r0 * m.Ht * c->esz;
+      d.x[f] = fx[f];
       d.x_k0[f] = f * m.Ht;
       d.ldx[f] = m.Ht;
     }
@@ -770,6 +805,19 @@ extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int3
        }));
   }
   return DFLASH_OK;
+}
+
+extern "C" dflash_status dflash_inject_context(dflash_ctx *c, void *stream, int32_t n_req,
+                                               const int32_t *req_ids, const int32_t *n_new,
+                                               int32_t reset, const void *const *feats) {
+  return inject_impl(c, stream, n_req, req_ids, n_new, reset, feats, 0);
+}
+
+extern "C" dflash_status dflash_inject_blocks(dflash_ctx *c, void *stream, int32_t n_req,
+                                              const int32_t *req_ids, const int32_t *n_new,
+                                              int32_t block_rows, const void *const *feats) {
+  if (c && block_rows < 1) return set_err(c, DFLASH_ERR_INVALID_ARG, "block_rows < 1");
+  return inject_impl(c, stream, n_req, req_ids, n_new, 0, feats, block_rows);
 }
 
 // ------------------------------------------------------------------------------ draft step

@@ -326,4 +326,34 @@ cudaError_t launch_embed_norm(int dtype, const ModelDims &m, int B, const int32_
                     m.eps, err);
 }
 
+// ---------------------------------------------------------------------- row gather
+// Packs the counted rows of the target's verify blocks: out[f][r] = in[f][src[r]] for every
+// feature tensor f; one CTA per (row, feature), 16-byte words when the row allows them.
+struct RowPtrs { const void *p[8]; };
+
+__global__ void k_gather_rows(int rows, long row_bytes, long out_stride, const int32_t *src, RowPtrs in,
+                              uint8_t *out) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x, f = blockIdx.y;
+  const uint8_t *a = (const uint8_t *)in.p[f] + (size_t)src[r] * row_bytes;
+  uint8_t *d = out + (size_t)f * out_stride + (size_t)r * row_bytes;
+  if (((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(d) | (uintptr_t)row_bytes) & 15) == 0) {
+    for (long i = threadIdx.x; i < row_bytes / 16; i += blockDim.x)
+      reinterpret_cast<uint4 *>(d)[i] = reinterpret_cast<const uint4 *>(a)[i];
+  } else {
+    for (long i = threadIdx.x; i < row_bytes; i += blockDim.x) d[i] = a[i];
+  }
+}
+
+cudaError_t launch_gather_rows(int n_feat, int rows, long row_bytes, const int32_t *src,
+                               const void *const *in, void *out, long out_stride, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (n_feat < 1 || n_feat > 8) return cudaErrorInvalidValue;
+  RowPtrs ip{};
+  for (int f = 0; f < n_feat; ++f) ip.p[f] = in[f];
+  return launch_pdl(k_gather_rows, dim3((unsigned)rows, (unsigned)n_feat), dim3(256), 0, s, rows, row_bytes,
+                    out_stride, src, ip, (uint8_t *)out);
+}
+
 }  // namespace dflash

@@ -87,6 +87,9 @@ cudaError_t launch_post_qkv(int dtype, const ModelDims &m, int B, const float *w
 cudaError_t launch_post_norm(int dtype, int M, int H, const float *ws, int S, float *x, OpOut out,
                              const void *w, float eps, int out_skip_k, cudaStream_t s);
 cudaError_t launch_post_swiglu(int M, int I, const float *ws, int S, OpOut h, cudaStream_t s);
+// out + f * out_stride + r * row_bytes  <-  in[f] + src[r] * row_bytes, r < rows, f < n_feat <= 8
+cudaError_t launch_gather_rows(int n_feat, int rows, long row_bytes, const int32_t *src,
+                               const void *const *in, void *out, long out_stride, cudaStream_t s);
 cudaError_t launch_post_kv(int dtype, const ModelDims &m, int T, const float *ws, int S,
                            const int32_t *slot, const int32_t *pos, const float2 *rope,
                            const void *const *k_norms, void *pool, cudaStream_t s);

@@ -169,6 +169,21 @@ dflash_status dflash_inject_context(dflash_ctx *ctx, void *stream, int32_t n_req
                                     const int32_t *req_ids, const int32_t *n_new,
                                     int32_t reset, const void *const *feats);
 
+/* Incremental injection straight from the target's verify block ("LLM的推理加速-DFlash"
+ * 关键创新 Step 3: after verification the accepted positions' target hidden states enter
+ * the draft cache): the same result as dflash_inject_context (reset 0) on the gathered rows.
+ *   block_rows >= 1: feats[f] is [n_req * block_rows, H_t] row-major (16-byte aligned);
+ *           rows [b * block_rows, (b + 1) * block_rows) belong to request req_ids[b].
+ *   n_new   [n_req] host, 0 <= n_new[b] <= block_rows: the first n_new[b] rows of request
+ *           b's block are appended (typically the accept length + 1 of its verify).
+ * The counted rows are packed by the library (into memory it grows on demand), so the
+ * caller passes the blocks as the target produced them.
+ * Errors: as dflash_inject_context; INVALID_ARG if block_rows < 1 or a count is out of
+ * range. */
+dflash_status dflash_inject_blocks(dflash_ctx *ctx, void *stream, int32_t n_req,
+                                   const int32_t *req_ids, const int32_t *n_new,
+                                   int32_t block_rows, const void *const *feats);
+
 /* One draft step for n_req live requests ("DFlash：把串行 Draft 变成并行“填空”" §4-4.4):
  *   req_ids  [n_req] host.
  *   anchors  [n_req] int32 DEVICE: the last verified token of each request.

@@ -82,6 +82,7 @@ def test_null_context_calls_are_rejected(lib):
     assert lib.dflash_truncate(None, 1, 0) == -1
     assert lib.dflash_last_error(None) == b""
     assert lib.dflash_free_pages(None) == 0
+    assert lib.dflash_inject_blocks(None, None, 1, None, None, 16, None) == -1
     out = ctypes.c_void_p()
     assert lib.dflash_create(None, None, 0, ctypes.byref(out)) == -1
     assert not out.value

@@ -274,3 +274,65 @@ def test_graph_replay_matches_eager(monkeypatch):
         p.ctx.close()
     for (a1, i1, v1), (a2, i2, v2) in zip(*results):
         assert torch.equal(a1, a2) and torch.equal(i1, i2) and torch.equal(v1, v2)
+
+
+@pytest.mark.parametrize("name,B,rows", [("mini_bf16", 1, 64), ("mini_bf16", 3, 100), ("mini_bf16", 3, 20),
+                                         ("tiny_f32", 2, 64)])
+def test_inject_blocks_appends_each_blocks_counted_prefix(name, B, rows):
+    """dflash_inject_blocks on whole verify blocks (K + 1 feature rows per request, counts
+    0..K+1 including both ends) against the oracle injecting the counted prefix of each block:
+    the cache rows, the context lengths and the next draft. The counted rows are packed
+    first: up to 32 of them take the fused cache-write epilogue, 39 the separate cache-write
+    kernel, and max_inject_rows 20 cuts the packed rows into chunks."""
+    cfg = get_config(name)
+    Q = cfg.block_k + 1
+    pair = Pair(cfg, _limits(max_batch=B, max_pages=48, max_positions=1024, max_inject_rows=rows))
+    reqs = list(range(20, 20 + B))
+    lens = [70, 129, 64][:B]
+    pair.inject(reqs, lens, "prefill", reset=True)
+    rng = np.random.default_rng(7)
+    counts = [[0, Q, 5][:B], [Q, Q, 7][:B], [Q, 1, 0][:B], rng.integers(1, Q + 1, size=B).tolist()]
+    if B == 1:
+        counts = [[0], [Q], [1], [9]]
+    for step, n_new in enumerate(counts):
+        blocks = [S.make_features(cfg, Q, 0, ("block", step), r) for r in reqs]
+        feats = [torch.cat([b[f] for b in blocks], 0).cuda().contiguous() for f in range(cfg.n_feat)]
+        pair.ctx.inject_blocks(reqs, n_new, Q, feats)
+        for r, b, n in zip(reqs, blocks, n_new):
+            pair.orc.inject(r, [to_np(x[:n]).astype(np.float64) for x in b])
+    kv_tol = 1e-4 if cfg.dtype == "f32" else 3e-2
+    equal = total = 0
+    for i, r in enumerate(reqs):
+        n_all = pair.ctx.context_len(r)
+        assert n_all == pair.orc.context_len(r) == lens[i] + sum(c[i] for c in counts)
+        for l in range(cfg.n_layers):
+            k, v = pair.ctx.export_kv(r, l, lens[i], n_all - lens[i])
+            for got, want in ((k, pair.orc.cache[r]["K"][l][lens[i]:]), (v, pair.orc.cache[r]["V"][l][lens[i]:])):
+                got = to_np(got)
+                np.testing.assert_allclose(got, want, atol=kv_tol, rtol=0)
+                equal += int(np.sum(got == want))
+                total += got.size
+    if cfg.dtype == "bf16":
+        assert equal > 0.999 * total, f"{equal} of {total} cached values equal"
+    anchors = S.make_anchors(cfg, B, 0, 3)
+    out = pair.ctx.draft(reqs, anchors.cuda(), want_logits=True)
+    lg, am = to_np(out["logits"]), out["argmax"].cpu().numpy()
+    ti, tv = out["topk_idx"].cpu().numpy(), to_np(out["topk_val"])
+    for i, r in enumerate(reqs):
+        w_am, w_idx, w_val, w_lg = pair.orc.draft(r, int(anchors[i]))
+        check_logits(cfg, lg[i], w_lg, f"req {r}")
+        check_argmax(am[i], w_lg, f"req {r}")
+        check_topk(ti[i], tv[i], w_lg, cfg.topk, LOGIT_TOL[cfg.dtype], f"req {r}")
+
+
+def test_inject_blocks_rejects_counts_outside_the_block():
+    cfg = get_config("mini_bf16")
+    from block_diffusion_speculative_inject_gb300 import DFlashError
+    pair = Pair(cfg, _limits(max_batch=2, max_pages=16, max_positions=512, max_inject_rows=64))
+    pair.inject([1, 2], [10, 10], "prefill", reset=True)
+    feats = [torch.zeros((2 * 16, cfg.target_hidden), dtype=torch.bfloat16, device="cuda")
+             for _ in range(cfg.n_feat)]
+    for n_new, rows in (([17, 1], 16), ([-1, 1], 16), ([1, 1], 0)):
+        with pytest.raises(DFlashError):
+            pair.ctx.inject_blocks([1, 2], n_new, rows, feats)
+        assert pair.ctx.context_len(1) == 10 and pair.ctx.context_len(2) == 10
