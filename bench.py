@@ -671,6 +671,8 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic: seeded N(0,0.02) weights, N(0,1) target hidden states, uniform ids",
            "config": {"workload": f"{cfg.name}: {WORKLOAD_TEXT.get(cfg.name, cfg.name)}",
+                      "batch": wl.B, "K": cfg.block_k,
+                      "context": list(wl.ctx) if wl.B <= 8 else [min(wl.ctx), max(wl.ctx)],
                       "sample": "request 0 of the batch per step",
                       **({"overrides": over} if over else {})},
            "cpu_baseline": {"value": round(v, 3), "unit": "draft tok/s", "cores": _cores(),
