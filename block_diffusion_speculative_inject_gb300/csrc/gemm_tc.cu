@@ -535,18 +535,43 @@ __global__ void __launch_bounds__(tc_threads<BN>(), BN <= 32 ? 3 : 1) k_gemm_tc(
     // every split's partial tile is staged; rank r owns columns (tokens) r, r + S, ...: each
     // epilogue warp takes one of them at a time, sums its 128 rows over all ranks in rank
     // order (lane l: rows l, l + 32, l + 64, l + 96) and applies the epilogue
+    constexpr int U = BN <= 32 ? 2 : 4;        // tokens per warp per round: loads in flight
+    const int rank = (int)cluster_ctarank();
+    const int ew = warp - 2;
+    // The epilogue's inputs that do not depend on the accumulator (the residual / stream
+    // rows, the RMSNorm sums of the row scale) for this warp's first round, loaded before
+    // the cluster barrier so that their latency overlaps the wait for the slowest split.
+    float pre_y[U][4], pre_ss[U];
+    if (warp >= 2) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = rank + p.S * ew + NW * p.S * u, m = m0 + c;
+        pre_ss[u] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pre_y[u][j] = 0.f;
+        if (c >= BN || m >= p.M) continue;
+        if (FN && p.rs_part)
+          for (int t = lane; t < p.rs_tiles; t += 32) pre_ss[u] += __ldg(p.rs_part + (size_t)t * p.M + m);
+        const float *src = (FN && p.epi == EPI_RESNORM) ? p.y : p.epi == EPI_RESID ? p.resid : nullptr;
+        if (src) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + lane + 32 * j;
+            if (n < p.N) pre_y[u][j] = src[(size_t)m * p.ldy + n];
+          }
+        }
+      }
+    }
     if (p.S > 1) cluster_sync_all();
     if (warp >= 2) {
-     const int rank = (int)cluster_ctarank();
-     const int ew = warp - 2;
      for (int w = 0; w < wm_live; ++w) {
       // weight tile w: rows n0w.. of the output, staged at [w][BN][128]
       const int ty = (int)blockIdx.y * WM + w, n0w = ty * TC_BM;
       const uint32_t base = smem_u32(gen_tiles) + (uint32_t)(w * BN * TC_BM * 4);
       const float *own = (const float *)gen_tiles + (size_t)w * BN * TC_BM;
       const int part = n0w < p.q_dim ? 0 : (n0w < p.q_dim + p.kv_dim ? 1 : 2);   // EPI_QKV
-      constexpr int U = BN <= 32 ? 2 : 4;      // tokens per warp per round: loads in flight
       for (int cb = rank + p.S * ew; cb < BN; cb += NW * U * p.S) {
+        const bool pre = w == 0 && cb == rank + p.S * ew;   // this round's inputs are loaded
         float a[U][4];
         float2 cs[U][2];
         int mu[U];
@@ -595,8 +620,9 @@ __global__ void __launch_bounds__(tc_threads<BN>(), BN <= 32 ? 3 : 1) k_gemm_tc(
           float *x = a[u];
           if (FN && p.rs_part) {
             // the producer left the RMSNorm's row scale: lane t holds tile t's sum of squares
-            float ss = 0.f;
-            for (int t = lane; t < p.rs_tiles; t += 32) ss += __ldg(p.rs_part + (size_t)t * p.M + m);
+            float ss = pre ? pre_ss[u] : 0.f;
+            if (!pre)
+              for (int t = lane; t < p.rs_tiles; t += 32) ss += __ldg(p.rs_part + (size_t)t * p.M + m);
             const float rs = rsqrtf(warp_sum(ss) / (float)p.rs_dim + p.eps);
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] *= rs;
@@ -644,7 +670,7 @@ __global__ void __launch_bounds__(tc_threads<BN>(), BN <= 32 ? 3 : 1) k_gemm_tc(
             for (int j = 0; j < 4; ++j) {
               const int n = n0w + lane + 32 * j;
               const size_t o = (size_t)m * p.ldy + n;
-              const float y = p.y ? p.y[o] + x[j] : x[j];       // no residual: the norm alone
+              const float y = p.y ? (pre ? pre_y[u][j] : p.y[o]) + x[j] : x[j];   // no residual: the norm alone
               if (p.y) p.y[o] = y;
               write_op(p.out, (size_t)orow * p.ldo + n, y * __bfloat162float(p.norm_w[n]));
               ss += y * y;
@@ -698,7 +724,7 @@ __global__ void __launch_bounds__(tc_threads<BN>(), BN <= 32 ? 3 : 1) k_gemm_tc(
             const int n = n0w + lane + 32 * j;
             if (n < p.N) {
               const size_t o = (size_t)m * p.ldy + n;
-              p.y[o] = p.epi == EPI_RESID ? p.resid[o] + x[j] : x[j];
+              p.y[o] = p.epi == EPI_RESID ? (pre ? pre_y[u][j] : p.resid[o]) + x[j] : x[j];
             }
           }
         }
