@@ -47,16 +47,23 @@ def _run(cfg_name, sample, steps, ctx_override=None, checked=None):
     reqs = list(range(B))
 
     def inject(n_new, tag, reset=False):
+        # the prefill as packed rows; a step's a + 1 positions per request as the target
+        # hands them over: a block of K + 1 feature rows per request (dflash_inject_blocks)
+        Q = cfg.block_k + 1
         parts = []
         for r, n in zip(reqs, n_new):
+            rows = n if reset else Q
             if r in sample:
-                f = S.make_features(cfg, n, 0, tag, r)
-                orc.inject(r, [to_np(x).astype(np.float64) for x in f], reset=reset)
+                f = S.make_features(cfg, rows, 0, tag, r)
+                orc.inject(r, [to_np(x[:n]).astype(np.float64) for x in f], reset=reset)
                 parts.append([x.cuda() for x in f])
             else:
-                parts.append(_device_feats(cfg, n, zlib.crc32(repr((tag, r)).encode())))
+                parts.append(_device_feats(cfg, rows, zlib.crc32(repr((tag, r)).encode())))
         feats = [torch.cat([p[f] for p in parts], 0).contiguous() for f in range(cfg.n_feat)]
-        ctx.inject(reqs, n_new, feats, reset=reset)
+        if reset:
+            ctx.inject(reqs, n_new, feats, reset=True)
+        else:
+            ctx.inject_blocks(reqs, n_new, Q, feats)
 
     inject(ctx_lens, "prefill", reset=True)
     anchors = S.make_anchors(cfg, B, 0, 0)
@@ -113,6 +120,7 @@ def test_q4b_b128_large_batch():
 
 def test_q27b_b8_long_context():
     """27B-target-shaped draft, 8 requests of context 32768, K=15; request 5, over 64
-    consecutive verify-driven steps (each injects the a + 1 positions its verify accepted),
-    drafts compared with the oracle at 8 of them, the cache rows of all 64 injections after."""
+    consecutive verify-driven steps (each injects the a + 1 positions its verify accepted, from
+    the K + 1-row verify block of target features), drafts compared with the oracle at 8 of
+    them, the cache rows of all 64 injections after."""
     _run("q27b_b8", sample=(5,), steps=64, checked=(0, 1, 2, 9, 21, 36, 50, 63))
