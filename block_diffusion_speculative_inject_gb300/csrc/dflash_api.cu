@@ -529,7 +529,7 @@ extern "C" dflash_status dflash_create(const dflash_config *cfg, const dflash_we
   c->free_pages.reserve(cfg->max_pages);
   for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
 
-  size_t inj = (size_t)2 * C * sizeof(int32_t);
+  size_t inj = (size_t)3 * C * sizeof(int32_t);      // slot, position, source row (inject_blocks)
   size_t drf = (size_t)(4 * cfg->max_batch + 1) * sizeof(int32_t) +
                (size_t)cfg->max_batch * c->max_pages_per_req * sizeof(int32_t);
   c->stage_cap = (std::max(inj, drf) + 255) / 256 * 256;
