@@ -578,6 +578,10 @@ def measure(args, cfg, over, ws, rank, local, device, headline=True):
         "e2e": e2e, "gpu_launches": launches,
         "host_enqueue_ms_per_step": round(host_enqueue * 1e3 / K_, 4),
         "ms_per_step_with_kernel_events": round(ms_events / len(again), 4),
+        "kernels_timing": ("CUDA events around every launch in a second pass over the same steps; "
+                           "the events add per-launch overhead and serialise the programmatic "
+                           "launches, so the classes' times overstate the step's share of short "
+                           "kernels and their sum exceeds ms_per_step"),
     }
     res["clocks"] = clk.summary()
     ctx.close()
