@@ -817,6 +817,8 @@ extern "C" dflash_status dflash_inject_blocks(dflash_ctx *c, void *stream, int32
                                               const int32_t *req_ids, const int32_t *n_new,
                                               int32_t block_rows, const void *const *feats) {
   if (c && block_rows < 1) return set_err(c, DFLASH_ERR_INVALID_ARG, "block_rows < 1");
+  if (c && (long)n_req * block_rows > 0x7fffffffL)
+    return set_err(c, DFLASH_ERR_INVALID_ARG, "n_req * block_rows exceeds 2^31 - 1 feature rows");
   return inject_impl(c, stream, n_req, req_ids, n_new, 0, feats, block_rows);
 }
 
