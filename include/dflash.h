@@ -178,8 +178,8 @@ dflash_status dflash_inject_context(dflash_ctx *ctx, void *stream, int32_t n_req
  *           b's block are appended (typically the accept length + 1 of its verify).
  * The counted rows are packed by the library (into memory it grows on demand), so the
  * caller passes the blocks as the target produced them.
- * Errors: as dflash_inject_context; INVALID_ARG if block_rows < 1 or a count is out of
- * range. */
+ * Errors: as dflash_inject_context; INVALID_ARG if block_rows < 1, n_req * block_rows
+ * exceeds 2^31 - 1, or a count is out of range. */
 dflash_status dflash_inject_blocks(dflash_ctx *ctx, void *stream, int32_t n_req,
                                    const int32_t *req_ids, const int32_t *n_new,
                                    int32_t block_rows, const void *const *feats);
